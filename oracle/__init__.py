@@ -1,0 +1,212 @@
+"""Reference (oracle) for row-wise numerically stable softmax: fp64, plain C, CPU.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline legs of ``bench.py`` may import this package.  The product path
+(``numerically_stable_online_gb300``) never imports it, and the two share no
+code: this package compiles ``softmax_ref.c`` with the host C compiler and calls
+it through ctypes.
+
+The arithmetic is in ``softmax_ref.c``; each function there cites the page
+section it follows.  This module only marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F32, F16, BF16 = 0, 1, 2
+_DTYPE_CODE = {"f32": F32, "f16": F16, "bf16": BF16}
+_ITEMSIZE = {F32: 4, F16: 2, BF16: 2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "softmax_ref.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile softmax_ref.c into oracle/_build/liboracle.so (plain -O2, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.orc_decode_f16.argtypes = [ctypes.c_uint16]
+        lib.orc_decode_f16.restype = D
+        lib.orc_decode_bf16.argtypes = [ctypes.c_uint16]
+        lib.orc_decode_bf16.restype = D
+        lib.orc_round_f16.argtypes = [D]
+        lib.orc_round_f16.restype = ctypes.c_uint16
+        lib.orc_round_bf16.argtypes = [D]
+        lib.orc_round_bf16.restype = ctypes.c_uint16
+        lib.orc_round_array.argtypes = [P, I64, I32, P]
+        lib.orc_decode_array.argtypes = [P, I64, I32, P]
+        lib.orc_softmax_rows.argtypes = [P, I32, I64, P, P, I64, P]
+        lib.orc_row_stats.argtypes = [P, I32, I64, P, P, I64, P, P]
+        lib.orc_merge_stats.argtypes = [P, P, P, P, P, P, I64]
+        lib.orc_online_elementwise.argtypes = [P, I64, I32, P, P]
+        lib.orc_online_tiled.argtypes = [P, I64, I64, P, P, P]
+        lib.orc_naive_softmax_f16.argtypes = [P, I64, P]
+        lib.orc_stable_softmax_f16.argtypes = [P, I64, P, P, P, P]
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    return _DTYPE_CODE[dtype]
+
+
+def _as_storage(x, dtype):
+    """x as a C-contiguous array of the storage type's raw bits (or float32)."""
+    code = _code(dtype)
+    a = np.ascontiguousarray(x)
+    if code == F32:
+        if a.dtype != np.float32:
+            raise TypeError("f32 input must be a float32 array")
+    else:
+        if a.dtype == np.float16 and code == F16:
+            a = a.view(np.uint16)
+        if a.dtype != np.uint16:
+            raise TypeError("f16/bf16 input must be given as uint16 bit patterns")
+    return a, code
+
+
+def _lengths(valid_len, rows):
+    if valid_len is None:
+        return None
+    v = np.ascontiguousarray(valid_len, dtype=np.int32)
+    if v.shape != (rows,):
+        raise ValueError("valid_len must have one entry per row")
+    return v
+
+
+def softmax_rows(x, dtype, rows: int, cols: int, valid_len=None, rows_sel=None) -> np.ndarray:
+    """fp64 softmax of rows of the [rows, cols] input (stored bits), per the declared policy.
+
+    rows_sel: optional list of row indices; the result then has len(rows_sel) rows.
+    """
+    lib = _load()
+    a, code = _as_storage(x, dtype)
+    if a.size != rows * cols:
+        raise ValueError("x has the wrong number of elements")
+    vl = _lengths(valid_len, rows)
+    sel = None if rows_sel is None else np.ascontiguousarray(rows_sel, dtype=np.int64)
+    n_sel = rows if sel is None else sel.size
+    p = np.empty((n_sel, cols), dtype=np.float64)
+    lib.orc_softmax_rows(_ptr(a), code, cols, _ptr(vl), _ptr(sel), n_sel, _ptr(p))
+    return p
+
+
+def row_stats(x, dtype, rows: int, cols: int, valid_len=None, rows_sel=None):
+    """fp64 (m, d) per row: m = max of the valid prefix, d = sum exp(x - m)."""
+    lib = _load()
+    a, code = _as_storage(x, dtype)
+    if a.size != rows * cols:
+        raise ValueError("x has the wrong number of elements")
+    vl = _lengths(valid_len, rows)
+    sel = None if rows_sel is None else np.ascontiguousarray(rows_sel, dtype=np.int64)
+    n_sel = rows if sel is None else sel.size
+    m = np.empty(n_sel, dtype=np.float64)
+    d = np.empty(n_sel, dtype=np.float64)
+    lib.orc_row_stats(_ptr(a), code, cols, _ptr(vl), _ptr(sel), n_sel, _ptr(m), _ptr(d))
+    return m, d
+
+
+def merge_stats(m_a, d_a, m_b, d_b):
+    """fp64 merge of two arrays of block summaries (empty block = (-inf, 0))."""
+    lib = _load()
+    arrs = [np.ascontiguousarray(np.atleast_1d(v), dtype=np.float64) for v in (m_a, d_a, m_b, d_b)]
+    n = arrs[0].size
+    if any(v.size != n for v in arrs):
+        raise ValueError("summary arrays differ in length")
+    m = np.empty(n, dtype=np.float64)
+    d = np.empty(n, dtype=np.float64)
+    lib.orc_merge_stats(*[_ptr(v) for v in arrs], _ptr(m), _ptr(d), n)
+    return m, d
+
+
+def round_to(p, dtype) -> np.ndarray:
+    """Round doubles to the storage type, ties to even, straight from fp64.
+
+    Returns uint16 bit patterns for f16/bf16 and uint32 bit patterns for f32.
+    """
+    lib = _load()
+    code = _code(dtype)
+    v = np.ascontiguousarray(p, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint32 if code == F32 else np.uint16)
+    lib.orc_round_array(_ptr(v), v.size, code, _ptr(out))
+    return out
+
+
+def decode(bits, dtype) -> np.ndarray:
+    """Widen stored values (float32 array, or uint16 bits for f16/bf16) to fp64."""
+    lib = _load()
+    a, code = _as_storage(bits, dtype)
+    out = np.empty(a.shape, dtype=np.float64)
+    lib.orc_decode_array(_ptr(a), a.size, code, _ptr(out))
+    return out
+
+
+def online_elementwise(x, rescale: bool = True):
+    """Per-element online recurrence; returns the (m_i, d_i) trace after each element."""
+    lib = _load()
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    m = np.empty(v.size)
+    d = np.empty(v.size)
+    lib.orc_online_elementwise(_ptr(v), v.size, 1 if rescale else 0, _ptr(m), _ptr(d))
+    return m, d
+
+
+def online_tiled(x, B: int):
+    """Tiled online update; returns per tile (m, corrected old d, d)."""
+    lib = _load()
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    nt = (v.size + B - 1) // B
+    m, c, d = np.empty(nt), np.empty(nt), np.empty(nt)
+    lib.orc_online_tiled(_ptr(v), v.size, B, _ptr(m), _ptr(c), _ptr(d))
+    return m, c, d
+
+
+def naive_softmax_f16(x) -> np.ndarray:
+    """The unshifted softmax evaluated in fp16 arithmetic (negative control)."""
+    lib = _load()
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    p = np.empty(v.size)
+    lib.orc_naive_softmax_f16(_ptr(v), v.size, _ptr(p))
+    return p
+
+
+def stable_softmax_f16(x):
+    """The max-shifted softmax evaluated in fp16 arithmetic: (shifted, exp, p, sum)."""
+    lib = _load()
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    sh, e, p = np.empty(v.size), np.empty(v.size), np.empty(v.size)
+    s = np.empty(1)
+    lib.orc_stable_softmax_f16(_ptr(v), v.size, _ptr(sh), _ptr(e), _ptr(p), _ptr(s))
+    return sh, e, p, float(s[0])
