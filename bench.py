@@ -1,0 +1,425 @@
+"""Benchmark: row softmax throughput on GB300 (algorithmic GB/s and rows/s).
+
+A step is one pass of the whole hot path (the row softmax) over one batch of
+the synthetic workload; the default workload is bf16 16384 x 4096 (N(0, 8^2)
+logits, no mask).  Inputs are resident in HBM when the timed region starts; to
+keep every step's reads and writes coming from HBM rather than L2, steps rotate
+over several input/output buffer sets whose combined size is far above L2.
+
+Prints one JSON line on rank 0:
+  value        algorithmic bytes (valid input read once + output written once
+               + row lengths) of all ranks' steps / max-over-ranks timed region
+  e2e          the same metric through the public call with the input copied
+               from pinned host memory and the output copied back every step
+  roofline     the softmax kernel's achieved bandwidth (CUDA events around every
+               launch in the timed region) against the measured HBM copy peak
+  cpu_baseline the fp64 CPU reference timed on this host on a bounded sample
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+For N > 1 it runs under torch.distributed.run, one independent replica per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from numerically_stable_online_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "softmax GB/s (read+write) and rows/s on 1 GB300; % of HBM peak"
+UNIT = "GB/s"
+L2_BYTES = 129 * 10 ** 6
+KERNEL_SOURCES = ["smx_device.cuh", "kernel_regs.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
+                  "launch_impl.cuh", "smx_api.cu"]
+
+
+# ---------------------------------------------------------------------------
+# Helpers that need no GPU (covered by the CPU tests).
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the job is as slow as its slowest rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_step: int, rows_per_step: int, steps: int, world: int, seconds: float):
+    """Whole-job throughput: every rank processes its own replica of the batch."""
+    total_bytes = bytes_per_step * steps * world
+    return {"gbs": total_bytes / seconds / 1e9, "rows_per_s": rows_per_step * steps * world / seconds}
+
+
+def rotation_sets(bytes_per_set: int, l2_bytes: int = L2_BYTES) -> int:
+    """Buffer sets to rotate over so a set is evicted from L2 before its reuse."""
+    return max(2, min(16, -(-3 * l2_bytes // max(1, bytes_per_set)) + 1))
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "numerically_stable_online_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"softmax_{workload}.md")
+    if not os.path.exists(path):
+        return None, None
+    text = open(path).read()
+    mh = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    mk = re.search(r"kernel:\s*(\S+)", text)
+    if not mh or not mt or mh.group(1) != source_hash():
+        return None, mk.group(1) if mk else None
+    return int(mt.group(1)), mk.group(1) if mk else None
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+        time.sleep(0.4)
+
+    def stop(self, t_begin: float, t_end: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        lines = [ln for ln in out.splitlines() if ln.strip()]
+        # samples arrive every ~100 ms from t0; attribute times by order
+        n = len(lines)
+        t_last = time.time()
+        samples = []
+        for i, ln in enumerate(lines):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            ts = self.t0 + (t_last - self.t0) * (i + 0.5) / max(n, 1)
+            samples.append((ts, parts))
+        inside = [p for ts, p in samples if t_begin - 0.15 <= ts <= t_end + 0.15] or \
+            [p for _, p in samples]
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for name, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# CPU reference leg.
+# ---------------------------------------------------------------------------
+
+def oracle_throughput(x_host, vl, w, budget_s: float, min_rows: int = 1):
+    """Time the fp64 reference on a bounded sample of the workload's rows."""
+    import oracle
+
+    rows, cols = w.rows, w.cols
+    t0 = time.perf_counter()
+    oracle.softmax_rows(x_host, w.in_dtype, rows, cols, vl, rows_sel=np.arange(min(rows, 16)))
+    per_row = (time.perf_counter() - t0) / min(rows, 16)
+    n = int(max(min_rows, min(rows, budget_s / max(per_row, 1e-9))))
+    sel = np.arange(n)
+    t0 = time.perf_counter()
+    oracle.softmax_rows(x_host, w.in_dtype, rows, cols, vl, rows_sel=sel)
+    dt = time.perf_counter() - t0
+    in_size = 4 if w.in_dtype == "f32" else 2
+    out_size = 4 if w.out_dtype == "f32" else 2
+    b = wl.algorithmic_bytes(n, cols, in_size, out_size, None if vl is None else vl[:n])
+    return b / dt / 1e9, n, dt, n / dt
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    x_host, vl = wl.host_input(w.name)
+    in_size = 4 if w.in_dtype == "f32" else 2
+    out_size = 4 if w.out_dtype == "f32" else 2
+    import oracle
+
+    oracle.build()
+    # size each step's sample so warm-up + timed steps take about a minute
+    t0 = time.perf_counter()
+    oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=np.arange(4))
+    per_row = (time.perf_counter() - t0) / 4
+    per_step_rows = int(max(1, min(w.rows, args.ref_budget / max(1, args.steps + args.warmup)
+                                   / per_row)))
+    sel_all = np.arange(w.rows)
+    for s in range(args.warmup):
+        sel = sel_all[(s * per_step_rows) % w.rows:][:per_step_rows]
+        oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+    tot_bytes, tot_rows = 0, 0
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        start = (s * per_step_rows) % w.rows
+        sel = sel_all[start:start + per_step_rows]
+        oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+        tot_bytes += wl.algorithmic_bytes(sel.size, w.cols, in_size, out_size,
+                                          None if vl is None else vl[sel])
+        tot_rows += sel.size
+    dt = time.perf_counter() - t0
+    value = tot_bytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, None),
+        "rows_per_s": tot_rows / dt,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step_rows} rows of {w.rows} per step (fp64 C reference, "
+                                   f"one thread)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, nsets):
+    c = {"workload": w.name, "rows": w.rows, "cols": w.cols, "in_dtype": w.in_dtype,
+         "out_dtype": w.out_dtype, "mask": "valid_len" if w.masked else None,
+         "description": w.description}
+    if nsets is not None:
+        c["l2"] = f"rotating {nsets} input/output buffer sets, larger than L2 together"
+    return c
+
+
+# ---------------------------------------------------------------------------
+# GPU leg.
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+
+    import numerically_stable_online_gb300 as smx
+    from numerically_stable_online_gb300 import build as smx_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        smx_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    smx.library()
+
+    x_host, vl_host = wl.host_input(w.name)
+    in_size = 4 if w.in_dtype == "f32" else 2
+    out_size = 4 if w.out_dtype == "f32" else 2
+    bytes_step = wl.algorithmic_bytes(w.rows, w.cols, in_size, out_size, vl_host)
+    set_bytes = w.rows * w.cols * (in_size + out_size)
+    nsets = rotation_sets(set_bytes)
+    x_cpu = wl.storage_to_torch(x_host, w.in_dtype).reshape(w.rows, w.cols)
+    xs = [x_cpu.to(dev) for _ in range(nsets)]
+    ys = [torch.empty((w.rows, w.cols), dtype=wl.torch_dtype(w.out_dtype), device=dev)
+          for _ in range(nsets)]
+    vl = None if vl_host is None else torch.from_numpy(vl_host).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    lib = smx.library()
+    P = lambda t: t.data_ptr()
+    in_code, out_code = smx.DTYPES[xs[0].dtype], smx.DTYPES[ys[0].dtype]
+    vl_ptr = None if vl is None else vl.data_ptr()
+    sptr = stream.cuda_stream
+
+    def step(i):
+        st = lib.smx_softmax_rows(P(xs[i % nsets]), P(ys[i % nsets]), w.rows, w.cols, vl_ptr,
+                                  in_code, out_code, sptr)
+        if st != 0:
+            raise smx.SmxError(st, "smx_softmax_rows")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert smx.last_device_status() == 0
+
+    sampler = ClockSampler(local)
+    if rank == 0 or world > 1:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(wall0, wall1)
+    status = smx.last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    agg = aggregate(bytes_step, w.rows, args.steps, world, elapsed_ms / 1e3)
+
+    # end to end through the public call: pinned host input in, output back
+    x_pin = x_cpu.pin_memory()
+    y_pin = torch.empty((w.rows, w.cols), dtype=ys[0].dtype).pin_memory()
+    vl_pin = None if vl_host is None else torch.from_numpy(vl_host).pin_memory()
+    e2e_steps = max(3, min(args.steps, 30))
+    xd, yd = xs[0], ys[0]
+    vld = None if vl_host is None else torch.empty_like(vl)
+    def e2e_step():
+        xd.copy_(x_pin, non_blocking=True)
+        if vld is not None:
+            vld.copy_(vl_pin, non_blocking=True)
+        smx.softmax_rows(xd, out=yd, valid_len=vld)
+        y_pin.copy_(yd, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = aggregate(bytes_step, w.rows, e2e_steps, world, e2e_ms / 1e3)
+    h2d = x_pin.numel() * x_pin.element_size() + (0 if vl_pin is None else vl_pin.numel() * 4)
+    d2h = y_pin.numel() * y_pin.element_size()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peak()
+    mean_launch_ms = statistics.fmean(launch_ms)
+    achieved = bytes_step / (mean_launch_ms / 1e3) / 1e9
+    traffic, kernel_name = profile_traffic(w.name)
+    cpu_gbs, cpu_rows, cpu_s, cpu_rps = oracle_throughput(x_host, vl_host, w, args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": agg["gbs"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, nsets),
+        "rows_per_s": agg["rows_per_s"],
+        "pct_of_hbm_peak": 100.0 * agg["gbs"] / world / peak,
+        "bytes_per_step": bytes_step,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "kernel": kernel_name, "algorithmic_bytes_per_launch": bytes_step,
+                     "mean_launch_us": mean_launch_ms * 1e3,
+                     "median_launch_us": statistics.median(launch_ms) * 1e3},
+        "cpu_baseline": {"value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {cpu_rows} of {w.rows} rows, fp64 C reference, one "
+                                   f"thread, {cpu_s:.1f} s"},
+        "e2e": {"value": e2e["gbs"], "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of CPU reference work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="seconds the reference arm spends over all its steps")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    w = wl.WORKLOADS[args.workload]
+    if w.name == "bf16_causal_8x32x4096x4096":
+        ap.error("the causal batch is a parity case, not a benchmark workload")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * smx.h - C ABI of the GB300 (sm_103a) row-wise numerically stable softmax.
+ *
+ * Operation (all calls): for each row r of a contiguous row-major [rows, cols]
+ * input x, with valid prefix length L_r (valid_len[r] clamped to [0, cols], or
+ * cols when valid_len is NULL),
+ *
+ *     m_r = max_{j < L_r} x[r, j]
+ *     d_r = sum_{j < L_r} exp(x[r, j] - m_r)
+ *     y[r, j] = exp(x[r, j] - m_r) / d_r   for j < L_r,   +0 for j >= L_r.
+ *
+ * This is the max-shifted softmax of "Softmax numerics architecture - max
+ * subtract, fp32 accumulate, fusion, online" (sections "The max-subtraction
+ * identity, and why it is exact" and "Online softmax: one recurrence, one fewer
+ * pass") and of "Kernel visualization: online softmax" ("Overview of safe
+ * softmax").  (m, d) is the block summary of "Stable softmax: keep the
+ * normalizer consistent as tiles arrive" and "Online stable softmax" ("Derive the
+ * update for two blocks"); d is in natural-log units.
+ *
+ * Declared policy for the cases those pages say need one ("Stable softmax...",
+ * second paragraph; "Online stable softmax", "Masks, empty rows, and
+ * precision"):
+ *   - masked lanes (j >= L_r) are excluded from the max and the sum and output +0;
+ *   - a row with L_r == 0, or whose valid lanes are all -inf, outputs +0 in every
+ *     lane; its statistics are (-inf, 0), the identity of the merge;
+ *   - a -inf valid lane outputs +0 and the rest of the row is normal;
+ *   - a NaN in the valid prefix makes every valid lane NaN; statistics (NaN, NaN);
+ *   - a +inf in the valid prefix (and no NaN) makes every valid lane NaN, as the
+ *     stable formula evaluates inf - inf; statistics (+inf, NaN).
+ *
+ * Precision: inputs are fp32, fp16 or bf16; the running maximum and the sum are
+ * held in fp32 whatever the input and output types ("Why the accumulator is
+ * fp32 even when the inputs are not"); the output type is chosen separately.
+ *
+ * Memory and ownership: every data pointer is a device pointer owned by the
+ * caller; the library never frees or retains it.  The library allocates no
+ * memory per call; it allocates one device status word per device on first use.
+ * Every call is asynchronous on `stream` (NULL is the legacy default stream) and
+ * returns after enqueueing its kernels.
+ *
+ * Errors: arguments are checked on the host before any launch; a bad argument
+ * returns an error code and nothing is enqueued.  A failed launch returns
+ * SMX_ERR_LAUNCH.  Errors found on the device (a bounded wait that ran out)
+ * are recorded in the device status word, read with smx_last_device_status().
+ */
+#ifndef SMX_H
+#define SMX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *smx_stream_t;
+
+typedef enum {
+    SMX_F32 = 0,  /* IEEE binary32 */
+    SMX_F16 = 1,  /* IEEE binary16 */
+    SMX_BF16 = 2  /* bfloat16: 8 exponent bits, 7 stored significand bits */
+} smx_dtype;
+
+typedef enum {
+    SMX_OK = 0,
+    SMX_ERR_INVALID_ARG = 1, /* NULL pointer with rows*cols > 0, negative size, bad dtype */
+    SMX_ERR_UNSUPPORTED = 2, /* no CUDA device, or the device is not sm_103 */
+    SMX_ERR_ALIAS = 3,       /* input and output byte ranges overlap */
+    SMX_ERR_LAUNCH = 4,      /* a kernel launch failed (the CUDA error is in smx_last_cuda_error) */
+    SMX_ERR_TIMEOUT = 5,     /* device: a bounded wait for staged data ran out */
+    SMX_ERR_DEVICE = 6       /* a CUDA runtime call failed */
+} smx_status;
+
+/*
+ * Softmax of each row.
+ *   x          device, [rows, cols] row-major, in_dtype; read only.
+ *   y          device, [rows, cols] row-major, out_dtype; fully written, masked
+ *              lanes included.  Must not overlap x (SMX_ERR_ALIAS).
+ *   rows, cols >= 0; rows == 0 or cols == 0 enqueues nothing and returns SMX_OK.
+ *   valid_len  device int32[rows] or NULL; each entry is clamped to [0, cols].
+ *   in_dtype, out_dtype: any of the three types, independently.
+ * Any alignment and any cols are accepted; 16-byte aligned x and y with
+ * cols * sizeof(type) a multiple of 16 take the vectorised kernels.
+ */
+smx_status smx_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
+                            const int32_t *valid_len, smx_dtype in_dtype,
+                            smx_dtype out_dtype, smx_stream_t stream);
+
+/*
+ * Block summary (m, d) of each row, fp32.
+ *   x, rows, cols, valid_len, in_dtype: as for smx_softmax_rows.
+ *   m_out, d_out: device float[rows], written.  d is sum exp(x - m) (natural
+ *   units).  Policy values as in the header comment: (-inf, 0) for empty or
+ *   all -inf rows, (NaN, NaN) with a NaN, (+inf, NaN) with a +inf.
+ */
+smx_status smx_softmax_row_stats(const void *x, float *m_out, float *d_out, int64_t rows,
+                                 int64_t cols, const int32_t *valid_len, smx_dtype in_dtype,
+                                 smx_stream_t stream);
+
+/*
+ * Element-wise merge of two arrays of block summaries ("Online stable softmax",
+ * "Derive the update for two blocks"):
+ *   m' = max(m_a, m_b),  d' = d_a exp(m_a - m') + d_b exp(m_b - m').
+ * An operand with m == -inf is the empty block and yields the other operand
+ * unchanged; a NaN m gives (NaN, NaN); m' == +inf gives (+inf, NaN).
+ *   all pointers: device float[n]; m_out/d_out may alias m_a/d_a or m_b/d_b
+ *   exactly (in place), but must not partially overlap them.
+ */
+smx_status smx_softmax_merge_stats(const float *m_a, const float *d_a, const float *m_b,
+                                   const float *d_b, float *m_out, float *d_out, int64_t n,
+                                   smx_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the status word of the
+ * current device: SMX_OK, or the first device-side error (SMX_ERR_TIMEOUT)
+ * recorded by a kernel since the last read.
+ */
+smx_status smx_last_device_status(smx_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *smx_status_string(smx_status status);
+
+/* The cudaError_t value (as int) of the last failed CUDA call on this thread, 0 if none. */
+int smx_last_cuda_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int smx_version(void);
+
+/*
+ * Testing hooks.  Process-wide, not thread-safe; they exist so that tests can
+ * reach every kernel on the shapes they choose.
+ *
+ * smx_debug_force_path(p): 0 = automatic choice; 1 = register-resident rows;
+ *   2 = thread-block-cluster rows; 3 = generic (scalar, two-pass) rows;
+ *   4 = persistent TMA-pipelined rows.  A forced path that cannot run the shape
+ *   falls back to the automatic choice.
+ * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
+ *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
+ * smx_debug_set_wait_limit(n): polls of a staging barrier before the kernel
+ *   gives up and records SMX_ERR_TIMEOUT (0 = default).  A test sets it to 1
+ *   to exercise the error path.
+ * smx_debug_last_path(): the path (1..4) the last softmax/stats call on this
+ *   thread used, 0 if none.
+ * smx_debug_set_regs_shape(threads, vpt): on path 1, use CTAs of `threads`
+ *   threads per row (32 = one warp per row) holding `vpt` 16-byte vectors each,
+ *   when that shape covers the row (0, 0 = automatic).
+ */
+void smx_debug_force_path(int path);
+void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes);
+void smx_debug_set_wait_limit(int64_t polls);
+int smx_debug_last_path(void);
+void smx_debug_set_regs_shape(int threads, int vpt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMX_H */

@@ -1,0 +1,175 @@
+"""Row-wise numerically stable softmax for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/smx.h``: each function marshals
+torch tensors (device memory and the current CUDA stream) into pointers and
+sizes and calls the same-named entry point of ``_build/libsmx.so``.  Every step
+of the computation runs in the library's CUDA kernels; there is no fallback.
+If the library has not been built (``python -m numerically_stable_online_gb300.build``)
+or no sm_103 device is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "SmxError", "library", "softmax_rows", "softmax_row_stats", "softmax_merge_stats",
+    "last_device_status", "status_string", "DTYPES",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsmx.so")
+
+SMX_F32, SMX_F16, SMX_BF16 = 0, 1, 2
+DTYPES = {torch.float32: SMX_F32, torch.float16: SMX_F16, torch.bfloat16: SMX_BF16}
+STATUS = {0: "SMX_OK", 1: "SMX_ERR_INVALID_ARG", 2: "SMX_ERR_UNSUPPORTED", 3: "SMX_ERR_ALIAS",
+          4: "SMX_ERR_LAUNCH", 5: "SMX_ERR_TIMEOUT", 6: "SMX_ERR_DEVICE"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SmxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _lib
+        text = lib.smx_status_string(status).decode() if lib is not None else STATUS.get(status, "?")
+        cuda = lib.smx_last_cuda_error() if lib is not None else 0
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({text}); cuda error {cuda}")
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run python -m numerically_stable_online_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        st = ctypes.c_int
+        lib.smx_softmax_rows.argtypes = [P, P, I64, I64, P, I32, I32, P]
+        lib.smx_softmax_rows.restype = st
+        lib.smx_softmax_row_stats.argtypes = [P, P, P, I64, I64, P, I32, P]
+        lib.smx_softmax_row_stats.restype = st
+        lib.smx_softmax_merge_stats.argtypes = [P, P, P, P, P, P, I64, P]
+        lib.smx_softmax_merge_stats.restype = st
+        lib.smx_last_device_status.argtypes = [P]
+        lib.smx_last_device_status.restype = st
+        lib.smx_status_string.argtypes = [st]
+        lib.smx_status_string.restype = ctypes.c_char_p
+        lib.smx_last_cuda_error.argtypes = []
+        lib.smx_last_cuda_error.restype = I32
+        lib.smx_version.argtypes = []
+        lib.smx_version.restype = I32
+        lib.smx_debug_force_path.argtypes = [I32]
+        lib.smx_debug_force_path.restype = None
+        lib.smx_debug_set_cluster.argtypes = [I32, I64]
+        lib.smx_debug_set_cluster.restype = None
+        lib.smx_debug_set_wait_limit.argtypes = [I64]
+        lib.smx_debug_set_wait_limit.restype = None
+        lib.smx_debug_last_path.argtypes = []
+        lib.smx_debug_last_path.restype = I32
+        lib.smx_debug_set_regs_shape.argtypes = [I32, I32]
+        lib.smx_debug_set_regs_shape.restype = None
+        _lib = lib
+        return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype(t: torch.dtype) -> int:
+    try:
+        return DTYPES[t]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t}: use float32, float16 or bfloat16") from None
+
+
+def _check_2d(x: torch.Tensor, name: str):
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D [rows, cols] tensor")
+
+
+def _lengths(valid_len, rows, device):
+    if valid_len is None:
+        return None
+    if not (valid_len.is_cuda and valid_len.dtype == torch.int32 and valid_len.is_contiguous()
+            and valid_len.numel() == rows and valid_len.device == device):
+        raise ValueError("valid_len must be a contiguous int32 CUDA tensor with one entry per row")
+    return valid_len.data_ptr()
+
+
+def softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None, valid_len: torch.Tensor | None = None,
+                 out_dtype: torch.dtype | None = None, stream=None) -> torch.Tensor:
+    """y[r, j] = exp(x[r, j] - m_r) / d_r over the valid prefix of each row; +0 elsewhere."""
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype or x.dtype, device=x.device)
+    _check_2d(out, "out")
+    if out.shape != x.shape or out.device != x.device:
+        raise ValueError("out must match x's shape and device")
+    st = library().smx_softmax_rows(x.data_ptr(), out.data_ptr(), rows, cols,
+                                    _lengths(valid_len, rows, x.device), _dtype(x.dtype),
+                                    _dtype(out.dtype), _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_rows")
+    return out
+
+
+def softmax_row_stats(x: torch.Tensor, valid_len: torch.Tensor | None = None, m_out=None, d_out=None,
+                      stream=None):
+    """Per-row block summary (m, d) in fp32: m = max, d = sum exp(x - m)."""
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if m_out is None:
+        m_out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if d_out is None:
+        d_out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    for t in (m_out, d_out):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == rows):
+            raise ValueError("m_out/d_out must be contiguous float32 CUDA tensors of length rows")
+    st = library().smx_softmax_row_stats(x.data_ptr(), m_out.data_ptr(), d_out.data_ptr(), rows, cols,
+                                         _lengths(valid_len, rows, x.device), _dtype(x.dtype),
+                                         _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_row_stats")
+    return m_out, d_out
+
+
+def softmax_merge_stats(m_a, d_a, m_b, d_b, m_out=None, d_out=None, stream=None):
+    """Element-wise merge of two arrays of (m, d) summaries (may run in place)."""
+    n = m_a.numel()
+    for t in (m_a, d_a, m_b, d_b):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == n):
+            raise ValueError("summaries must be contiguous float32 CUDA tensors of one length")
+    if m_out is None:
+        m_out = torch.empty_like(m_a)
+    if d_out is None:
+        d_out = torch.empty_like(d_a)
+    st = library().smx_softmax_merge_stats(m_a.data_ptr(), d_a.data_ptr(), m_b.data_ptr(),
+                                           d_b.data_ptr(), m_out.data_ptr(), d_out.data_ptr(), n,
+                                           _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_merge_stats")
+    return m_out, d_out
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word (0 = ok)."""
+    return library().smx_last_device_status(_stream(stream))
+
+
+def status_string(status: int) -> str:
+    return library().smx_status_string(status).decode()

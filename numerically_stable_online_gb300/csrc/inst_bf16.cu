@@ -1,0 +1,12 @@
+// Kernel instantiations for bf16 inputs (one translation unit per input type).
+#include "launch_impl.cuh"
+
+namespace smx {
+cudaError_t launch_in_bf16(const Call& c, const Plan& p) { return launch_in<__nv_bfloat16>(c, p); }
+int cluster_capacity_bf16(int cluster, int64_t smem_bytes) {
+  return cluster_capacity<__nv_bfloat16>(cluster, smem_bytes);
+}
+int pipe_occupancy_bf16(int vpt, int threads, int64_t smem_bytes) {
+  return pipe_occupancy<__nv_bfloat16>(vpt, threads, smem_bytes);
+}
+}  // namespace smx

@@ -1,0 +1,12 @@
+// Kernel instantiations for f16 inputs (one translation unit per input type).
+#include "launch_impl.cuh"
+
+namespace smx {
+cudaError_t launch_in_f16(const Call& c, const Plan& p) { return launch_in<__half>(c, p); }
+int cluster_capacity_f16(int cluster, int64_t smem_bytes) {
+  return cluster_capacity<__half>(cluster, smem_bytes);
+}
+int pipe_occupancy_f16(int vpt, int threads, int64_t smem_bytes) {
+  return pipe_occupancy<__half>(vpt, threads, smem_bytes);
+}
+}  // namespace smx

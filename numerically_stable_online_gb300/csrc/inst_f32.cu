@@ -1,0 +1,12 @@
+// Kernel instantiations for f32 inputs (one translation unit per input type).
+#include "launch_impl.cuh"
+
+namespace smx {
+cudaError_t launch_in_f32(const Call& c, const Plan& p) { return launch_in<float>(c, p); }
+int cluster_capacity_f32(int cluster, int64_t smem_bytes) {
+  return cluster_capacity<float>(cluster, smem_bytes);
+}
+int pipe_occupancy_f32(int vpt, int threads, int64_t smem_bytes) {
+  return pipe_occupancy<float>(vpt, threads, smem_bytes);
+}
+}  // namespace smx

@@ -1,0 +1,236 @@
+// Kernel selection and launch for one input type.  Included once per input
+// type by inst_f32.cu, inst_f16.cu and inst_bf16.cu (so the instantiations
+// compile in parallel) with SMX_IN_T and SMX_SUFFIX defined.
+#pragma once
+
+#include "kernel_cluster.cuh"
+#include "kernel_generic.cuh"
+#include "kernel_pipe.cuh"
+#include "kernel_regs.cuh"
+#include "smx_launch.h"
+
+namespace smx {
+namespace {
+
+constexpr int64_t MAX_GRID_X_ROWS = int64_t(1) << 30;
+constexpr int64_t MAX_GRID_Y = 65535;
+
+template <typename InT, typename OutT, int MODE, int VPT, bool WR>
+cudaError_t launch_regs_vpt(const Call& c, const Plan& p) {
+  constexpr int V = Elem<InT>::V;
+  if constexpr (VPT * V > 32) {
+    return cudaErrorInvalidValue;
+  } else {
+    const int rows_per_cta = WR ? p.threads / 32 : 1;
+    for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
+      const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
+      const unsigned grid = (unsigned)((n + rows_per_cta - 1) / rows_per_cta);
+      k_rows_regs<InT, OutT, VPT, WR, MODE><<<grid, p.threads, 0, c.stream>>>(
+          static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, r0 + n, c.cols,
+          c.valid_len, r0);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+}
+
+template <typename InT, typename OutT, int MODE, bool WR>
+cudaError_t launch_regs_wr(const Call& c, const Plan& p) {
+  switch (p.vpt) {
+    case 1: return launch_regs_vpt<InT, OutT, MODE, 1, WR>(c, p);
+    case 2: return launch_regs_vpt<InT, OutT, MODE, 2, WR>(c, p);
+    case 4: return launch_regs_vpt<InT, OutT, MODE, 4, WR>(c, p);
+    case 8: return launch_regs_vpt<InT, OutT, MODE, 8, WR>(c, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename InT, typename OutT, int MODE>
+cudaError_t prepare_cluster_kernel(int64_t smem_bytes) {
+  auto kern = k_rows_cluster<InT, OutT, CLUSTER_RV, MODE>;
+  // per device: the largest dynamic shared memory size set so far
+  static int64_t set_bytes[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (set_bytes[dev] < smem_bytes) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    set_bytes[dev] = smem_bytes;
+  }
+  return cudaSuccess;
+}
+
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_cluster(const Call& c, const Plan& p) {
+  const int64_t smem_bytes = p.smem_elems * (int64_t)sizeof(InT) > 16
+                                 ? p.smem_elems * (int64_t)sizeof(InT)
+                                 : 16;
+  cudaError_t e = prepare_cluster_kernel<InT, OutT, MODE>(smem_bytes);
+  if (e != cudaSuccess) return e;
+  for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_Y) {
+    const int64_t n = c.rows - r0 < MAX_GRID_Y ? c.rows - r0 : MAX_GRID_Y;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.cluster, (unsigned)n, 1);
+    cfg.blockDim = dim3(CLUSTER_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_rows_cluster<InT, OutT, CLUSTER_RV, MODE>,
+                           static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out,
+                           c.d_out, r0 + n, c.cols, c.valid_len, r0, p.chunk, p.smem_elems,
+                           c.max_polls, c.status);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename InT, typename OutT, int MODE, int VPT>
+cudaError_t prepare_pipe_kernel(int64_t smem_bytes) {
+  static int64_t set_bytes[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (set_bytes[dev] < smem_bytes) {
+    e = cudaFuncSetAttribute(k_rows_pipe<InT, OutT, VPT, MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    if (e != cudaSuccess) return e;
+    set_bytes[dev] = smem_bytes;
+  }
+  return cudaSuccess;
+}
+
+inline int64_t pipe_smem_bytes(const Plan& p) {
+  return (int64_t)p.stages * p.slot_bytes + 16LL * p.stages +
+         4LL * 2 * p.groups * p.warps_per_group;
+}
+
+template <typename InT, typename OutT, int MODE, int VPT>
+cudaError_t launch_pipe_vpt(const Call& c, const Plan& p) {
+  constexpr int V = Elem<InT>::V;
+  if constexpr (VPT * V > 32) {
+    return cudaErrorInvalidValue;
+  } else {
+    const int64_t smem = pipe_smem_bytes(p);
+    cudaError_t e = prepare_pipe_kernel<InT, OutT, MODE, VPT>(smem);
+    if (e != cudaSuccess) return e;
+    const int threads = (1 + p.groups * p.warps_per_group) * 32;
+    PipeShape sh{p.stages, p.groups, p.warps_per_group, p.slot_bytes};
+    k_rows_pipe<InT, OutT, VPT, MODE><<<(unsigned)p.ctas, threads, (size_t)smem, c.stream>>>(
+        static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, c.rows, c.cols,
+        c.valid_len, sh, c.max_polls, c.status);
+    return cudaGetLastError();
+  }
+}
+
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_pipe(const Call& c, const Plan& p) {
+  switch (p.vpt) {
+    case 1: return launch_pipe_vpt<InT, OutT, MODE, 1>(c, p);
+    case 2: return launch_pipe_vpt<InT, OutT, MODE, 2>(c, p);
+    case 4: return launch_pipe_vpt<InT, OutT, MODE, 4>(c, p);
+    case 8: return launch_pipe_vpt<InT, OutT, MODE, 8>(c, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_generic(const Call& c) {
+  for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
+    const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
+    k_rows_generic<InT, OutT, MODE><<<(unsigned)n, GENERIC_THREADS, 0, c.stream>>>(
+        static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, r0 + n, c.cols,
+        c.valid_len, r0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_typed(const Call& c, const Plan& p) {
+  switch (p.path) {
+    case PATH_REGS:
+      return p.warp_rows ? launch_regs_wr<InT, OutT, MODE, true>(c, p)
+                         : launch_regs_wr<InT, OutT, MODE, false>(c, p);
+    case PATH_CLUSTER: return launch_cluster<InT, OutT, MODE>(c, p);
+    case PATH_GENERIC: return launch_generic<InT, OutT, MODE>(c);
+    case PATH_PIPE: return launch_pipe<InT, OutT, MODE>(c, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename InT>
+cudaError_t launch_in(const Call& c, const Plan& p) {
+  if (c.mode == MODE_STATS) return launch_typed<InT, float, MODE_STATS>(c, p);
+  switch (c.out_dtype) {
+    case 0: return launch_typed<InT, float, MODE_SOFTMAX>(c, p);
+    case 1: return launch_typed<InT, __half, MODE_SOFTMAX>(c, p);
+    case 2: return launch_typed<InT, __nv_bfloat16, MODE_SOFTMAX>(c, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename InT>
+int cluster_capacity(int cluster, int64_t smem_bytes) {
+  // the softmax kernel with fp32 output stands for the family (same resources)
+  if (prepare_cluster_kernel<InT, float, MODE_SOFTMAX>(smem_bytes) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3(CLUSTER_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_rows_cluster<InT, float, CLUSTER_RV, MODE_SOFTMAX>,
+                                     &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <typename InT>
+int pipe_occupancy(int vpt, int threads, int64_t smem_bytes) {
+  // the bf16-output softmax kernel stands for the family
+  auto query = [&](auto kern) -> int {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem_bytes) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  };
+  constexpr int V = Elem<InT>::V;
+  switch (vpt) {
+    case 1: return query(k_rows_pipe<InT, __nv_bfloat16, 1, MODE_SOFTMAX>);
+    case 2: return query(k_rows_pipe<InT, __nv_bfloat16, 2, MODE_SOFTMAX>);
+    case 4: return query(k_rows_pipe<InT, __nv_bfloat16, 4, MODE_SOFTMAX>);
+    case 8:
+      if constexpr (8 * V <= 32) return query(k_rows_pipe<InT, __nv_bfloat16, 8, MODE_SOFTMAX>);
+      return 0;
+    default: return 0;
+  }
+}
+
+}  // namespace
+}  // namespace smx

@@ -1,0 +1,399 @@
+// Host side of the C ABI declared in include/smx.h: argument checks, the
+// per-device property cache, the choice of kernel, and launches.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/smx.h"
+#include "kernel_generic.cuh"
+#include "smx_launch.h"
+
+namespace smx {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr int64_t DEFAULT_MAX_POLLS = int64_t(1) << 21;
+// shared memory kept back from the cluster kernel's staging area for its
+// static arrays (barriers, per-warp partials, the CTA summary)
+constexpr int64_t CLUSTER_STATIC_SMEM = 1024;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  int64_t smem_optin = 0;
+  int* status = nullptr;   // device status word
+  int max_cluster[3] = {0, 0, 0};  // per input type, 0 = not queried yet
+};
+
+DeviceInfo g_dev[MAX_DEVICES];
+std::mutex g_mutex;
+
+// testing hooks
+std::atomic<int> g_force_path{0};
+std::atomic<int> g_max_cluster{0};
+std::atomic<int64_t> g_smem_cap{0};
+std::atomic<int64_t> g_wait_limit{0};
+std::atomic<int> g_regs_threads{0};
+std::atomic<int> g_regs_vpt{0};
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_path = 0;
+
+int elem_size(int dtype) { return dtype == SMX_F32 ? 4 : 2; }
+bool valid_dtype(int d) { return d == SMX_F32 || d == SMX_F16 || d == SMX_BF16; }
+
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  if (a == nullptr || b == nullptr || na <= 0 || nb <= 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + (uintptr_t)nb && b0 < a0 + (uintptr_t)na;
+}
+
+smx_status cuda_fail(cudaError_t e, smx_status code) {
+  t_last_cuda_error = (int)e;
+  return code;
+}
+
+// Current device's cached properties; allocates its status word on first use.
+smx_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_UNSUPPORTED);
+  if (dev < 0 || dev >= MAX_DEVICES) return SMX_ERR_UNSUPPORTED;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d.ready) {
+      int major = 0, minor = 0, sms = 0, optin = 0;
+      if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+              cudaSuccess)
+        return cuda_fail(e, SMX_ERR_DEVICE);
+      d.supported = (major == 10 && minor == 3);
+      d.sm_count = sms;
+      d.smem_optin = optin;
+      if (d.supported) {
+        int* s = nullptr;
+        if ((e = cudaMalloc(&s, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+        if ((e = cudaMemset(s, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+        d.status = s;
+      }
+      d.ready = true;
+    }
+  }
+  if (!d.supported) return SMX_ERR_UNSUPPORTED;
+  *out = &d;
+  return SMX_OK;
+}
+
+int cluster_capacity(int in_dtype, int cluster, int64_t smem_bytes) {
+  switch (in_dtype) {
+    case SMX_F32: return cluster_capacity_f32(cluster, smem_bytes);
+    case SMX_F16: return cluster_capacity_f16(cluster, smem_bytes);
+    default: return cluster_capacity_bf16(cluster, smem_bytes);
+  }
+}
+
+int64_t cluster_smem_cap_bytes(const DeviceInfo& d) {
+  int64_t cap = d.smem_optin - CLUSTER_STATIC_SMEM;
+  const int64_t dbg = g_smem_cap.load();
+  if (dbg > 0 && dbg < cap) cap = dbg;
+  return cap / 16 * 16;
+}
+
+// Largest cluster size (power of two up to 16) that can be resident with the
+// full staging area; cached per device and input type.
+int max_cluster_size(DeviceInfo& d, int in_dtype) {
+  if (d.max_cluster[in_dtype] == 0) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const int64_t smem = d.smem_optin - CLUSTER_STATIC_SMEM;
+    int best = 1;
+    for (int c = 16; c >= 2; c >>= 1) {
+      if (cluster_capacity(in_dtype, c, smem / 16 * 16) > 0) {
+        best = c;
+        break;
+      }
+    }
+    d.max_cluster[in_dtype] = best;
+  }
+  int c = d.max_cluster[in_dtype];
+  const int dbg = g_max_cluster.load();
+  if (dbg > 0 && dbg < c) c = dbg;
+  return c;
+}
+
+bool plan_regs(int64_t cols, int in_dtype, Plan* p) {
+  const int V = 16 / elem_size(in_dtype);
+  const int64_t nvec = cols / V;
+  const int max_vpt = 32 / V;
+  int vpt = 0;
+  int64_t G = 0;
+  const int dbg_t = g_regs_threads.load(), dbg_v = g_regs_vpt.load();
+  if (dbg_t > 0 && dbg_v > 0 && dbg_v <= max_vpt && (dbg_t % 32) == 0 && dbg_t <= 1024 &&
+      (int64_t)dbg_t * dbg_v >= nvec) {
+    vpt = dbg_v;
+    G = dbg_t;
+  } else {
+    for (int v = 1; v <= max_vpt; v <<= 1) {
+      const int64_t g = ((nvec + v - 1) / v + 31) / 32 * 32;
+      if (g <= 256) {
+        vpt = v;
+        G = g;
+        break;
+      }
+    }
+    if (vpt == 0) {
+      vpt = max_vpt;
+      G = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
+      if (G > 1024) return false;
+    }
+  }
+  p->path = PATH_REGS;
+  p->vpt = vpt;
+  p->warp_rows = (G == 32);
+  p->threads = p->warp_rows ? 256 : (int)G;
+  return true;
+}
+
+int pipe_occupancy(int in_dtype, int vpt, int threads, int64_t smem) {
+  switch (in_dtype) {
+    case SMX_F32: return pipe_occupancy_f32(vpt, threads, smem);
+    case SMX_F16: return pipe_occupancy_f16(vpt, threads, smem);
+    default: return pipe_occupancy_bf16(vpt, threads, smem);
+  }
+}
+
+// Pipelined path for rows of at most 32 KiB: a consumer group of WG warps per
+// row, each thread holding vpt 16-byte vectors; about 16 consumer warps and
+// 96 KiB of row slots per CTA; as many CTAs as fit on every SM.
+constexpr int64_t PIPE_STAGE_BUDGET = 96 * 1024;
+
+bool plan_pipe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
+  const int es = elem_size(in_dtype), V = 16 / es;
+  const int64_t rb = cols * es;
+  if (rb > PIPE_MAX_ROW_BYTES) return false;
+  const int64_t nvec = cols / V;
+  int vpt = 32 / V;
+  while (vpt > 1 && 32LL * (vpt / 2) >= nvec) vpt /= 2;
+  const int64_t G = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
+  const int WG = (int)(G / 32);
+  if (WG > 16) return false;
+  const int NG = WG == 1 ? 16 : (16 / WG < 15 ? 16 / WG : 15);
+  const int slot = (int)((rb + 127) / 128 * 128);
+  int S = (int)(PIPE_STAGE_BUDGET / slot) / NG * NG;
+  if (S < NG) S = NG;
+  p->path = PATH_PIPE;
+  p->vpt = vpt;
+  p->warps_per_group = WG;
+  p->groups = NG;
+  p->stages = S;
+  p->slot_bytes = slot;
+  const int threads = (1 + NG * WG) * 32;
+  const int64_t smem = (int64_t)S * slot + 16LL * S + 8LL * NG * WG;
+  const int occ = pipe_occupancy(in_dtype, vpt, threads, smem);
+  if (occ <= 0) return false;
+  const int64_t ctas = (int64_t)occ * d.sm_count;
+  p->ctas = (int)(rows < ctas ? rows : ctas);
+  return true;
+}
+
+void plan_cluster(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
+  const int es = elem_size(in_dtype);
+  const int V = 16 / es;
+  const int64_t smem_elems_cap = cluster_smem_cap_bytes(d) / es;
+  const int64_t per_cta = smem_elems_cap + (int64_t)CLUSTER_THREADS * CLUSTER_RV * V;
+  const int maxc = max_cluster_size(d, in_dtype);
+  int c = 1;
+  while (c < maxc && (int64_t)c * per_cta < cols) c <<= 1;
+  int64_t chunk = (cols + c - 1) / c;
+  chunk = (chunk + V - 1) / V * V;
+  p->path = PATH_CLUSTER;
+  p->cluster = c;
+  p->chunk = chunk;
+  p->smem_elems = chunk < smem_elems_cap ? chunk : smem_elems_cap;
+}
+
+smx_status run(Call& c, DeviceInfo& dev) {
+  const int es_in = elem_size(c.in_dtype);
+  const bool vec_ok =
+      (reinterpret_cast<uintptr_t>(c.x) % 16 == 0) &&
+      (c.mode == MODE_STATS || reinterpret_cast<uintptr_t>(c.y) % 16 == 0) &&
+      ((c.cols * es_in) % 16 == 0) && c.cols > 0;
+  Plan p;
+  const int force = g_force_path.load();
+  bool planned = false;
+  if (vec_ok) {
+    if (force == PATH_CLUSTER) {
+      plan_cluster(dev, c.cols, c.in_dtype, &p);
+      planned = true;
+    } else if (force != PATH_GENERIC) {
+      if (force != PATH_REGS) planned = plan_pipe(dev, c.rows, c.cols, c.in_dtype, &p);
+      if (!planned) planned = plan_regs(c.cols, c.in_dtype, &p);
+      if (!planned) {
+        plan_cluster(dev, c.cols, c.in_dtype, &p);
+        planned = true;
+      }
+    }
+  }
+  if (!planned) p.path = PATH_GENERIC;
+  c.status = dev.status;
+  const int64_t wl = g_wait_limit.load();
+  c.max_polls = wl > 0 ? wl : DEFAULT_MAX_POLLS;
+  cudaError_t e;
+  switch (c.in_dtype) {
+    case SMX_F32: e = launch_in_f32(c, p); break;
+    case SMX_F16: e = launch_in_f16(c, p); break;
+    default: e = launch_in_bf16(c, p); break;
+  }
+  t_last_path = p.path;
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
+  return SMX_OK;
+}
+
+}  // namespace
+
+// Element-wise merge of two arrays of (m, d) summaries; may run in place.
+__global__ void __launch_bounds__(256)
+    k_merge_stats(const float* m_a, const float* d_a, const float* m_b, const float* d_b,
+                  float* m_o, float* d_o, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const MD r = md_merge(MD{m_a[i], d_a[i]}, MD{m_b[i], d_b[i]});
+    m_o[i] = r.m;
+    d_o[i] = r.d;
+  }
+}
+
+
+cudaError_t launch_merge(const float* m_a, const float* d_a, const float* m_b, const float* d_b,
+                         float* m_o, float* d_o, int64_t n, cudaStream_t stream) {
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  k_merge_stats<<<(unsigned)blocks, 256, 0, stream>>>(m_a, d_a, m_b, d_b, m_o, d_o, n);
+  return cudaGetLastError();
+}
+
+}  // namespace smx
+
+using namespace smx;
+
+extern "C" {
+
+smx_status smx_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
+                            const int32_t* valid_len, smx_dtype in_dtype, smx_dtype out_dtype,
+                            smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return SMX_OK;
+  if (x == nullptr || y == nullptr) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype), ny = rows * cols * elem_size(out_dtype);
+  if (overlaps(x, nx, y, ny)) return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, y, ny)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
+         MODE_SOFTMAX, reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  return run(c, *dev);
+}
+
+smx_status smx_softmax_row_stats(const void* x, float* m_out, float* d_out, int64_t rows,
+                                 int64_t cols, const int32_t* valid_len, smx_dtype in_dtype,
+                                 smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype)) return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0) return SMX_OK;
+  if (m_out == nullptr || d_out == nullptr || (cols > 0 && x == nullptr)) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype);
+  if (overlaps(x, nx, m_out, rows * 4) || overlaps(x, nx, d_out, rows * 4) ||
+      overlaps(m_out, rows * 4, d_out, rows * 4))
+    return SMX_ERR_ALIAS;
+  if (valid_len && (overlaps(valid_len, rows * 4, m_out, rows * 4) ||
+                    overlaps(valid_len, rows * 4, d_out, rows * 4)))
+    return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{x, nullptr, m_out, d_out, rows, cols, valid_len, (int)in_dtype, SMX_F32, MODE_STATS,
+         reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  return run(c, *dev);
+}
+
+smx_status smx_softmax_merge_stats(const float* m_a, const float* d_a, const float* m_b,
+                                   const float* d_b, float* m_out, float* d_out, int64_t n,
+                                   smx_stream_t stream) {
+  if (n < 0) return SMX_ERR_INVALID_ARG;
+  if (n == 0) return SMX_OK;
+  if (!m_a || !d_a || !m_b || !d_b || !m_out || !d_out) return SMX_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 4) return SMX_ERR_INVALID_ARG;
+  const int64_t nb = n * 4;
+  const void* ins[4] = {m_a, d_a, m_b, d_b};
+  const void* outs[2] = {m_out, d_out};
+  if (overlaps(m_out, nb, d_out, nb)) return SMX_ERR_ALIAS;
+  for (const void* o : outs)
+    for (const void* i : ins)
+      if (o != i && overlaps(o, nb, i, nb)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  const cudaError_t e =
+      launch_merge(m_a, d_a, m_b, d_b, m_out, d_out, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
+  return SMX_OK;
+}
+
+smx_status smx_last_device_status(smx_stream_t stream) {
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+  int v = 0;
+  if ((e = cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, SMX_ERR_DEVICE);
+  if (v != 0 && (e = cudaMemset(dev->status, 0, sizeof(int))) != cudaSuccess)
+    return cuda_fail(e, SMX_ERR_DEVICE);
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+  return v == 0 ? SMX_OK : (smx_status)(v & DEV_TIMEOUT ? SMX_ERR_TIMEOUT : SMX_ERR_DEVICE);
+}
+
+const char* smx_status_string(smx_status status) {
+  switch (status) {
+    case SMX_OK: return "ok";
+    case SMX_ERR_INVALID_ARG: return "invalid argument";
+    case SMX_ERR_UNSUPPORTED: return "no sm_103 CUDA device";
+    case SMX_ERR_ALIAS: return "input and output overlap";
+    case SMX_ERR_LAUNCH: return "kernel launch failed";
+    case SMX_ERR_TIMEOUT: return "device: bounded wait for staged data ran out";
+    case SMX_ERR_DEVICE: return "CUDA runtime call failed";
+    default: return "unknown status";
+  }
+}
+
+int smx_last_cuda_error(void) { return t_last_cuda_error; }
+
+int smx_version(void) { return 100; }
+
+void smx_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 4 ? path : 0); }
+
+void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
+  g_max_cluster.store(max_cluster > 0 ? max_cluster : 0);
+  g_smem_cap.store(smem_bytes > 0 ? smem_bytes : 0);
+}
+
+void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls > 0 ? polls : 0); }
+
+int smx_debug_last_path(void) { return t_last_path; }
+
+void smx_debug_set_regs_shape(int threads, int vpt) {
+  g_regs_threads.store(threads > 0 ? threads : 0);
+  g_regs_vpt.store(vpt > 0 ? vpt : 0);
+}
+
+}  // extern "C"

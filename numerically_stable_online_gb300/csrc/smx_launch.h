@@ -1,0 +1,64 @@
+// Internal interface between the host API (smx_api.cu) and the per-input-type
+// kernel instantiation units (inst_*.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace smx {
+
+enum Path : int { PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_PIPE = 4 };
+
+struct Call {
+  const void* x;
+  void* y;
+  float* m_out;
+  float* d_out;
+  int64_t rows, cols;
+  const int32_t* valid_len;
+  int in_dtype, out_dtype;  // smx_dtype values
+  int mode;                 // 0 softmax, 1 row statistics
+  cudaStream_t stream;
+  int* status;              // device status word
+  int64_t max_polls;        // bound of each staging wait
+};
+
+struct Plan {
+  int path = PATH_GENERIC;
+  // register-resident rows
+  int threads = 256;  // threads per CTA
+  int vpt = 1;        // 16-byte vectors per thread
+  bool warp_rows = false;
+  // pipelined rows (threads = (1 + groups * warps_per_group) * 32)
+  int stages = 0, groups = 0, warps_per_group = 0, slot_bytes = 0, ctas = 0;
+  // cluster rows
+  int cluster = 1;
+  int64_t chunk = 0;       // elements per CTA
+  int64_t smem_elems = 0;  // staged elements per CTA
+};
+
+constexpr int CLUSTER_RV = 2;  // register vectors per thread on the cluster path
+constexpr int CLUSTER_THREADS = 1024;
+
+// Launch the planned kernel(s) for one input type; returns the first CUDA error.
+cudaError_t launch_in_f32(const Call& c, const Plan& p);
+cudaError_t launch_in_f16(const Call& c, const Plan& p);
+cudaError_t launch_in_bf16(const Call& c, const Plan& p);
+
+// Clusters of `cluster` CTAs with `smem_bytes` of dynamic shared memory each that
+// can be resident at once (0 if that cluster size cannot launch).
+int cluster_capacity_f32(int cluster, int64_t smem_bytes);
+int cluster_capacity_f16(int cluster, int64_t smem_bytes);
+int cluster_capacity_bf16(int cluster, int64_t smem_bytes);
+
+// Resident CTAs per SM of the pipelined kernel for this input type and shape.
+int pipe_occupancy_f32(int vpt, int threads, int64_t smem_bytes);
+int pipe_occupancy_f16(int vpt, int threads, int64_t smem_bytes);
+int pipe_occupancy_bf16(int vpt, int threads, int64_t smem_bytes);
+
+constexpr int PIPE_MAX_ROW_BYTES = 32768;
+
+cudaError_t launch_merge(const float* m_a, const float* d_a, const float* m_b, const float* d_b,
+                         float* m_o, float* d_o, int64_t n, cudaStream_t stream);
+
+}  // namespace smx

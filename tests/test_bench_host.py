@@ -1,0 +1,81 @@
+"""Host-side logic of bench.py, on CPU: the whole-job aggregation, the
+max-over-ranks timing with two gloo ranks, the L2 rotation, and the reference
+arm's JSON line (fp64 CPU reference only, no GPU)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_aggregate_is_whole_job():
+    a = bench.aggregate(bytes_per_step=1000, rows_per_step=10, steps=4, world=2, seconds=2.0)
+    assert a["gbs"] == 1000 * 4 * 2 / 2.0 / 1e9
+    assert a["rows_per_s"] == 10 * 4 * 2 / 2.0
+
+
+def test_rotation_covers_l2():
+    for set_bytes in (512_000, 64 * 2**20, 268_435_456, 4 * 2**30):
+        n = bench.rotation_sets(set_bytes)
+        assert 2 <= n <= 16
+        assert (n - 1) * set_bytes >= bench.L2_BYTES or n == 16
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        out[rank] = bench.max_over_ranks(1.5 + rank, world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == 2.5
+
+
+def test_reference_arm_json_line():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "f32_64x1000", "--steps", "3", "--warmup", "3",
+                        "--ref-budget", "1"], capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "f32_64x1000", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_bench_rejects_too_few_warmups():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
