@@ -42,8 +42,12 @@ from numerically_stable_online_gb300 import workloads as wl  # noqa: E402
 METRIC = "softmax GB/s (read+write) and rows/s on 1 GB300; % of HBM peak"
 UNIT = "GB/s"
 L2_BYTES = 129 * 10 ** 6
-KERNEL_SOURCES = ["smx_device.cuh", "kernel_regs.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
-                  "launch_impl.cuh", "smx_api.cu"]
+LAUNCH_SAMPLE = 8
+PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_regs.cuh",
+                  "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh", "launch_impl.cuh",
+                  "smx_api.cu"]
 
 
 # ---------------------------------------------------------------------------
@@ -289,6 +293,7 @@ def run_ours(args, w):
     in_code, out_code = smx.DTYPES[xs[0].dtype], smx.DTYPES[ys[0].dtype]
     vl_ptr = None if vl is None else vl.data_ptr()
     sptr = stream.cuda_stream
+    lib.smx_debug_force_path(PATHS[args.path])
 
     def step(i):
         st = lib.smx_softmax_rows(P(xs[i % nsets]), P(ys[i % nsets]), w.rows, w.cols, vl_ptr,
@@ -300,12 +305,16 @@ def run_ours(args, w):
         step(i)
     torch.cuda.synchronize(dev)
     assert smx.last_device_status() == 0
+    used_path = lib.smx_debug_last_path()
 
     sampler = ClockSampler(local)
     if rank == 0 or world > 1:
         sampler.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # per-launch durations from event pairs around every LAUNCH_SAMPLE-th step
+    # (an event pair around every launch would add its own gaps to the steps)
+    sampled = set(range(0, args.steps, LAUNCH_SAMPLE))
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for i in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -314,9 +323,12 @@ def run_ours(args, w):
     wall0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(i)
-        ev[i][1].record(stream)
+        if i in sampled:
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        else:
+            step(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -327,7 +339,7 @@ def run_ours(args, w):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
     elapsed_ms = t_start.elapsed_time(t_end)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    launch_ms = [a.elapsed_time(b) for a, b in ev.values()]
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     agg = aggregate(bytes_step, w.rows, args.steps, world, elapsed_ms / 1e3)
 
@@ -375,7 +387,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": agg["gbs"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(w, nsets),
+        "config": dict(config_of(w, nsets), path=PATH_NAMES.get(used_path, used_path)),
         "rows_per_s": agg["rows_per_s"],
         "pct_of_hbm_peak": 100.0 * agg["gbs"] / world / peak,
         "bytes_per_step": bytes_step,
@@ -383,7 +395,7 @@ def run_ours(args, w):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "kernel": kernel_name, "algorithmic_bytes_per_launch": bytes_step,
-                     "mean_launch_us": mean_launch_ms * 1e3,
+                     "mean_launch_us": mean_launch_ms * 1e3, "launches_timed": len(launch_ms),
                      "median_launch_us": statistics.median(launch_ms) * 1e3},
         "cpu_baseline": {"value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"first {cpu_rows} of {w.rows} rows, fp64 C reference, one "
@@ -408,6 +420,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU reference work for cpu_baseline")
+    ap.add_argument("--path", choices=sorted(PATHS), default="auto",
+                    help="kernel family (diagnostics; the library chooses with auto)")
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds the reference arm spends over all its steps")
     args = ap.parse_args(argv)

@@ -132,8 +132,8 @@ int smx_version(void);
  *
  * smx_debug_force_path(p): 0 = automatic choice; 1 = register-resident rows;
  *   2 = thread-block-cluster rows; 3 = generic (scalar, two-pass) rows;
- *   4 = persistent TMA-pipelined rows.  A forced path that cannot run the shape
- *   falls back to the automatic choice.
+ *   4 = persistent rows with the next rows prefetched (cp.async).  A forced
+ *   path that cannot run the shape falls back to the automatic choice.
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
  * smx_debug_set_wait_limit(n): polls of a staging barrier before the kernel
@@ -141,15 +141,18 @@ int smx_version(void);
  *   to exercise the error path.
  * smx_debug_last_path(): the path (1..4) the last softmax/stats call on this
  *   thread used, 0 if none.
- * smx_debug_set_regs_shape(threads, vpt): on path 1, use CTAs of `threads`
- *   threads per row (32 = one warp per row) holding `vpt` 16-byte vectors each,
- *   when that shape covers the row (0, 0 = automatic).
+ * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of
+ *   `threads` threads per row (32 = one warp per row, path 1 only) holding `vpt`
+ *   16-byte vectors each, when that shape covers the row (0, 0 = automatic).
+ * smx_debug_set_stream_depth(n): rows prefetched per CTA on path 4 (2 or 3;
+ *   0 = automatic).
  */
 void smx_debug_force_path(int path);
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes);
 void smx_debug_set_wait_limit(int64_t polls);
 int smx_debug_last_path(void);
 void smx_debug_set_regs_shape(int threads, int vpt);
+void smx_debug_set_stream_depth(int depth);
 
 #ifdef __cplusplus
 }

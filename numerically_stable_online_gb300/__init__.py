@@ -77,6 +77,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_last_path.restype = I32
         lib.smx_debug_set_regs_shape.argtypes = [I32, I32]
         lib.smx_debug_set_regs_shape.restype = None
+        lib.smx_debug_set_stream_depth.argtypes = [I32]
+        lib.smx_debug_set_stream_depth.restype = None
         _lib = lib
         return lib
 

@@ -6,7 +6,7 @@ cudaError_t launch_in_bf16(const Call& c, const Plan& p) { return launch_in<__nv
 int cluster_capacity_bf16(int cluster, int64_t smem_bytes) {
   return cluster_capacity<__nv_bfloat16>(cluster, smem_bytes);
 }
-int pipe_occupancy_bf16(int vpt, int threads, int64_t smem_bytes) {
-  return pipe_occupancy<__nv_bfloat16>(vpt, threads, smem_bytes);
+int stream_occupancy_bf16(int vpt, int threads, int depth) {
+  return stream_occupancy<__nv_bfloat16>(vpt, threads, depth);
 }
 }  // namespace smx

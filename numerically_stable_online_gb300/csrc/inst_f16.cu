@@ -6,7 +6,7 @@ cudaError_t launch_in_f16(const Call& c, const Plan& p) { return launch_in<__hal
 int cluster_capacity_f16(int cluster, int64_t smem_bytes) {
   return cluster_capacity<__half>(cluster, smem_bytes);
 }
-int pipe_occupancy_f16(int vpt, int threads, int64_t smem_bytes) {
-  return pipe_occupancy<__half>(vpt, threads, smem_bytes);
+int stream_occupancy_f16(int vpt, int threads, int depth) {
+  return stream_occupancy<__half>(vpt, threads, depth);
 }
 }  // namespace smx

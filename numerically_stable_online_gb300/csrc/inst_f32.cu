@@ -6,7 +6,7 @@ cudaError_t launch_in_f32(const Call& c, const Plan& p) { return launch_in<float
 int cluster_capacity_f32(int cluster, int64_t smem_bytes) {
   return cluster_capacity<float>(cluster, smem_bytes);
 }
-int pipe_occupancy_f32(int vpt, int threads, int64_t smem_bytes) {
-  return pipe_occupancy<float>(vpt, threads, smem_bytes);
+int stream_occupancy_f32(int vpt, int threads, int depth) {
+  return stream_occupancy<float>(vpt, threads, depth);
 }
 }  // namespace smx

@@ -29,74 +29,13 @@
 // barrier, so no CTA of the cluster is left waiting.
 #pragma once
 
-#include "kernel_regs.cuh"
+#include "row_core.cuh"
+#include "smx_async.cuh"
 #include "smx_launch.h"
 
 namespace smx {
 
 constexpr int CLUSTER_PIECES = 8;
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_peer_f32(const float* local, uint32_t rank) {
-  uint32_t raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: at most max_polls polls, backing off with nanosleep.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int64_t max_polls) {
-  for (int64_t i = 0; i < max_polls; ++i) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (i >= 16) __nanosleep(64);
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // Fold one vector of V elements into a thread's running (m, d): the tiled
 // online update with the tile = this vector.  Masked lanes hold -inf.
@@ -128,6 +67,21 @@ __device__ __forceinline__ void mask_tail(float (&f)[V], int64_t e0, int64_t L) 
 #pragma unroll
   for (int i = 0; i < V; ++i)
     if (e0 + i >= L) f[i] = neg_inf();
+}
+
+// One element's output on the normalise pass: e^(x - M) / D.  fp32 outputs use
+// the compensated exponential; 16-bit outputs one FFMA with the per-row
+// constant c2 = RN(-M log2 e + s) and rD2 = 2^(-s + c2_err) / D, where c2_err is
+// the exact rounding residual of c2 (s = 8 for bf16 keeps its subnormals, as in
+// row_core.cuh).  Here D comes from other CTAs' sums, so the rounding of c2
+// does not cancel and must be carried explicitly.
+template <typename OutT>
+__device__ __forceinline__ float cluster_out(float x, float M, float c2, float rD, float rD2) {
+  if constexpr (ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE) {
+    return __fmul_rn(exp_shift_accurate(x, M), rD);
+  } else {
+    return __fmul_rn(ex2_ftz(__fmaf_rn(x, L2E_HI, c2)), rD2);
+  }
 }
 
 template <typename InT, typename OutT, int RV, int MODE>
@@ -162,12 +116,12 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
   const int64_t c_nv = c1 > c0 ? (c1 - c0) / V : 0;
   int64_t vend = ((L + V - 1) / V) * V;  // valid data rounded up to a vector
   if (vend > c1) vend = c1;
-  const int64_t v_nv = vend > c0 ? (vend - c0) / V : 0;           // valid vectors
+  const int64_t v_nv = vend > c0 ? (vend - c0) / V : 0;               // valid vectors
   const int64_t a_nv = smem_elems / V < c_nv ? smem_elems / V : c_nv;  // staged region
-  const int64_t s_nv = a_nv < v_nv ? a_nv : v_nv;                 // staged and valid
+  const int64_t s_nv = a_nv < v_nv ? a_nv : v_nv;                     // staged and valid
   const int64_t b_nv = a_nv + (int64_t)T * RV < c_nv ? a_nv + (int64_t)T * RV : c_nv;
 
-  // Piece layout of the staged region.
+  // Issue the staged region's copies, one mbarrier per piece.
   const int64_t piece_nv = (s_nv + CLUSTER_PIECES - 1) / CLUSTER_PIECES;
   if (t == 0) {
     for (int p = 0; p < CLUSTER_PIECES; ++p) mbar_init(smem_addr(&bars[p]), 1);
@@ -186,7 +140,7 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     }
   }
 
-  // Register part: vector A + k*T + t of the chunk.
+  // Register part: vector a_nv + k*T + t of the chunk.
   float r[RV][V];
 #pragma unroll
   for (int k = 0; k < RV; ++k) {
@@ -200,8 +154,8 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     }
   }
 
-  // Pass 1: this thread's running (m, d).
-  float m = neg_inf(), d = 0.0f;
+  // Pass 1a: exact maximum of the on-chip part (pieces processed as they land).
+  float mx = neg_inf();
   bool timed_out = false;
   for (int p = 0; p < CLUSTER_PIECES; ++p) {
     const int64_t p0 = (int64_t)p * piece_nv;
@@ -213,20 +167,69 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
       float f[V];
       unpack16<InT>(*reinterpret_cast<const uint4*>(sx + vi * V), f);
       mask_tail<V>(f, c0 + vi * V, L);
-      online_fold<V>(m, d, f);
+#pragma unroll
+      for (int i = 0; i < V; ++i) mx = fmax_nan(mx, f[i]);
     }
   }
 #pragma unroll
-  for (int k = 0; k < RV; ++k) online_fold<V>(m, d, r[k]);
-  for (int64_t vi = b_nv + t; vi < v_nv; vi += T) {  // streamed remainder, first read
+  for (int k = 0; k < RV; ++k)
+#pragma unroll
+    for (int i = 0; i < V; ++i) mx = fmax_nan(mx, r[k][i]);
+  mx = warp_max_nan(mx);
+  if (lane == 0) s_m[warp] = mx;
+  __syncthreads();
+  const float m_c = warp_max_nan(lane < (T >> 5) ? s_m[lane] : neg_inf());
+
+  // Pass 1b: sum of e^(x - m_c) over the on-chip part, one FFMA + exp2 per
+  // element; the rounding of c = -m_c log2 e is common to every term and is
+  // corrected once (stats_correct).
+  float sum = 0.0f;
+  if (m_c != neg_inf()) {
+    const bool huge = !(fabsf(m_c) < 1e38f);
+    const float c = huge ? 0.0f : __fmul_rn(-m_c, L2E_HI);
+    auto term = [&](float v) {
+      return huge ? ex2_ftz(__fmul_rn(__fsub_rn(v, m_c), L2E_HI)) : ex2_ftz(__fmaf_rn(v, L2E_HI, c));
+    };
+    for (int64_t vi = t; vi < s_nv; vi += T) {
+      float f[V];
+      unpack16<InT>(*reinterpret_cast<const uint4*>(sx + vi * V), f);
+      mask_tail<V>(f, c0 + vi * V, L);
+      float e[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) e[i] = term(f[i]);
+#pragma unroll
+      for (int w = V / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) e[i] = __fadd_rn(e[i], e[i + w]);
+      sum = __fadd_rn(sum, e[0]);
+    }
+#pragma unroll
+    for (int k = 0; k < RV; ++k) {
+      float e[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) e[i] = term(r[k][i]);
+#pragma unroll
+      for (int w = V / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) e[i] = __fadd_rn(e[i], e[i + w]);
+      sum = __fadd_rn(sum, e[0]);
+    }
+    sum = stats_correct(sum, m_c);
+  }
+  // Streamed remainder (rows longer than the cluster holds), first read:
+  // the per-thread tiled online update, merged with the on-chip summary.
+  float m_s = neg_inf(), d_s = 0.0f;
+  for (int64_t vi = b_nv + t; vi < v_nv; vi += T) {
     float f[V];
     load_vec16<InT>(xr + c0 + vi * V, f);
     mask_tail<V>(f, c0 + vi * V, L);
-    online_fold<V>(m, d, f);
+    online_fold<V>(m_s, d_s, f);
   }
+  MD md = md_merge(MD{m_c, sum}, MD{m_s, d_s});
 
   // CTA summary: warp butterfly, then the per-warp summaries.
-  MD md = warp_merge(MD{m, d});
+  md = warp_merge(md);
+  __syncthreads();  // s_m is reused
   if (lane == 0) {
     s_m[warp] = md.m;
     s_d[warp] = md.d;
@@ -258,45 +261,67 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     OutT* yr = y + row * cols;
     const bool zero_row = (M == neg_inf());
     const bool nan_row = !zero_row && (D != D);
-    const float rD = recip_refined(D);
-    auto emit = [&](int64_t vi, const float (&f)[V]) {
-      const int64_t e0 = c0 + vi * V;
-      float p[V];
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        if (zero_row) p[i] = 0.0f;
-        else if (nan_row) p[i] = (e0 + i < L) ? qnan() : 0.0f;
-        else p[i] = __fmul_rn(exp_for<OutT, MODE_SOFTMAX>(f[i], M), rD);
+    if (!zero_row && !nan_row) {
+      constexpr float SC = ExpPolicy<OutT, MODE_SOFTMAX>::SCALE_LOG2;
+      const bool huge = !(fabsf(M) < 1e38f);
+      const float rD = recip_refined(D);
+      float c2 = SC, c2_err = 0.0f;
+      if (!huge) {
+        const float a = __fmul_rn(-M, L2E_HI);
+        const float e1 = __fmaf_rn(-M, L2E_HI, -a);  // exact residual of the product
+        c2 = __fadd_rn(a, SC);
+        const float bb = __fsub_rn(c2, a);           // TwoSum(a, SC) residual
+        const float e2 = __fadd_rn(__fsub_rn(a, __fsub_rn(c2, bb)), __fsub_rn(SC, bb));
+        c2_err = __fadd_rn(e1, e2);
       }
-      store_vec<OutT, V>(yr + e0, p);
-    };
-    // staged region (vectors past the valid data were never loaded: zeros)
-    for (int64_t vi = t; vi < a_nv; vi += T) {
-      float f[V];
-      if (vi < s_nv) {
-        unpack16<InT>(*reinterpret_cast<const uint4*>(sx + vi * V), f);
-        mask_tail<V>(f, c0 + vi * V, L);
-      } else {
+      // 2^-SC / D, times 2^(c2_err) ~ 1 + c2_err ln 2
+      const float rD2 = __fmul_rn(__fmul_rn(rD, SC == 0.0f ? 1.0f : 0.00390625f),
+                                  __fmaf_rn(c2_err, LN2, 1.0f));
+      auto emit = [&](int64_t vi, const float (&f)[V]) {
+        float p[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) f[i] = neg_inf();
+        for (int i = 0; i < V; ++i) {
+          const float xv = huge ? __fsub_rn(f[i], M) : f[i];
+          p[i] = cluster_out<OutT>(xv, huge ? 0.0f : M, c2, rD, rD2);
+        }
+        store_vec<OutT, V>(yr + c0 + vi * V, p);
+      };
+      for (int64_t vi = t; vi < a_nv; vi += T) {
+        float f[V];
+        if (vi < s_nv) {
+          unpack16<InT>(*reinterpret_cast<const uint4*>(sx + vi * V), f);
+          mask_tail<V>(f, c0 + vi * V, L);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) f[i] = neg_inf();
+        }
+        emit(vi, f);
       }
-      emit(vi, f);
-    }
 #pragma unroll
-    for (int k = 0; k < RV; ++k) {
-      const int64_t vi = a_nv + (int64_t)k * T + t;
-      if (vi < b_nv) emit(vi, r[k]);
-    }
-    for (int64_t vi = b_nv + t; vi < c_nv; vi += T) {  // streamed remainder, second read
-      float f[V];
-      if (vi < v_nv) {
-        load_vec16<InT>(xr + c0 + vi * V, f);
-        mask_tail<V>(f, c0 + vi * V, L);
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) f[i] = neg_inf();
+      for (int k = 0; k < RV; ++k) {
+        const int64_t vi = a_nv + (int64_t)k * T + t;
+        if (vi < b_nv) emit(vi, r[k]);
       }
-      emit(vi, f);
+      for (int64_t vi = b_nv + t; vi < c_nv; vi += T) {  // streamed remainder, second read
+        float f[V];
+        if (vi < v_nv) {
+          load_vec16<InT>(xr + c0 + vi * V, f);
+          mask_tail<V>(f, c0 + vi * V, L);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) f[i] = neg_inf();
+        }
+        emit(vi, f);
+      }
+    } else {
+      // policy rows: zeros, or NaN in the valid lanes
+      for (int64_t vi = t; vi < c_nv; vi += T) {
+        const int64_t e0 = c0 + vi * V;
+        float p[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) p[i] = (nan_row && e0 + i < L) ? qnan() : 0.0f;
+        store_vec<OutT, V>(yr + e0, p);
+      }
     }
   }
 
@@ -306,7 +331,7 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     for (int p = 0; p < CLUSTER_PIECES; ++p) {
       const int64_t p0 = (int64_t)p * piece_nv;
       if (p0 >= s_nv) break;
-      mbar_wait_bounded(smem_addr(&bars[p]), 0, int64_t(1) << 22);
+      mbar_wait_bounded(smem_addr(&bars[p]), 0, int64_t(1) << 21);
     }
   }
   cluster_wait();  // no CTA leaves while a peer may still read its summary

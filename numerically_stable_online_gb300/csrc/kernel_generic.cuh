@@ -12,7 +12,7 @@
 // cols * sizeof(type) not a multiple of 16.
 #pragma once
 
-#include "kernel_regs.cuh"
+#include "row_core.cuh"
 
 namespace smx {
 

@@ -5,7 +5,7 @@
 
 #include "kernel_cluster.cuh"
 #include "kernel_generic.cuh"
-#include "kernel_pipe.cuh"
+#include "kernel_stream.cuh"
 #include "kernel_regs.cuh"
 #include "smx_launch.h"
 
@@ -95,52 +95,46 @@ cudaError_t launch_cluster(const Call& c, const Plan& p) {
   return cudaSuccess;
 }
 
-template <typename InT, typename OutT, int MODE, int VPT>
-cudaError_t prepare_pipe_kernel(int64_t smem_bytes) {
-  static int64_t set_bytes[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (set_bytes[dev] < smem_bytes) {
-    e = cudaFuncSetAttribute(k_rows_pipe<InT, OutT, VPT, MODE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
-    if (e != cudaSuccess) return e;
-    set_bytes[dev] = smem_bytes;
-  }
-  return cudaSuccess;
-}
-
-inline int64_t pipe_smem_bytes(const Plan& p) {
-  return (int64_t)p.stages * p.slot_bytes + 16LL * p.stages +
-         4LL * 2 * p.groups * p.warps_per_group;
-}
-
-template <typename InT, typename OutT, int MODE, int VPT>
-cudaError_t launch_pipe_vpt(const Call& c, const Plan& p) {
+template <typename InT, typename OutT, int MODE, int VPT, int DEPTH>
+cudaError_t launch_stream_vd(const Call& c, const Plan& p) {
   constexpr int V = Elem<InT>::V;
-  if constexpr (VPT * V > 32) {
+  // at most 16 elements per thread with the compensated exponential (fp32
+  // outputs) and 32 otherwise
+  if constexpr (VPT * V > (ExpPolicy<OutT, MODE>::ACCURATE ? 16 : 32)) {
     return cudaErrorInvalidValue;
   } else {
-    const int64_t smem = pipe_smem_bytes(p);
-    cudaError_t e = prepare_pipe_kernel<InT, OutT, MODE, VPT>(smem);
+    auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH>;
+    const int64_t smem = stream_smem_bytes(DEPTH, VPT, p.threads);
+    static int64_t set_bytes[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int threads = (1 + p.groups * p.warps_per_group) * 32;
-    PipeShape sh{p.stages, p.groups, p.warps_per_group, p.slot_bytes};
-    k_rows_pipe<InT, OutT, VPT, MODE><<<(unsigned)p.ctas, threads, (size_t)smem, c.stream>>>(
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (set_bytes[dev] < smem) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      set_bytes[dev] = smem;
+    }
+    kern<<<(unsigned)p.ctas, p.threads, (size_t)smem, c.stream>>>(
         static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, c.rows, c.cols,
-        c.valid_len, sh, c.max_polls, c.status);
+        c.valid_len);
     return cudaGetLastError();
   }
 }
 
+template <typename InT, typename OutT, int MODE, int VPT>
+cudaError_t launch_stream_v(const Call& c, const Plan& p) {
+  return p.stages == 3 ? launch_stream_vd<InT, OutT, MODE, VPT, 3>(c, p)
+                       : launch_stream_vd<InT, OutT, MODE, VPT, 2>(c, p);
+}
+
 template <typename InT, typename OutT, int MODE>
-cudaError_t launch_pipe(const Call& c, const Plan& p) {
+cudaError_t launch_stream(const Call& c, const Plan& p) {
   switch (p.vpt) {
-    case 1: return launch_pipe_vpt<InT, OutT, MODE, 1>(c, p);
-    case 2: return launch_pipe_vpt<InT, OutT, MODE, 2>(c, p);
-    case 4: return launch_pipe_vpt<InT, OutT, MODE, 4>(c, p);
-    case 8: return launch_pipe_vpt<InT, OutT, MODE, 8>(c, p);
+    case 1: return launch_stream_v<InT, OutT, MODE, 1>(c, p);
+    case 2: return launch_stream_v<InT, OutT, MODE, 2>(c, p);
+    case 4: return launch_stream_v<InT, OutT, MODE, 4>(c, p);
+    case 8: return launch_stream_v<InT, OutT, MODE, 8>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -166,7 +160,7 @@ cudaError_t launch_typed(const Call& c, const Plan& p) {
                          : launch_regs_wr<InT, OutT, MODE, false>(c, p);
     case PATH_CLUSTER: return launch_cluster<InT, OutT, MODE>(c, p);
     case PATH_GENERIC: return launch_generic<InT, OutT, MODE>(c);
-    case PATH_PIPE: return launch_pipe<InT, OutT, MODE>(c, p);
+    case PATH_STREAM: return launch_stream<InT, OutT, MODE>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -207,26 +201,35 @@ int cluster_capacity(int cluster, int64_t smem_bytes) {
 }
 
 template <typename InT>
-int pipe_occupancy(int vpt, int threads, int64_t smem_bytes) {
+int stream_occupancy(int vpt, int threads, int depth) {
   // the bf16-output softmax kernel stands for the family
+  const int64_t smem = stream_smem_bytes(depth, vpt, threads);
   auto query = [&](auto kern) -> int {
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem_bytes) !=
-            cudaSuccess) {
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
     return n;
   };
   constexpr int V = Elem<InT>::V;
+  const bool d3 = depth == 3;
   switch (vpt) {
-    case 1: return query(k_rows_pipe<InT, __nv_bfloat16, 1, MODE_SOFTMAX>);
-    case 2: return query(k_rows_pipe<InT, __nv_bfloat16, 2, MODE_SOFTMAX>);
-    case 4: return query(k_rows_pipe<InT, __nv_bfloat16, 4, MODE_SOFTMAX>);
+    case 1:
+      return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 3>)
+                : query(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 2>);
+    case 2:
+      return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 3>)
+                : query(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 2>);
+    case 4:
+      return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 3>)
+                : query(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 2>);
     case 8:
-      if constexpr (8 * V <= 32) return query(k_rows_pipe<InT, __nv_bfloat16, 8, MODE_SOFTMAX>);
+      if constexpr (8 * V <= 32)
+        return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 3>)
+                  : query(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 2>);
       return 0;
     default: return 0;
   }

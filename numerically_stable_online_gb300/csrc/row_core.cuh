@@ -1,0 +1,155 @@
+// Per-row work shared by the register-resident and the streamed kernels: a
+// row is held by a group of G threads, VPT 16-byte vectors per thread, widened
+// to fp32; thread g's vector j starts at element (j*G + g)*V.
+//
+// The exponent argument.  "Softmax numerics architecture...", section "On CPU,
+// and the pitfalls worth naming", folds log2 e into one constant so that the
+// kernel calls exp2; here the whole shift is folded too:
+//     u_j = fma(x_j, L2E_HI, c),  c = RN(-M * L2E_HI) (+ s),
+// one FFMA per element, exact product and one rounding of a result near the
+// row's own range.  The rounding of c is an offset common to every element, so
+// it cancels in p_j = e_j / sum_k e_k ("The max-subtraction identity, and why
+// it is exact": any common shift cancels); the statistics path, which reports
+// d itself, multiplies the sum once by 2^(c_lo) with c_lo the exact residual of
+// c.  For bf16 outputs s = 8 scales every e_j by 2^8 (cancelled by the same
+// argument) so that the flush-to-zero exp2 never flushes a value that would
+// round to a nonzero bf16 subnormal (those need e_j >= 2^-134).  fp32 outputs
+// use the compensated exponential of smx_device.cuh instead.
+#pragma once
+
+#include <type_traits>
+
+#include "smx_device.cuh"
+
+namespace smx {
+
+enum : int { MODE_SOFTMAX = 0, MODE_STATS = 1 };
+
+template <typename OutT, int MODE>
+struct ExpPolicy {
+  static constexpr bool ACCURATE = (MODE == MODE_SOFTMAX) && std::is_same<OutT, float>::value;
+  static constexpr float SCALE_LOG2 =
+      (MODE == MODE_SOFTMAX && std::is_same<OutT, __nv_bfloat16>::value) ? 8.0f : 0.0f;
+};
+
+// e^(x - M) one element at a time (cluster and generic kernels): compensated
+// for fp32 outputs, the plain form otherwise (bf16 outputs keep subnormals).
+template <typename OutT, int MODE>
+__device__ __forceinline__ float exp_for(float x, float M) {
+  if constexpr (ExpPolicy<OutT, MODE>::ACCURATE) {
+    return exp_shift_accurate(x, M);
+  } else {
+    return exp_shift_fast<(MODE == MODE_SOFTMAX && std::is_same<OutT, __nv_bfloat16>::value)>(x, M);
+  }
+}
+
+// Masked load of one vector: lanes at or past L become -inf (the exclusion
+// value).  SMEM selects a shared-memory source.
+template <typename InT, bool SMEM>
+__device__ __forceinline__ void load_masked(const InT* p, int e0, int L, float (&f)[Elem<InT>::V]) {
+  constexpr int V = Elem<InT>::V;
+  if (e0 + V <= L) {
+    if constexpr (SMEM) unpack16<InT>(*reinterpret_cast<const uint4*>(p), f);
+    else load_vec16<InT>(p, f);
+  } else if (e0 < L) {
+    if constexpr (SMEM) unpack16<InT>(*reinterpret_cast<const uint4*>(p), f);
+    else load_vec16<InT>(p, f);
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (e0 + i >= L) f[i] = neg_inf();
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) f[i] = neg_inf();
+  }
+}
+
+template <int VPT, int V>
+__device__ __forceinline__ float local_max(const float (&v)[VPT][V]) {
+  float m = neg_inf();
+#pragma unroll
+  for (int j = 0; j < VPT; ++j)
+#pragma unroll
+    for (int i = 0; i < V; ++i) m = fmax_nan(m, v[j][i]);
+  return m;
+}
+
+// Replace v by the exponentials against the row maximum M and return this
+// thread's share of their sum (pairwise within each vector).  Requires M != -inf.
+template <typename OutT, int MODE, int VPT, int V>
+__device__ __forceinline__ float exp_and_sum(float (&v)[VPT][V], float M) {
+  using P = ExpPolicy<OutT, MODE>;
+  float s = 0.0f;
+  if constexpr (P::ACCURATE) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[j][i] = exp_shift_accurate(v[j][i], M);
+  } else if (fabsf(M) < 1e38f) {
+    const float c = __fmaf_rn(-M, L2E_HI, P::SCALE_LOG2);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[j][i] = ex2_ftz(__fmaf_rn(v[j][i], L2E_HI, c));
+  } else {
+    // |M| near the top of the fp32 range: -M * log2 e would overflow, so
+    // subtract first (a difference that overflows is -inf and gives 0)
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        v[j][i] = ex2_ftz(__fmaf_rn(__fsub_rn(v[j][i], M), L2E_HI, P::SCALE_LOG2));
+  }
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    float sk[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) sk[i] = v[j][i];
+#pragma unroll
+    for (int w = V / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) sk[i] = __fadd_rn(sk[i], sk[i + w]);
+    s = __fadd_rn(s, sk[0]);
+  }
+  return s;
+}
+
+// The statistics path's d: the sum of exp2(fma(x, L2E_HI, c_hi)) times
+// 2^(c_lo), c_lo the exact rounding residual of c_hi = RN(-M * L2E_HI).
+__device__ __forceinline__ float stats_correct(float sum, float M) {
+  if (!(fabsf(M) < 1e38f)) return sum;  // the subtract-first branch has no offset
+  const float c_hi = __fmul_rn(-M, L2E_HI);
+  const float c_lo = __fmaf_rn(-M, L2E_HI, -c_hi);
+  return __fmaf_rn(sum, __fmul_rn(c_lo, LN2), sum);
+}
+
+// Normalise and store the row held in v (exponentials), or the policy's zero /
+// NaN row.  Uniform branches per row; one multiply per element on normal rows.
+template <typename OutT, int VPT, int V>
+__device__ __forceinline__ void store_row(OutT* yr, int G, int g, int ncols, int L, const float (&v)[VPT][V],
+                                          bool zero_row, bool nan_row, float rD) {
+  if (!zero_row && !nan_row) {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e0 = (j * G + g) * V;
+      if (e0 < ncols) {
+        float p[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) p[i] = __fmul_rn(v[j][i], rD);
+        store_vec<OutT, V>(yr + e0, p);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e0 = (j * G + g) * V;
+      if (e0 < ncols) {
+        float p[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) p[i] = (nan_row && e0 + i < L) ? qnan() : 0.0f;
+        store_vec<OutT, V>(yr + e0, p);
+      }
+    }
+  }
+}
+
+}  // namespace smx

@@ -39,6 +39,7 @@ std::atomic<int64_t> g_smem_cap{0};
 std::atomic<int64_t> g_wait_limit{0};
 std::atomic<int> g_regs_threads{0};
 std::atomic<int> g_regs_vpt{0};
+std::atomic<int> g_stream_depth{0};
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
@@ -127,10 +128,12 @@ int max_cluster_size(DeviceInfo& d, int in_dtype) {
   return c;
 }
 
-bool plan_regs(int64_t cols, int in_dtype, Plan* p) {
+bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
   const int V = 16 / elem_size(in_dtype);
   const int64_t nvec = cols / V;
-  const int max_vpt = 32 / V;
+  // the compensated exponential (fp32 outputs) keeps more live registers per
+  // element: at most 16 elements per thread there, 32 otherwise
+  const int max_vpt = (accurate_exp ? 16 : 32) / V;
   int vpt = 0;
   int64_t G = 0;
   const int dbg_t = g_regs_threads.load(), dbg_v = g_regs_vpt.load();
@@ -139,19 +142,21 @@ bool plan_regs(int64_t cols, int in_dtype, Plan* p) {
     vpt = dbg_v;
     G = dbg_t;
   } else {
-    for (int v = 1; v <= max_vpt; v <<= 1) {
-      const int64_t g = ((nvec + v - 1) / v + 31) / 32 * 32;
-      if (g <= 256) {
-        vpt = v;
-        G = g;
-        break;
+    // measured on GB300: two vectors per thread and 64..256 threads per row
+    // are best; then four, one, eight vectors
+    const int order[4] = {2, 4, 1, 8};
+    for (int pass = 0; pass < 2 && vpt == 0; ++pass) {
+      for (int v : order) {
+        if (v > max_vpt) continue;
+        const int64_t g = ((nvec + v - 1) / v + 31) / 32 * 32;
+        if (pass == 0 ? (g >= 64 && g <= 256) : g <= 1024) {
+          vpt = v;
+          G = g;
+          break;
+        }
       }
     }
-    if (vpt == 0) {
-      vpt = max_vpt;
-      G = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
-      if (G > 1024) return false;
-    }
+    if (vpt == 0) return false;
   }
   p->path = PATH_REGS;
   p->vpt = vpt;
@@ -160,44 +165,37 @@ bool plan_regs(int64_t cols, int in_dtype, Plan* p) {
   return true;
 }
 
-int pipe_occupancy(int in_dtype, int vpt, int threads, int64_t smem) {
+int stream_occupancy(int in_dtype, int vpt, int threads, int depth) {
   switch (in_dtype) {
-    case SMX_F32: return pipe_occupancy_f32(vpt, threads, smem);
-    case SMX_F16: return pipe_occupancy_f16(vpt, threads, smem);
-    default: return pipe_occupancy_bf16(vpt, threads, smem);
+    case SMX_F32: return stream_occupancy_f32(vpt, threads, depth);
+    case SMX_F16: return stream_occupancy_f16(vpt, threads, depth);
+    default: return stream_occupancy_bf16(vpt, threads, depth);
   }
 }
 
-// Pipelined path for rows of at most 32 KiB: a consumer group of WG warps per
-// row, each thread holding vpt 16-byte vectors; about 16 consumer warps and
-// 96 KiB of row slots per CTA; as many CTAs as fit on every SM.
-constexpr int64_t PIPE_STAGE_BUDGET = 96 * 1024;
-
-bool plan_pipe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
-  const int es = elem_size(in_dtype), V = 16 / es;
-  const int64_t rb = cols * es;
-  if (rb > PIPE_MAX_ROW_BYTES) return false;
-  const int64_t nvec = cols / V;
-  int vpt = 32 / V;
-  while (vpt > 1 && 32LL * (vpt / 2) >= nvec) vpt /= 2;
-  const int64_t G = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
-  const int WG = (int)(G / 32);
-  if (WG > 16) return false;
-  const int NG = WG == 1 ? 16 : (16 / WG < 15 ? 16 / WG : 15);
-  const int slot = (int)((rb + 127) / 128 * 128);
-  int S = (int)(PIPE_STAGE_BUDGET / slot) / NG * NG;
-  if (S < NG) S = NG;
-  p->path = PATH_PIPE;
-  p->vpt = vpt;
-  p->warps_per_group = WG;
-  p->groups = NG;
-  p->stages = S;
-  p->slot_bytes = slot;
-  const int threads = (1 + NG * WG) * 32;
-  const int64_t smem = (int64_t)S * slot + 16LL * S + 8LL * NG * WG;
-  const int occ = pipe_occupancy(in_dtype, vpt, threads, smem);
+// Streamed path for rows of at most 32 KiB: the CTA shape of the register path
+// (threads per row, vectors per thread; at least two warps), two rows
+// prefetched per CTA, and as many persistent CTAs as are resident on all SMs.
+bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
+  const int es = elem_size(in_dtype);
+  if (cols * es > STREAM_MAX_ROW_BYTES) return false;
+  Plan r;
+  if (!plan_regs(cols, in_dtype, accurate_exp, &r) || r.warp_rows) {
+    const int V = 16 / es;
+    const int64_t nvec = cols / V;
+    r.threads = 64;
+    r.vpt = 1;
+    while (64LL * r.vpt < nvec) r.vpt <<= 1;
+    if (r.vpt * V > (accurate_exp ? 16 : 32)) return false;
+  }
+  const int depth = g_stream_depth.load() == 3 ? 3 : 2;
+  const int occ = stream_occupancy(in_dtype, r.vpt, r.threads, depth);
   if (occ <= 0) return false;
   const int64_t ctas = (int64_t)occ * d.sm_count;
+  p->path = PATH_STREAM;
+  p->threads = r.threads;
+  p->vpt = r.vpt;
+  p->stages = depth;
   p->ctas = (int)(rows < ctas ? rows : ctas);
   return true;
 }
@@ -232,8 +230,9 @@ smx_status run(Call& c, DeviceInfo& dev) {
       plan_cluster(dev, c.cols, c.in_dtype, &p);
       planned = true;
     } else if (force != PATH_GENERIC) {
-      if (force != PATH_REGS) planned = plan_pipe(dev, c.rows, c.cols, c.in_dtype, &p);
-      if (!planned) planned = plan_regs(c.cols, c.in_dtype, &p);
+      const bool acc = c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32;
+      if (force != PATH_REGS) planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, &p);
+      if (!planned) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       if (!planned) {
         plan_cluster(dev, c.cols, c.in_dtype, &p);
         planned = true;
@@ -390,6 +389,8 @@ void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
 void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls > 0 ? polls : 0); }
 
 int smx_debug_last_path(void) { return t_last_path; }
+
+void smx_debug_set_stream_depth(int depth) { g_stream_depth.store(depth > 0 ? depth : 0); }
 
 void smx_debug_set_regs_shape(int threads, int vpt) {
   g_regs_threads.store(threads > 0 ? threads : 0);

@@ -7,7 +7,7 @@
 
 namespace smx {
 
-enum Path : int { PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_PIPE = 4 };
+enum Path : int { PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_STREAM = 4 };
 
 struct Call {
   const void* x;
@@ -29,8 +29,8 @@ struct Plan {
   int threads = 256;  // threads per CTA
   int vpt = 1;        // 16-byte vectors per thread
   bool warp_rows = false;
-  // pipelined rows (threads = (1 + groups * warps_per_group) * 32)
-  int stages = 0, groups = 0, warps_per_group = 0, slot_bytes = 0, ctas = 0;
+  // streamed rows: `stages` rows prefetched per CTA (2 or 3), `ctas` CTAs
+  int stages = 0, ctas = 0;
   // cluster rows
   int cluster = 1;
   int64_t chunk = 0;       // elements per CTA
@@ -51,12 +51,18 @@ int cluster_capacity_f32(int cluster, int64_t smem_bytes);
 int cluster_capacity_f16(int cluster, int64_t smem_bytes);
 int cluster_capacity_bf16(int cluster, int64_t smem_bytes);
 
-// Resident CTAs per SM of the pipelined kernel for this input type and shape.
-int pipe_occupancy_f32(int vpt, int threads, int64_t smem_bytes);
-int pipe_occupancy_f16(int vpt, int threads, int64_t smem_bytes);
-int pipe_occupancy_bf16(int vpt, int threads, int64_t smem_bytes);
+// Resident CTAs per SM of the streamed kernel for this input type and shape.
+int stream_occupancy_f32(int vpt, int threads, int depth);
+int stream_occupancy_f16(int vpt, int threads, int depth);
+int stream_occupancy_bf16(int vpt, int threads, int depth);
 
-constexpr int PIPE_MAX_ROW_BYTES = 32768;
+constexpr int STREAM_MAX_ROW_BYTES = 32768;
+
+// Dynamic shared memory of the streamed kernel: `depth` rows of vpt 16-byte
+// vectors for each of the CTA's threads.
+inline int64_t stream_smem_bytes(int depth, int vpt, int threads) {
+  return (int64_t)depth * vpt * threads * 16;
+}
 
 cudaError_t launch_merge(const float* m_a, const float* d_a, const float* m_b, const float* d_b,
                          float* m_o, float* d_o, int64_t n, cudaStream_t stream);

@@ -323,3 +323,112 @@ void orc_stable_softmax_f16(const double *x, int64_t n, double *shifted, double 
     for (int64_t j = 0; j < n; ++j) p[j] = f16(e[j] / s);
     *sum_out = s;
 }
+
+/* ---------------------------------------------------------------------------
+ * Log-space outputs ("Softmax numerics architecture...", section "Log-sum-exp:
+ * log-probabilities without probabilities"):
+ *   LSE(x) = m + log(sum_j exp(x_j - m)),  log_softmax(x)_i = x_i - LSE(x),
+ *   CE(x, t) = LSE(x) - x_t.
+ * Over the valid prefix with the same policy: an empty / all -inf row has
+ * LSE = -inf and log_softmax outputs -inf in its valid lanes (log 0); a NaN row
+ * NaN; a +inf row NaN.  Masked lanes output -inf (log of the +0 probability).
+ * ------------------------------------------------------------------------- */
+void orc_log_softmax_rows(const void *x, int dtype, int64_t cols, const int32_t *valid_len,
+                          const int64_t *sel, int64_t n_sel, double *out, double *lse_out)
+{
+    for (int64_t i = 0; i < n_sel; ++i) {
+        int64_t r = sel ? sel[i] : i;
+        int64_t L = row_len(valid_len, r, cols);
+        int64_t base = r * cols;
+        double m, d;
+        int cls = row_stats_one(x, dtype, base, L, &m, &d);
+        double lse = cls == 0 ? m + log(d) : (cls == 1 ? -INFINITY : NAN);
+        if (lse_out) lse_out[i] = lse;
+        double *o = out ? out + i * cols : NULL;
+        if (!o) continue;
+        for (int64_t j = 0; j < cols; ++j) o[j] = -INFINITY;
+        for (int64_t j = 0; j < L; ++j) {
+            if (cls == 0) o[j] = load_elem(x, dtype, base + j) - lse;
+            else if (cls == 2) o[j] = NAN;
+        }
+    }
+}
+
+/* Normalise rows with given statistics: y_j = exp(x_j - m) / d over the valid
+ * prefix (+0 beyond), the step that completes a softmax whose statistics were
+ * merged from blocks ("Online stable softmax": only m and l of the prefix are
+ * needed).  m == -inf gives a zero row; a NaN m or d, or m == +inf, NaN lanes. */
+void orc_apply_stats(const void *x, int dtype, int64_t cols, const int32_t *valid_len,
+                     const double *m_in, const double *d_in, const int64_t *sel, int64_t n_sel,
+                     double *p)
+{
+    for (int64_t i = 0; i < n_sel; ++i) {
+        int64_t r = sel ? sel[i] : i;
+        int64_t L = row_len(valid_len, r, cols);
+        int64_t base = r * cols;
+        double m = m_in[r], d = d_in[r];
+        double *out = p + i * cols;
+        for (int64_t j = 0; j < cols; ++j) out[j] = 0.0;
+        if (m == -INFINITY || L == 0) continue;
+        int bad = isnan(m) || isnan(d) || m == INFINITY;
+        for (int64_t j = 0; j < L; ++j)
+            out[j] = bad ? NAN : exp(load_elem(x, dtype, base + j) - m) / d;
+    }
+}
+
+/* Softmax vector-Jacobian product ("The Jacobian, and the backward pass that
+ * never divides"): for upstream gradient g and the softmax p of the row,
+ * dx_i = p_i (g_i - sum_j g_j p_j).  p is computed here from x (three-pass);
+ * masked lanes and empty rows give dx = 0; NaN rows NaN. */
+void orc_softmax_backward(const void *x, int dtype, const double *g, int64_t cols,
+                          const int32_t *valid_len, const int64_t *sel, int64_t n_sel, double *dx)
+{
+    for (int64_t i = 0; i < n_sel; ++i) {
+        int64_t r = sel ? sel[i] : i;
+        int64_t L = row_len(valid_len, r, cols);
+        double *o = dx + i * cols;
+        const double *gr = g + r * cols;
+        double m, d;
+        int cls = row_stats_one(x, dtype, r * cols, L, &m, &d);
+        for (int64_t j = 0; j < cols; ++j) o[j] = 0.0;
+        if (cls == 1) continue;
+        if (cls == 2) { for (int64_t j = 0; j < L; ++j) o[j] = NAN; continue; }
+        double gp = 0.0;
+        for (int64_t j = 0; j < L; ++j) gp += gr[j] * (exp(load_elem(x, dtype, r * cols + j) - m) / d);
+        for (int64_t j = 0; j < L; ++j) {
+            double pj = exp(load_elem(x, dtype, r * cols + j) - m) / d;
+            o[j] = pj * (gr[j] - gp);
+        }
+    }
+}
+
+/* Cross-entropy with logits and its fused gradient ("Log-sum-exp..." and "The
+ * Jacobian, and the backward pass that never divides"): loss_r = LSE(x_r) -
+ * x_r[t_r], grad_rj = p_rj - [j == t_r].  A target outside [0, L) is ignored:
+ * loss 0 and gradient 0 for the row (the convention of an ignored index). */
+void orc_cross_entropy(const void *x, int dtype, int64_t cols, const int32_t *valid_len,
+                       const int64_t *target, const int64_t *sel, int64_t n_sel, double *loss,
+                       double *grad)
+{
+    for (int64_t i = 0; i < n_sel; ++i) {
+        int64_t r = sel ? sel[i] : i;
+        int64_t L = row_len(valid_len, r, cols);
+        int64_t base = r * cols;
+        int64_t t = target[r];
+        double *gr = grad ? grad + i * cols : NULL;
+        if (gr) for (int64_t j = 0; j < cols; ++j) gr[j] = 0.0;
+        if (t < 0 || t >= L) { loss[i] = 0.0; continue; }
+        double m, d;
+        int cls = row_stats_one(x, dtype, base, L, &m, &d);
+        if (cls != 0) {
+            loss[i] = NAN;
+            if (gr) for (int64_t j = 0; j < L; ++j) gr[j] = NAN;
+            continue;
+        }
+        double lse = m + log(d);
+        loss[i] = lse - load_elem(x, dtype, base + t);
+        if (gr)
+            for (int64_t j = 0; j < L; ++j)
+                gr[j] = exp(load_elem(x, dtype, base + j) - m) / d - (j == t ? 1.0 : 0.0);
+    }
+}

@@ -22,7 +22,8 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 PAIRS = [(a, b) for a in DT for b in DT]
-PATH_REGS, PATH_CLUSTER, PATH_GENERIC = 1, 2, 3
+PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM = 1, 2, 3, 4
+ALL_PATHS = [PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -37,6 +38,7 @@ def built():
     lib.smx_debug_set_cluster(0, 0)
     lib.smx_debug_set_wait_limit(0)
     lib.smx_debug_set_regs_shape(0, 0)
+    lib.smx_debug_set_stream_depth(0)
 
 
 @pytest.fixture
@@ -46,6 +48,7 @@ def lib(built):
     built.smx_debug_set_cluster(0, 0)
     built.smx_debug_set_wait_limit(0)
     built.smx_debug_set_regs_shape(0, 0)
+    built.smx_debug_set_stream_depth(0)
 
 
 DEV = "cuda:0"
@@ -93,7 +96,7 @@ def stored(vals, dtype):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("in_dtype,out_dtype", PAIRS)
-@pytest.mark.parametrize("path", [PATH_REGS, PATH_CLUSTER, PATH_GENERIC])
+@pytest.mark.parametrize("path", ALL_PATHS)
 def test_worked_rows(lib, in_dtype, out_dtype, path):
     lib.smx_debug_force_path(path)
     for name, row in wl.WORKED_ROWS.items():
@@ -210,7 +213,7 @@ def test_valid_lengths_clamped(lib):
     rows, cols = 6, 64
     x = stored(np.random.default_rng(1).normal(0, 3, rows * cols), "f32")
     vl = np.array([0, 1, 63, 64, 1000, -7], np.int32)
-    for path in (PATH_REGS, PATH_CLUSTER, PATH_GENERIC):
+    for path in ALL_PATHS:
         lib.smx_debug_force_path(path)
         run_and_compare(x, "f32", "f32", rows, cols, vl)
         run_and_compare(stored(np.random.default_rng(2).normal(0, 3, rows * cols), "bf16"),
@@ -230,7 +233,7 @@ POLICY_ROWS = [
 
 
 @pytest.mark.parametrize("in_dtype,out_dtype", PAIRS)
-@pytest.mark.parametrize("path", [PATH_REGS, PATH_CLUSTER, PATH_GENERIC])
+@pytest.mark.parametrize("path", ALL_PATHS)
 def test_policy_rows(lib, in_dtype, out_dtype, path):
     lib.smx_debug_force_path(path)
     rows = np.array(POLICY_ROWS, np.float32)
@@ -248,9 +251,32 @@ def test_subnormal_bf16_outputs(lib):
     as bf16 subnormals, not flushed."""
     row = np.array([0.0, -88.0, -90.0, -92.0, -95.0, -100.0, -87.5, -91.3], np.float32)
     for in_dtype in ("f32", "bf16"):
-        for path in (PATH_REGS, PATH_CLUSTER, PATH_GENERIC):
+        for path in ALL_PATHS:
             lib.smx_debug_force_path(path)
             run_and_compare(stored(row, in_dtype), in_dtype, "bf16", 1, 8)
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype,cols", [("bf16", "bf16", 512), ("f16", "f16", 1024),
+                                                     ("f32", "f32", 1000), ("bf16", "f32", 4096),
+                                                     ("f32", "bf16", 8192), ("bf16", "bf16", 16384)])
+@pytest.mark.parametrize("depth", [2, 3, 7])
+def test_stream_ring_many_rows(lib, in_dtype, out_dtype, cols, depth):
+    """Many rows per persistent CTA, so the ring of row slots wraps many times;
+    lengths include 0, 1 and cols."""
+    rows = max(600, 8_000_000 // cols)
+    rng = np.random.default_rng(cols)
+    x = stored(rng.normal(0, 7, rows * cols), in_dtype)
+    vl = rng.integers(0, cols + 1, size=rows).astype(np.int32)
+    vl[::97] = 0
+    vl[1::89] = 1
+    vl[2::83] = cols
+    lib.smx_debug_force_path(PATH_STREAM)
+    lib.smx_debug_set_stream_depth(depth)
+    run_and_compare(x, in_dtype, out_dtype, rows, cols, vl)
+    assert lib.smx_debug_last_path() == PATH_STREAM
+    m, d = gpu_stats(x, in_dtype, rows, cols, vl)
+    m_ref, d_ref = oracle.row_stats(x, in_dtype, rows, cols, vl)
+    check_stats(m, d, m_ref, d_ref)
 
 
 @pytest.mark.parametrize("cap", [1, 2, 4, 8, 16])
@@ -303,7 +329,7 @@ def check_stats(m, d, m_ref, d_ref, rel=2e-6):
 
 
 @pytest.mark.parametrize("in_dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("path", [PATH_REGS, PATH_CLUSTER, PATH_GENERIC])
+@pytest.mark.parametrize("path", ALL_PATHS)
 def test_row_stats(lib, in_dtype, path):
     lib.smx_debug_force_path(path)
     rows, cols = 12, 4096
