@@ -136,9 +136,11 @@ int smx_version(void);
  *   path that cannot run the shape falls back to the automatic choice.
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
- * smx_debug_set_wait_limit(n): polls of a staging barrier before the kernel
- *   gives up and records SMX_ERR_TIMEOUT (0 = default).  A test sets it to 1
- *   to exercise the error path.
+ * smx_debug_set_wait_limit(n): n > 0: polls of a staging barrier (path 2)
+ *   before the kernel gives up and records SMX_ERR_TIMEOUT; 0 = default; n < 0:
+ *   each CTA of path 2 first waits -n polls on a barrier that nothing signals,
+ *   records SMX_ERR_TIMEOUT when that wait runs out (it always does), then
+ *   works normally -- a deterministic probe of the error path.
  * smx_debug_last_path(): the path (1..4) the last softmax/stats call on this
  *   thread used, 0 if none.
  * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of

@@ -72,27 +72,23 @@ cudaError_t launch_cluster(const Call& c, const Plan& p) {
                                  : 16;
   cudaError_t e = prepare_cluster_kernel<InT, OutT, MODE>(smem_bytes);
   if (e != cudaSuccess) return e;
-  for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_Y) {
-    const int64_t n = c.rows - r0 < MAX_GRID_Y ? c.rows - r0 : MAX_GRID_Y;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.cluster, (unsigned)n, 1);
-    cfg.blockDim = dim3(CLUSTER_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem_bytes;
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_rows_cluster<InT, OutT, CLUSTER_RV, MODE>,
-                           static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out,
-                           c.d_out, r0 + n, c.cols, c.valid_len, r0, p.chunk, p.smem_elems,
-                           c.max_polls, c.status);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  // persistent: p.ctas clusters, each walking its rows
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.cluster, (unsigned)p.ctas, 1);
+  cfg.blockDim = dim3(CLUSTER_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_rows_cluster<InT, OutT, CLUSTER_RV, MODE>,
+                            static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out,
+                            c.rows, c.cols, c.valid_len, p.chunk, p.smem_elems, c.max_polls,
+                            c.status);
 }
 
 template <typename InT, typename OutT, int MODE, int VPT, int DEPTH>

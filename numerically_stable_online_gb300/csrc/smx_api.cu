@@ -200,7 +200,7 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
   return true;
 }
 
-void plan_cluster(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
+bool plan_cluster(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
   const int es = elem_size(in_dtype);
   const int V = 16 / es;
   const int64_t smem_elems_cap = cluster_smem_cap_bytes(d) / es;
@@ -210,10 +210,18 @@ void plan_cluster(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
   while (c < maxc && (int64_t)c * per_cta < cols) c <<= 1;
   int64_t chunk = (cols + c - 1) / c;
   chunk = (chunk + V - 1) / V * V;
+  // in-chunk vector indices are 32-bit
+  if (chunk / V > (int64_t)1 << 30) return false;
+  const int64_t smem_elems = chunk < smem_elems_cap ? chunk : smem_elems_cap;
+  const int64_t smem_bytes = smem_elems * es > 16 ? smem_elems * es : 16;
+  const int resident = cluster_capacity(in_dtype, c, smem_bytes);
+  if (resident <= 0) return false;
   p->path = PATH_CLUSTER;
   p->cluster = c;
   p->chunk = chunk;
-  p->smem_elems = chunk < smem_elems_cap ? chunk : smem_elems_cap;
+  p->smem_elems = smem_elems;
+  p->ctas = (int)(rows < resident ? rows : resident);  // persistent clusters
+  return true;
 }
 
 smx_status run(Call& c, DeviceInfo& dev) {
@@ -227,22 +235,18 @@ smx_status run(Call& c, DeviceInfo& dev) {
   bool planned = false;
   if (vec_ok) {
     if (force == PATH_CLUSTER) {
-      plan_cluster(dev, c.cols, c.in_dtype, &p);
-      planned = true;
+      planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     } else if (force != PATH_GENERIC) {
       const bool acc = c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32;
       if (force != PATH_REGS) planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, &p);
       if (!planned) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
-      if (!planned) {
-        plan_cluster(dev, c.cols, c.in_dtype, &p);
-        planned = true;
-      }
+      if (!planned) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     }
   }
   if (!planned) p.path = PATH_GENERIC;
   c.status = dev.status;
   const int64_t wl = g_wait_limit.load();
-  c.max_polls = wl > 0 ? wl : DEFAULT_MAX_POLLS;
+  c.max_polls = wl != 0 ? wl : DEFAULT_MAX_POLLS;
   cudaError_t e;
   switch (c.in_dtype) {
     case SMX_F32: e = launch_in_f32(c, p); break;
@@ -386,7 +390,7 @@ void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
   g_smem_cap.store(smem_bytes > 0 ? smem_bytes : 0);
 }
 
-void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls > 0 ? polls : 0); }
+void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls); }
 
 int smx_debug_last_path(void) { return t_last_path; }
 

@@ -22,6 +22,7 @@ namespace smx {
 constexpr float L2E_HI = 1.44269502162933349609375f;  // 0x3FB8AA3B
 constexpr float L2E_LO = 1.925963033500011079e-08f;   // 0x32A57060
 constexpr float LN2 = 0.693147182464599609375f;       // 0x3F317218
+constexpr float L2E_LO_LN2 = 1.3349759e-08f;          // fp32(L2E_LO * ln 2)
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
@@ -85,11 +86,13 @@ __device__ __forceinline__ float exp_shift_accurate(float x, float m) {
   const float z = __fsub_rn(t, x);
   const float t_lo = __fadd_rn(__fsub_rn(x, __fsub_rn(t, z)), __fsub_rn(-m, z));
   const float u = __fmul_rn(t, L2E_HI);
-  float u_lo = __fmaf_rn(t, L2E_HI, -u);
-  u_lo = __fmaf_rn(t, L2E_LO, u_lo);
-  u_lo = __fmaf_rn(t_lo, L2E_HI, u_lo);
+  // ln 2 * (u_exact - u): the exact product residual, the t * L2E_LO term and
+  // t_lo * log2 e, each scaled by ln 2 (ln 2 * log2 e = 1 up to 2^-25, which is
+  // far below these terms' own size)
+  const float r = __fmaf_rn(t, L2E_HI, -u);
+  const float corr = __fmaf_rn(r, LN2, __fmaf_rn(t, L2E_LO_LN2, t_lo));
   const float e = ex2_ftz(u);
-  return __fmaf_rn(e, __fmul_rn(u_lo, LN2), e);
+  return __fmaf_rn(e, corr, e);
 }
 
 // ---------------------------------------------------------------------------
