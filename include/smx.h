@@ -146,8 +146,10 @@ int smx_version(void);
  * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of
  *   `threads` threads per row (32 = one warp per row, path 1 only) holding `vpt`
  *   16-byte vectors each, when that shape covers the row (0, 0 = automatic).
- * smx_debug_set_stream_depth(n): rows prefetched per CTA on path 4 (2 or 3;
- *   0 = automatic).
+ * smx_debug_set_stream_depth(n): rows prefetched per CTA on path 4 (2, 3 or
+ *   4; 0 = automatic).
+ * smx_debug_set_stream_ctas(n): n resident CTAs per SM on path 4, at most as
+ *   many as fit (0 = automatic).
  */
 void smx_debug_force_path(int path);
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes);
@@ -155,6 +157,7 @@ void smx_debug_set_wait_limit(int64_t polls);
 int smx_debug_last_path(void);
 void smx_debug_set_regs_shape(int threads, int vpt);
 void smx_debug_set_stream_depth(int depth);
+void smx_debug_set_stream_ctas(int per_sm);
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_regs_shape.restype = None
         lib.smx_debug_set_stream_depth.argtypes = [I32]
         lib.smx_debug_set_stream_depth.restype = None
+        lib.smx_debug_set_stream_ctas.argtypes = [I32]
+        lib.smx_debug_set_stream_ctas.restype = None
         _lib = lib
         return lib
 

@@ -120,8 +120,11 @@ cudaError_t launch_stream_vd(const Call& c, const Plan& p) {
 
 template <typename InT, typename OutT, int MODE, int VPT>
 cudaError_t launch_stream_v(const Call& c, const Plan& p) {
-  return p.stages == 3 ? launch_stream_vd<InT, OutT, MODE, VPT, 3>(c, p)
-                       : launch_stream_vd<InT, OutT, MODE, VPT, 2>(c, p);
+  switch (p.stages) {
+    case 3: return launch_stream_vd<InT, OutT, MODE, VPT, 3>(c, p);
+    case 4: return launch_stream_vd<InT, OutT, MODE, VPT, 4>(c, p);
+    default: return launch_stream_vd<InT, OutT, MODE, VPT, 2>(c, p);
+  }
 }
 
 template <typename InT, typename OutT, int MODE>
@@ -211,21 +214,27 @@ int stream_occupancy(int vpt, int threads, int depth) {
     return n;
   };
   constexpr int V = Elem<InT>::V;
-  const bool d3 = depth == 3;
+  auto by_depth = [&](auto k2, auto k3, auto k4) {
+    return depth == 3 ? query(k3) : (depth == 4 ? query(k4) : query(k2));
+  };
   switch (vpt) {
     case 1:
-      return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 3>)
-                : query(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 2>);
+      return by_depth(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 2>,
+                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 3>,
+                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 4>);
     case 2:
-      return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 3>)
-                : query(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 2>);
+      return by_depth(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 2>,
+                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 3>,
+                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 4>);
     case 4:
-      return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 3>)
-                : query(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 2>);
+      return by_depth(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 2>,
+                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 3>,
+                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 4>);
     case 8:
       if constexpr (8 * V <= 32)
-        return d3 ? query(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 3>)
-                  : query(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 2>);
+        return by_depth(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 2>,
+                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 3>,
+                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 4>);
       return 0;
     default: return 0;
   }

@@ -84,20 +84,41 @@ __device__ __forceinline__ float exp_and_sum(float (&v)[VPT][V], float M) {
     for (int j = 0; j < VPT; ++j)
 #pragma unroll
       for (int i = 0; i < V; ++i) v[j][i] = exp_shift_accurate(v[j][i], M);
-  } else if (fabsf(M) < 1e38f) {
-    const float c = __fmaf_rn(-M, L2E_HI, P::SCALE_LOG2);
-#pragma unroll
-    for (int j = 0; j < VPT; ++j)
-#pragma unroll
-      for (int i = 0; i < V; ++i) v[j][i] = ex2_ftz(__fmaf_rn(v[j][i], L2E_HI, c));
   } else {
-    // |M| near the top of the fp32 range: -M * log2 e would overflow, so
-    // subtract first (a difference that overflows is -inf and gives 0)
+    // u = x * L2E_HI + c two lanes at a time (f32x2), then exp2 per lane; with
+    // |M| near the top of the fp32 range -M * log2 e would overflow, so there
+    // x - M is taken first (a difference that overflows is -inf and gives 0)
+    const bool huge = !(fabsf(M) < 1e38f);
+    const float c = huge ? P::SCALE_LOG2 : __fmaf_rn(-M, L2E_HI, P::SCALE_LOG2);
+    const float msub = huge ? M : 0.0f;
+    const unsigned long long k2 = pk(L2E_HI, L2E_HI), c2 = pk(c, c);
 #pragma unroll
-    for (int j = 0; j < VPT; ++j)
+    for (int j = 0; j < VPT; ++j) {
+      if (huge) {
 #pragma unroll
-      for (int i = 0; i < V; ++i)
-        v[j][i] = ex2_ftz(__fmaf_rn(__fsub_rn(v[j][i], M), L2E_HI, P::SCALE_LOG2));
+        for (int i = 0; i < V; ++i) v[j][i] = __fsub_rn(v[j][i], msub);
+      }
+#pragma unroll
+      for (int i = 0; i < V; i += 2) {
+        const unsigned long long u = fma2(pk(v[j][i], v[j][i + 1]), k2, c2);
+        v[j][i] = ex2_ftz(pk_lo(u));
+        v[j][i + 1] = ex2_ftz(pk_hi(u));
+      }
+    }
+    // pairwise sums, two partial sums at a time
+    unsigned long long acc = pk(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      unsigned long long q[V / 2];
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) q[i] = pk(v[j][2 * i], v[j][2 * i + 1]);
+#pragma unroll
+      for (int w = V / 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) q[i] = add2(q[i], q[i + w]);
+      acc = add2(acc, q[0]);
+    }
+    return __fadd_rn(pk_lo(acc), pk_hi(acc));
   }
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
@@ -133,8 +154,13 @@ __device__ __forceinline__ void store_row(OutT* yr, int G, int g, int ncols, int
       const int e0 = (j * G + g) * V;
       if (e0 < ncols) {
         float p[V];
+        const unsigned long long r2 = pk(rD, rD);
 #pragma unroll
-        for (int i = 0; i < V; ++i) p[i] = __fmul_rn(v[j][i], rD);
+        for (int i = 0; i < V; i += 2) {
+          const unsigned long long q = mul2(pk(v[j][i], v[j][i + 1]), r2);
+          p[i] = pk_lo(q);
+          p[i + 1] = pk_hi(q);
+        }
         store_vec<OutT, V>(yr + e0, p);
       }
     }

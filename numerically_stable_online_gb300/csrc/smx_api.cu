@@ -40,6 +40,7 @@ std::atomic<int64_t> g_wait_limit{0};
 std::atomic<int> g_regs_threads{0};
 std::atomic<int> g_regs_vpt{0};
 std::atomic<int> g_stream_depth{0};
+std::atomic<int> g_stream_ctas_per_sm{0};
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
@@ -175,8 +176,13 @@ int stream_occupancy(int in_dtype, int vpt, int threads, int depth) {
 
 // Streamed path for rows of at most 32 KiB: the CTA shape of the register path
 // (threads per row, vectors per thread; at least two warps), two rows
-// prefetched per CTA, and as many persistent CTAs as are resident on all SMs.
-bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
+// prefetched per CTA, and enough persistent CTAs per SM to keep about 48 KiB of
+// row reads in flight on every SM (measured on GB300: fewer CTAs starve HBM,
+// more only contend; with lengths given, rows are taken as half valid).
+constexpr int64_t STREAM_INFLIGHT_BYTES = 48 * 1024;
+
+bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
+                 bool has_lengths, Plan* p) {
   const int es = elem_size(in_dtype);
   if (cols * es > STREAM_MAX_ROW_BYTES) return false;
   Plan r;
@@ -188,9 +194,18 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
     while (64LL * r.vpt < nvec) r.vpt <<= 1;
     if (r.vpt * V > (accurate_exp ? 16 : 32)) return false;
   }
-  const int depth = g_stream_depth.load() == 3 ? 3 : 2;
-  const int occ = stream_occupancy(in_dtype, r.vpt, r.threads, depth);
-  if (occ <= 0) return false;
+  const int dd = g_stream_depth.load();
+  const int depth = (dd == 3 || dd == 4) ? dd : 2;
+  const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth);
+  if (occ_max <= 0) return false;
+  int occ = occ_max;
+  int64_t row_read = cols * es;
+  if (has_lengths) row_read = (row_read + 1) / 2;
+  int64_t want = STREAM_INFLIGHT_BYTES / ((int64_t)depth * (row_read > 0 ? row_read : 1));
+  if (want < 1) want = 1;
+  if (want < occ) occ = (int)want;
+  const int forced = g_stream_ctas_per_sm.load();
+  if (forced > 0) occ = forced < occ_max ? forced : occ_max;
   const int64_t ctas = (int64_t)occ * d.sm_count;
   p->path = PATH_STREAM;
   p->threads = r.threads;
@@ -238,7 +253,8 @@ smx_status run(Call& c, DeviceInfo& dev) {
       planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     } else if (force != PATH_GENERIC) {
       const bool acc = c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32;
-      if (force != PATH_REGS) planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, &p);
+      if (force != PATH_REGS)
+        planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, &p);
       if (!planned) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       if (!planned) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     }
@@ -395,6 +411,8 @@ void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls); }
 int smx_debug_last_path(void) { return t_last_path; }
 
 void smx_debug_set_stream_depth(int depth) { g_stream_depth.store(depth > 0 ? depth : 0); }
+
+void smx_debug_set_stream_ctas(int per_sm) { g_stream_ctas_per_sm.store(per_sm > 0 ? per_sm : 0); }
 
 void smx_debug_set_regs_shape(int threads, int vpt) {
   g_regs_threads.store(threads > 0 ? threads : 0);

@@ -132,10 +132,12 @@ __device__ __forceinline__ MD md_merge(MD a, MD b) {
 // ---------------------------------------------------------------------------
 // Warp reductions (butterfly over all 32 lanes, every lane gets the result).
 // ---------------------------------------------------------------------------
+// One instruction on sm_100-family GPUs: the warp's NaN-propagating maximum
+// delivered to every lane.
 __device__ __forceinline__ float warp_max_nan(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
+  float r;
+  asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -154,6 +156,42 @@ __device__ __forceinline__ MD warp_merge(MD v) {
   v.m = __shfl_sync(0xffffffffu, v.m, 0);
   v.d = __shfl_sync(0xffffffffu, v.d, 0);
   return v;
+}
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (one f32x2 instruction for two lanes' worth of arithmetic;
+// each half is rounded exactly as the scalar operation would be).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long pk(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float pk_lo(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float pk_hi(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // ---------------------------------------------------------------------------
