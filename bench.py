@@ -43,11 +43,11 @@ METRIC = "softmax GB/s (read+write) and rows/s on 1 GB300; % of HBM peak"
 UNIT = "GB/s"
 L2_BYTES = 129 * 10 ** 6
 LAUNCH_SAMPLE = 8
-PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4}
+PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4, "split": 5}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_regs.cuh",
-                  "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh", "launch_impl.cuh",
-                  "smx_api.cu"]
+                  "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
+                  "launch_impl.cuh", "smx_api.cu"]
 
 
 # ---------------------------------------------------------------------------

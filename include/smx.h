@@ -33,8 +33,11 @@
  * fp32 even when the inputs are not"); the output type is chosen separately.
  *
  * Memory and ownership: every data pointer is a device pointer owned by the
- * caller; the library never frees or retains it.  The library allocates no
- * memory per call; it allocates one device status word per device on first use.
+ * caller; the library never frees or retains it.  It allocates one device
+ * status word per device on first use, and the long-row path (rows too long for
+ * one CTA) takes a small stream-ordered scratch allocation per call for its
+ * chunk summaries (cudaMallocAsync / cudaFreeAsync on `stream`: 8 bytes per
+ * 16 KiB chunk of an L2-sized slab of rows).  No other call allocates.
  * Every call is asynchronous on `stream` (NULL is the legacy default stream) and
  * returns after enqueueing its kernels.
  *
@@ -132,8 +135,9 @@ int smx_version(void);
  *
  * smx_debug_force_path(p): 0 = automatic choice; 1 = register-resident rows;
  *   2 = thread-block-cluster rows; 3 = generic (scalar, two-pass) rows;
- *   4 = persistent rows with the next rows prefetched (cp.async).  A forced
- *   path that cannot run the shape falls back to the automatic choice.
+ *   4 = persistent rows with the next rows prefetched (cp.async); 5 = long
+ *   rows in L2-sized slabs (chunk summaries, then merge and normalise).  A
+ *   forced path that cannot run the shape falls back to the automatic choice.
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
  * smx_debug_set_wait_limit(n): n > 0: polls of a staging barrier (path 2)
@@ -141,7 +145,7 @@ int smx_version(void);
  *   each CTA of path 2 first waits -n polls on a barrier that nothing signals,
  *   records SMX_ERR_TIMEOUT when that wait runs out (it always does), then
  *   works normally -- a deterministic probe of the error path.
- * smx_debug_last_path(): the path (1..4) the last softmax/stats call on this
+ * smx_debug_last_path(): the path (1..5) the last softmax/stats call on this
  *   thread used, 0 if none.
  * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of
  *   `threads` threads per row (32 = one warp per row, path 1 only) holding `vpt`
@@ -149,7 +153,14 @@ int smx_version(void);
  * smx_debug_set_stream_depth(n): rows prefetched per CTA on path 4 (2, 3 or
  *   4; 0 = automatic).
  * smx_debug_set_stream_ctas(n): n resident CTAs per SM on path 4, at most as
- *   many as fit (0 = automatic).
+ *   many as fit (0 = automatic; also path 5).
+ * smx_debug_set_split_slab(bytes): slab size of path 5 (0 = half the L2).
+ * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
+ *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
+ *   first; -1 = automatic (1 and 2).
+ * smx_debug_set_cluster_staging(m): how path 2 stages its shared-memory part:
+ *   1 = bulk asynchronous copies (TMA) with one mbarrier per piece, 2 = per-
+ *   thread cp.async; 0 = automatic.
  */
 void smx_debug_force_path(int path);
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes);
@@ -158,6 +169,9 @@ int smx_debug_last_path(void);
 void smx_debug_set_regs_shape(int threads, int vpt);
 void smx_debug_set_stream_depth(int depth);
 void smx_debug_set_stream_ctas(int per_sm);
+void smx_debug_set_cluster_staging(int mode);
+void smx_debug_set_split_slab(int64_t bytes);
+void smx_debug_set_split_hints(int stats, int apply);
 
 #ifdef __cplusplus
 }

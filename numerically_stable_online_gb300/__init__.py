@@ -81,6 +81,12 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_stream_depth.restype = None
         lib.smx_debug_set_stream_ctas.argtypes = [I32]
         lib.smx_debug_set_stream_ctas.restype = None
+        lib.smx_debug_set_cluster_staging.argtypes = [I32]
+        lib.smx_debug_set_cluster_staging.restype = None
+        lib.smx_debug_set_split_slab.argtypes = [I64]
+        lib.smx_debug_set_split_slab.restype = None
+        lib.smx_debug_set_split_hints.argtypes = [I32, I32]
+        lib.smx_debug_set_split_hints.restype = None
         _lib = lib
         return lib
 

@@ -9,4 +9,5 @@ int cluster_capacity_bf16(int cluster, int64_t smem_bytes) {
 int stream_occupancy_bf16(int vpt, int threads, int depth) {
   return stream_occupancy<__nv_bfloat16>(vpt, threads, depth);
 }
+int split_occupancy_bf16(int threads) { return split_occupancy<__nv_bfloat16>(threads); }
 }  // namespace smx

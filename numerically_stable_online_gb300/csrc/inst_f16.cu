@@ -9,4 +9,5 @@ int cluster_capacity_f16(int cluster, int64_t smem_bytes) {
 int stream_occupancy_f16(int vpt, int threads, int depth) {
   return stream_occupancy<__half>(vpt, threads, depth);
 }
+int split_occupancy_f16(int threads) { return split_occupancy<__half>(threads); }
 }  // namespace smx

@@ -9,4 +9,5 @@ int cluster_capacity_f32(int cluster, int64_t smem_bytes) {
 int stream_occupancy_f32(int vpt, int threads, int depth) {
   return stream_occupancy<float>(vpt, threads, depth);
 }
+int split_occupancy_f32(int threads) { return split_occupancy<float>(threads); }
 }  // namespace smx

@@ -71,49 +71,6 @@ __device__ __forceinline__ void mask_tail(float (&f)[V], int64_t e0, int64_t L) 
     if (e0 + i >= L) f[i] = neg_inf();
 }
 
-// One element's output on the normalise pass: e^(x - M) / D.  fp32 outputs use
-// the compensated exponential; 16-bit outputs one FFMA with the per-row
-// constant c2 = RN(-M log2 e + s) and rD2 = 2^(-s + c2_err) / D, where c2_err is
-// the exact rounding residual of c2 (s = 8 for bf16 keeps its subnormals, as in
-// row_core.cuh).  Here D comes from other CTAs' sums, so the rounding of c2
-// does not cancel and is carried explicitly.  With |M| near the top of the
-// fp32 range (huge) the difference is taken first instead.
-struct OutConst {
-  float M, c2, rD, rD2;
-  bool huge;
-};
-
-template <typename OutT>
-__device__ __forceinline__ OutConst make_out_const(float M, float D) {
-  constexpr float SC = ExpPolicy<OutT, MODE_SOFTMAX>::SCALE_LOG2;
-  OutConst k;
-  k.M = M;
-  k.huge = !(fabsf(M) < 1e38f);
-  k.rD = recip_refined(D);
-  k.c2 = SC;
-  float c2_err = 0.0f;
-  if (!k.huge) {
-    const float a = __fmul_rn(-M, L2E_HI);
-    const float e1 = __fmaf_rn(-M, L2E_HI, -a);  // exact residual of the product
-    k.c2 = __fadd_rn(a, SC);
-    const float bb = __fsub_rn(k.c2, a);         // TwoSum(a, SC) residual
-    const float e2 = __fadd_rn(__fsub_rn(a, __fsub_rn(k.c2, bb)), __fsub_rn(SC, bb));
-    c2_err = __fadd_rn(e1, e2);
-  }
-  k.rD2 = __fmul_rn(__fmul_rn(k.rD, SC == 0.0f ? 1.0f : 0.00390625f), __fmaf_rn(c2_err, LN2, 1.0f));
-  return k;
-}
-
-template <typename OutT>
-__device__ __forceinline__ float cluster_out(float x, const OutConst& k) {
-  if constexpr (ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE) {
-    return __fmul_rn(exp_shift_accurate(x, k.M), k.rD);
-  } else {
-    const float u = k.huge ? __fmaf_rn(__fsub_rn(x, k.M), L2E_HI, k.c2) : __fmaf_rn(x, L2E_HI, k.c2);
-    return __fmul_rn(ex2_ftz(u), k.rD2);
-  }
-}
-
 // Unpack one staged vector; only the vector holding the end of the valid
 // prefix needs masking.
 template <typename InT, int V>
@@ -123,7 +80,27 @@ __device__ __forceinline__ void staged_vec(const InT* sx, int vi, int v_nv_full,
   if (vi >= v_nv_full) mask_tail<V>(f, e0, L);
 }
 
-template <typename InT, typename OutT, int RV, int MODE>
+// cp.async.wait_group with a run-time count (0..7).
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
+}
+
+// Staging of the shared-memory part.  TMA: thread 0 issues one bulk copy per
+// piece and every thread waits on the piece's mbarrier.  Otherwise every thread
+// copies its own vectors of the piece with cp.async (one commit group per
+// piece) and waits on its own groups; every pass visits the staged region with
+// the same thread-to-vector map (piece p, vectors p*P + t + k*T), so a thread
+// only ever reads what it staged itself and the stage needs no barrier.
+template <typename InT, typename OutT, int RV, int MODE, bool TMA>
 __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     k_rows_cluster(const InT* __restrict__ x, OutT* __restrict__ y, float* __restrict__ m_out,
                    float* __restrict__ d_out, int64_t rows, int64_t cols,
@@ -131,12 +108,19 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
                    int64_t max_polls, int* __restrict__ status) {
   constexpr int V = Elem<InT>::V;
   constexpr int NP = CLUSTER_PIECES;
+  // fp32 in and out: the sum pass computes the compensated e^(x - m_c) once and
+  // keeps it (in place of x in shared memory, and in the register part); the
+  // normalise pass is then one multiply by e^(m_c - M) / D
+  constexpr bool KEEP_E = ExpPolicy<OutT, MODE>::ACCURATE && std::is_same<InT, float>::value;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const InT* sx = reinterpret_cast<const InT*>(smem_raw);
+  float* se = reinterpret_cast<float*>(smem_raw);  // the kept exponentials (KEEP_E)
   __shared__ __align__(8) uint64_t bars[NP];
   __shared__ __align__(8) uint64_t never_bar;  // the error-path probe: nothing signals it
   __shared__ float s_m[32], s_d[32];
-  __shared__ float s_cta[2][2];  // this CTA's (m, d) per row parity, read by the peers
+  // every CTA's (m, d) for the row, pushed here by its owner; two slots by row
+  // parity (see the exchange below)
+  __shared__ float s_all[2][16][2];
 
   const int T = CLUSTER_THREADS;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -162,17 +146,48 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     if (vend > c1) vend = c1;
     return vend > c0 ? (int)((vend - c0) / V) : 0;
   };
-  // thread 0: issue the valid part of staged piece p of `row` (one phase of bars[p])
+  auto piece_end = [&](int p, int lim) { return (p + 1) * P < lim ? (p + 1) * P : lim; };
+  // stage the valid part of piece p of `row` (s_nv staged-and-valid vectors)
   auto fill_piece = [&](int64_t row, int s_nv, int p) {
-    const int p0 = p * P;
-    int p1 = p0 + P < s_nv ? p0 + P : s_nv;
-    if (p1 > p0) {
-      const uint32_t bytes = (uint32_t)(p1 - p0) * 16u;
-      mbar_arrive_expect_tx(smem_addr(&bars[p]), bytes);
-      bulk_load_g2s(smem_addr(smem_raw + (size_t)p0 * 16), x + row * cols + c0 + (int64_t)p0 * V, bytes,
-                    smem_addr(&bars[p]));
+    const InT* src = x + row * cols + c0;
+    if constexpr (TMA) {
+      if (t != 0) return;
+      // order this CTA's earlier generic-proxy accesses of the piece (reads,
+      // and the kept exponentials' writes) before the copy's async-proxy writes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const int p0 = p * P, p1 = piece_end(p, s_nv);
+      if (p1 > p0) {
+        const uint32_t bytes = (uint32_t)(p1 - p0) * 16u;
+        mbar_arrive_expect_tx(smem_addr(&bars[p]), bytes);
+        bulk_load_g2s(smem_addr(smem_raw + (size_t)p0 * 16), src + (int64_t)p0 * V, bytes,
+                      smem_addr(&bars[p]));
+      } else {
+        mbar_arrive(smem_addr(&bars[p]));
+      }
     } else {
-      mbar_arrive(smem_addr(&bars[p]));
+      const int p1 = piece_end(p, s_nv);
+      for (int vi = p * P + t; vi < p1; vi += T)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_raw + (size_t)vi * 16)),
+                     "l"(src + (int64_t)vi * V)
+                     : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+  };
+  auto load_regs = [&](int64_t row, float (&r)[RV][V]) {
+    const int64_t L = length_of(row);
+    const int v_nv = valid_vectors(L);
+    const int v_full = (int)((L > c0 ? (L - c0) : 0) / V);
+    const InT* src = x + row * cols + c0;
+#pragma unroll
+    for (int k = 0; k < RV; ++k) {
+      const int vi = a_nv + k * T + t;
+      if (vi < b_nv && vi < v_nv) {
+        load_vec16<InT>(src + (int64_t)vi * V, r[k]);
+        if (vi >= v_full) mask_tail<V>(r[k], c0 + (int64_t)vi * V, L);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) r[k][i] = neg_inf();
+      }
     }
   };
 
@@ -185,12 +200,14 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     // polls on a barrier nothing arrives on, which must run out and be reported
     if (max_polls < 0 && !mbar_wait_bounded(smem_addr(&never_bar), 0, -max_polls))
       atomicOr(status, DEV_TIMEOUT);
-    if (row_first < rows) {
-      const int s_nv0 = min(a_nv, valid_vectors(length_of(row_first)));
-      for (int p = 0; p < NP; ++p) fill_piece(row_first, s_nv0, p);
-    }
   }
   __syncthreads();
+  float r[RV][V];
+  if (row_first < rows) {
+    const int s_nv0 = min(a_nv, valid_vectors(length_of(row_first)));
+    for (int p = 0; p < NP; ++p) fill_piece(row_first, s_nv0, p);
+    load_regs(row_first, r);
+  }
 
   if (max_polls < 0) max_polls = int64_t(1) << 21;
   bool timed_out = false;
@@ -202,30 +219,19 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     const int s_nv = a_nv < v_nv ? a_nv : v_nv;               // staged and valid
     const InT* xr = x + row * cols + c0;
     const int64_t next_row = row + gridDim.y;
-    int next_s_nv = 0;
-    if (t == 0 && next_row < rows) next_s_nv = min(a_nv, valid_vectors(length_of(next_row)));
-
-    // Register part: vector a_nv + k*T + t of the chunk.
-    float r[RV][V];
-#pragma unroll
-    for (int k = 0; k < RV; ++k) {
-      const int vi = a_nv + k * T + t;
-      if (vi < b_nv && vi < v_nv) {
-        load_vec16<InT>(xr + (int64_t)vi * V, r[k]);
-        if (vi >= v_full) mask_tail<V>(r[k], c0 + (int64_t)vi * V, L);
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) r[k][i] = neg_inf();
-      }
-    }
+    const int next_s_nv = next_row < rows ? min(a_nv, valid_vectors(length_of(next_row))) : 0;
 
     // Pass 1a: exact maximum of the on-chip part, pieces processed as they land.
     float mx = neg_inf();
     for (int p = 0; p < NP; ++p) {
-      // after one wait has run out, later waits get a single poll each
-      if (!mbar_wait_bounded(smem_addr(&bars[p]), (uint32_t)par, timed_out ? 1 : max_polls))
-        timed_out = true;
-      const int p1 = (p + 1) * P < s_nv ? (p + 1) * P : s_nv;
+      if constexpr (TMA) {
+        // after one wait has run out, later waits get a single poll each
+        if (!mbar_wait_bounded(smem_addr(&bars[p]), (uint32_t)par, timed_out ? 1 : max_polls))
+          timed_out = true;
+      } else {
+        cp_async_wait_dyn(NP - 1 - p);  // this thread's copies of pieces 0..p have landed
+      }
+      const int p1 = piece_end(p, s_nv);
       for (int vi = p * P + t; vi < p1; vi += T) {
         float f[V];
         staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
@@ -242,17 +248,33 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     __syncthreads();
     const float m_c = warp_max_nan(lane < (T >> 5) ? s_m[lane] : neg_inf());
 
-    // Pass 1b: sum of e^(x - m_c) over the on-chip part: one FFMA + exp2 per
-    // element; the rounding of c = -m_c log2 e, common to every term, is
-    // corrected once (stats_correct).
+    // Pass 1b: sum of e^(x - m_c) over the on-chip part.
     float sum = 0.0f;
-    if (m_c != neg_inf()) {
+    if (KEEP_E && m_c != neg_inf()) {
+      for (int p = 0; p < NP; ++p) {
+        const int p1 = piece_end(p, s_nv);
+        for (int vi = p * P + t; vi < p1; vi += T) {
+          float f[V];
+          staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
+#pragma unroll
+          for (int i = 0; i < V; ++i) f[i] = exp_shift_accurate(f[i], m_c);
+          *reinterpret_cast<float4*>(se + (int64_t)vi * V) = make_float4(f[0], f[1], f[2], f[3]);
+          sum = __fadd_rn(sum, __fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < RV; ++k) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) r[k][i] = exp_shift_accurate(r[k][i], m_c);
+        sum = __fadd_rn(sum, __fadd_rn(__fadd_rn(r[k][0], r[k][1]), __fadd_rn(r[k][2], r[k][3])));
+      }
+    } else if (m_c != neg_inf()) {
+      // one FFMA + exp2 per element; the rounding of c = -m_c log2 e, common to
+      // every term, is corrected once (stats_correct)
       const bool huge = !(fabsf(m_c) < 1e38f);
       const float c = huge ? 0.0f : __fmul_rn(-m_c, L2E_HI);
       const float msub = huge ? m_c : 0.0f;
-      for (int vi = t; vi < s_nv; vi += T) {
-        float f[V];
-        staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
+      auto add_terms = [&](const float (&f)[V]) {
         float e[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) e[i] = ex2_ftz(__fmaf_rn(__fsub_rn(f[i], msub), L2E_HI, c));
@@ -261,18 +283,17 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) e[i] = __fadd_rn(e[i], e[i + w]);
         sum = __fadd_rn(sum, e[0]);
+      };
+      for (int p = 0; p < NP; ++p) {
+        const int p1 = piece_end(p, s_nv);
+        for (int vi = p * P + t; vi < p1; vi += T) {
+          float f[V];
+          staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
+          add_terms(f);
+        }
       }
 #pragma unroll
-      for (int k = 0; k < RV; ++k) {
-        float e[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) e[i] = ex2_ftz(__fmaf_rn(__fsub_rn(r[k][i], msub), L2E_HI, c));
-#pragma unroll
-        for (int w = V / 2; w > 0; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) e[i] = __fadd_rn(e[i], e[i + w]);
-        sum = __fadd_rn(sum, e[0]);
-      }
+      for (int k = 0; k < RV; ++k) add_terms(r[k]);
       sum = stats_correct(sum, m_c);
     }
     // Streamed remainder, first read: the per-thread tiled online update.
@@ -283,35 +304,46 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
       if (vi >= v_full) mask_tail<V>(f, c0 + (int64_t)vi * V, L);
       online_fold<V>(m_s, d_s, f);
     }
-    MD md = md_merge(MD{m_c, sum}, MD{m_s, d_s});
-
-    // CTA summary: warp butterfly, then the per-warp summaries.
-    md = warp_merge(md);
-    __syncthreads();  // s_m is reused
-    if (lane == 0) {
-      s_m[warp] = md.m;
-      s_d[warp] = md.d;
+    // CTA summary.  Every thread's on-chip sum is relative to the same m_c, so
+    // without a streamed remainder the summary is (m_c, plain sum); with one,
+    // the threads' (m, d) pairs are merged.
+    MD md;
+    if (b_nv >= v_nv) {
+      float ssum = warp_sum(sum);
+      __syncthreads();  // s_m is reused
+      if (lane == 0) s_d[warp] = ssum;
+      __syncthreads();
+      md = MD{m_c, warp_sum(lane < (T >> 5) ? s_d[lane] : 0.0f)};
+    } else {
+      md = warp_merge(md_merge(MD{m_c, sum}, MD{m_s, d_s}));
+      __syncthreads();  // s_m is reused
+      if (lane == 0) {
+        s_m[warp] = md.m;
+        s_d[warp] = md.d;
+      }
+      __syncthreads();
+      md = warp_merge(lane < (T >> 5) ? MD{s_m[lane], s_d[lane]} : MD{neg_inf(), 0.0f});
     }
-    __syncthreads();
-    md = warp_merge(lane < (T >> 5) ? MD{s_m[lane], s_d[lane]} : MD{neg_inf(), 0.0f});
-    if (t == 0) {
-      s_cta[par][0] = md.m;
-      s_cta[par][1] = md.d;
+    // push this CTA's summary into slot [par][crank] of every CTA of the cluster
+    if (warp == 0 && lane < (int)csize) {
+      st_peer_f32(&s_all[par][crank][0], lane, md.m);
+      st_peer_f32(&s_all[par][crank][1], lane, md.d);
     }
     if constexpr (MODE == MODE_STATS) {
       // all staged reads are done (the barriers above): refill every piece now
-      if (t == 0 && next_row < rows && !timed_out)
+      if (next_row < rows && !timed_out)
         for (int p = 0; p < NP; ++p) fill_piece(next_row, next_s_nv, p);
     }
-    // Exchange through distributed shared memory.  The summaries alternate
-    // between two slots by row parity: a peer reads slot par of this row
-    // before it reaches the next row's barrier, and this CTA rewrites slot par
-    // only two rows later, after that barrier.
+    // Exchange through distributed shared memory: the pushes above, then one
+    // cluster barrier (release/acquire) makes every summary visible locally.
+    // The slots alternate by row parity: slot par of every CTA is read before
+    // that CTA reaches the next row's barrier, and is written again only two
+    // rows later, after that barrier.
     __syncwarp();
     cluster_arrive();
     cluster_wait();
     MD all{neg_inf(), 0.0f};
-    if (lane < (int)csize) all = MD{ld_peer_f32(&s_cta[par][0], lane), ld_peer_f32(&s_cta[par][1], lane)};
+    if (lane < (int)csize) all = MD{s_all[par][lane][0], s_all[par][lane][1]};
     all = warp_merge(all);  // rank order, identical bits in every lane
 
     const float M = all.m, D = all.d;
@@ -320,16 +352,27 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
         m_out[row] = M;
         d_out[row] = M == neg_inf() ? 0.0f : D;
       }
+      if (next_row < rows) load_regs(next_row, r);
     } else {
       OutT* yr = y + row * cols + c0;
       const bool zero_row = (M == neg_inf());
       const bool nan_row = !zero_row && (D != D);
       const OutConst kc = make_out_const<OutT>(M, D);
-      auto emit = [&](int vi, const float (&f)[V], bool valid_vec) {
+      // KEEP_E: e^(m_c - M) / D, the one factor between a kept e and y
+      const float scale_c = (m_c == neg_inf() || zero_row || nan_row)
+                                ? 0.0f
+                                : __fmul_rn(rescale_factor(m_c, M), kc.rD);
+      // f holds kept exponentials (is_e: the on-chip part with KEEP_E) or inputs
+      auto emit = [&](int vi, const float (&f)[V], bool valid_vec, bool is_e) {
         float pv[V];
         if (!zero_row && !nan_row) {
+          if (KEEP_E && is_e) {
 #pragma unroll
-          for (int i = 0; i < V; ++i) pv[i] = valid_vec ? cluster_out<OutT>(f[i], kc) : 0.0f;
+            for (int i = 0; i < V; ++i) pv[i] = valid_vec ? __fmul_rn(f[i], scale_c) : 0.0f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) pv[i] = valid_vec ? out_value<OutT>(f[i], kc) : 0.0f;
+          }
         } else {
           const int64_t e0 = c0 + (int64_t)vi * V;
 #pragma unroll
@@ -338,23 +381,32 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
         store_vec<OutT, V>(yr + (int64_t)vi * V, pv);
       };
       for (int p = 0; p < NP; ++p) {
-        const int p0 = p * P, p1 = (p + 1) * P < a_nv ? (p + 1) * P : a_nv;
-        for (int vi = p0 + t; vi < p1; vi += T) {
+        const int p1 = piece_end(p, a_nv);
+        for (int vi = p * P + t; vi < p1; vi += T) {
           float f[V];
           const bool valid_vec = vi < s_nv;
-          if (valid_vec) staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
-          emit(vi, f, valid_vec);
+          if (valid_vec) {
+            if constexpr (KEEP_E) {
+              const float4 e4 = *reinterpret_cast<const float4*>(se + (int64_t)vi * V);
+              f[0] = e4.x; f[1] = e4.y; f[2] = e4.z; f[3] = e4.w;
+            } else {
+              staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
+            }
+          }
+          emit(vi, f, valid_vec, true);
         }
-        __syncthreads();  // piece p is consumed: refill it with the next row
-        // (not after a wait of thread 0 ran out: that barrier's phase may
-        // still be pending, and a second arrive on it is not allowed)
-        if (t == 0 && next_row < rows && !timed_out) fill_piece(next_row, next_s_nv, p);
+        // piece p is consumed: refill it with the next row (TMA: after every
+        // thread is done with it; a wait of thread 0 that ran out leaves that
+        // barrier's phase pending, and a second arrive on it is not allowed)
+        if constexpr (TMA) __syncthreads();
+        if (next_row < rows && !timed_out) fill_piece(next_row, next_s_nv, p);
       }
 #pragma unroll
       for (int k = 0; k < RV; ++k) {
         const int vi = a_nv + k * T + t;
-        if (vi < b_nv) emit(vi, r[k], true);
+        if (vi < b_nv) emit(vi, r[k], vi < v_nv, true);
       }
+      if (next_row < rows) load_regs(next_row, r);  // in flight while the remainder is written
       for (int vi = b_nv + t; vi < c_nv; vi += T) {  // streamed remainder, second read
         float f[V];
         const bool valid_vec = vi < v_nv;
@@ -362,16 +414,20 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
           load_vec16<InT>(xr + (int64_t)vi * V, f);
           if (vi >= v_full) mask_tail<V>(f, c0 + (int64_t)vi * V, L);
         }
-        emit(vi, f, valid_vec);
+        emit(vi, f, valid_vec, false);
       }
     }
   }
 
-  if (timed_out) {
-    atomicOr(status, DEV_TIMEOUT);
-    // let this CTA's own copies land before its shared memory is released
-    const int last = rows > row_first ? (int)(((rows - 1 - row_first) / gridDim.y) & 1) : 0;
-    for (int p = 0; p < NP; ++p) mbar_wait_bounded(smem_addr(&bars[p]), (uint32_t)last, int64_t(1) << 21);
+  if constexpr (TMA) {
+    if (timed_out) {
+      atomicOr(status, DEV_TIMEOUT);
+      // let this CTA's own copies land before its shared memory is released
+      const int last = rows > row_first ? (int)(((rows - 1 - row_first) / gridDim.y) & 1) : 0;
+      for (int p = 0; p < NP; ++p) mbar_wait_bounded(smem_addr(&bars[p]), (uint32_t)last, int64_t(1) << 21);
+    }
+  } else {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   }
   // no CTA leaves while a peer may still read its last summary
   __syncwarp();

@@ -1,29 +1,71 @@
-// Persistent row softmax that keeps the next rows' reads in flight while it
-// reduces the current one; rows of up to 32 KiB.
+// Persistent row softmax that keeps the next items' reads in flight while it
+// reduces the current one.
 //
-// Same arithmetic as the register-resident kernel (kernel_regs.cuh, via
-// row_core.cuh): exact row maximum, exponentials against it with their fp32
-// sum, one normalising multiply; one HBM read and one HBM write per element.
-// The register kernel's CTA holds no reads in flight while it reduces its row;
-// here a persistent CTA of G threads walks the rows blockIdx.x,
-// blockIdx.x + gridDim.x, ... and every thread prefetches its own 16-byte
-// vectors of the next DEPTH rows into its own shared-memory words with
-// cp.async (one commit group per row).  Each thread reads back only what it
-// copied itself, so the prefetch needs no barrier; a row's group is awaited
-// with cp.async.wait_group just before the row is used.
+// An item is a whole row (rows of up to 32 KiB), or one chunk of a long row.
+// The arithmetic is the register-resident kernel's (kernel_regs.cuh, via
+// row_core.cuh): exact maximum, exponentials against it with their fp32 sum,
+// one normalising multiply; one HBM read and one HBM write per element.  The
+// register kernel's CTA holds no reads in flight while it reduces its row;
+// here a persistent CTA of G threads walks its items and every thread
+// prefetches its own 16-byte vectors of the next DEPTH items into its own
+// shared-memory words with cp.async (one commit group per item).  Each thread
+// reads back only what it copied itself, so the prefetch needs no barrier; an
+// item's group is awaited with cp.async.wait_group just before the item is used.
+//
+// Whole rows (CHUNKED = false) are dealt round robin: CTA b takes rows
+// b, b + gridDim.x, ...  Chunks (CHUNKED = true) are dealt in contiguous runs:
+// CTA b takes items [b n / gridDim.x, (b + 1) n / gridDim.x), so a CTA meets
+// each of its rows in consecutive items.
+//
+// Modes (the same walk):
+//   MODE_SOFTMAX  whole rows: y = e^(x - m) / d.
+//   MODE_STATS    the (m, d) block summary of each item ("Stable softmax: keep
+//                 the normalizer consistent as tiles arrive", third paragraph),
+//                 at m_out[k], d_out[k] (k counted from the launch's first item;
+//                 for whole rows, the row - row0).
+//   MODE_APPLY    chunks only: merge the row's chunk summaries m_in, d_in
+//                 ("Online stable softmax", "Derive the update for two blocks";
+//                 once per row a CTA meets) and normalise the chunk with the
+//                 merged (M, D) -- the step that completes a softmax whose
+//                 summaries were computed apart.
 #pragma once
 
 #include "row_core.cuh"
 
 namespace smx {
 
+enum : int { MODE_APPLY = 2 };
+
+// The items of one launch: item k is chunk k % nchunks of row row0 + k / nchunks.
+struct Items {
+  int64_t n;     // items in the launch
+  int64_t row0;  // first row
+  int64_t cols;  // row length
+  int chunk;     // elements per item (a multiple of the vector width; a row's last item may be shorter)
+  int nchunks;   // items per row (1: whole rows)
+  int l2_hint;   // chunked reads only: 0 none, 1 keep in L2 (evict_last), 2 evict_first
+};
+
 __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async16_hint(uint32_t smem_dst, const void* gsrc, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_dst),
+               "l"(gsrc), "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+  uint64_t p = 0;
+  if (hint == 1)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // SMX_STREAM_MAXNREG (a build-time tuning knob) caps the registers per thread,
@@ -34,51 +76,110 @@ __device__ __forceinline__ void cp_async_wait() {
 #define SMX_STREAM_REGS __launch_bounds__(1024)
 #endif
 
-template <typename InT, typename OutT, int VPT, int MODE, int DEPTH>
+template <typename InT, typename OutT, int VPT, int MODE, int DEPTH, bool CHUNKED>
 __global__ void SMX_STREAM_REGS
     k_rows_stream(const InT* __restrict__ x, OutT* __restrict__ y, float* __restrict__ m_out,
-                  float* __restrict__ d_out, int64_t rows, int64_t cols,
-                  const int32_t* __restrict__ valid_len) {
+                  float* __restrict__ d_out, const float* __restrict__ m_in,
+                  const float* __restrict__ d_in, Items it, const int32_t* __restrict__ valid_len) {
+  static_assert(CHUNKED || MODE != MODE_APPLY, "the apply mode walks chunks");
   constexpr int V = Elem<InT>::V;
   extern __shared__ __align__(16) uint4 sbuf[];  // [DEPTH][VPT][G]: thread g owns column g
-  // s_max alternates between rows: a row with no valid lane skips the sum's
-  // barrier, so only the next row's max barrier separates reads from rewrites
-  __shared__ float s_max[2][32], s_sum[32];
+  // s_max alternates between items: an item with no valid lane skips the sum's
+  // barrier, so only the next item's max barrier separates reads from rewrites
+  // (s_mm, s_dd alternate between row merges for the same reason)
+  __shared__ float s_max[2][32], s_sum[32], s_mm[2][32], s_dd[2][32];
 
   const int G = blockDim.x, g = threadIdx.x, lane = g & 31, warp = g >> 5, nw = G >> 5;
-  const int ncols = (int)cols;
   const uint32_t my_slot = static_cast<uint32_t>(__cvta_generic_to_shared(sbuf + g));
   const uint32_t slot_stride = (uint32_t)(VPT * G * 16);  // bytes between ring slots
+  const int ncols = (int)(CHUNKED ? it.chunk : it.cols);
 
-  auto length_of = [&](int64_t row) {
-    if (valid_len == nullptr) return ncols;
-    const int v = __ldg(valid_len + row);
-    return v < 0 ? 0 : (v > ncols ? ncols : v);
+  // An item's place: k, its row r (from row0) and chunk c.  Two cursors walk
+  // the CTA's items without dividing: `cur` at the item being reduced, `pf`
+  // DEPTH items ahead at the next one to prefetch.
+  struct Cursor {
+    int64_t k, r;
+    int c;
   };
-  // copy this thread's vectors of `row` into ring slot d; always one group
-  auto prefetch = [&](int64_t row, int d) {
-    int L = 0;
-    if (row < rows) {
-      L = length_of(row);
-      const InT* xr = x + row * cols;
+  int64_t k_end;
+  Cursor cur;
+  if constexpr (CHUNKED) {
+    const int64_t kb = (int64_t)blockIdx.x * it.n / gridDim.x;
+    k_end = (int64_t)(blockIdx.x + 1) * it.n / gridDim.x;
+    cur = Cursor{kb, kb / it.nchunks, (int)(kb % it.nchunks)};
+  } else {
+    k_end = it.n;
+    cur = Cursor{(int64_t)blockIdx.x, (int64_t)blockIdx.x, 0};
+  }
+  auto advance = [&](Cursor& q) {
+    if constexpr (CHUNKED) {
+      ++q.k;
+      if (++q.c == it.nchunks) {
+        q.c = 0;
+        ++q.r;
+      }
+    } else {
+      q.k += gridDim.x;
+      q.r = q.k;
+    }
+  };
+  // elements of an item, and its share of the row's valid prefix
+  auto item_len = [&](const Cursor& q) -> int {
+    if constexpr (CHUNKED) {
+      const int64_t rest = it.cols - (int64_t)q.c * it.chunk;
+      return rest < it.chunk ? (int)rest : it.chunk;
+    } else {
+      return ncols;
+    }
+  };
+  auto item_valid = [&](const Cursor& q) -> int {
+    const int len = item_len(q);
+    if (valid_len == nullptr) return len;
+    const int64_t v = __ldg(valid_len + it.row0 + q.r);
+    const int64_t L = (v < 0 ? 0 : (v > it.cols ? it.cols : v)) - (int64_t)q.c * ncols;
+    return (int)(L < 0 ? 0 : (L > len ? len : L));
+  };
+  const uint64_t pol = (CHUNKED && it.l2_hint != 0) ? l2_policy(it.l2_hint) : 0;
+  // copy this thread's vectors of item q into ring slot d; always one group
+  auto prefetch = [&](const Cursor& q, int d) -> int {
+    int Lk = 0;
+    if (q.k < k_end) {
+      Lk = item_valid(q);
+      const InT* xr = x + (it.row0 + q.r) * it.cols + (int64_t)q.c * ncols;
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
         const int e0 = (j * G + g) * V;
-        if (e0 < L) cp_async16(my_slot + d * slot_stride + j * G * 16, xr + e0);
+        if (e0 < Lk) {
+          const uint32_t dst = my_slot + d * slot_stride + j * G * 16;
+          if (CHUNKED && it.l2_hint != 0)
+            cp_async16_hint(dst, xr + e0, pol);
+          else
+            cp_async16(dst, xr + e0);
+        }
       }
     }
     cp_async_commit();
-    return L;
+    return Lk;
   };
 
-  int64_t row = blockIdx.x;
+  Cursor pf = cur;
   int Ls[DEPTH];
 #pragma unroll
-  for (int d = 0; d < DEPTH; ++d) Ls[d] = prefetch(row + (int64_t)d * gridDim.x, d);
+  for (int d = 0; d < DEPTH; ++d) {
+    Ls[d] = prefetch(pf, d);
+    advance(pf);
+  }
 
-  for (int d = 0, par = 0; row < rows; row += gridDim.x, par ^= 1) {
-    cp_async_wait<DEPTH - 1>();  // this thread's copies of `row` have landed
+  // the apply mode's merged summary of the row it is in
+  int64_t have_row = -1;
+  MD row_md{neg_inf(), 0.0f};
+  int mpar = 0;
+
+  for (int d = 0, par = 0; cur.k < k_end; advance(cur), par ^= 1) {
+    cp_async_wait<DEPTH - 1>();  // this thread's copies of the item have landed
     const int L = Ls[0];
+    const int len = item_len(cur);
+    const int64_t row = it.row0 + cur.r;
     float v[VPT][V];
     const InT* sx = reinterpret_cast<const InT*>(sbuf + (size_t)d * VPT * G);
 #pragma unroll
@@ -86,37 +187,101 @@ __global__ void SMX_STREAM_REGS
       const int e0 = (j * G + g) * V;
       load_masked<InT, true>(sx + e0, e0, L, v[j]);
     }
-    float mx = warp_max_nan(local_max(v));
-    // the slot's words are in registers now: refill it with the row DEPTH ahead
+    // the slot's words are in registers now: refill it with the item DEPTH ahead
 #pragma unroll
     for (int i = 0; i + 1 < DEPTH; ++i) Ls[i] = Ls[i + 1];
-    Ls[DEPTH - 1] = prefetch(row + (int64_t)DEPTH * gridDim.x, d);
+    Ls[DEPTH - 1] = prefetch(pf, d);
+    advance(pf);
     d = d + 1 == DEPTH ? 0 : d + 1;
 
-    if (lane == 0) s_max[par][warp] = mx;
-    __syncthreads();
-    mx = warp_max_nan(lane < nw ? s_max[par][lane] : neg_inf());
-    const float M = mx;
-    float Dsum = 0.0f;
-    if (M != neg_inf()) {
-      float sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
-      if (lane == 0) s_sum[warp] = sum;
-      __syncthreads();
-      Dsum = warp_sum(lane < nw ? s_sum[lane] : 0.0f);
-    }
-    if constexpr (MODE == MODE_STATS) {
-      if (g == 0) {
-        m_out[row] = M;
-        d_out[row] = M == neg_inf() ? 0.0f : stats_correct(Dsum, M);
+    if constexpr (MODE == MODE_APPLY) {
+      if (cur.r != have_row) {  // uniform: every thread walks the same items
+        MD acc{neg_inf(), 0.0f};
+        const int64_t k0 = cur.r * it.nchunks;
+        for (int i = g; i < it.nchunks; i += G)
+          acc = md_merge(acc, MD{__ldg(m_in + k0 + i), __ldg(d_in + k0 + i)});
+        acc = warp_merge(acc);
+        if (lane == 0) {
+          s_mm[mpar][warp] = acc.m;
+          s_dd[mpar][warp] = acc.d;
+        }
+        __syncthreads();
+        row_md = warp_merge(lane < nw ? MD{s_mm[mpar][lane], s_dd[mpar][lane]} : MD{neg_inf(), 0.0f});
+        mpar ^= 1;
+        have_row = cur.r;
+      }
+      const float M = row_md.m, Dr = row_md.d;
+      const bool zero_row = (M == neg_inf());
+      const bool nan_row = !zero_row && (Dr != Dr);
+      const OutConst kc = make_out_const<OutT>(M, Dr);
+      OutT* yr = y + row * it.cols + (int64_t)cur.c * ncols;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int e0 = (j * G + g) * V;
+        if (e0 < len) {
+          float p[V];
+          if (!zero_row && !nan_row) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) p[i] = out_value<OutT>(v[j][i], kc);
+          } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) p[i] = (nan_row && e0 + i < L) ? qnan() : 0.0f;
+          }
+          store_vec<OutT, V>(yr + e0, p);
+        }
       }
     } else {
-      const bool zero_row = (M == neg_inf());
-      const bool nan_row = !zero_row && (Dsum != Dsum);
-      store_row<OutT, VPT, V>(y + row * cols, G, g, ncols, L, v, zero_row, nan_row,
-                              recip_refined(Dsum));
+      float mx = warp_max_nan(local_max(v));
+      if (lane == 0) s_max[par][warp] = mx;
+      __syncthreads();
+      const float M = warp_max_nan(lane < nw ? s_max[par][lane] : neg_inf());
+      float Dsum = 0.0f;
+      if (M != neg_inf()) {
+        float sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
+        if (lane == 0) s_sum[warp] = sum;
+        __syncthreads();
+        Dsum = warp_sum(lane < nw ? s_sum[lane] : 0.0f);
+      }
+      if constexpr (MODE == MODE_STATS) {
+        if (g == 0) {
+          m_out[cur.k] = M;
+          d_out[cur.k] = M == neg_inf() ? 0.0f : stats_correct(Dsum, M);
+        }
+      } else {
+        const bool zero_row = (M == neg_inf());
+        const bool nan_row = !zero_row && (Dsum != Dsum);
+        store_row<OutT, VPT, V>(y + row * it.cols, G, g, len, L, v, zero_row, nan_row,
+                                recip_refined(Dsum));
+      }
     }
   }
   cp_async_wait<0>();  // no copy may still target this CTA's shared memory at exit
+}
+
+// Row statistics of long rows: merge each row's nchunks chunk summaries
+// (consecutive in m_in, d_in) into (m_out[r], d_out[r]); one CTA per row.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
+    k_merge_chunk_stats(const float* __restrict__ m_in, const float* __restrict__ d_in, int nchunks,
+                        float* __restrict__ m_out, float* __restrict__ d_out) {
+  __shared__ float s_mm[THREADS / 32], s_dd[THREADS / 32];
+  const int g = threadIdx.x, lane = g & 31, warp = g >> 5;
+  const int64_t k0 = (int64_t)blockIdx.x * nchunks;
+  MD acc{neg_inf(), 0.0f};
+  for (int i = g; i < nchunks; i += THREADS) acc = md_merge(acc, MD{m_in[k0 + i], d_in[k0 + i]});
+  acc = warp_merge(acc);
+  if (lane == 0) {
+    s_mm[warp] = acc.m;
+    s_dd[warp] = acc.d;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    acc = warp_merge(lane < THREADS / 32 ? MD{s_mm[lane], s_dd[lane]} : MD{neg_inf(), 0.0f});
+    if (lane == 0) {
+      m_out[blockIdx.x] = acc.m;
+      d_out[blockIdx.x] = acc.m == neg_inf() ? 0.0f : acc.d;
+    }
+  }
 }
 
 }  // namespace smx

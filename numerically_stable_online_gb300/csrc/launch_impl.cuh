@@ -46,9 +46,9 @@ cudaError_t launch_regs_wr(const Call& c, const Plan& p) {
   }
 }
 
-template <typename InT, typename OutT, int MODE>
+template <typename InT, typename OutT, int MODE, bool TMA>
 cudaError_t prepare_cluster_kernel(int64_t smem_bytes) {
-  auto kern = k_rows_cluster<InT, OutT, CLUSTER_RV, MODE>;
+  auto kern = k_rows_cluster<InT, OutT, CLUSTER_RV, MODE, TMA>;
   // per device: the largest dynamic shared memory size set so far
   static int64_t set_bytes[64] = {0};
   int dev = 0;
@@ -65,12 +65,12 @@ cudaError_t prepare_cluster_kernel(int64_t smem_bytes) {
   return cudaSuccess;
 }
 
-template <typename InT, typename OutT, int MODE>
-cudaError_t launch_cluster(const Call& c, const Plan& p) {
+template <typename InT, typename OutT, int MODE, bool TMA>
+cudaError_t launch_cluster_t(const Call& c, const Plan& p) {
   const int64_t smem_bytes = p.smem_elems * (int64_t)sizeof(InT) > 16
                                  ? p.smem_elems * (int64_t)sizeof(InT)
                                  : 16;
-  cudaError_t e = prepare_cluster_kernel<InT, OutT, MODE>(smem_bytes);
+  cudaError_t e = prepare_cluster_kernel<InT, OutT, MODE, TMA>(smem_bytes);
   if (e != cudaSuccess) return e;
   // persistent: p.ctas clusters, each walking its rows
   cudaLaunchConfig_t cfg = {};
@@ -85,21 +85,29 @@ cudaError_t launch_cluster(const Call& c, const Plan& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_rows_cluster<InT, OutT, CLUSTER_RV, MODE>,
+  return cudaLaunchKernelEx(&cfg, k_rows_cluster<InT, OutT, CLUSTER_RV, MODE, TMA>,
                             static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out,
                             c.rows, c.cols, c.valid_len, p.chunk, p.smem_elems, c.max_polls,
                             c.status);
 }
 
-template <typename InT, typename OutT, int MODE, int VPT, int DEPTH>
-cudaError_t launch_stream_vd(const Call& c, const Plan& p) {
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_cluster(const Call& c, const Plan& p) {
+  return p.stage_tma ? launch_cluster_t<InT, OutT, MODE, true>(c, p)
+                     : launch_cluster_t<InT, OutT, MODE, false>(c, p);
+}
+
+// One launch of the streamed kernel over the items `it`.
+template <typename InT, typename OutT, int MODE, int VPT, int DEPTH, bool CHUNKED>
+cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float* m_out, float* d_out,
+                            const float* m_in, const float* d_in) {
   constexpr int V = Elem<InT>::V;
   // at most 16 elements per thread with the compensated exponential (fp32
   // outputs) and 32 otherwise
-  if constexpr (VPT * V > (ExpPolicy<OutT, MODE>::ACCURATE ? 16 : 32)) {
+  if constexpr (VPT * V > ((ExpPolicy<OutT, MODE>::ACCURATE || MODE == MODE_APPLY) ? 16 : 32)) {
     return cudaErrorInvalidValue;
   } else {
-    auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH>;
+    auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH, CHUNKED>;
     const int64_t smem = stream_smem_bytes(DEPTH, VPT, p.threads);
     static int64_t set_bytes[64] = {0};
     int dev = 0;
@@ -111,31 +119,74 @@ cudaError_t launch_stream_vd(const Call& c, const Plan& p) {
       if (e != cudaSuccess) return e;
       set_bytes[dev] = smem;
     }
-    kern<<<(unsigned)p.ctas, p.threads, (size_t)smem, c.stream>>>(
-        static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, c.rows, c.cols,
+    const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
+    kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
+        static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), m_out, d_out, m_in, d_in, it,
         c.valid_len);
     return cudaGetLastError();
   }
 }
 
 template <typename InT, typename OutT, int MODE, int VPT>
-cudaError_t launch_stream_v(const Call& c, const Plan& p) {
+cudaError_t launch_stream_v(const Call& c, const Plan& p, const Items& it) {
   switch (p.stages) {
-    case 3: return launch_stream_vd<InT, OutT, MODE, VPT, 3>(c, p);
-    case 4: return launch_stream_vd<InT, OutT, MODE, VPT, 4>(c, p);
-    default: return launch_stream_vd<InT, OutT, MODE, VPT, 2>(c, p);
+    case 3: return launch_stream_k<InT, OutT, MODE, VPT, 3, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
+    case 4: return launch_stream_k<InT, OutT, MODE, VPT, 4, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
+    default: return launch_stream_k<InT, OutT, MODE, VPT, 2, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
   }
 }
 
+// Whole rows (softmax or row statistics).
 template <typename InT, typename OutT, int MODE>
 cudaError_t launch_stream(const Call& c, const Plan& p) {
+  const Items it{c.rows, 0, c.cols, (int)c.cols, 1, 0};
   switch (p.vpt) {
-    case 1: return launch_stream_v<InT, OutT, MODE, 1>(c, p);
-    case 2: return launch_stream_v<InT, OutT, MODE, 2>(c, p);
-    case 4: return launch_stream_v<InT, OutT, MODE, 4>(c, p);
-    case 8: return launch_stream_v<InT, OutT, MODE, 8>(c, p);
+    case 1: return launch_stream_v<InT, OutT, MODE, 1>(c, p, it);
+    case 2: return launch_stream_v<InT, OutT, MODE, 2>(c, p, it);
+    case 4: return launch_stream_v<InT, OutT, MODE, 4>(c, p, it);
+    case 8: return launch_stream_v<InT, OutT, MODE, 8>(c, p, it);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Long rows in slabs of rows: per slab, the streamed kernel computes every
+// chunk's summary, then normalises every chunk with its row's merged (M, D)
+// (row statistics merge the summaries instead).  Chunks are 16 elements per
+// thread.  The summaries live in a stream-ordered scratch allocation for the
+// call, or in p.scratch when given.
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_split(const Call& c, const Plan& p) {
+  constexpr int SV = 16 / Elem<InT>::V;
+  const int64_t slab = p.slab_rows;
+  const size_t part_n = (size_t)slab * p.nchunks;
+  const size_t bytes = split_scratch_bytes(slab, p.nchunks);
+  char* base = reinterpret_cast<char*>(p.scratch);
+  cudaError_t e = cudaSuccess;
+  if (base == nullptr) {
+    e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, c.stream);
+    if (e != cudaSuccess) return e;
+  }
+  float* pm = reinterpret_cast<float*>(base);
+  float* pd = pm + part_n;
+  for (int64_t r0 = 0; r0 < c.rows && e == cudaSuccess; r0 += slab) {
+    const int64_t n = c.rows - r0 < slab ? c.rows - r0 : slab;
+    const Items st{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, p.l2_hint_stats};
+    e = launch_stream_k<InT, float, MODE_STATS, SV, 2, true>(c, p, st, pm, pd, nullptr, nullptr);
+    if (e != cudaSuccess) break;
+    if constexpr (MODE == MODE_SOFTMAX) {
+      const Items ap{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, p.l2_hint_apply};
+      e = launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
+    } else {
+      k_merge_chunk_stats<256><<<(unsigned)n, 256, 0, c.stream>>>(pm, pd, p.nchunks, c.m_out + r0,
+                                                                   c.d_out + r0);
+      e = cudaGetLastError();
+    }
+  }
+  if (p.scratch == nullptr) {
+    const cudaError_t f = cudaFreeAsync(base, c.stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
 }
 
 template <typename InT, typename OutT, int MODE>
@@ -160,6 +211,7 @@ cudaError_t launch_typed(const Call& c, const Plan& p) {
     case PATH_CLUSTER: return launch_cluster<InT, OutT, MODE>(c, p);
     case PATH_GENERIC: return launch_generic<InT, OutT, MODE>(c);
     case PATH_STREAM: return launch_stream<InT, OutT, MODE>(c, p);
+    case PATH_SPLIT: return launch_split<InT, OutT, MODE>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -178,7 +230,7 @@ cudaError_t launch_in(const Call& c, const Plan& p) {
 template <typename InT>
 int cluster_capacity(int cluster, int64_t smem_bytes) {
   // the softmax kernel with fp32 output stands for the family (same resources)
-  if (prepare_cluster_kernel<InT, float, MODE_SOFTMAX>(smem_bytes) != cudaSuccess) return 0;
+  if (prepare_cluster_kernel<InT, float, MODE_SOFTMAX, true>(smem_bytes) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cluster, 1, 1);
   cfg.blockDim = dim3(CLUSTER_THREADS, 1, 1);
@@ -191,7 +243,7 @@ int cluster_capacity(int cluster, int64_t smem_bytes) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_rows_cluster<InT, float, CLUSTER_RV, MODE_SOFTMAX>,
+  if (cudaOccupancyMaxActiveClusters(&n, k_rows_cluster<InT, float, CLUSTER_RV, MODE_SOFTMAX, true>,
                                      &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -219,25 +271,46 @@ int stream_occupancy(int vpt, int threads, int depth) {
   };
   switch (vpt) {
     case 1:
-      return by_depth(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 2>,
-                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 3>,
-                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 4>);
+      return by_depth(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 2, false>,
+                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 3, false>,
+                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 4, false>);
     case 2:
-      return by_depth(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 2>,
-                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 3>,
-                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 4>);
+      return by_depth(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 2, false>,
+                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 3, false>,
+                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 4, false>);
     case 4:
-      return by_depth(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 2>,
-                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 3>,
-                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 4>);
+      return by_depth(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 2, false>,
+                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 3, false>,
+                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 4, false>);
     case 8:
       if constexpr (8 * V <= 32)
-        return by_depth(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 2>,
-                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 3>,
-                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 4>);
+        return by_depth(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 2, false>,
+                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 3, false>,
+                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 4, false>);
       return 0;
     default: return 0;
   }
+}
+
+// Resident CTAs per SM of the long-row kernels (the fp32-output apply kernel,
+// the largest, and the statistics kernel) at `threads` threads.
+template <typename InT>
+int split_occupancy(int threads) {
+  constexpr int SV = 16 / Elem<InT>::V;
+  const int64_t smem = stream_smem_bytes(2, SV, threads);
+  auto query = [&](auto kern) -> int {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  };
+  const int a = query(k_rows_stream<InT, float, SV, MODE_APPLY, 2, true>);
+  const int b = query(k_rows_stream<InT, float, SV, MODE_STATS, 2, true>);
+  return a < b ? a : b;
 }
 
 }  // namespace

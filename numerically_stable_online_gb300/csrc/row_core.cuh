@@ -178,4 +178,47 @@ __device__ __forceinline__ void store_row(OutT* yr, int G, int g, int ncols, int
   }
 }
 
+// e^(x - M) / D for one element (pass 2, and the cluster kernel's normalise
+// pass): compensated for fp32 outputs; otherwise one FFMA with the per-row
+// constant c2 = RN(-M log2 e + s) and rD2 = 2^(-s + c2_err) / D, c2_err the
+// exact rounding residual of c2 (s = 8 for bf16 keeps its subnormals, as in
+// row_core.cuh).  The summaries come from other CTAs, so the rounding of c2
+// does not cancel against the sum and is carried explicitly.  With |M| near
+// the top of the fp32 range (huge) the difference is taken first instead.
+struct OutConst {
+  float M, c2, rD, rD2;
+  bool huge;
+};
+
+template <typename OutT>
+__device__ __forceinline__ OutConst make_out_const(float M, float D) {
+  constexpr float SC = ExpPolicy<OutT, MODE_SOFTMAX>::SCALE_LOG2;
+  OutConst k;
+  k.M = M;
+  k.huge = !(fabsf(M) < 1e38f);
+  k.rD = recip_refined(D);
+  k.c2 = SC;
+  float c2_err = 0.0f;
+  if (!k.huge) {
+    const float a = __fmul_rn(-M, L2E_HI);
+    const float e1 = __fmaf_rn(-M, L2E_HI, -a);  // exact residual of the product
+    k.c2 = __fadd_rn(a, SC);
+    const float bb = __fsub_rn(k.c2, a);         // TwoSum(a, SC) residual
+    const float e2 = __fadd_rn(__fsub_rn(a, __fsub_rn(k.c2, bb)), __fsub_rn(SC, bb));
+    c2_err = __fadd_rn(e1, e2);
+  }
+  k.rD2 = __fmul_rn(__fmul_rn(k.rD, SC == 0.0f ? 1.0f : 0.00390625f), __fmaf_rn(c2_err, LN2, 1.0f));
+  return k;
+}
+
+template <typename OutT>
+__device__ __forceinline__ float out_value(float x, const OutConst& k) {
+  if constexpr (ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE) {
+    return __fmul_rn(exp_shift_accurate(x, k.M), k.rD);
+  } else {
+    const float u = k.huge ? __fmaf_rn(__fsub_rn(x, k.M), L2E_HI, k.c2) : __fmaf_rn(x, L2E_HI, k.c2);
+    return __fmul_rn(ex2_ftz(u), k.rD2);
+  }
+}
+
 }  // namespace smx

@@ -25,6 +25,7 @@ struct DeviceInfo {
   bool supported = false;
   int sm_count = 0;
   int64_t smem_optin = 0;
+  int64_t l2_bytes = 0;
   int* status = nullptr;   // device status word
   int max_cluster[3] = {0, 0, 0};  // per input type, 0 = not queried yet
 };
@@ -41,6 +42,9 @@ std::atomic<int> g_regs_threads{0};
 std::atomic<int> g_regs_vpt{0};
 std::atomic<int> g_stream_depth{0};
 std::atomic<int> g_stream_ctas_per_sm{0};
+std::atomic<int> g_cluster_stage{0};  // 0 automatic, 1 bulk copies, 2 cp.async
+std::atomic<int64_t> g_split_slab_bytes{0};
+std::atomic<int> g_split_hint_stats{-1}, g_split_hint_apply{-1};
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
@@ -69,16 +73,18 @@ smx_status device_info(DeviceInfo** out) {
   if (!d.ready) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!d.ready) {
-      int major = 0, minor = 0, sms = 0, optin = 0;
+      int major = 0, minor = 0, sms = 0, optin = 0, l2 = 0;
       if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
-              cudaSuccess)
+              cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess)
         return cuda_fail(e, SMX_ERR_DEVICE);
       d.supported = (major == 10 && minor == 3);
       d.sm_count = sms;
       d.smem_optin = optin;
+      d.l2_bytes = l2;
       if (d.supported) {
         int* s = nullptr;
         if ((e = cudaMalloc(&s, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
@@ -215,6 +221,47 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
   return true;
 }
 
+// Long rows in slabs of about half the L2 (the statistics pass leaves the slab
+// in L2 for the normalising pass's re-read), chunks of 16 elements per thread of
+// 256-thread CTAs, on the streamed kernel.
+bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
+  const int es = elem_size(in_dtype);
+  const int V = 16 / es;
+  const int vpt = 16 / V;  // 16 elements per thread: the compensated exponential fits
+  const int threads = 256;
+  const int64_t chunk = (int64_t)threads * vpt * V;
+  const int64_t nchunks = (cols + chunk - 1) / chunk;
+  if (nchunks > ((int64_t)1 << 30)) return false;
+  int64_t slab_bytes = d.l2_bytes / 2;
+  const int64_t dbg = g_split_slab_bytes.load();
+  if (dbg > 0) slab_bytes = dbg;
+  int64_t slab = slab_bytes / (cols * es);
+  if (slab < 1) slab = 1;
+  if (slab * nchunks > ((int64_t)1 << 31)) slab = ((int64_t)1 << 31) / nchunks;
+  int occ_max = 0;
+  switch (in_dtype) {
+    case SMX_F32: occ_max = split_occupancy_f32(threads); break;
+    case SMX_F16: occ_max = split_occupancy_f16(threads); break;
+    default: occ_max = split_occupancy_bf16(threads); break;
+  }
+  if (occ_max <= 0) return false;
+  int occ = occ_max;
+  const int forced = g_stream_ctas_per_sm.load();
+  if (forced > 0) occ = forced < occ_max ? forced : occ_max;
+  p->path = PATH_SPLIT;
+  p->threads = threads;
+  p->vpt = vpt;
+  p->stages = 2;
+  p->ctas = occ * d.sm_count;
+  p->chunk = chunk;
+  p->nchunks = (int)nchunks;
+  p->slab_rows = slab;
+  const int hs = g_split_hint_stats.load(), ha = g_split_hint_apply.load();
+  p->l2_hint_stats = hs >= 0 ? hs : 1;  // the statistics pass's reads stay for the re-read
+  p->l2_hint_apply = ha >= 0 ? ha : 2;  // the normalising pass's reads are the last
+  return true;
+}
+
 bool plan_cluster(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
   const int es = elem_size(in_dtype);
   const int V = 16 / es;
@@ -236,6 +283,8 @@ bool plan_cluster(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan*
   p->chunk = chunk;
   p->smem_elems = smem_elems;
   p->ctas = (int)(rows < resident ? rows : resident);  // persistent clusters
+  p->resident_clusters = resident;
+  p->stage_tma = g_cluster_stage.load() != 2;
   return true;
 }
 
@@ -251,11 +300,21 @@ smx_status run(Call& c, DeviceInfo& dev) {
   if (vec_ok) {
     if (force == PATH_CLUSTER) {
       planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
+    } else if (force == PATH_SPLIT) {
+      planned = plan_split(dev, c.cols, c.in_dtype, &p);
     } else if (force != PATH_GENERIC) {
       const bool acc = c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32;
       if (force != PATH_REGS)
         planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, &p);
       if (!planned) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
+      // rows longer than one CTA holds: a row per thread-block cluster when the
+      // rows fill every resident cluster, else (a few very long rows) L2 slabs,
+      // which spread every row over all SMs
+      if (!planned) {
+        planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
+        if (planned && c.rows < p.resident_clusters) planned = false;
+      }
+      if (!planned) planned = plan_split(dev, c.cols, c.in_dtype, &p);
       if (!planned) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     }
   }
@@ -399,7 +458,7 @@ int smx_last_cuda_error(void) { return t_last_cuda_error; }
 
 int smx_version(void) { return 100; }
 
-void smx_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 4 ? path : 0); }
+void smx_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 5 ? path : 0); }
 
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
   g_max_cluster.store(max_cluster > 0 ? max_cluster : 0);
@@ -411,6 +470,15 @@ void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls); }
 int smx_debug_last_path(void) { return t_last_path; }
 
 void smx_debug_set_stream_depth(int depth) { g_stream_depth.store(depth > 0 ? depth : 0); }
+
+void smx_debug_set_split_slab(int64_t bytes) { g_split_slab_bytes.store(bytes > 0 ? bytes : 0); }
+
+void smx_debug_set_split_hints(int stats, int apply) {
+  g_split_hint_stats.store(stats >= 0 && stats <= 2 ? stats : -1);
+  g_split_hint_apply.store(apply >= 0 && apply <= 2 ? apply : -1);
+}
+
+void smx_debug_set_cluster_staging(int mode) { g_cluster_stage.store(mode == 1 || mode == 2 ? mode : 0); }
 
 void smx_debug_set_stream_ctas(int per_sm) { g_stream_ctas_per_sm.store(per_sm > 0 ? per_sm : 0); }
 

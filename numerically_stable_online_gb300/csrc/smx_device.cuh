@@ -82,7 +82,6 @@ __device__ __forceinline__ float exp_shift_fast(float x, float m) {
 // would otherwise produce NaN.  A NaN operand still yields NaN.
 __device__ __forceinline__ float exp_shift_accurate(float x, float m) {
   const float t = __fsub_rn(x, m);
-  if (t < -110.0f) return 0.0f;
   const float z = __fsub_rn(t, x);
   const float t_lo = __fadd_rn(__fsub_rn(x, __fsub_rn(t, z)), __fsub_rn(-m, z));
   const float u = __fmul_rn(t, L2E_HI);
@@ -92,7 +91,8 @@ __device__ __forceinline__ float exp_shift_accurate(float x, float m) {
   const float r = __fmaf_rn(t, L2E_HI, -u);
   const float corr = __fmaf_rn(r, LN2, __fmaf_rn(t, L2E_LO_LN2, t_lo));
   const float e = ex2_ftz(u);
-  return __fmaf_rn(e, corr, e);
+  // selected, not branched: the TwoSum of an infinite t is NaN
+  return t < -110.0f ? 0.0f : __fmaf_rn(e, corr, e);
 }
 
 // ---------------------------------------------------------------------------

@@ -7,7 +7,7 @@
 
 namespace smx {
 
-enum Path : int { PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_STREAM = 4 };
+enum Path : int { PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_STREAM = 4, PATH_SPLIT = 5 };
 
 struct Call {
   const void* x;
@@ -35,6 +35,14 @@ struct Plan {
   int cluster = 1;
   int64_t chunk = 0;       // elements per CTA
   int64_t smem_elems = 0;  // staged elements per CTA
+  bool stage_tma = true;   // stage with bulk copies (TMA) or per-thread cp.async
+  // split rows: slabs of slab_rows rows, chunks of `chunk` elements
+  int64_t slab_rows = 0;
+  int l2_hint_stats = 0;  // L2 policies of the two passes' reads (Items::l2_hint)
+  int l2_hint_apply = 0;
+  int resident_clusters = 0;
+  int nchunks = 0;
+  float* scratch = nullptr;  // caller-provided summaries (else allocated per call)
 };
 
 constexpr int CLUSTER_RV = 2;  // register vectors per thread on the cluster path
@@ -55,8 +63,17 @@ int cluster_capacity_bf16(int cluster, int64_t smem_bytes);
 int stream_occupancy_f32(int vpt, int threads, int depth);
 int stream_occupancy_f16(int vpt, int threads, int depth);
 int stream_occupancy_bf16(int vpt, int threads, int depth);
+int split_occupancy_f32(int threads);
+int split_occupancy_f16(int threads);
+int split_occupancy_bf16(int threads);
 
 constexpr int STREAM_MAX_ROW_BYTES = 32768;
+
+// Scratch of the long-row slab path for slabs of `slab` rows of `nchunks`
+// chunks: the chunk summaries (m, then d).
+inline size_t split_scratch_bytes(int64_t slab, int64_t nchunks) {
+  return (size_t)(2 * slab * nchunks) * sizeof(float);
+}
 
 // Dynamic shared memory of the streamed kernel: `depth` rows of vpt 16-byte
 // vectors for each of the CTA's threads.

@@ -22,8 +22,8 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 PAIRS = [(a, b) for a in DT for b in DT]
-PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM = 1, 2, 3, 4
-ALL_PATHS = [PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM]
+PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM, PATH_SPLIT = 1, 2, 3, 4, 5
+ALL_PATHS = [PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM, PATH_SPLIT]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,6 +49,8 @@ def lib(built):
     built.smx_debug_set_wait_limit(0)
     built.smx_debug_set_regs_shape(0, 0)
     built.smx_debug_set_stream_depth(0)
+    built.smx_debug_set_cluster_staging(0)
+    built.smx_debug_set_split_slab(0)
 
 
 DEV = "cuda:0"
@@ -279,10 +281,13 @@ def test_stream_ring_many_rows(lib, in_dtype, out_dtype, cols, depth):
     check_stats(m, d, m_ref, d_ref)
 
 
+@pytest.mark.parametrize("staging", [1, 2])
 @pytest.mark.parametrize("cap", [1, 2, 4, 8, 16])
-def test_cluster_sizes_and_streamed_remainder(lib, cap):
-    """Cluster path with each cluster size, and with the staging area cut to 32 KiB
-    so that part of each chunk is streamed from global memory twice."""
+def test_cluster_sizes_and_streamed_remainder(lib, cap, staging):
+    """Cluster path with each cluster size and both ways of staging (bulk copies,
+    per-thread cp.async), and with the staging area cut to 32 KiB so that part of
+    each chunk is streamed from global memory twice."""
+    lib.smx_debug_set_cluster_staging(staging)
     rows, cols = 3, 300000
     rng = np.random.default_rng(cap)
     x32 = (rng.normal(0, 1, rows * cols) + np.tile(np.linspace(0, 20, cols), rows)).astype(np.float32)
@@ -346,13 +351,59 @@ def test_row_stats(lib, in_dtype, path):
         check_stats(m, d, m_ref, d_ref)
 
 
-def test_row_stats_long_rows(lib):
+@pytest.mark.parametrize("in_dtype,out_dtype", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f32"),
+                                                ("f32", "f16")])
+@pytest.mark.parametrize("slab", [0, 1 << 20])
+def test_split_long_rows(lib, in_dtype, out_dtype, slab):
+    """L2-slab path: chunk summaries then merge and normalise; ragged last chunks,
+    varied lengths (0, 1, a chunk boundary, all), and slabs of one or many rows."""
+    rows, cols = 9, 40000 + 8 * 7
+    rng = np.random.default_rng(rows + slab)
+    x32 = (rng.normal(0, 3, (rows, cols)) + np.linspace(-5, 25, cols)[None, :]).astype(np.float32)
+    x32[6, 1234] = np.nan
+    x32[7, 99] = np.inf
+    x = stored(x32.reshape(-1), in_dtype)
+    vl = np.array([cols, 0, 1, 4096, 8192, 39999, cols, 5000, cols], np.int32)
+    lib.smx_debug_force_path(PATH_SPLIT)
+    lib.smx_debug_set_split_slab(slab)
+    run_and_compare(x, in_dtype, out_dtype, rows, cols, vl)
+    assert lib.smx_debug_last_path() == PATH_SPLIT
+    run_and_compare(x, in_dtype, out_dtype, rows, cols, None)
+    m, d = gpu_stats(x, in_dtype, rows, cols, vl)
+    m_ref, d_ref = oracle.row_stats(x, in_dtype, rows, cols, vl)
+    check_stats(m, d, m_ref, d_ref)
+
+
+@pytest.mark.parametrize("staging", [1, 2])
+def test_row_stats_long_rows(lib, staging):
+    lib.smx_debug_set_cluster_staging(staging)
+    lib.smx_debug_force_path(PATH_CLUSTER)
     name = "f32_64x1048576_rise"
     x, _ = wl.host_input(name, rows=4)
     m, d = gpu_stats(x, "f32", 4, 1048576)
     m_ref, d_ref = oracle.row_stats(x, "f32", 4, 1048576)
     check_stats(m, d, m_ref, d_ref)
     assert lib.smx_debug_last_path() == PATH_CLUSTER
+
+
+@pytest.mark.parametrize("staging", [1, 2])
+def test_cluster_many_rows_per_cluster(lib, staging):
+    """More rows than resident clusters, so every cluster walks several rows and
+    refills its staged pieces from the next row; lengths vary per row."""
+    lib.smx_debug_set_cluster_staging(staging)
+    lib.smx_debug_force_path(PATH_CLUSTER)
+    rows, cols = 41, 200000
+    rng = np.random.default_rng(41)
+    x32 = rng.normal(0, 4, rows * cols).astype(np.float32)
+    vl = rng.integers(0, cols + 1, size=rows).astype(np.int32)
+    vl[::5] = cols
+    vl[3] = 0
+    for out in ("f32", "bf16"):
+        run_and_compare(x32, "f32", out, rows, cols, vl)
+    run_and_compare(stored(x32, "f16"), "f16", "f16", rows, cols, vl)
+    m, d = gpu_stats(x32, "f32", rows, cols, vl)
+    m_ref, d_ref = oracle.row_stats(x32, "f32", rows, cols, vl)
+    check_stats(m, d, m_ref, d_ref)
 
 
 def test_merge_stats_against_reference(lib):
