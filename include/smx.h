@@ -37,7 +37,9 @@
  * status word per device on first use, and the long-row path (rows too long for
  * one CTA) takes a small stream-ordered scratch allocation per call for its
  * chunk summaries (cudaMallocAsync / cudaFreeAsync on `stream`: 8 bytes per
- * 16 KiB chunk of an L2-sized slab of rows).  No other call allocates.
+ * chunk of 4096 elements of an L2-sized slab of rows); its variant
+ * smx_softmax_rows_fixed_scratch uses a fixed array instead.  No other call
+ * allocates.
  * Every call is asynchronous on `stream` (NULL is the legacy default stream) and
  * returns after enqueueing its kernels.
  *
@@ -71,7 +73,8 @@ typedef enum {
     SMX_ERR_ALIAS = 3,       /* input and output byte ranges overlap */
     SMX_ERR_LAUNCH = 4,      /* a kernel launch failed (the CUDA error is in smx_last_cuda_error) */
     SMX_ERR_TIMEOUT = 5,     /* device: a bounded wait for staged data ran out */
-    SMX_ERR_DEVICE = 6       /* a CUDA runtime call failed */
+    SMX_ERR_DEVICE = 6,      /* a CUDA runtime call failed */
+    SMX_ERR_TOO_LARGE = 7    /* smx_softmax_rows_fixed_scratch: a row needs more scratch than it has */
 } smx_status;
 
 /*
@@ -88,6 +91,44 @@ typedef enum {
 smx_status smx_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
                             const int32_t *valid_len, smx_dtype in_dtype,
                             smx_dtype out_dtype, smx_stream_t stream);
+
+/*
+ * smx_softmax_rows, computed without allocating any device memory.
+ *
+ * The method's pages have no counterpart to this call; it exists for callers
+ * that cannot let a library allocate: a process whose device memory is all
+ * handed out by its own allocator under a fixed budget, or a steady-state loop
+ * that must never meet an allocator's latency or an out-of-memory failure in
+ * the middle of a step.  smx_softmax_rows takes a small stream-ordered
+ * allocation per call on its long-row path; this call runs that path with its
+ * chunk summaries in one fixed array of 256 KiB of device memory that the
+ * library holds per device from the time it is loaded.
+ *
+ * Arguments, results, policy and errors are those of smx_softmax_rows (the
+ * outputs agree with it within the stated tolerances: the same arithmetic, in
+ * the long-row kernels for every row length).  Inputs that are not 16-byte
+ * aligned, or whose row size in bytes is not a multiple of 16, run the scalar
+ * kernel, which takes no scratch.
+ *
+ * Limit: one row's chunk summaries must fit the array: at most 32768 chunks of
+ * 4096 elements, i.e. cols <= 134217728; a longer aligned row returns
+ * SMX_ERR_TOO_LARGE before anything is enqueued.  Rows are processed in slabs
+ * small enough for the array.
+ *
+ * Set-up: the first call on each device queries its properties and looks up
+ * the array's address (the device must be current); make that first call
+ * before capturing the stream into a graph or otherwise relying on the call
+ * doing nothing but enqueue kernels.  Nothing in the array needs to start at
+ * zero: every summary is written before it is read, within the same call.
+ *
+ * Concurrency: all calls on one device share the one array.  Two calls whose
+ * kernels can overlap on the device (different streams with no ordering between
+ * them) race on it and may produce wrong results; order them on one stream or
+ * with events.
+ */
+smx_status smx_softmax_rows_fixed_scratch(const void *x, void *y, int64_t rows, int64_t cols,
+                                          const int32_t *valid_len, smx_dtype in_dtype,
+                                          smx_dtype out_dtype, smx_stream_t stream);
 
 /*
  * Block summary (m, d) of each row, fp32.

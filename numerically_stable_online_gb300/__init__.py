@@ -16,7 +16,8 @@ import threading
 import torch
 
 __all__ = [
-    "SmxError", "library", "softmax_rows", "softmax_row_stats", "softmax_merge_stats",
+    "SmxError", "library", "softmax_rows", "softmax_rows_fixed_scratch", "softmax_row_stats",
+    "softmax_merge_stats",
     "last_device_status", "status_string", "DTYPES",
 ]
 
@@ -26,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsmx.so")
 SMX_F32, SMX_F16, SMX_BF16 = 0, 1, 2
 DTYPES = {torch.float32: SMX_F32, torch.float16: SMX_F16, torch.bfloat16: SMX_BF16}
 STATUS = {0: "SMX_OK", 1: "SMX_ERR_INVALID_ARG", 2: "SMX_ERR_UNSUPPORTED", 3: "SMX_ERR_ALIAS",
-          4: "SMX_ERR_LAUNCH", 5: "SMX_ERR_TIMEOUT", 6: "SMX_ERR_DEVICE"}
+          4: "SMX_ERR_LAUNCH", 5: "SMX_ERR_TIMEOUT", 6: "SMX_ERR_DEVICE", 7: "SMX_ERR_TOO_LARGE"}
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +56,8 @@ def library() -> ctypes.CDLL:
         st = ctypes.c_int
         lib.smx_softmax_rows.argtypes = [P, P, I64, I64, P, I32, I32, P]
         lib.smx_softmax_rows.restype = st
+        lib.smx_softmax_rows_fixed_scratch.argtypes = [P, P, I64, I64, P, I32, I32, P]
+        lib.smx_softmax_rows_fixed_scratch.restype = st
         lib.smx_softmax_row_stats.argtypes = [P, P, P, I64, I64, P, I32, P]
         lib.smx_softmax_row_stats.restype = st
         lib.smx_softmax_merge_stats.argtypes = [P, P, P, P, P, P, I64, P]
@@ -135,6 +138,32 @@ def softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None, valid_len: to
                                     _dtype(out.dtype), _stream(stream))
     if st != 0:
         raise SmxError(st, "smx_softmax_rows")
+    return out
+
+
+def softmax_rows_fixed_scratch(x: torch.Tensor, out: torch.Tensor | None = None,
+                               valid_len: torch.Tensor | None = None,
+                               out_dtype: torch.dtype | None = None, stream=None) -> torch.Tensor:
+    """softmax_rows without any device allocation inside the library call.
+
+    The long-row kernels keep their chunk summaries in one fixed per-device
+    array (256 KiB); calls that can overlap on the device race on it, so issue
+    them on one stream.  Rows longer than 134217728 elements raise
+    SMX_ERR_TOO_LARGE.  (``out=None`` allocates the output here, in torch,
+    before the call.)
+    """
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype or x.dtype, device=x.device)
+    _check_2d(out, "out")
+    if out.shape != x.shape or out.device != x.device:
+        raise ValueError("out must match x's shape and device")
+    st = library().smx_softmax_rows_fixed_scratch(x.data_ptr(), out.data_ptr(), rows, cols,
+                                                  _lengths(valid_len, rows, x.device),
+                                                  _dtype(x.dtype), _dtype(out.dtype), _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_rows_fixed_scratch")
     return out
 
 

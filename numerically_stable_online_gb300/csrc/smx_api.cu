@@ -11,6 +11,12 @@
 #include "kernel_generic.cuh"
 #include "smx_launch.h"
 
+// Scratch of smx_softmax_rows_fixed_scratch: 2 floats per chunk, 32768 chunks
+// of one slab (256 KiB).  A default slab (half the L2) holds well under 8192
+// chunks of 4096 elements.
+constexpr int64_t FIXED_SCRATCH_FLOATS = 65536;
+static __device__ __align__(256) float g_fixed_scratch[FIXED_SCRATCH_FLOATS];
+
 namespace smx {
 namespace {
 
@@ -333,6 +339,57 @@ smx_status run(Call& c, DeviceInfo& dev) {
   return SMX_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// smx_softmax_rows_fixed_scratch: the long-row path with its chunk summaries in
+// a fixed device array instead of a per-call allocation.
+
+
+struct FixedSetup {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  int64_t l2_bytes = 0;
+  float* scratch = nullptr;  // this device's copy of g_fixed_scratch
+};
+FixedSetup g_fixed[MAX_DEVICES];
+
+// Current device's properties and scratch address; no allocation.
+smx_status fixed_setup(FixedSetup** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_UNSUPPORTED);
+  if (dev < 0 || dev >= MAX_DEVICES) return SMX_ERR_UNSUPPORTED;
+  FixedSetup& f = g_fixed[dev];
+  if (!f.ready) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!f.ready) {
+      int major = 0, minor = 0, sms = 0, l2 = 0;
+      if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess)
+        return cuda_fail(e, SMX_ERR_DEVICE);
+      f.supported = (major == 10 && minor == 3);
+      f.sm_count = sms;
+      f.l2_bytes = l2;
+      if (f.supported) {
+        void* a = nullptr;
+        if ((e = cudaGetSymbolAddress(&a, g_fixed_scratch)) != cudaSuccess)
+          return cuda_fail(e, SMX_ERR_DEVICE);
+        f.scratch = static_cast<float*>(a);
+      }
+      f.ready = true;
+    }
+  }
+  if (!f.supported) return SMX_ERR_UNSUPPORTED;
+  *out = &f;
+  return SMX_OK;
+}
+
+// Chunks per row of the long-row path (4096 elements each, any type).
+int64_t fixed_chunks(int64_t cols) { return (cols + 4095) / 4096; }
+
 }  // namespace
 
 // Element-wise merge of two arrays of (m, d) summaries; may run in place.
@@ -379,6 +436,50 @@ smx_status smx_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
   Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
          MODE_SOFTMAX, reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
   return run(c, *dev);
+}
+
+smx_status smx_softmax_rows_fixed_scratch(const void* x, void* y, int64_t rows, int64_t cols,
+                                          const int32_t* valid_len, smx_dtype in_dtype,
+                                          smx_dtype out_dtype, smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return SMX_OK;
+  if (x == nullptr || y == nullptr) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype), ny = rows * cols * elem_size(out_dtype);
+  if (overlaps(x, nx, y, ny)) return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, y, ny)) return SMX_ERR_ALIAS;
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(y) % 16 == 0) &&
+                      ((cols * elem_size(in_dtype)) % 16 == 0);
+  // one row's chunk summaries must fit (a slab holds at least one row)
+  if (vec_ok && 2 * fixed_chunks(cols) > FIXED_SCRATCH_FLOATS) return SMX_ERR_TOO_LARGE;
+  FixedSetup* f = nullptr;
+  smx_status s = fixed_setup(&f);
+  if (s != SMX_OK) return s;
+  Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
+         MODE_SOFTMAX, reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  Plan p;
+  if (vec_ok) {
+    DeviceInfo d;
+    d.sm_count = f->sm_count;
+    d.l2_bytes = f->l2_bytes;
+    if (!plan_split(d, cols, in_dtype, &p)) return SMX_ERR_UNSUPPORTED;
+    const int64_t cap = FIXED_SCRATCH_FLOATS / (2 * (int64_t)p.nchunks);
+    if (p.slab_rows > cap) p.slab_rows = cap;
+    p.scratch = f->scratch;
+  } else {
+    p.path = PATH_GENERIC;  // the scalar kernel takes no scratch
+  }
+  cudaError_t e;
+  switch (c.in_dtype) {
+    case SMX_F32: e = launch_in_f32(c, p); break;
+    case SMX_F16: e = launch_in_f16(c, p); break;
+    default: e = launch_in_bf16(c, p); break;
+  }
+  t_last_path = p.path;
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
+  return SMX_OK;
 }
 
 smx_status smx_softmax_row_stats(const void* x, float* m_out, float* d_out, int64_t rows,
@@ -450,6 +551,7 @@ const char* smx_status_string(smx_status status) {
     case SMX_ERR_LAUNCH: return "kernel launch failed";
     case SMX_ERR_TIMEOUT: return "device: bounded wait for staged data ran out";
     case SMX_ERR_DEVICE: return "CUDA runtime call failed";
+    case SMX_ERR_TOO_LARGE: return "row too long for the fixed scratch";
     default: return "unknown status";
   }
 }

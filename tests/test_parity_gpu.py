@@ -51,6 +51,8 @@ def lib(built):
     built.smx_debug_set_stream_depth(0)
     built.smx_debug_set_cluster_staging(0)
     built.smx_debug_set_split_slab(0)
+    built.smx_debug_set_split_hints(-1, -1)
+    built.smx_debug_set_stream_ctas(0)
 
 
 DEV = "cuda:0"

@@ -1,0 +1,135 @@
+"""smx_softmax_rows_fixed_scratch: softmax without any device allocation.
+
+The call runs the long-row kernels with their chunk summaries in a fixed
+per-device array instead of a per-call allocation.  Its outputs are compared
+with smx_softmax_rows (the allocating entry point) on the same inputs, on two
+calls in a row (the second reuses the array the first wrote), within the
+tolerance both entry points meet against the fp64 reference: fp32 outputs
+within 4e-6 relative of each other (each is within 2e-6 of the exact value),
+fp16/bf16 outputs within 2 units in the last place (each is within 1), masked
+lanes +0 in both.  A few rows are also checked against the reference itself.
+
+This file is collected last so that it also runs after every other GPU test
+in the same process; it passes alone as well.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import numerically_stable_online_gb300 as smx
+import oracle
+from numerically_stable_online_gb300 import workloads as wl
+from tests import parity
+
+DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+DEV = "cuda:0"
+SMX_ERR_TOO_LARGE = 7
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from numerically_stable_online_gb300 import build
+
+    build.build()
+    lib = smx.library()
+    yield lib
+    lib.smx_debug_set_split_slab(0)
+
+
+def close(a: torch.Tensor, b: torch.Tensor, valid_len):
+    """Element-wise agreement of two softmax outputs of one input."""
+    rows, cols = b.shape
+    lens = np.full(rows, cols) if valid_len is None else np.clip(valid_len.cpu().numpy(), 0, cols)
+    masked = torch.from_numpy(np.arange(cols)[None, :] >= lens[:, None]).to(a.device)
+    if a.dtype == torch.float32:
+        ai, bi = a.view(torch.int32), b.view(torch.int32)
+        assert bool(((ai == 0) | ~masked).all()) and bool(((bi == 0) | ~masked).all())
+        af, bf = a.double(), b.double()
+        big = bf >= 1e-30
+        rel = ((af - bf).abs() / bf.clamp_min(1e-300))[big]
+        assert rel.numel() == 0 or float(rel.max()) <= 4e-6
+        assert bool(((af - bf).abs()[~big] <= 4e-30).all())
+    else:
+        ai, bi = a.view(torch.int16).int(), b.view(torch.int16).int()
+        assert bool(((ai == 0) | ~masked).all()) and bool(((bi == 0) | ~masked).all())
+        # outputs are non-negative: their bit patterns are ordered like their values
+        assert int((ai - bi).abs().max()) <= 2
+
+
+def run_pair(x, out_dtype, valid_len):
+    y0 = smx.softmax_rows(x, valid_len=valid_len, out_dtype=out_dtype)
+    y1 = smx.softmax_rows_fixed_scratch(x, valid_len=valid_len, out_dtype=out_dtype)
+    y2 = smx.softmax_rows_fixed_scratch(x, valid_len=valid_len, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    close(y1, y0, valid_len)
+    close(y2, y0, valid_len)
+    assert torch.equal(y1.view(torch.uint8), y2.view(torch.uint8))  # same kernels, same order
+    return y1
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("in_t,out_t", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f32"), ("bf16", "f16")])
+def test_long_rows_match_allocating_call(lib, in_t, out_t):
+    rows, cols = 5, 300_000  # 74 chunks of 4096, the last one ragged
+    g = torch.Generator().manual_seed(2201)
+    x = (torch.randn(rows, cols, generator=g, dtype=torch.float64) * 4).to(DT[in_t])
+    vl = torch.tensor([cols, 0, 123_457, 4096, cols - 1], dtype=torch.int32)
+    y = run_pair(x.to(DEV), DT[out_t], vl.to(DEV))
+    # and against the reference itself
+    xs = wl.torch_to_storage(x).reshape(-1)
+    p = oracle.softmax_rows(xs, in_t, rows, cols, vl.numpy())
+    parity.compare(wl.torch_to_storage(y.cpu()), p, out_t, vl.numpy())
+
+
+@pytest.mark.gpu
+def test_slabs_bounded_by_the_fixed_array(lib):
+    # 1024 chunks per row: the array holds 32 rows of chunk summaries, so a very
+    # large requested slab is cut to 32 rows and 40 rows take two slabs
+    lib.smx_debug_set_split_slab(1 << 40)
+    try:
+        rows, cols = 40, 4096 * 1024
+        g = torch.Generator(device=DEV).manual_seed(2202)
+        x = (torch.randn(rows, cols, generator=g, device=DEV) * 3).to(torch.bfloat16)
+        vl = torch.full((rows,), cols, dtype=torch.int32)
+        vl[7] = 1_000_003
+        vl[33] = 0
+        vl = vl.to(DEV)
+        y = run_pair(x, torch.bfloat16, vl)
+    finally:
+        lib.smx_debug_set_split_slab(0)
+    for r in (0, 7, 31, 32, 39):  # rows either side of the slab boundary
+        xs = wl.torch_to_storage(x[r:r + 1].cpu()).reshape(-1)
+        lr = vl[r:r + 1].cpu().numpy()
+        p = oracle.softmax_rows(xs, "bf16", 1, cols, lr)
+        parity.compare(wl.torch_to_storage(y[r:r + 1].cpu()), p, "bf16", lr)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("offset,cols", [(0, 1000), (1, 1001), (0, 4096), (0, 12288)])
+def test_short_and_unaligned_rows(lib, offset, cols):
+    rows = 33
+    g = torch.Generator().manual_seed(2203 + cols)
+    flat = (torch.randn(rows * cols + offset, generator=g) * 5).to(DEV)
+    x = flat[offset:].view(rows, cols)  # offset 1: not 16-byte aligned, the scalar kernel
+    vl = torch.randint(0, cols + 3, (rows,), generator=g, dtype=torch.int32).to(DEV)
+    run_pair(x, torch.float32, vl)
+
+
+def test_oversize_row_rejected_before_any_device_work():
+    """A row needing more than the array's 32768 chunks is refused on the host.
+
+    The pointers are never dereferenced (the size check precedes every device
+    call), so placeholder addresses serve; runs without a GPU.
+    """
+    from numerically_stable_online_gb300 import build
+
+    build.build()
+    lib = smx.library()
+    cols = 4096 * 32768 + 4096
+    x_addr, y_addr = 1 << 40, 1 << 42  # 16-byte aligned, non-overlapping ranges
+    st = lib.smx_softmax_rows_fixed_scratch(ctypes.c_void_p(x_addr), ctypes.c_void_p(y_addr), 1, cols,
+                                            None, 0, 0, None)
+    assert st == SMX_ERR_TOO_LARGE
+    assert lib.smx_status_string(st).decode() == "row too long for the fixed scratch"
