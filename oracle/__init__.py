@@ -68,6 +68,10 @@ def _load():
         lib.orc_online_tiled.argtypes = [P, I64, I64, P, P, P]
         lib.orc_naive_softmax_f16.argtypes = [P, I64, P]
         lib.orc_stable_softmax_f16.argtypes = [P, I64, P, P, P, P]
+        lib.orc_log_softmax_rows.argtypes = [P, I32, I64, P, P, I64, P, P]
+        lib.orc_apply_stats.argtypes = [P, I32, I64, P, P, P, P, I64, P]
+        lib.orc_softmax_backward.argtypes = [P, P, I32, I64, P, P, I64, P]
+        lib.orc_cross_entropy.argtypes = [P, I32, I64, P, P, P, I64, P, P]
         _lib = lib
         return lib
 
@@ -210,3 +214,74 @@ def stable_softmax_f16(x):
     s = np.empty(1)
     lib.orc_stable_softmax_f16(_ptr(v), v.size, _ptr(sh), _ptr(e), _ptr(p), _ptr(s))
     return sh, e, p, float(s[0])
+
+
+def _rows_args(x, dtype, rows, cols, valid_len, rows_sel):
+    a, code = _as_storage(x, dtype)
+    if a.size != rows * cols:
+        raise ValueError("x has the wrong number of elements")
+    vl = _lengths(valid_len, rows)
+    sel = None if rows_sel is None else np.ascontiguousarray(rows_sel, dtype=np.int64)
+    n_sel = rows if sel is None else sel.size
+    return a, code, vl, sel, n_sel
+
+
+def log_softmax_rows(x, dtype, rows: int, cols: int, valid_len=None, rows_sel=None):
+    """fp64 (log_softmax [n, cols], LSE [n]) of the selected rows.
+
+    log_softmax_j = x_j - LSE over the valid prefix, -inf in masked lanes;
+    LSE = m + log d (-inf for an empty row, NaN for a NaN or +inf row).
+    """
+    lib = _load()
+    a, code, vl, sel, n_sel = _rows_args(x, dtype, rows, cols, valid_len, rows_sel)
+    out = np.empty((n_sel, cols), dtype=np.float64)
+    lse = np.empty(n_sel, dtype=np.float64)
+    lib.orc_log_softmax_rows(_ptr(a), code, cols, _ptr(vl), _ptr(sel), n_sel, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def apply_stats(x, dtype, rows: int, cols: int, m, d, valid_len=None, rows_sel=None):
+    """fp64 exp(x - m_r) / d_r over each valid prefix (+0 beyond), with given per-row (m, d)."""
+    lib = _load()
+    a, code, vl, sel, n_sel = _rows_args(x, dtype, rows, cols, valid_len, rows_sel)
+    mm = np.ascontiguousarray(m, dtype=np.float64)
+    dd = np.ascontiguousarray(d, dtype=np.float64)
+    if mm.shape != (rows,) or dd.shape != (rows,):
+        raise ValueError("m and d must have one entry per row")
+    p = np.empty((n_sel, cols), dtype=np.float64)
+    lib.orc_apply_stats(_ptr(a), code, cols, _ptr(vl), _ptr(mm), _ptr(dd), _ptr(sel), n_sel, _ptr(p))
+    return p
+
+
+def softmax_backward(p, g, dtype, rows: int, cols: int, valid_len=None, rows_sel=None):
+    """fp64 dx = p (g - sum(g p)) per row over the valid prefix (0 beyond).
+
+    p and g are stored values of one type (float32, or uint16 bits).
+    """
+    lib = _load()
+    a, code, vl, sel, n_sel = _rows_args(p, dtype, rows, cols, valid_len, rows_sel)
+    b, code_g = _as_storage(g, dtype)
+    if b.size != rows * cols:
+        raise ValueError("g has the wrong number of elements")
+    dx = np.empty((n_sel, cols), dtype=np.float64)
+    lib.orc_softmax_backward(_ptr(a), _ptr(b), code, cols, _ptr(vl), _ptr(sel), n_sel, _ptr(dx))
+    return dx
+
+
+def cross_entropy(x, dtype, rows: int, cols: int, target, valid_len=None, rows_sel=None,
+                  want_grad: bool = True):
+    """fp64 (loss [n], grad [n, cols] or None) of cross-entropy with logits.
+
+    loss = LSE - x_t, grad = softmax - onehot(t); a target outside the valid
+    prefix is ignored (loss 0, gradient 0).
+    """
+    lib = _load()
+    a, code, vl, sel, n_sel = _rows_args(x, dtype, rows, cols, valid_len, rows_sel)
+    t = np.ascontiguousarray(target, dtype=np.int64)
+    if t.shape != (rows,):
+        raise ValueError("target must have one entry per row")
+    loss = np.empty(n_sel, dtype=np.float64)
+    grad = np.empty((n_sel, cols), dtype=np.float64) if want_grad else None
+    lib.orc_cross_entropy(_ptr(a), code, cols, _ptr(vl), _ptr(t), _ptr(sel), n_sel, _ptr(loss),
+                          _ptr(grad))
+    return loss, grad

@@ -377,28 +377,25 @@ void orc_apply_stats(const void *x, int dtype, int64_t cols, const int32_t *vali
 }
 
 /* Softmax vector-Jacobian product ("The Jacobian, and the backward pass that
- * never divides"): for upstream gradient g and the softmax p of the row,
- * dx_i = p_i (g_i - sum_j g_j p_j).  p is computed here from x (three-pass);
- * masked lanes and empty rows give dx = 0; NaN rows NaN. */
-void orc_softmax_backward(const void *x, int dtype, const double *g, int64_t cols,
+ * never divides"): the Jacobian diag(p) - p p^T is never formed; for the
+ * upstream gradient g, dx_i = p_i (g_i - sum_j g_j p_j).  p is the softmax of
+ * the row as the forward pass stored it and g the gradient, both in `dtype`;
+ * the sum runs over the valid prefix, and masked lanes (where p is the constant
+ * +0, so no input there affects the loss) give dx = 0.  Plain IEEE double
+ * arithmetic otherwise: a NaN among the valid p or g makes every valid lane NaN. */
+void orc_softmax_backward(const void *p, const void *g, int dtype, int64_t cols,
                           const int32_t *valid_len, const int64_t *sel, int64_t n_sel, double *dx)
 {
     for (int64_t i = 0; i < n_sel; ++i) {
         int64_t r = sel ? sel[i] : i;
         int64_t L = row_len(valid_len, r, cols);
+        int64_t base = r * cols;
         double *o = dx + i * cols;
-        const double *gr = g + r * cols;
-        double m, d;
-        int cls = row_stats_one(x, dtype, r * cols, L, &m, &d);
-        for (int64_t j = 0; j < cols; ++j) o[j] = 0.0;
-        if (cls == 1) continue;
-        if (cls == 2) { for (int64_t j = 0; j < L; ++j) o[j] = NAN; continue; }
         double gp = 0.0;
-        for (int64_t j = 0; j < L; ++j) gp += gr[j] * (exp(load_elem(x, dtype, r * cols + j) - m) / d);
-        for (int64_t j = 0; j < L; ++j) {
-            double pj = exp(load_elem(x, dtype, r * cols + j) - m) / d;
-            o[j] = pj * (gr[j] - gp);
-        }
+        for (int64_t j = 0; j < L; ++j) gp += load_elem(g, dtype, base + j) * load_elem(p, dtype, base + j);
+        for (int64_t j = 0; j < cols; ++j) o[j] = 0.0;
+        for (int64_t j = 0; j < L; ++j)
+            o[j] = load_elem(p, dtype, base + j) * (load_elem(g, dtype, base + j) - gp);
     }
 }
 
