@@ -142,6 +142,47 @@ smx_status smx_softmax_row_stats(const void *x, float *m_out, float *d_out, int6
                                  smx_stream_t stream);
 
 /*
+ * log_softmax of each row ("Softmax numerics architecture - max subtract, fp32
+ * accumulate, fusion, online", section "Log-sum-exp: log-probabilities without
+ * probabilities"): y[r, j] = x[r, j] - LSE_r over the valid prefix, evaluated as
+ * (x - m) - log d so that a large m adds no rounding, and -inf (the log of the
+ * +0 probability) in masked lanes.  Policy (the softmax policy in log space):
+ * an empty or all -inf row is -inf everywhere; a NaN or +inf row has NaN in its
+ * valid lanes and -inf in its masked lanes.
+ *   Arguments, types, alignment, aliasing and errors: as smx_softmax_rows.
+ */
+smx_status smx_log_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
+                                const int32_t *valid_len, smx_dtype in_dtype,
+                                smx_dtype out_dtype, smx_stream_t stream);
+
+/*
+ * Log-sum-exp of each row (same section): LSE_r = m_r + log d_r, fp32.
+ *   lse_out: device float[rows], written.  -inf for an empty or all -inf row,
+ *   NaN for a NaN or +inf row.  Other arguments as smx_softmax_row_stats.
+ */
+smx_status smx_softmax_lse(const void *x, float *lse_out, int64_t rows, int64_t cols,
+                           const int32_t *valid_len, smx_dtype in_dtype, smx_stream_t stream);
+
+/*
+ * Normalise each row with given statistics: y[r, j] = exp(x[r, j] - m[r]) / d[r]
+ * over the valid prefix, +0 beyond.  This is the last step of a softmax whose
+ * row statistics were computed in pieces and merged ("Online stable softmax",
+ * "Derive the update for two blocks": only the prefix's m and d are needed),
+ * e.g. over column blocks of a row held in different buffers: row_stats per
+ * block, merge_stats, then apply_stats per block.
+ *   m_in, d_in: device float[rows]; (m, d) must be statistics of a set of
+ *   values containing the row's valid prefix (m at least its maximum, d >= 1 when
+ *   m is finite), as row_stats and merge_stats produce; otherwise the lanes are
+ *   whatever the arithmetic gives.  m == -inf gives a +0 row; a NaN m or d, or
+ *   m == +inf, gives NaN in the valid lanes.
+ *   y must not overlap x, m_in, d_in or valid_len.  Other arguments as
+ *   smx_softmax_rows.
+ */
+smx_status smx_softmax_apply_stats(const void *x, const float *m_in, const float *d_in, void *y,
+                                   int64_t rows, int64_t cols, const int32_t *valid_len,
+                                   smx_dtype in_dtype, smx_dtype out_dtype, smx_stream_t stream);
+
+/*
  * Element-wise merge of two arrays of block summaries ("Online stable softmax",
  * "Derive the update for two blocks"):
  *   m' = max(m_a, m_b),  d' = d_a exp(m_a - m') + d_b exp(m_b - m').

@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "SmxError", "library", "softmax_rows", "softmax_rows_fixed_scratch", "softmax_row_stats",
-    "softmax_merge_stats",
+    "softmax_merge_stats", "log_softmax_rows", "softmax_lse", "softmax_apply_stats",
     "last_device_status", "status_string", "DTYPES",
 ]
 
@@ -62,6 +62,12 @@ def library() -> ctypes.CDLL:
         lib.smx_softmax_row_stats.restype = st
         lib.smx_softmax_merge_stats.argtypes = [P, P, P, P, P, P, I64, P]
         lib.smx_softmax_merge_stats.restype = st
+        lib.smx_log_softmax_rows.argtypes = [P, P, I64, I64, P, I32, I32, P]
+        lib.smx_log_softmax_rows.restype = st
+        lib.smx_softmax_lse.argtypes = [P, P, I64, I64, P, I32, P]
+        lib.smx_softmax_lse.restype = st
+        lib.smx_softmax_apply_stats.argtypes = [P, P, P, P, I64, I64, P, I32, I32, P]
+        lib.smx_softmax_apply_stats.restype = st
         lib.smx_last_device_status.argtypes = [P]
         lib.smx_last_device_status.restype = st
         lib.smx_status_string.argtypes = [st]
@@ -203,6 +209,66 @@ def softmax_merge_stats(m_a, d_a, m_b, d_b, m_out=None, d_out=None, stream=None)
     if st != 0:
         raise SmxError(st, "smx_softmax_merge_stats")
     return m_out, d_out
+
+
+def _rows_vec(t, rows, device, name):
+    if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == rows
+            and t.device == device):
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of length rows")
+    return t.data_ptr()
+
+
+def log_softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None,
+                     valid_len: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                     stream=None) -> torch.Tensor:
+    """y[r, j] = (x[r, j] - m_r) - log d_r over the valid prefix; -inf elsewhere."""
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype or x.dtype, device=x.device)
+    _check_2d(out, "out")
+    if out.shape != x.shape or out.device != x.device:
+        raise ValueError("out must match x's shape and device")
+    st = library().smx_log_softmax_rows(x.data_ptr(), out.data_ptr(), rows, cols,
+                                        _lengths(valid_len, rows, x.device), _dtype(x.dtype),
+                                        _dtype(out.dtype), _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_log_softmax_rows")
+    return out
+
+
+def softmax_lse(x: torch.Tensor, valid_len: torch.Tensor | None = None, out=None, stream=None):
+    """Per-row log-sum-exp m + log d in fp32."""
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    st = library().smx_softmax_lse(x.data_ptr(), _rows_vec(out, rows, x.device, "out"), rows, cols,
+                                   _lengths(valid_len, rows, x.device), _dtype(x.dtype),
+                                   _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_lse")
+    return out
+
+
+def softmax_apply_stats(x: torch.Tensor, m: torch.Tensor, d: torch.Tensor, out: torch.Tensor | None = None,
+                        valid_len: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                        stream=None) -> torch.Tensor:
+    """y[r, j] = exp(x[r, j] - m[r]) / d[r] over the valid prefix, +0 elsewhere."""
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype or x.dtype, device=x.device)
+    _check_2d(out, "out")
+    if out.shape != x.shape or out.device != x.device:
+        raise ValueError("out must match x's shape and device")
+    st = library().smx_softmax_apply_stats(x.data_ptr(), _rows_vec(m, rows, x.device, "m"),
+                                           _rows_vec(d, rows, x.device, "d"), out.data_ptr(), rows,
+                                           cols, _lengths(valid_len, rows, x.device),
+                                           _dtype(x.dtype), _dtype(out.dtype), _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_apply_stats")
+    return out
 
 
 def last_device_status(stream=None) -> int:

@@ -22,19 +22,26 @@
 //   MODE_STATS    the (m, d) block summary of each item ("Stable softmax: keep
 //                 the normalizer consistent as tiles arrive", third paragraph),
 //                 at m_out[k], d_out[k] (k counted from the launch's first item;
-//                 for whole rows, the row - row0).
-//   MODE_APPLY    chunks only: merge the row's chunk summaries m_in, d_in
-//                 ("Online stable softmax", "Derive the update for two blocks";
-//                 once per row a CTA meets) and normalise the chunk with the
-//                 merged (M, D) -- the step that completes a softmax whose
-//                 summaries were computed apart.
+//                 for whole rows, the row - row0).  With d_out == nullptr
+//                 (whole rows) m_out receives LSE = m + log d instead
+//                 ("Softmax numerics architecture...", "Log-sum-exp:
+//                 log-probabilities without probabilities").
+//   MODE_LOG      whole rows: log_softmax y = (x - m) - log d, the same section;
+//                 -inf in masked lanes (the log of their +0 probability).
+//   MODE_APPLY    chunks only: the row's (M, D) -- given per row (Items::
+//                 row_stats), or merged from the row's chunk summaries m_in,
+//                 d_in ("Online stable softmax", "Derive the update for two
+//                 blocks"; once per row a CTA meets) -- normalises the chunk:
+//                 the step that completes a softmax whose summaries were
+//                 computed apart.
+//   MODE_APPLY_LOG  as MODE_APPLY, writing log_softmax.
 #pragma once
 
 #include "row_core.cuh"
 
 namespace smx {
 
-enum : int { MODE_APPLY = 2 };
+enum : int { MODE_APPLY = 2, MODE_LOG = 3, MODE_APPLY_LOG = 4 };
 
 // The items of one launch: item k is chunk k % nchunks of row row0 + k / nchunks.
 struct Items {
@@ -44,6 +51,7 @@ struct Items {
   int chunk;     // elements per item (a multiple of the vector width; a row's last item may be shorter)
   int nchunks;   // items per row (1: whole rows)
   int l2_hint;   // chunked reads only: 0 none, 1 keep in L2 (evict_last), 2 evict_first
+  int row_stats; // apply modes: 1 = (m_in[r], d_in[r]) per row, 0 = merge the row's chunk summaries
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
@@ -81,7 +89,8 @@ __global__ void SMX_STREAM_REGS
     k_rows_stream(const InT* __restrict__ x, OutT* __restrict__ y, float* __restrict__ m_out,
                   float* __restrict__ d_out, const float* __restrict__ m_in,
                   const float* __restrict__ d_in, Items it, const int32_t* __restrict__ valid_len) {
-  static_assert(CHUNKED || MODE != MODE_APPLY, "the apply mode walks chunks");
+  constexpr bool APPLY = (MODE == MODE_APPLY || MODE == MODE_APPLY_LOG);
+  static_assert(CHUNKED || !APPLY, "the apply modes walk chunks");
   constexpr int V = Elem<InT>::V;
   extern __shared__ __align__(16) uint4 sbuf[];  // [DEPTH][VPT][G]: thread g owns column g
   // s_max alternates between items: an item with no valid lane skips the sum's
@@ -173,6 +182,7 @@ __global__ void SMX_STREAM_REGS
   // the apply mode's merged summary of the row it is in
   int64_t have_row = -1;
   MD row_md{neg_inf(), 0.0f};
+  float row_ld = 0.0f;  // log of row_md.d (the log modes)
   int mpar = 0;
 
   for (int d = 0, par = 0; cur.k < k_end; advance(cur), par ^= 1) {
@@ -194,40 +204,49 @@ __global__ void SMX_STREAM_REGS
     advance(pf);
     d = d + 1 == DEPTH ? 0 : d + 1;
 
-    if constexpr (MODE == MODE_APPLY) {
+    if constexpr (APPLY) {
       if (cur.r != have_row) {  // uniform: every thread walks the same items
-        MD acc{neg_inf(), 0.0f};
-        const int64_t k0 = cur.r * it.nchunks;
-        for (int i = g; i < it.nchunks; i += G)
-          acc = md_merge(acc, MD{__ldg(m_in + k0 + i), __ldg(d_in + k0 + i)});
-        acc = warp_merge(acc);
-        if (lane == 0) {
-          s_mm[mpar][warp] = acc.m;
-          s_dd[mpar][warp] = acc.d;
+        if (it.row_stats) {
+          row_md = MD{__ldg(m_in + cur.r), __ldg(d_in + cur.r)};
+        } else {
+          MD acc{neg_inf(), 0.0f};
+          const int64_t k0 = cur.r * it.nchunks;
+          for (int i = g; i < it.nchunks; i += G)
+            acc = md_merge(acc, MD{__ldg(m_in + k0 + i), __ldg(d_in + k0 + i)});
+          acc = warp_merge(acc);
+          if (lane == 0) {
+            s_mm[mpar][warp] = acc.m;
+            s_dd[mpar][warp] = acc.d;
+          }
+          __syncthreads();
+          row_md = warp_merge(lane < nw ? MD{s_mm[mpar][lane], s_dd[mpar][lane]} : MD{neg_inf(), 0.0f});
+          mpar ^= 1;
         }
-        __syncthreads();
-        row_md = warp_merge(lane < nw ? MD{s_mm[mpar][lane], s_dd[mpar][lane]} : MD{neg_inf(), 0.0f});
-        mpar ^= 1;
         have_row = cur.r;
+        row_ld = logf(row_md.d);
       }
       const float M = row_md.m, Dr = row_md.d;
       const bool zero_row = (M == neg_inf());
-      const bool nan_row = !zero_row && (Dr != Dr);
-      const OutConst kc = make_out_const<OutT>(M, Dr);
+      const bool nan_row = !zero_row && (Dr != Dr || M != M || M == pos_inf());
       OutT* yr = y + row * it.cols + (int64_t)cur.c * ncols;
+      if constexpr (MODE == MODE_APPLY_LOG) {
+        store_log<OutT, VPT, V>(yr, G, g, len, L, v, zero_row, nan_row, M, row_ld);
+      } else {
+        const OutConst kc = make_out_const<OutT>(M, Dr);
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int e0 = (j * G + g) * V;
-        if (e0 < len) {
-          float p[V];
-          if (!zero_row && !nan_row) {
+        for (int j = 0; j < VPT; ++j) {
+          const int e0 = (j * G + g) * V;
+          if (e0 < len) {
+            float p[V];
+            if (!zero_row && !nan_row) {
 #pragma unroll
-            for (int i = 0; i < V; ++i) p[i] = out_value<OutT>(v[j][i], kc);
-          } else {
+              for (int i = 0; i < V; ++i) p[i] = out_value<OutT>(v[j][i], kc);
+            } else {
 #pragma unroll
-            for (int i = 0; i < V; ++i) p[i] = (nan_row && e0 + i < L) ? qnan() : 0.0f;
+              for (int i = 0; i < V; ++i) p[i] = (nan_row && e0 + i < L) ? qnan() : 0.0f;
+            }
+            store_vec<OutT, V>(yr + e0, p);
           }
-          store_vec<OutT, V>(yr + e0, p);
         }
       }
     } else {
@@ -237,16 +256,28 @@ __global__ void SMX_STREAM_REGS
       const float M = warp_max_nan(lane < nw ? s_max[par][lane] : neg_inf());
       float Dsum = 0.0f;
       if (M != neg_inf()) {
-        float sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
+        float sum;
+        if constexpr (MODE == MODE_LOG) sum = warp_sum(sum_exp(v, M));  // v keeps x
+        else sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
         if (lane == 0) s_sum[warp] = sum;
         __syncthreads();
         Dsum = warp_sum(lane < nw ? s_sum[lane] : 0.0f);
       }
       if constexpr (MODE == MODE_STATS) {
         if (g == 0) {
-          m_out[cur.k] = M;
-          d_out[cur.k] = M == neg_inf() ? 0.0f : stats_correct(Dsum, M);
+          const float dk = M == neg_inf() ? 0.0f : stats_correct(Dsum, M);
+          if (d_out != nullptr) {
+            m_out[cur.k] = M;
+            d_out[cur.k] = dk;
+          } else {
+            m_out[cur.k] = M == neg_inf() ? neg_inf() : __fadd_rn(M, logf(dk));
+          }
         }
+      } else if constexpr (MODE == MODE_LOG) {
+        const bool zero_row = (M == neg_inf());
+        const bool nan_row = !zero_row && (Dsum != Dsum);
+        const float ld = zero_row ? 0.0f : logf(stats_correct(Dsum, M));
+        store_log<OutT, VPT, V>(y + row * it.cols, G, g, len, L, v, zero_row, nan_row, M, ld);
       } else {
         const bool zero_row = (M == neg_inf());
         const bool nan_row = !zero_row && (Dsum != Dsum);
@@ -259,7 +290,8 @@ __global__ void SMX_STREAM_REGS
 }
 
 // Row statistics of long rows: merge each row's nchunks chunk summaries
-// (consecutive in m_in, d_in) into (m_out[r], d_out[r]); one CTA per row.
+// (consecutive in m_in, d_in) into (m_out[r], d_out[r]), or into
+// m_out[r] = LSE when d_out is null; one CTA per row.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
     k_merge_chunk_stats(const float* __restrict__ m_in, const float* __restrict__ d_in, int nchunks,
@@ -278,8 +310,13 @@ __global__ void __launch_bounds__(THREADS)
   if (warp == 0) {
     acc = warp_merge(lane < THREADS / 32 ? MD{s_mm[lane], s_dd[lane]} : MD{neg_inf(), 0.0f});
     if (lane == 0) {
-      m_out[blockIdx.x] = acc.m;
-      d_out[blockIdx.x] = acc.m == neg_inf() ? 0.0f : acc.d;
+      const float d = acc.m == neg_inf() ? 0.0f : acc.d;
+      if (d_out != nullptr) {
+        m_out[blockIdx.x] = acc.m;
+        d_out[blockIdx.x] = d;
+      } else {  // LSE = m + log d
+        m_out[blockIdx.x] = acc.m == neg_inf() ? neg_inf() : __fadd_rn(acc.m, logf(d));
+      }
     }
   }
 }

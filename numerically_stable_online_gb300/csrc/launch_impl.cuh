@@ -136,57 +136,77 @@ cudaError_t launch_stream_v(const Call& c, const Plan& p, const Items& it) {
   }
 }
 
-// Whole rows (softmax or row statistics).
+// Whole rows: softmax, row statistics (or LSE), log_softmax; or the apply mode
+// with the given per-row statistics, each row one chunk.
 template <typename InT, typename OutT, int MODE>
 cudaError_t launch_stream(const Call& c, const Plan& p) {
-  const Items it{c.rows, 0, c.cols, (int)c.cols, 1, 0};
-  switch (p.vpt) {
-    case 1: return launch_stream_v<InT, OutT, MODE, 1>(c, p, it);
-    case 2: return launch_stream_v<InT, OutT, MODE, 2>(c, p, it);
-    case 4: return launch_stream_v<InT, OutT, MODE, 4>(c, p, it);
-    case 8: return launch_stream_v<InT, OutT, MODE, 8>(c, p, it);
-    default: return cudaErrorInvalidValue;
+  if constexpr (MODE == MODE_APPLY) {
+    const Items it{c.rows, 0, c.cols, (int)c.cols, 1, 0, 1};
+    switch (p.vpt) {
+      case 1: return launch_stream_k<InT, OutT, MODE, 1, 2, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+      case 2: return launch_stream_k<InT, OutT, MODE, 2, 2, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+      case 4: return launch_stream_k<InT, OutT, MODE, 4, 2, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    const Items it{c.rows, 0, c.cols, (int)c.cols, 1, 0, 0};
+    switch (p.vpt) {
+      case 1: return launch_stream_v<InT, OutT, MODE, 1>(c, p, it);
+      case 2: return launch_stream_v<InT, OutT, MODE, 2>(c, p, it);
+      case 4: return launch_stream_v<InT, OutT, MODE, 4>(c, p, it);
+      case 8: return launch_stream_v<InT, OutT, MODE, 8>(c, p, it);
+      default: return cudaErrorInvalidValue;
+    }
   }
 }
 
-// Long rows in slabs of rows: per slab, the streamed kernel computes every
-// chunk's summary, then normalises every chunk with its row's merged (M, D)
-// (row statistics merge the summaries instead).  Chunks are 16 elements per
-// thread.  The summaries live in a stream-ordered scratch allocation for the
-// call, or in p.scratch when given.
+// Long rows in chunks of 16 elements per thread.  Softmax and log_softmax, in
+// slabs of rows: the streamed kernel computes every chunk's summary, then
+// normalises every chunk with its row's merged (M, D); row statistics (or LSE)
+// merge the summaries instead.  The summaries live in a stream-ordered scratch
+// allocation for the call, or in p.scratch when given.  The apply mode has its
+// statistics and takes one pass over all rows.
 template <typename InT, typename OutT, int MODE>
 cudaError_t launch_split(const Call& c, const Plan& p) {
   constexpr int SV = 16 / Elem<InT>::V;
-  const int64_t slab = p.slab_rows;
-  const size_t part_n = (size_t)slab * p.nchunks;
-  const size_t bytes = split_scratch_bytes(slab, p.nchunks);
-  char* base = reinterpret_cast<char*>(p.scratch);
-  cudaError_t e = cudaSuccess;
-  if (base == nullptr) {
-    e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, c.stream);
-    if (e != cudaSuccess) return e;
-  }
-  float* pm = reinterpret_cast<float*>(base);
-  float* pd = pm + part_n;
-  for (int64_t r0 = 0; r0 < c.rows && e == cudaSuccess; r0 += slab) {
-    const int64_t n = c.rows - r0 < slab ? c.rows - r0 : slab;
-    const Items st{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, p.l2_hint_stats};
-    e = launch_stream_k<InT, float, MODE_STATS, SV, 2, true>(c, p, st, pm, pd, nullptr, nullptr);
-    if (e != cudaSuccess) break;
-    if constexpr (MODE == MODE_SOFTMAX) {
-      const Items ap{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, p.l2_hint_apply};
-      e = launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
-    } else {
-      k_merge_chunk_stats<256><<<(unsigned)n, 256, 0, c.stream>>>(pm, pd, p.nchunks, c.m_out + r0,
-                                                                   c.d_out + r0);
-      e = cudaGetLastError();
+  if constexpr (MODE == MODE_APPLY) {
+    const Items it{c.rows * p.nchunks, 0, c.cols, (int)p.chunk, p.nchunks, 0, 1};
+    return launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, it, nullptr, nullptr, c.m_in,
+                                                               c.d_in);
+  } else {
+    const int64_t slab = p.slab_rows;
+    const size_t part_n = (size_t)slab * p.nchunks;
+    const size_t bytes = split_scratch_bytes(slab, p.nchunks);
+    char* base = reinterpret_cast<char*>(p.scratch);
+    cudaError_t e = cudaSuccess;
+    if (base == nullptr) {
+      e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, c.stream);
+      if (e != cudaSuccess) return e;
     }
+    float* pm = reinterpret_cast<float*>(base);
+    float* pd = pm + part_n;
+    for (int64_t r0 = 0; r0 < c.rows && e == cudaSuccess; r0 += slab) {
+      const int64_t n = c.rows - r0 < slab ? c.rows - r0 : slab;
+      const Items st{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, p.l2_hint_stats, 0};
+      e = launch_stream_k<InT, float, MODE_STATS, SV, 2, true>(c, p, st, pm, pd, nullptr, nullptr);
+      if (e != cudaSuccess) break;
+      const Items ap{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, p.l2_hint_apply, 0};
+      if constexpr (MODE == MODE_SOFTMAX) {
+        e = launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
+      } else if constexpr (MODE == MODE_LOG) {
+        e = launch_stream_k<InT, OutT, MODE_APPLY_LOG, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
+      } else {
+        k_merge_chunk_stats<256><<<(unsigned)n, 256, 0, c.stream>>>(
+            pm, pd, p.nchunks, c.m_out + r0, c.d_out == nullptr ? nullptr : c.d_out + r0);
+        e = cudaGetLastError();
+      }
+    }
+    if (p.scratch == nullptr) {
+      const cudaError_t f = cudaFreeAsync(base, c.stream);
+      if (e == cudaSuccess) e = f;
+    }
+    return e;
   }
-  if (p.scratch == nullptr) {
-    const cudaError_t f = cudaFreeAsync(base, c.stream);
-    if (e == cudaSuccess) e = f;
-  }
-  return e;
 }
 
 template <typename InT, typename OutT, int MODE>
@@ -194,8 +214,8 @@ cudaError_t launch_generic(const Call& c) {
   for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
     const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
     k_rows_generic<InT, OutT, MODE><<<(unsigned)n, GENERIC_THREADS, 0, c.stream>>>(
-        static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, r0 + n, c.cols,
-        c.valid_len, r0);
+        static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, c.m_in, c.d_in,
+        r0 + n, c.cols, c.valid_len, r0);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -204,11 +224,16 @@ cudaError_t launch_generic(const Call& c) {
 
 template <typename InT, typename OutT, int MODE>
 cudaError_t launch_typed(const Call& c, const Plan& p) {
+  constexpr bool CLASSIC = (MODE == MODE_SOFTMAX || MODE == MODE_STATS);
   switch (p.path) {
     case PATH_REGS:
-      return p.warp_rows ? launch_regs_wr<InT, OutT, MODE, true>(c, p)
-                         : launch_regs_wr<InT, OutT, MODE, false>(c, p);
-    case PATH_CLUSTER: return launch_cluster<InT, OutT, MODE>(c, p);
+      if constexpr (CLASSIC)
+        return p.warp_rows ? launch_regs_wr<InT, OutT, MODE, true>(c, p)
+                           : launch_regs_wr<InT, OutT, MODE, false>(c, p);
+      return cudaErrorInvalidValue;
+    case PATH_CLUSTER:
+      if constexpr (CLASSIC) return launch_cluster<InT, OutT, MODE>(c, p);
+      return cudaErrorInvalidValue;
     case PATH_GENERIC: return launch_generic<InT, OutT, MODE>(c);
     case PATH_STREAM: return launch_stream<InT, OutT, MODE>(c, p);
     case PATH_SPLIT: return launch_split<InT, OutT, MODE>(c, p);
@@ -216,13 +241,23 @@ cudaError_t launch_typed(const Call& c, const Plan& p) {
   }
 }
 
+template <typename InT, int MODE>
+cudaError_t launch_out(const Call& c, const Plan& p) {
+  switch (c.out_dtype) {
+    case 0: return launch_typed<InT, float, MODE>(c, p);
+    case 1: return launch_typed<InT, __half, MODE>(c, p);
+    case 2: return launch_typed<InT, __nv_bfloat16, MODE>(c, p);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <typename InT>
 cudaError_t launch_in(const Call& c, const Plan& p) {
-  if (c.mode == MODE_STATS) return launch_typed<InT, float, MODE_STATS>(c, p);
-  switch (c.out_dtype) {
-    case 0: return launch_typed<InT, float, MODE_SOFTMAX>(c, p);
-    case 1: return launch_typed<InT, __half, MODE_SOFTMAX>(c, p);
-    case 2: return launch_typed<InT, __nv_bfloat16, MODE_SOFTMAX>(c, p);
+  switch (c.mode) {
+    case MODE_SOFTMAX: return launch_out<InT, MODE_SOFTMAX>(c, p);
+    case MODE_STATS: return launch_typed<InT, float, MODE_STATS>(c, p);
+    case MODE_APPLY: return launch_out<InT, MODE_APPLY>(c, p);
+    case MODE_LOG: return launch_out<InT, MODE_LOG>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -78,12 +78,20 @@ __device__ __forceinline__ float local_max(const float (&v)[VPT][V]) {
 template <typename OutT, int MODE, int VPT, int V>
 __device__ __forceinline__ float exp_and_sum(float (&v)[VPT][V], float M) {
   using P = ExpPolicy<OutT, MODE>;
-  float s = 0.0f;
   if constexpr (P::ACCURATE) {
+    float s = 0.0f;
 #pragma unroll
-    for (int j = 0; j < VPT; ++j)
+    for (int j = 0; j < VPT; ++j) {
+      float sk[V];
 #pragma unroll
-      for (int i = 0; i < V; ++i) v[j][i] = exp_shift_accurate(v[j][i], M);
+      for (int i = 0; i < V; ++i) sk[i] = v[j][i] = exp_shift_accurate(v[j][i], M);
+#pragma unroll
+      for (int w = V / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) sk[i] = __fadd_rn(sk[i], sk[i + w]);
+      s = __fadd_rn(s, sk[0]);
+    }
+    return s;
   } else {
     // u = x * L2E_HI + c two lanes at a time (f32x2), then exp2 per lane; with
     // |M| near the top of the fp32 range -M * log2 e would overflow, so there
@@ -120,18 +128,57 @@ __device__ __forceinline__ float exp_and_sum(float (&v)[VPT][V], float M) {
     }
     return __fadd_rn(pk_lo(acc), pk_hi(acc));
   }
+}
+
+// This thread's share of sum_j e^(x_j - M) as the statistics path forms it
+// (to be corrected by stats_correct), leaving v unchanged.  Requires M != -inf.
+template <int VPT, int V>
+__device__ __forceinline__ float sum_exp(const float (&v)[VPT][V], float M) {
+  const bool huge = !(fabsf(M) < 1e38f);
+  const float c = huge ? 0.0f : __fmul_rn(-M, L2E_HI);
+  const float msub = huge ? M : 0.0f;
+  const unsigned long long k2 = pk(L2E_HI, L2E_HI), c2 = pk(c, c);
+  unsigned long long acc = pk(0.0f, 0.0f);
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
-    float sk[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) sk[i] = v[j][i];
-#pragma unroll
-    for (int w = V / 2; w > 0; w >>= 1)
-#pragma unroll
-      for (int i = 0; i < w; ++i) sk[i] = __fadd_rn(sk[i], sk[i + w]);
-    s = __fadd_rn(s, sk[0]);
+    for (int i = 0; i < V; i += 2) {
+      const float a = huge ? __fsub_rn(v[j][i], msub) : v[j][i];
+      const float b = huge ? __fsub_rn(v[j][i + 1], msub) : v[j][i + 1];
+      const unsigned long long u = fma2(pk(a, b), k2, c2);
+      acc = add2(acc, pk(ex2_ftz(pk_lo(u)), ex2_ftz(pk_hi(u))));
+    }
   }
-  return s;
+  return __fadd_rn(pk_lo(acc), pk_hi(acc));
+}
+
+// Store log_softmax of the row held in v (inputs x): (x - M) - ld with
+// ld = log D, two subtractions so that the result does not carry the rounding
+// of a large M + log D; -inf in masked lanes (x = -inf there already) and on
+// zero rows; NaN in the valid lanes of NaN rows.
+template <typename OutT, int VPT, int V>
+__device__ __forceinline__ void store_log(OutT* yr, int G, int g, int ncols, int L, const float (&v)[VPT][V],
+                                          bool zero_row, bool nan_row, float M, float ld) {
+  const unsigned long long nm = pk(-M, -M), nl = pk(-ld, -ld);
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int e0 = (j * G + g) * V;
+    if (e0 < ncols) {
+      float q[V];
+      if (!zero_row && !nan_row) {
+#pragma unroll
+        for (int i = 0; i < V; i += 2) {
+          const unsigned long long t = add2(add2(pk(v[j][i], v[j][i + 1]), nm), nl);
+          q[i] = pk_lo(t);
+          q[i + 1] = pk_hi(t);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) q[i] = (nan_row && e0 + i < L) ? qnan() : neg_inf();
+      }
+      store_vec<OutT, V>(yr + e0, q);
+    }
+  }
 }
 
 // The statistics path's d: the sum of exp2(fma(x, L2E_HI, c_hi)) times

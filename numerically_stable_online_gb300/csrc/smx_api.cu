@@ -194,7 +194,7 @@ int stream_occupancy(int in_dtype, int vpt, int threads, int depth) {
 constexpr int64_t STREAM_INFLIGHT_BYTES = 48 * 1024;
 
 bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
-                 bool has_lengths, Plan* p) {
+                 bool has_lengths, bool apply, Plan* p) {
   const int es = elem_size(in_dtype);
   if (cols * es > STREAM_MAX_ROW_BYTES) return false;
   Plan r;
@@ -207,7 +207,7 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
     if (r.vpt * V > (accurate_exp ? 16 : 32)) return false;
   }
   const int dd = g_stream_depth.load();
-  const int depth = (dd == 3 || dd == 4) ? dd : 2;
+  const int depth = (!apply && (dd == 3 || dd == 4)) ? dd : 2;  // the apply kernel prefetches 2
   const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth);
   if (occ_max <= 0) return false;
   int occ = occ_max;
@@ -300,28 +300,34 @@ smx_status run(Call& c, DeviceInfo& dev) {
       (reinterpret_cast<uintptr_t>(c.x) % 16 == 0) &&
       (c.mode == MODE_STATS || reinterpret_cast<uintptr_t>(c.y) % 16 == 0) &&
       ((c.cols * es_in) % 16 == 0) && c.cols > 0;
+  // softmax and (m, d) statistics run on every kernel; LSE, log_softmax and
+  // the apply mode on the streamed, long-row and generic ones
+  const bool classic = c.mode == MODE_SOFTMAX || (c.mode == MODE_STATS && c.d_out != nullptr);
   Plan p;
   const int force = g_force_path.load();
   bool planned = false;
   if (vec_ok) {
-    if (force == PATH_CLUSTER) {
+    if (force == PATH_CLUSTER && classic) {
       planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     } else if (force == PATH_SPLIT) {
       planned = plan_split(dev, c.cols, c.in_dtype, &p);
     } else if (force != PATH_GENERIC) {
-      const bool acc = c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32;
-      if (force != PATH_REGS)
-        planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, &p);
-      if (!planned) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
+      // the compensated exponential (fp32 softmax outputs, and every apply
+      // output) holds 16 elements per thread at most
+      const bool acc = (c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32) || c.mode == MODE_APPLY;
+      if (force != PATH_REGS || !classic)
+        planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr,
+                              c.mode == MODE_APPLY, &p);
+      if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       // rows longer than one CTA holds: a row per thread-block cluster when the
       // rows fill every resident cluster, else (a few very long rows) L2 slabs,
       // which spread every row over all SMs
-      if (!planned) {
+      if (!planned && classic) {
         planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
         if (planned && c.rows < p.resident_clusters) planned = false;
       }
       if (!planned) planned = plan_split(dev, c.cols, c.in_dtype, &p);
-      if (!planned) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
+      if (!planned && classic) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     }
   }
   if (!planned) p.path = PATH_GENERIC;
@@ -501,6 +507,62 @@ smx_status smx_softmax_row_stats(const void* x, float* m_out, float* d_out, int6
   if (s != SMX_OK) return s;
   Call c{x, nullptr, m_out, d_out, rows, cols, valid_len, (int)in_dtype, SMX_F32, MODE_STATS,
          reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  return run(c, *dev);
+}
+
+smx_status smx_log_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
+                                const int32_t* valid_len, smx_dtype in_dtype, smx_dtype out_dtype,
+                                smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return SMX_OK;
+  if (x == nullptr || y == nullptr) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype), ny = rows * cols * elem_size(out_dtype);
+  if (overlaps(x, nx, y, ny)) return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, y, ny)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
+         MODE_LOG, reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  return run(c, *dev);
+}
+
+smx_status smx_softmax_lse(const void* x, float* lse_out, int64_t rows, int64_t cols,
+                           const int32_t* valid_len, smx_dtype in_dtype, smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype)) return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0) return SMX_OK;
+  if (lse_out == nullptr || (cols > 0 && x == nullptr)) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype);
+  if (overlaps(x, nx, lse_out, rows * 4)) return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, lse_out, rows * 4)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{x, nullptr, lse_out, nullptr, rows, cols, valid_len, (int)in_dtype, SMX_F32, MODE_STATS,
+         reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  return run(c, *dev);
+}
+
+smx_status smx_softmax_apply_stats(const void* x, const float* m_in, const float* d_in, void* y,
+                                   int64_t rows, int64_t cols, const int32_t* valid_len,
+                                   smx_dtype in_dtype, smx_dtype out_dtype, smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return SMX_OK;
+  if (x == nullptr || y == nullptr || m_in == nullptr || d_in == nullptr) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype), ny = rows * cols * elem_size(out_dtype);
+  if (overlaps(x, nx, y, ny) || overlaps(m_in, rows * 4, y, ny) || overlaps(d_in, rows * 4, y, ny))
+    return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, y, ny)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
+         MODE_APPLY, reinterpret_cast<cudaStream_t>(stream), nullptr, 0, m_in, d_in};
   return run(c, *dev);
 }
 

@@ -167,15 +167,9 @@ __device__ __forceinline__ unsigned long long pk(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float pk_lo(unsigned long long v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo;
-}
+__device__ __forceinline__ float pk_lo(unsigned long long v) { return __uint_as_float((unsigned)v); }
 __device__ __forceinline__ float pk_hi(unsigned long long v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return hi;
+  return __uint_as_float((unsigned)(v >> 32));
 }
 __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
                                                     unsigned long long c) {

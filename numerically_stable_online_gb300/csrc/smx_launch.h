@@ -17,10 +17,13 @@ struct Call {
   int64_t rows, cols;
   const int32_t* valid_len;
   int in_dtype, out_dtype;  // smx_dtype values
-  int mode;                 // 0 softmax, 1 row statistics
+  int mode;                 // 0 softmax, 1 row statistics (LSE if d_out is null), 2 apply given
+                            // statistics, 3 log_softmax (the kernels' MODE_* values)
   cudaStream_t stream;
   int* status;              // device status word
   int64_t max_polls;        // bound of each staging wait
+  const float* m_in = nullptr;  // apply: per-row statistics
+  const float* d_in = nullptr;
 };
 
 struct Plan {

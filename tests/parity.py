@@ -69,3 +69,75 @@ def compare(y, p, out_dtype, valid_len=None, rows_sel=None):
         stats["frac_exact"] = float((diff == 0).mean()) if diff.size else 1.0
         assert stats["max_ulp"] <= 1, f"max ulp difference {stats['max_ulp']}"
     return stats
+
+
+# ---------------------------------------------------------------------------
+# Log-space outputs.  The kernels form log_softmax as (x - m) - log d in fp32
+# with d the fp32 sum: each subtraction rounds once (relative 2^-24 of |x - m|
+# <= |y| + log d, and of |y|), log d comes from the correctly rounded-to-1-ulp
+# logf of a sum whose relative error is at most 2^-18 (64 roundings or
+# approximations of 2^-24 each along the summation tree and the exponentials),
+# and an error e in d moves log d by e.  So
+#     |y - ref| <= 2^-22 (|ref| + log d) + 2^-18
+# for fp32 outputs, plus one unit of the format's spacing at |ref| for fp16 and
+# bf16 outputs.  LSE = m + log d: |lse - ref| <= 2^-23 |ref| + 2^-22 log d + 2^-18.
+# Masked lanes and the lanes of empty / all -inf rows are -inf bit for bit.
+# ---------------------------------------------------------------------------
+LOG_ABS = 2.0 ** -18
+NEG_INF_BITS = {"f32": 0xFF800000, "f16": 0xFC00, "bf16": 0xFF80}
+# magnitudes that round to infinity: the largest finite value plus half its spacing
+OVERFLOW = {"f32": 2.0**128 - 2.0**103, "f16": 65520.0, "bf16": 2.0**128 - 2.0**119}
+
+
+def format_spacing(v, fmt):
+    """Spacing of the fp16 / bf16 grid at |v| (subnormal spacing at the bottom)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 1e-300)))
+    if fmt == "bf16":
+        return 2.0 ** np.maximum(e - 7, -133)
+    return 2.0 ** np.maximum(e - 10, -24)
+
+
+def _decoded(y, out_dtype, n, cols):
+    if out_dtype == "f32":
+        y = np.asarray(y, dtype=np.float32).reshape(n, cols)
+        return y.astype(np.float64), y.view(np.uint32).astype(np.int64)
+    bits = np.asarray(y).view(np.uint16).reshape(n, cols)
+    return oracle.decode(bits, out_dtype), bits.astype(np.int64)
+
+
+def compare_log(y, ref, log_d, out_dtype, valid_len=None, rows_sel=None):
+    """y: stored log_softmax output; ref: fp64 reference [n, cols]; log_d: fp64 [n]."""
+    n, cols = ref.shape
+    L = lengths(n, cols, None if valid_len is None else
+                (np.asarray(valid_len)[rows_sel] if rows_sel is not None else valid_len))
+    masked = np.arange(cols)[None, :] >= L[:, None]
+    yv, bits = _decoded(y, out_dtype, n, cols)
+    ninf = NEG_INF_BITS[out_dtype]
+    assert np.all(bits[masked] == ninf), "masked lanes must be -inf"
+    nan_rows = np.isnan(ref).any(axis=1)
+    assert np.all(np.isnan(yv[nan_rows[:, None] & ~masked])), "NaN rows must be NaN"
+    # probability 0, or a log-probability beyond the format's range (rounds to -inf)
+    inf_lanes = ~nan_rows[:, None] & ~masked & (ref <= -OVERFLOW[out_dtype])
+    assert np.all(bits[inf_lanes] == ninf), "lanes of probability 0 must be -inf"
+    ok = ~nan_rows[:, None] & ~masked & np.isfinite(ref) & (ref > -OVERFLOW[out_dtype])
+    ld = np.broadcast_to(np.asarray(log_d, dtype=np.float64)[:, None], ref.shape)
+    tol = 2.0 ** -22 * (np.abs(ref) + ld) + LOG_ABS
+    if out_dtype != "f32":
+        tol = tol + format_spacing(ref, out_dtype)
+    err = np.abs(yv[ok] - ref[ok])
+    worst = float((err / tol[ok]).max()) if ok.any() else 0.0
+    assert worst <= 1.0, f"log_softmax error {worst:.3f} x tolerance"
+    return {"max_err_over_tol": worst, "max_abs": float(err.max()) if ok.any() else 0.0}
+
+
+def compare_lse(lse, ref, log_d):
+    lse = np.asarray(lse, dtype=np.float64)
+    assert np.array_equal(np.isnan(lse), np.isnan(ref)), "NaN rows"
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref)), "empty rows are -inf"
+    ok = np.isfinite(ref)
+    tol = 2.0 ** -23 * np.abs(ref[ok]) + 2.0 ** -22 * np.asarray(log_d)[ok] + LOG_ABS
+    err = np.abs(lse[ok] - ref[ok])
+    worst = float((err / tol).max()) if ok.any() else 0.0
+    assert worst <= 1.0, f"LSE error {worst:.3f} x tolerance"
+    return {"lse_err_over_tol": worst}
