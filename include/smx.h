@@ -183,6 +183,45 @@ smx_status smx_softmax_apply_stats(const void *x, const float *m_in, const float
                                    smx_dtype in_dtype, smx_dtype out_dtype, smx_stream_t stream);
 
 /*
+ * Softmax backward ("Softmax numerics architecture...", section "The
+ * Jacobian, and the backward pass that never divides"): the vector-Jacobian
+ * product, without forming the Jacobian diag(p) - p p^T:
+ *     dx[r, j] = p[r, j] (g[r, j] - s_r),   s_r = sum_{k < L_r} g[r, k] p[r, k]
+ * over the valid prefix, dx = 0 in masked lanes.
+ *   p        device [rows, cols], dtype: the forward softmax as stored.
+ *   g        device [rows, cols], dtype: the upstream gradient dL/dy.
+ *   dx       device [rows, cols], dx_dtype: written (masked lanes included).
+ *            Must not overlap p, g or valid_len (SMX_ERR_ALIAS).
+ *   valid_len, rows, cols: as smx_softmax_rows.  The sum is fp32 whatever the
+ *   types.  A NaN among a row's valid p or g makes its valid lanes NaN.
+ */
+smx_status smx_softmax_backward(const void *p, const void *g, void *dx, int64_t rows, int64_t cols,
+                                const int32_t *valid_len, smx_dtype dtype, smx_dtype dx_dtype,
+                                smx_stream_t stream);
+
+/*
+ * Cross-entropy with logits and its fused gradient ("Softmax numerics
+ * architecture...", sections "Log-sum-exp: log-probabilities without
+ * probabilities" and "The Jacobian, and the backward pass that never divides"):
+ *     loss[r] = LSE_r - x[r, t_r] = (m_r - x[r, t_r]) + log d_r      (fp32)
+ *     grad[r, j] = p[r, j] - [j == t_r]   over the valid prefix, 0 beyond.
+ * The gradient is formed directly (never through -1/p), so every component
+ * lies in [-1, 1].
+ *   x        device [rows, cols] logits, in_dtype.
+ *   target   device int64[rows]: the target index of each row.  A target
+ *            outside [0, L_r) is ignored: loss 0 and a zero gradient row.
+ *   loss     device float[rows], written.  NaN for a row with a valid target
+ *            whose valid prefix holds a NaN or +inf or only -inf.
+ *   grad     device [rows, cols] in grad_dtype, written; or NULL for the loss
+ *            alone (one read of x).  Must not overlap x, target, loss or
+ *            valid_len.
+ *   valid_len, rows, cols: as smx_softmax_rows.
+ */
+smx_status smx_cross_entropy(const void *x, const int64_t *target, float *loss, void *grad,
+                             int64_t rows, int64_t cols, const int32_t *valid_len, smx_dtype in_dtype,
+                             smx_dtype grad_dtype, smx_stream_t stream);
+
+/*
  * Element-wise merge of two arrays of block summaries ("Online stable softmax",
  * "Derive the update for two blocks"):
  *   m' = max(m_a, m_b),  d' = d_a exp(m_a - m') + d_b exp(m_b - m').

@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "SmxError", "library", "softmax_rows", "softmax_rows_fixed_scratch", "softmax_row_stats",
     "softmax_merge_stats", "log_softmax_rows", "softmax_lse", "softmax_apply_stats",
+    "softmax_backward", "cross_entropy",
     "last_device_status", "status_string", "DTYPES",
 ]
 
@@ -68,6 +69,10 @@ def library() -> ctypes.CDLL:
         lib.smx_softmax_lse.restype = st
         lib.smx_softmax_apply_stats.argtypes = [P, P, P, P, I64, I64, P, I32, I32, P]
         lib.smx_softmax_apply_stats.restype = st
+        lib.smx_softmax_backward.argtypes = [P, P, P, I64, I64, P, I32, I32, P]
+        lib.smx_softmax_backward.restype = st
+        lib.smx_cross_entropy.argtypes = [P, P, P, P, I64, I64, P, I32, I32, P]
+        lib.smx_cross_entropy.restype = st
         lib.smx_last_device_status.argtypes = [P]
         lib.smx_last_device_status.restype = st
         lib.smx_status_string.argtypes = [st]
@@ -269,6 +274,56 @@ def softmax_apply_stats(x: torch.Tensor, m: torch.Tensor, d: torch.Tensor, out: 
     if st != 0:
         raise SmxError(st, "smx_softmax_apply_stats")
     return out
+
+
+def softmax_backward(p: torch.Tensor, g: torch.Tensor, out: torch.Tensor | None = None,
+                     valid_len: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                     stream=None) -> torch.Tensor:
+    """dx = p (g - sum(g p)) per row over the valid prefix (0 elsewhere)."""
+    _check_2d(p, "p")
+    _check_2d(g, "g")
+    if g.shape != p.shape or g.dtype != p.dtype or g.device != p.device:
+        raise ValueError("g must match p's shape, dtype and device")
+    rows, cols = p.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype or p.dtype, device=p.device)
+    _check_2d(out, "out")
+    if out.shape != p.shape or out.device != p.device:
+        raise ValueError("out must match p's shape and device")
+    st = library().smx_softmax_backward(p.data_ptr(), g.data_ptr(), out.data_ptr(), rows, cols,
+                                        _lengths(valid_len, rows, p.device), _dtype(p.dtype),
+                                        _dtype(out.dtype), _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_softmax_backward")
+    return out
+
+
+def cross_entropy(x: torch.Tensor, target: torch.Tensor, valid_len: torch.Tensor | None = None,
+                  with_grad: bool = True, grad: torch.Tensor | None = None,
+                  grad_dtype: torch.dtype | None = None, loss: torch.Tensor | None = None, stream=None):
+    """(loss [rows] fp32, grad [rows, cols] or None): loss = LSE - x_t, grad = p - onehot(t)."""
+    _check_2d(x, "x")
+    rows, cols = x.shape
+    if not (target.is_cuda and target.dtype == torch.int64 and target.is_contiguous()
+            and target.numel() == rows and target.device == x.device):
+        raise ValueError("target must be a contiguous int64 CUDA tensor with one entry per row")
+    if loss is None:
+        loss = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if with_grad and grad is None:
+        grad = torch.empty((rows, cols), dtype=grad_dtype or x.dtype, device=x.device)
+    if grad is not None:
+        _check_2d(grad, "grad")
+        if grad.shape != x.shape or grad.device != x.device:
+            raise ValueError("grad must match x's shape and device")
+    st = library().smx_cross_entropy(x.data_ptr(), target.data_ptr(),
+                                     _rows_vec(loss, rows, x.device, "loss"),
+                                     None if grad is None else grad.data_ptr(), rows, cols,
+                                     _lengths(valid_len, rows, x.device), _dtype(x.dtype),
+                                     _dtype(grad.dtype if grad is not None else x.dtype),
+                                     _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_cross_entropy")
+    return loss, grad
 
 
 def last_device_status(stream=None) -> int:

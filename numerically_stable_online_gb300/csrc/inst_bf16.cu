@@ -10,4 +10,7 @@ int stream_occupancy_bf16(int vpt, int threads, int depth) {
   return stream_occupancy<__nv_bfloat16>(vpt, threads, depth);
 }
 int split_occupancy_bf16(int threads) { return split_occupancy<__nv_bfloat16>(threads); }
+int backward_occupancy_bf16(int vpt, int threads) {
+  return backward_occupancy<__nv_bfloat16>(vpt, threads);
+}
 }  // namespace smx

@@ -10,4 +10,7 @@ int stream_occupancy_f32(int vpt, int threads, int depth) {
   return stream_occupancy<float>(vpt, threads, depth);
 }
 int split_occupancy_f32(int threads) { return split_occupancy<float>(threads); }
+int backward_occupancy_f32(int vpt, int threads) {
+  return backward_occupancy<float>(vpt, threads);
+}
 }  // namespace smx

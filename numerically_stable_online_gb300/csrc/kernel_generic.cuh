@@ -12,8 +12,9 @@
 // cols * sizeof(type) not a multiple of 16.
 //
 // The same kernel takes the other modes of the streamed kernel on such shapes:
-// row statistics (LSE when d_out is null), log_softmax (MODE_LOG), and
-// normalising with given per-row (m_in, d_in) (MODE_APPLY, no first pass).
+// row statistics (LSE when d_out is null), log_softmax (MODE_LOG), normalising
+// with given per-row (m_in, d_in) (MODE_APPLY, no first pass), and
+// cross-entropy (MODE_CE: loss, and the gradient when y is given).
 #pragma once
 
 #include "kernel_stream.cuh"
@@ -27,7 +28,8 @@ __global__ void __launch_bounds__(GENERIC_THREADS)
     k_rows_generic(const InT* __restrict__ x, OutT* __restrict__ y, float* __restrict__ m_out,
                    float* __restrict__ d_out, const float* __restrict__ m_in,
                    const float* __restrict__ d_in, int64_t rows, int64_t cols,
-                   const int32_t* __restrict__ valid_len, int64_t row0) {
+                   const int32_t* __restrict__ valid_len, int64_t row0,
+                   const int64_t* __restrict__ target, float* __restrict__ loss) {
   __shared__ float s_m[GENERIC_THREADS / 32], s_d[GENERIC_THREADS / 32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int64_t row = row0 + blockIdx.x;
@@ -90,6 +92,29 @@ __global__ void __launch_bounds__(GENERIC_THREADS)
         d_out[row] = D;
       } else {  // LSE = m + log d
         m_out[row] = M == neg_inf() ? neg_inf() : __fadd_rn(M, logf(D));
+      }
+    }
+  } else if constexpr (MODE == MODE_CE) {
+    const int64_t tg = __ldg(target + row);
+    const bool ignored = tg < 0 || tg >= L;
+    const bool bad = M == neg_inf() || M != M || D != D;
+    if (t == 0) {
+      float out = 0.0f;
+      if (!ignored)
+        out = bad ? qnan() : __fadd_rn(__fsub_rn(M, Elem<InT>::to_f32(xr[tg])), logf(D));
+      loss[row] = out;
+    }
+    if (y != nullptr) {
+      OutT* yr = y + row * cols;
+      const float rD = recip_refined(D);
+      for (int64_t j = t; j < cols; j += GENERIC_THREADS) {
+        float q = 0.0f;
+        if (!ignored && j < L) {
+          if (bad) q = qnan();
+          else q = __fmul_rn(exp_for<OutT, MODE_SOFTMAX>(Elem<InT>::to_f32(xr[j]), M), rD);
+          if (j == tg) q = __fsub_rn(q, 1.0f);
+        }
+        yr[j] = Elem<OutT>::from_f32(q);
       }
     }
   } else if constexpr (MODE == MODE_LOG) {

@@ -35,13 +35,65 @@
 //                 the step that completes a softmax whose summaries were
 //                 computed apart.
 //   MODE_APPLY_LOG  as MODE_APPLY, writing log_softmax.
+//   MODE_CE       whole rows: cross-entropy with logits (the same section and
+//                 "The Jacobian, and the backward pass that never divides"):
+//                 loss = LSE - x_t = (m - x_t) + log d, and, when y is given,
+//                 the fused gradient y = p - onehot(t).  A target outside the
+//                 valid prefix is ignored: loss 0 and a zero gradient row.
+//   MODE_APPLY_CE   chunks: MODE_CE with the row's merged (M, D).
 #pragma once
 
 #include "row_core.cuh"
 
 namespace smx {
 
-enum : int { MODE_APPLY = 2, MODE_LOG = 3, MODE_APPLY_LOG = 4 };
+enum : int { MODE_APPLY = 2, MODE_LOG = 3, MODE_APPLY_LOG = 4, MODE_CE = 5, MODE_APPLY_CE = 6 };
+
+// Cross-entropy epilogue of one item, elements [begin, begin + len) of its row
+// with L of them valid; v holds x (-inf in masked lanes).  The thread holding
+// x_t writes the row's loss; y (nullable) receives p - onehot(t).
+template <typename OutT, int VPT, int V>
+__device__ __forceinline__ void ce_item(OutT* yr, float* loss, int64_t row, int G, int g, int len,
+                                        int L, const float (&v)[VPT][V], float M, float D, float ld,
+                                        bool bad_row, int64_t t, int64_t Lrow, int64_t begin) {
+  const bool ignored = t < 0 || t >= Lrow;
+  const int64_t tl64 = t - begin;
+  const int tl = (!ignored && tl64 >= 0 && tl64 < len) ? (int)tl64 : -1;
+  if (tl >= 0 && (tl / V) % G == g) {
+    const int jo = tl / V / G, io = tl % V;
+    float xt = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (j == jo && i == io) xt = v[j][i];
+    loss[row] = bad_row ? qnan() : __fadd_rn(__fsub_rn(M, xt), ld);
+  }
+  if (ignored && begin == 0 && g == 0) loss[row] = 0.0f;
+  if (yr == nullptr) return;
+  const OutConst kc = make_out_const<OutT>(M, D);
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int e0 = (j * G + g) * V;
+    if (e0 < len) {
+      float q[V];
+      if (ignored) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) q[i] = 0.0f;
+      } else if (bad_row) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) q[i] = e0 + i < L ? qnan() : 0.0f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          q[i] = out_value<OutT>(v[j][i], kc);
+          if (e0 + i == tl) q[i] = __fsub_rn(q[i], 1.0f);
+        }
+      }
+      store_vec<OutT, V>(yr + e0, q);
+    }
+  }
+}
 
 // The items of one launch: item k is chunk k % nchunks of row row0 + k / nchunks.
 struct Items {
@@ -88,8 +140,9 @@ template <typename InT, typename OutT, int VPT, int MODE, int DEPTH, bool CHUNKE
 __global__ void SMX_STREAM_REGS
     k_rows_stream(const InT* __restrict__ x, OutT* __restrict__ y, float* __restrict__ m_out,
                   float* __restrict__ d_out, const float* __restrict__ m_in,
-                  const float* __restrict__ d_in, Items it, const int32_t* __restrict__ valid_len) {
-  constexpr bool APPLY = (MODE == MODE_APPLY || MODE == MODE_APPLY_LOG);
+                  const float* __restrict__ d_in, Items it, const int32_t* __restrict__ valid_len,
+                  const int64_t* __restrict__ target, float* __restrict__ loss) {
+  constexpr bool APPLY = (MODE == MODE_APPLY || MODE == MODE_APPLY_LOG || MODE == MODE_APPLY_CE);
   static_assert(CHUNKED || !APPLY, "the apply modes walk chunks");
   constexpr int V = Elem<InT>::V;
   extern __shared__ __align__(16) uint4 sbuf[];  // [DEPTH][VPT][G]: thread g owns column g
@@ -147,6 +200,11 @@ __global__ void SMX_STREAM_REGS
     const int64_t v = __ldg(valid_len + it.row0 + q.r);
     const int64_t L = (v < 0 ? 0 : (v > it.cols ? it.cols : v)) - (int64_t)q.c * ncols;
     return (int)(L < 0 ? 0 : (L > len ? len : L));
+  };
+  auto row_valid = [&](int64_t row) -> int64_t {  // the row's valid prefix length
+    if (valid_len == nullptr) return it.cols;
+    const int64_t v = __ldg(valid_len + row);
+    return v < 0 ? 0 : (v > it.cols ? it.cols : v);
   };
   const uint64_t pol = (CHUNKED && it.l2_hint != 0) ? l2_policy(it.l2_hint) : 0;
   // copy this thread's vectors of item q into ring slot d; always one group
@@ -231,6 +289,10 @@ __global__ void SMX_STREAM_REGS
       OutT* yr = y + row * it.cols + (int64_t)cur.c * ncols;
       if constexpr (MODE == MODE_APPLY_LOG) {
         store_log<OutT, VPT, V>(yr, G, g, len, L, v, zero_row, nan_row, M, row_ld);
+      } else if constexpr (MODE == MODE_APPLY_CE) {
+        ce_item<OutT, VPT, V>(y == nullptr ? nullptr : yr, loss, row, G, g, len, L, v, M, Dr, row_ld,
+                              zero_row || nan_row, __ldg(target + row), row_valid(row),
+                              (int64_t)cur.c * ncols);
       } else {
         const OutConst kc = make_out_const<OutT>(M, Dr);
 #pragma unroll
@@ -257,7 +319,7 @@ __global__ void SMX_STREAM_REGS
       float Dsum = 0.0f;
       if (M != neg_inf()) {
         float sum;
-        if constexpr (MODE == MODE_LOG) sum = warp_sum(sum_exp(v, M));  // v keeps x
+        if constexpr (MODE == MODE_LOG || MODE == MODE_CE) sum = warp_sum(sum_exp(v, M));  // v keeps x
         else sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
         if (lane == 0) s_sum[warp] = sum;
         __syncthreads();
@@ -273,6 +335,13 @@ __global__ void SMX_STREAM_REGS
             m_out[cur.k] = M == neg_inf() ? neg_inf() : __fadd_rn(M, logf(dk));
           }
         }
+      } else if constexpr (MODE == MODE_CE) {
+        const bool zero_row = (M == neg_inf());
+        const bool nan_row = !zero_row && (Dsum != Dsum);
+        const float D = zero_row ? 0.0f : stats_correct(Dsum, M);
+        ce_item<OutT, VPT, V>(y == nullptr ? nullptr : y + row * it.cols, loss, row, G, g, len, L, v, M,
+                              D, zero_row ? 0.0f : logf(D), zero_row || nan_row, __ldg(target + row),
+                              row_valid(row), 0);
       } else if constexpr (MODE == MODE_LOG) {
         const bool zero_row = (M == neg_inf());
         const bool nan_row = !zero_row && (Dsum != Dsum);
@@ -318,6 +387,45 @@ __global__ void __launch_bounds__(THREADS)
         m_out[blockIdx.x] = acc.m == neg_inf() ? neg_inf() : __fadd_rn(acc.m, logf(d));
       }
     }
+  }
+}
+
+// Cross-entropy loss of long rows without a gradient: merge each row's chunk
+// summaries, read x_t, write loss = (M - x_t) + log D (0 for an ignored target);
+// one CTA per row of the slab starting at row0.
+template <typename InT, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+    k_merge_chunk_ce(const float* __restrict__ m_in, const float* __restrict__ d_in, int nchunks,
+                     const InT* __restrict__ x, int64_t cols, const int64_t* __restrict__ target,
+                     const int32_t* __restrict__ valid_len, int64_t row0, float* __restrict__ loss) {
+  __shared__ float s_mm[THREADS / 32], s_dd[THREADS / 32];
+  const int g = threadIdx.x, lane = g & 31, warp = g >> 5;
+  const int64_t k0 = (int64_t)blockIdx.x * nchunks;
+  MD acc{neg_inf(), 0.0f};
+  for (int i = g; i < nchunks; i += THREADS) acc = md_merge(acc, MD{m_in[k0 + i], d_in[k0 + i]});
+  acc = warp_merge(acc);
+  if (lane == 0) {
+    s_mm[warp] = acc.m;
+    s_dd[warp] = acc.d;
+  }
+  __syncthreads();
+  if (g == 0) {
+    acc = MD{neg_inf(), 0.0f};
+    for (int w = 0; w < THREADS / 32; ++w) acc = md_merge(acc, MD{s_mm[w], s_dd[w]});
+    const int64_t row = row0 + blockIdx.x;
+    int64_t L = cols;
+    if (valid_len != nullptr) {
+      const int64_t v = valid_len[row];
+      L = v < 0 ? 0 : (v > cols ? cols : v);
+    }
+    const int64_t t = target[row];
+    float out = 0.0f;
+    if (t >= 0 && t < L) {
+      const bool bad = acc.m == neg_inf() || acc.m != acc.m || acc.m == pos_inf() || acc.d != acc.d;
+      const float xt = Elem<InT>::to_f32(x[row * cols + t]);
+      out = bad ? qnan() : __fadd_rn(__fsub_rn(acc.m, xt), logf(acc.d));
+    }
+    loss[row] = out;
   }
 }
 

@@ -3,6 +3,7 @@
 // compile in parallel) with SMX_IN_T and SMX_SUFFIX defined.
 #pragma once
 
+#include "kernel_backward.cuh"
 #include "kernel_cluster.cuh"
 #include "kernel_generic.cuh"
 #include "kernel_stream.cuh"
@@ -103,8 +104,10 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
                             const float* m_in, const float* d_in) {
   constexpr int V = Elem<InT>::V;
   // at most 16 elements per thread with the compensated exponential (fp32
-  // outputs) and 32 otherwise
-  if constexpr (VPT * V > ((ExpPolicy<OutT, MODE>::ACCURATE || MODE == MODE_APPLY) ? 16 : 32)) {
+  // outputs) or a per-element exponential after the sum, and 32 otherwise
+  constexpr bool PER_ELEMENT_EXP = ExpPolicy<OutT, MODE>::ACCURATE || MODE == MODE_APPLY ||
+                                   MODE == MODE_CE || MODE == MODE_APPLY_CE;
+  if constexpr (VPT * V > (PER_ELEMENT_EXP ? 16 : 32)) {
     return cudaErrorInvalidValue;
   } else {
     auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH, CHUNKED>;
@@ -122,7 +125,7 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
     const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
     kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
         static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), m_out, d_out, m_in, d_in, it,
-        c.valid_len);
+        c.valid_len, c.target, c.loss);
     return cudaGetLastError();
   }
 }
@@ -195,6 +198,14 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
         e = launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
       } else if constexpr (MODE == MODE_LOG) {
         e = launch_stream_k<InT, OutT, MODE_APPLY_LOG, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
+      } else if constexpr (MODE == MODE_CE) {
+        if (c.y != nullptr) {
+          e = launch_stream_k<InT, OutT, MODE_APPLY_CE, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
+        } else {
+          k_merge_chunk_ce<InT, 256><<<(unsigned)n, 256, 0, c.stream>>>(
+              pm, pd, p.nchunks, static_cast<const InT*>(c.x), c.cols, c.target, c.valid_len, r0, c.loss);
+          e = cudaGetLastError();
+        }
       } else {
         k_merge_chunk_stats<256><<<(unsigned)n, 256, 0, c.stream>>>(
             pm, pd, p.nchunks, c.m_out + r0, c.d_out == nullptr ? nullptr : c.d_out + r0);
@@ -215,11 +226,114 @@ cudaError_t launch_generic(const Call& c) {
     const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
     k_rows_generic<InT, OutT, MODE><<<(unsigned)n, GENERIC_THREADS, 0, c.stream>>>(
         static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, c.m_in, c.d_in,
-        r0 + n, c.cols, c.valid_len, r0);
+        r0 + n, c.cols, c.valid_len, r0, c.target, c.loss);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// Softmax backward.  c.x = p, c.g = g, c.y = dx.
+template <typename InT, typename OutT, int VPT, int MODE>
+cudaError_t launch_bwd_k(const Call& c, const Plan& p, const Items& it, float* part_out,
+                         const float* part_in) {
+  auto kern = k_backward<InT, OutT, VPT, MODE, 2>;
+  const int64_t smem = 2 * stream_smem_bytes(2, VPT, p.threads);
+  static int64_t set_bytes[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (set_bytes[dev] < smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    set_bytes[dev] = smem;
+  }
+  const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
+  kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
+      static_cast<const InT*>(c.x), static_cast<const InT*>(c.g), static_cast<OutT*>(c.y), part_out,
+      part_in, it, c.valid_len);
+  return cudaGetLastError();
+}
+
+template <typename InT, typename OutT>
+cudaError_t launch_backward(const Call& c, const Plan& p) {
+  constexpr int V = Elem<InT>::V;
+  constexpr int SV = 16 / V;
+  if (p.path == PATH_GENERIC) {
+    for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
+      const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
+      k_backward_generic<InT, OutT><<<(unsigned)n, 256, 0, c.stream>>>(
+          static_cast<const InT*>(c.x), static_cast<const InT*>(c.g), static_cast<OutT*>(c.y), c.cols,
+          c.valid_len, r0);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  if (p.path == PATH_STREAM) {
+    const Items it{c.rows, 0, c.cols, (int)c.cols, 1, 0, 0};
+    switch (p.vpt) {
+      case 1: return launch_bwd_k<InT, OutT, 1, BWD_ROWS>(c, p, it, nullptr, nullptr);
+      case 2: return launch_bwd_k<InT, OutT, 2, BWD_ROWS>(c, p, it, nullptr, nullptr);
+      case 4:
+        if constexpr (4 * V <= 16) return launch_bwd_k<InT, OutT, 4, BWD_ROWS>(c, p, it, nullptr, nullptr);
+        return cudaErrorInvalidValue;
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.path != PATH_SPLIT) return cudaErrorInvalidValue;
+  // long rows: per slab, the chunks' partial dots, then dx per chunk
+  const int64_t slab = p.slab_rows;
+  const size_t bytes = (size_t)slab * p.nchunks * sizeof(float);
+  char* base = reinterpret_cast<char*>(p.scratch);
+  cudaError_t e = cudaSuccess;
+  if (base == nullptr) {
+    e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, c.stream);
+    if (e != cudaSuccess) return e;
+  }
+  float* part = reinterpret_cast<float*>(base);
+  for (int64_t r0 = 0; r0 < c.rows && e == cudaSuccess; r0 += slab) {
+    const int64_t n = c.rows - r0 < slab ? c.rows - r0 : slab;
+    const Items it{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, 0, 0};
+    e = launch_bwd_k<InT, float, SV, BWD_DOT>(c, p, it, part, nullptr);
+    if (e == cudaSuccess) e = launch_bwd_k<InT, OutT, SV, BWD_APPLY>(c, p, it, nullptr, part);
+  }
+  if (p.scratch == nullptr) {
+    const cudaError_t f = cudaFreeAsync(base, c.stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
+}
+
+template <typename InT>
+int backward_occupancy(int vpt, int threads) {
+  constexpr int V = Elem<InT>::V;
+  auto query = [&](auto kern, int v) -> int {
+    const int64_t smem = 2 * stream_smem_bytes(2, v, threads);
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  };
+  switch (vpt) {
+    case 0: {  // chunks: the fp32-output apply kernel stands for both passes
+      const int a = query(k_backward<InT, float, 16 / V, BWD_APPLY, 2>, 16 / V);
+      const int b = query(k_backward<InT, float, 16 / V, BWD_DOT, 2>, 16 / V);
+      return a < b ? a : b;
+    }
+    case 1: return query(k_backward<InT, float, 1, BWD_ROWS, 2>, 1);
+    case 2: return query(k_backward<InT, float, 2, BWD_ROWS, 2>, 2);
+    case 4:
+      if constexpr (4 * V <= 16) return query(k_backward<InT, float, 4, BWD_ROWS, 2>, 4);
+      return 0;
+    default: return 0;
+  }
 }
 
 template <typename InT, typename OutT, int MODE>
@@ -253,11 +367,21 @@ cudaError_t launch_out(const Call& c, const Plan& p) {
 
 template <typename InT>
 cudaError_t launch_in(const Call& c, const Plan& p) {
+  if (c.mode == CALL_BACKWARD) {
+    switch (c.out_dtype) {
+      case 0: return launch_backward<InT, float>(c, p);
+      case 1: return launch_backward<InT, __half>(c, p);
+      case 2: return launch_backward<InT, __nv_bfloat16>(c, p);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (c.mode) {
     case MODE_SOFTMAX: return launch_out<InT, MODE_SOFTMAX>(c, p);
     case MODE_STATS: return launch_typed<InT, float, MODE_STATS>(c, p);
     case MODE_APPLY: return launch_out<InT, MODE_APPLY>(c, p);
     case MODE_LOG: return launch_out<InT, MODE_LOG>(c, p);
+    case MODE_CE:
+      return c.y == nullptr ? launch_typed<InT, float, MODE_CE>(c, p) : launch_out<InT, MODE_CE>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }

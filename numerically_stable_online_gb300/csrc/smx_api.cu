@@ -294,11 +294,101 @@ bool plan_cluster(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan*
   return true;
 }
 
+int backward_occupancy(int in_dtype, int vpt, int threads) {
+  switch (in_dtype) {
+    case SMX_F32: return backward_occupancy_f32(vpt, threads);
+    case SMX_F16: return backward_occupancy_f16(vpt, threads);
+    default: return backward_occupancy_bf16(vpt, threads);
+  }
+}
+
+// Softmax backward: rows of up to 16 KiB per CTA (at most 16 elements per
+// thread: two inputs held), with enough persistent CTAs for about 48 KiB of
+// reads in flight per SM; longer rows in chunks of 4096 elements (two passes
+// per L2-sized slab); the scalar kernel for unaligned shapes.
+void plan_backward(DeviceInfo& d, const Call& c, bool vec_ok, Plan* p) {
+  p->path = PATH_GENERIC;
+  if (!vec_ok) return;
+  const int force = g_force_path.load();
+  if (force == PATH_GENERIC) return;
+  const int es = elem_size(c.in_dtype);
+  const int V = 16 / es;
+  const int64_t row_bytes = c.cols * es;
+  if (row_bytes <= BWD_MAX_ROW_BYTES && force != PATH_SPLIT) {
+    const int64_t nvec = c.cols / V;
+    int vpt = 1;
+    while (vpt * V < 16 && (nvec + vpt - 1) / vpt > 256) vpt <<= 1;
+    int64_t threads = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
+    if (threads < 64) threads = 64;
+    if (threads <= 1024) {
+      const int occ_max = backward_occupancy(c.in_dtype, vpt, (int)threads);
+      if (occ_max > 0) {
+        int64_t read = 2 * row_bytes;
+        if (c.valid_len != nullptr) read = (read + 1) / 2;
+        int64_t want = STREAM_INFLIGHT_BYTES / (2 * (read > 0 ? read : 1));
+        if (want < 1) want = 1;
+        int occ = want < occ_max ? (int)want : occ_max;
+        const int forced = g_stream_ctas_per_sm.load();
+        if (forced > 0) occ = forced < occ_max ? forced : occ_max;
+        const int64_t ctas = (int64_t)occ * d.sm_count;
+        p->path = PATH_STREAM;
+        p->threads = (int)threads;
+        p->vpt = vpt;
+        p->stages = 2;
+        p->ctas = (int)(c.rows < ctas ? c.rows : ctas);
+        return;
+      }
+    }
+  }
+  const int vpt = 16 / V;
+  const int threads = 256;
+  const int64_t chunk = (int64_t)threads * vpt * V;
+  const int64_t nchunks = (c.cols + chunk - 1) / chunk;
+  if (nchunks > ((int64_t)1 << 30)) return;
+  const int occ_max = backward_occupancy(c.in_dtype, 0, threads);
+  if (occ_max <= 0) return;
+  int occ = occ_max;
+  const int forced = g_stream_ctas_per_sm.load();
+  if (forced > 0) occ = forced < occ_max ? forced : occ_max;
+  int64_t slab_bytes = d.l2_bytes / 2;
+  const int64_t dbg = g_split_slab_bytes.load();
+  if (dbg > 0) slab_bytes = dbg;
+  int64_t slab = slab_bytes / (2 * row_bytes);
+  if (slab < 1) slab = 1;
+  if (slab * nchunks > ((int64_t)1 << 31)) slab = ((int64_t)1 << 31) / nchunks;
+  p->path = PATH_SPLIT;
+  p->threads = threads;
+  p->vpt = vpt;
+  p->stages = 2;
+  p->ctas = occ * d.sm_count;
+  p->chunk = chunk;
+  p->nchunks = (int)nchunks;
+  p->slab_rows = slab;
+}
+
+smx_status run_backward(Call& c, DeviceInfo& dev) {
+  const int es = elem_size(c.in_dtype);
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(c.x) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(c.g) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(c.y) % 16 == 0) && ((c.cols * es) % 16 == 0);
+  Plan p;
+  plan_backward(dev, c, vec_ok, &p);
+  cudaError_t e;
+  switch (c.in_dtype) {
+    case SMX_F32: e = launch_in_f32(c, p); break;
+    case SMX_F16: e = launch_in_f16(c, p); break;
+    default: e = launch_in_bf16(c, p); break;
+  }
+  t_last_path = p.path;
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
+  return SMX_OK;
+}
+
 smx_status run(Call& c, DeviceInfo& dev) {
   const int es_in = elem_size(c.in_dtype);
   const bool vec_ok =
       (reinterpret_cast<uintptr_t>(c.x) % 16 == 0) &&
-      (c.mode == MODE_STATS || reinterpret_cast<uintptr_t>(c.y) % 16 == 0) &&
+      (c.y == nullptr || reinterpret_cast<uintptr_t>(c.y) % 16 == 0) &&
       ((c.cols * es_in) % 16 == 0) && c.cols > 0;
   // softmax and (m, d) statistics run on every kernel; LSE, log_softmax and
   // the apply mode on the streamed, long-row and generic ones
@@ -314,7 +404,8 @@ smx_status run(Call& c, DeviceInfo& dev) {
     } else if (force != PATH_GENERIC) {
       // the compensated exponential (fp32 softmax outputs, and every apply
       // output) holds 16 elements per thread at most
-      const bool acc = (c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32) || c.mode == MODE_APPLY;
+      const bool acc = (c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32) || c.mode == MODE_APPLY ||
+                       c.mode == MODE_CE;
       if (force != PATH_REGS || !classic)
         planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr,
                               c.mode == MODE_APPLY, &p);
@@ -563,6 +654,51 @@ smx_status smx_softmax_apply_stats(const void* x, const float* m_in, const float
   if (s != SMX_OK) return s;
   Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
          MODE_APPLY, reinterpret_cast<cudaStream_t>(stream), nullptr, 0, m_in, d_in};
+  return run(c, *dev);
+}
+
+smx_status smx_softmax_backward(const void* p, const void* g, void* dx, int64_t rows, int64_t cols,
+                                const int32_t* valid_len, smx_dtype dtype, smx_dtype dx_dtype,
+                                smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(dtype) || !valid_dtype(dx_dtype)) return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return SMX_OK;
+  if (p == nullptr || g == nullptr || dx == nullptr) return SMX_ERR_INVALID_ARG;
+  const int64_t n = rows * cols * elem_size(dtype), nd = rows * cols * elem_size(dx_dtype);
+  if (overlaps(p, n, dx, nd) || overlaps(g, n, dx, nd)) return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, dx, nd)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{p, dx, nullptr, nullptr, rows, cols, valid_len, (int)dtype, (int)dx_dtype, CALL_BACKWARD,
+         reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  c.g = g;
+  return run_backward(c, *dev);
+}
+
+smx_status smx_cross_entropy(const void* x, const int64_t* target, float* loss, void* grad,
+                             int64_t rows, int64_t cols, const int32_t* valid_len, smx_dtype in_dtype,
+                             smx_dtype grad_dtype, smx_stream_t stream) {
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(grad_dtype))
+    return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0) return SMX_OK;
+  if (loss == nullptr || target == nullptr || (cols > 0 && x == nullptr)) return SMX_ERR_INVALID_ARG;
+  const int64_t nx = rows * cols * elem_size(in_dtype), ng = rows * cols * elem_size(grad_dtype);
+  if (overlaps(loss, rows * 4, x, nx) || overlaps(loss, rows * 4, target, rows * 8) ||
+      (valid_len && overlaps(loss, rows * 4, valid_len, rows * 4)))
+    return SMX_ERR_ALIAS;
+  if (grad != nullptr &&
+      (overlaps(grad, ng, x, nx) || overlaps(grad, ng, target, rows * 8) ||
+       overlaps(grad, ng, loss, rows * 4) || (valid_len && overlaps(grad, ng, valid_len, rows * 4))))
+    return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  Call c{x, cols > 0 ? grad : nullptr, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype,
+         (int)grad_dtype, MODE_CE, reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  c.target = target;
+  c.loss = loss;
   return run(c, *dev);
 }
 

@@ -18,13 +18,20 @@ struct Call {
   const int32_t* valid_len;
   int in_dtype, out_dtype;  // smx_dtype values
   int mode;                 // 0 softmax, 1 row statistics (LSE if d_out is null), 2 apply given
-                            // statistics, 3 log_softmax (the kernels' MODE_* values)
+                            // statistics, 3 log_softmax, 5 cross-entropy (the kernels' MODE_*
+                            // values), CALL_BACKWARD
   cudaStream_t stream;
   int* status;              // device status word
   int64_t max_polls;        // bound of each staging wait
   const float* m_in = nullptr;  // apply: per-row statistics
   const float* d_in = nullptr;
+  const void* g = nullptr;      // backward: the upstream gradient (x is the forward output p)
+  const int64_t* target = nullptr;  // cross-entropy: target index per row
+  float* loss = nullptr;            // cross-entropy: loss per row
 };
+
+// Call::mode of the softmax backward (past the kernels' MODE_* values).
+constexpr int CALL_BACKWARD = 8;
 
 struct Plan {
   int path = PATH_GENERIC;
@@ -69,6 +76,12 @@ int stream_occupancy_bf16(int vpt, int threads, int depth);
 int split_occupancy_f32(int threads);
 int split_occupancy_f16(int threads);
 int split_occupancy_bf16(int threads);
+// ... of the backward kernels: whole rows (vpt, threads) or chunks (vpt = 0).
+int backward_occupancy_f32(int vpt, int threads);
+int backward_occupancy_f16(int vpt, int threads);
+int backward_occupancy_bf16(int vpt, int threads);
+
+constexpr int BWD_MAX_ROW_BYTES = 16384;  // whole rows per CTA; longer rows in chunks
 
 constexpr int STREAM_MAX_ROW_BYTES = 32768;
 

@@ -141,3 +141,72 @@ def compare_lse(lse, ref, log_d):
     worst = float((err / tol).max()) if ok.any() else 0.0
     assert worst <= 1.0, f"LSE error {worst:.3f} x tolerance"
     return {"lse_err_over_tol": worst}
+
+
+# ---------------------------------------------------------------------------
+# Softmax backward: s = sum g p is an fp32 sum of FMAs whose error is at most
+# 2^-18 of sum |g p| (as for d above); dx = RN(p RN(g - s)) adds a relative
+# 2^-24 twice.  So |dx - ref| <= 2^-22 |ref| + |p| 2^-18 (|g| + sum |g p|), plus
+# one unit of the format's spacing at |ref| for fp16 / bf16 outputs.
+# Cross-entropy: loss = RN(RN(m - x_t) + log d) with m - x_t <= loss, so
+# |loss - ref| <= 2^-22 (|ref| + log d) + 2^-18; the gradient p - onehot carries
+# p's error, at most 2e-6 from the exponential and 2^-18 from d, relative to p:
+# |grad - ref| <= 6e-6 p + 2^-24 (+ the format's spacing), p = ref + onehot.
+# Masked lanes and ignored rows are +0 bit for bit.
+# ---------------------------------------------------------------------------
+def _check_zero_and_nan(bits, yv, masked, nan_lanes, zero_rows=None):
+    zl = masked if zero_rows is None else (masked | zero_rows[:, None])
+    assert np.all(bits[zl] == 0), "masked lanes / ignored rows must be +0"
+    assert np.all(np.isnan(yv[nan_lanes])), "NaN lanes"
+
+
+def compare_backward(dx, ref, p_vals, g_vals, out_dtype, valid_len=None):
+    n, cols = ref.shape
+    L = lengths(n, cols, valid_len)
+    masked = np.arange(cols)[None, :] >= L[:, None]
+    yv, bits = _decoded(dx, out_dtype, n, cols)
+    nan_lanes = np.isnan(ref) & ~masked
+    _check_zero_and_nan(bits, yv, masked, nan_lanes)
+    ok = ~masked & ~np.isnan(ref)
+    gp = np.where(masked, 0.0, np.abs(g_vals * p_vals)).sum(axis=1)[:, None]
+    tol = 2.0 ** -22 * np.abs(ref) + np.abs(p_vals) * 2.0 ** -18 * (np.abs(g_vals) + gp)
+    if out_dtype != "f32":
+        tol = tol + format_spacing(ref, out_dtype)
+    tol = tol + 1e-38  # exact zeros compare equal
+    err = np.abs(yv[ok] - ref[ok])
+    worst = float((err / tol[ok]).max()) if ok.any() else 0.0
+    assert worst <= 1.0, f"backward error {worst:.3f} x tolerance"
+    return {"bwd_err_over_tol": worst}
+
+
+def compare_ce(loss, grad, ref_loss, ref_grad, log_d, target, out_dtype, valid_len=None):
+    n = ref_loss.shape[0]
+    loss = np.asarray(loss, dtype=np.float64)
+    assert np.array_equal(np.isnan(loss), np.isnan(ref_loss)), "NaN losses"
+    ok = ~np.isnan(ref_loss)
+    assert np.all(np.isfinite(loss[ok]) == np.isfinite(ref_loss[ok]))
+    fin = ok & np.isfinite(ref_loss)
+    tol = 2.0 ** -22 * (np.abs(ref_loss[fin]) + np.asarray(log_d)[fin]) + LOG_ABS
+    err = np.abs(loss[fin] - ref_loss[fin])
+    stats = {"loss_err_over_tol": float((err / tol).max()) if fin.any() else 0.0}
+    assert stats["loss_err_over_tol"] <= 1.0, f"loss error {stats['loss_err_over_tol']:.3f} x tol"
+    if grad is None:
+        return stats
+    cols = ref_grad.shape[1]
+    L = lengths(n, cols, valid_len)
+    masked = np.arange(cols)[None, :] >= L[:, None]
+    t = np.asarray(target, dtype=np.int64)
+    ignored = (t < 0) | (t >= L)
+    yv, bits = _decoded(grad, out_dtype, n, cols)
+    nan_lanes = np.isnan(ref_grad) & ~masked
+    _check_zero_and_nan(bits, yv, masked, nan_lanes, ignored)
+    onehot = (np.arange(cols)[None, :] == t[:, None]) & ~ignored[:, None]
+    pv = np.where(onehot, ref_grad + 1.0, ref_grad)
+    gok = ~masked & ~ignored[:, None] & ~np.isnan(ref_grad)
+    tol = 6e-6 * np.abs(pv) + 2.0 ** -24
+    if out_dtype != "f32":
+        tol = tol + format_spacing(ref_grad, out_dtype)
+    err = np.abs(yv[gok] - ref_grad[gok])
+    stats["grad_err_over_tol"] = float((err / tol[gok]).max()) if gok.any() else 0.0
+    assert stats["grad_err_over_tol"] <= 1.0, f"grad error {stats['grad_err_over_tol']:.3f} x tol"
+    return stats
