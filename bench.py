@@ -16,7 +16,10 @@ Prints one JSON line on rank 0:
   cpu_baseline the fp64 CPU reference timed on this host on a bounded sample
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--op softmax|log_softmax|lse|apply_stats|
+                                              backward|cross_entropy]
+--op times another entry point on the same workload (default: the softmax);
+its bytes are that operation's algorithmic bytes (workloads.op_bytes).
 For N > 1 it runs under torch.distributed.run, one independent replica per GPU.
 """
 from __future__ import annotations
@@ -47,7 +50,13 @@ PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4, "split":
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_regs.cuh",
                   "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
-                  "launch_impl.cuh", "smx_api.cu"]
+                  "kernel_backward.cuh", "launch_impl.cuh", "smx_api.cu"]
+
+
+def metric_of(op: str) -> str:
+    if op == "softmax":
+        return METRIC
+    return f"{op} GB/s (algorithmic bytes read+write) and rows/s on 1 GB300; % of HBM peak"
 
 
 # ---------------------------------------------------------------------------
@@ -93,10 +102,10 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profile_traffic(workload: str):
+def profile_traffic(workload: str, op: str = "softmax"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
     or None when there is none or the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"softmax_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{op}_{workload}.md")
     if not os.path.exists(path):
         return None, None
     text = open(path).read()
@@ -179,23 +188,66 @@ class ClockSampler:
 # CPU reference leg.
 # ---------------------------------------------------------------------------
 
-def oracle_throughput(x_host, vl, w, budget_s: float, min_rows: int = 1):
-    """Time the fp64 reference on a bounded sample of the workload's rows."""
+def oracle_inputs(op: str, w, x_host, vl):
+    """Host-side inputs the op's reference needs beyond x (seeded, like the GPU leg's)."""
+    rows = w.rows
+    extra = {}
+    if op == "apply_stats":
+        import oracle
+
+        m, d = oracle.row_stats(x_host, w.in_dtype, rows, w.cols, vl)
+        extra["m"], extra["d"] = m.astype(np.float32).astype(np.float64), d.astype(np.float32).astype(np.float64)
+    if op == "cross_entropy":
+        extra["target"] = op_targets(rows, w.cols)
+    if op == "backward":
+        extra["g"] = wl.to_storage(np.random.default_rng(77).normal(0, 1, rows * w.cols).astype(np.float32),
+                                   w.in_dtype)
+    return extra
+
+
+def op_targets(rows: int, cols: int) -> np.ndarray:
+    return np.random.default_rng(78).integers(0, cols, rows).astype(np.int64)
+
+
+def oracle_call(op: str, w, x_host, vl, extra, sel):
+    """The op's fp64 reference on the rows `sel` (for backward, x_host stands in for p)."""
     import oracle
 
-    rows, cols = w.rows, w.cols
+    if op == "softmax":
+        oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+    elif op == "log_softmax":
+        oracle.log_softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+    elif op == "lse":
+        oracle.row_stats(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+    elif op == "apply_stats":
+        oracle.apply_stats(x_host, w.in_dtype, w.rows, w.cols, extra["m"], extra["d"], vl, rows_sel=sel)
+    elif op == "backward":
+        oracle.softmax_backward(x_host, extra["g"], w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+    elif op == "cross_entropy":
+        oracle.cross_entropy(x_host, w.in_dtype, w.rows, w.cols, extra["target"], vl, rows_sel=sel)
+    else:
+        raise ValueError(op)
+
+
+def sample_bytes(op: str, w, vl, sel) -> int:
+    in_size = 4 if w.in_dtype == "f32" else 2
+    out_size = 4 if w.out_dtype == "f32" else 2
+    return wl.op_bytes(op, sel.size, w.cols, in_size, out_size, None if vl is None else vl[sel])
+
+
+def oracle_throughput(x_host, vl, w, budget_s: float, min_rows: int = 1, op: str = "softmax"):
+    """Time the fp64 reference on a bounded sample of the workload's rows."""
+    extra = oracle_inputs(op, w, x_host, vl)
+    rows = w.rows
     t0 = time.perf_counter()
-    oracle.softmax_rows(x_host, w.in_dtype, rows, cols, vl, rows_sel=np.arange(min(rows, 16)))
+    oracle_call(op, w, x_host, vl, extra, np.arange(min(rows, 16)))
     per_row = (time.perf_counter() - t0) / min(rows, 16)
     n = int(max(min_rows, min(rows, budget_s / max(per_row, 1e-9))))
     sel = np.arange(n)
     t0 = time.perf_counter()
-    oracle.softmax_rows(x_host, w.in_dtype, rows, cols, vl, rows_sel=sel)
+    oracle_call(op, w, x_host, vl, extra, sel)
     dt = time.perf_counter() - t0
-    in_size = 4 if w.in_dtype == "f32" else 2
-    out_size = 4 if w.out_dtype == "f32" else 2
-    b = wl.algorithmic_bytes(n, cols, in_size, out_size, None if vl is None else vl[:n])
-    return b / dt / 1e9, n, dt, n / dt
+    return sample_bytes(op, w, vl, sel) / dt / 1e9, n, dt, n / dt
 
 
 def run_reference(args, w):
@@ -203,37 +255,36 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     x_host, vl = wl.host_input(w.name)
-    in_size = 4 if w.in_dtype == "f32" else 2
-    out_size = 4 if w.out_dtype == "f32" else 2
     import oracle
 
     oracle.build()
+    op = args.op
+    extra = oracle_inputs(op, w, x_host, vl)
     # size each step's sample so warm-up + timed steps take about a minute
     t0 = time.perf_counter()
-    oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=np.arange(4))
+    oracle_call(op, w, x_host, vl, extra, np.arange(4))
     per_row = (time.perf_counter() - t0) / 4
     per_step_rows = int(max(1, min(w.rows, args.ref_budget / max(1, args.steps + args.warmup)
                                    / per_row)))
     sel_all = np.arange(w.rows)
     for s in range(args.warmup):
         sel = sel_all[(s * per_step_rows) % w.rows:][:per_step_rows]
-        oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+        oracle_call(op, w, x_host, vl, extra, sel)
     tot_bytes, tot_rows = 0, 0
     t0 = time.perf_counter()
     for s in range(args.steps):
         start = (s * per_step_rows) % w.rows
         sel = sel_all[start:start + per_step_rows]
-        oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
-        tot_bytes += wl.algorithmic_bytes(sel.size, w.cols, in_size, out_size,
-                                          None if vl is None else vl[sel])
+        oracle_call(op, w, x_host, vl, extra, sel)
+        tot_bytes += sample_bytes(op, w, vl, sel)
         tot_rows += sel.size
     dt = time.perf_counter() - t0
     value = tot_bytes / dt / 1e9
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w, None),
+        "impl": "reference", "metric": metric_of(op), "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w, None, op),
         "rows_per_s": tot_rows / dt,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{per_step_rows} rows of {w.rows} per step (fp64 C reference, "
@@ -244,10 +295,12 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, nsets):
+def config_of(w, nsets, op="softmax"):
     c = {"workload": w.name, "rows": w.rows, "cols": w.cols, "in_dtype": w.in_dtype,
          "out_dtype": w.out_dtype, "mask": "valid_len" if w.masked else None,
          "description": w.description}
+    if op != "softmax":
+        c["op"] = op
     if nsets is not None:
         c["l2"] = f"rotating {nsets} input/output buffer sets, larger than L2 together"
     return c
@@ -256,6 +309,118 @@ def config_of(w, nsets):
 # ---------------------------------------------------------------------------
 # GPU leg.
 # ---------------------------------------------------------------------------
+
+class GpuOp:
+    """Device buffers of one operation over `nsets` rotating sets, its launch
+    through the raw C ABI (the timed steps) and its end-to-end step through the
+    public Python call with host copies both ways."""
+
+    def __init__(self, op, w, x_host, vl_host, dev, torch, smx, stream):
+        self.op, self.w, self.torch, self.smx = op, w, torch, smx
+        self.lib = smx.library()
+        self.sptr = stream.cuda_stream
+        in_size = 4 if w.in_dtype == "f32" else 2
+        out_size = 4 if w.out_dtype == "f32" else 2
+        rows, cols = w.rows, w.cols
+        self.bytes_step = wl.op_bytes(op, rows, cols, in_size, out_size, vl_host)
+        dense_out = op != "lse"
+        set_bytes = rows * cols * (in_size * (2 if op == "backward" else 1) + (out_size if dense_out else 0))
+        self.nsets = rotation_sets(set_bytes)
+        out_dt = wl.torch_dtype(w.out_dtype)
+        self.x_cpu = wl.storage_to_torch(x_host, w.in_dtype).reshape(rows, cols)
+        self.vl_host = vl_host
+        self.vl = None if vl_host is None else torch.from_numpy(vl_host).to(dev)
+        x0 = self.x_cpu.to(dev)
+        if op == "backward":
+            # p: the softmax of the workload (what a forward pass stored); g: N(0, 1)
+            p0 = smx.softmax_rows(x0, valid_len=self.vl)
+            self.g_cpu = wl.storage_to_torch(
+                wl.to_storage(np.random.default_rng(77).normal(0, 1, rows * cols).astype(np.float32),
+                              w.in_dtype), w.in_dtype).reshape(rows, cols)
+            self.xs = [p0.clone() for _ in range(self.nsets)]
+            self.gs = [self.g_cpu.to(dev) for _ in range(self.nsets)]
+            self.x_cpu = p0.cpu()
+        else:
+            self.xs = [x0.clone() for _ in range(self.nsets)]
+        self.ys = ([torch.empty((rows, cols), dtype=out_dt, device=dev) for _ in range(self.nsets)]
+                   if dense_out else [torch.empty(rows, dtype=torch.float32, device=dev)
+                                      for _ in range(self.nsets)])
+        if op == "apply_stats":
+            self.m, self.d = smx.softmax_row_stats(x0, valid_len=self.vl)
+        if op == "cross_entropy":
+            self.t_cpu = torch.from_numpy(op_targets(rows, cols))
+            self.t = self.t_cpu.to(dev)
+            self.loss = [torch.empty(rows, dtype=torch.float32, device=dev) for _ in range(self.nsets)]
+        del x0
+        self.in_code = smx.DTYPES[self.xs[0].dtype]
+        self.out_code = smx.DTYPES[out_dt]
+        self.vl_ptr = None if self.vl is None else self.vl.data_ptr()
+
+    def launch(self, i):
+        k = i % self.nsets
+        w, lib, x, y = self.w, self.lib, self.xs[k].data_ptr(), self.ys[k].data_ptr()
+        op = self.op
+        if op == "softmax":
+            st = lib.smx_softmax_rows(x, y, w.rows, w.cols, self.vl_ptr, self.in_code, self.out_code, self.sptr)
+        elif op == "log_softmax":
+            st = lib.smx_log_softmax_rows(x, y, w.rows, w.cols, self.vl_ptr, self.in_code, self.out_code,
+                                          self.sptr)
+        elif op == "lse":
+            st = lib.smx_softmax_lse(x, y, w.rows, w.cols, self.vl_ptr, self.in_code, self.sptr)
+        elif op == "apply_stats":
+            st = lib.smx_softmax_apply_stats(x, self.m.data_ptr(), self.d.data_ptr(), y, w.rows, w.cols,
+                                             self.vl_ptr, self.in_code, self.out_code, self.sptr)
+        elif op == "backward":
+            st = lib.smx_softmax_backward(x, self.gs[k].data_ptr(), y, w.rows, w.cols, self.vl_ptr,
+                                          self.in_code, self.out_code, self.sptr)
+        else:
+            st = lib.smx_cross_entropy(x, self.t.data_ptr(), self.loss[k].data_ptr(), y, w.rows, w.cols,
+                                       self.vl_ptr, self.in_code, self.out_code, self.sptr)
+        if st != 0:
+            raise self.smx.SmxError(st, op)
+
+    def e2e(self):
+        """(step function, H2D bytes, D2H bytes) through the public call."""
+        torch, smx, op = self.torch, self.smx, self.op
+        x_pin = self.x_cpu.pin_memory()
+        xd, yd = self.xs[0], self.ys[0]
+        y_pin = torch.empty(yd.shape, dtype=yd.dtype).pin_memory()
+        vl_pin = None if self.vl_host is None else torch.from_numpy(self.vl_host).pin_memory()
+        vld = None if vl_pin is None else torch.empty_like(self.vl)
+        extra_in = []  # (pinned host, device) pairs copied in every step
+        if op == "backward":
+            extra_in.append((self.g_cpu.pin_memory(), self.gs[0]))
+        if op == "apply_stats":
+            extra_in += [(self.m.cpu().pin_memory(), torch.empty_like(self.m)),
+                         (self.d.cpu().pin_memory(), torch.empty_like(self.d))]
+        if op == "cross_entropy":
+            extra_in.append((self.t_cpu.pin_memory(), torch.empty_like(self.t)))
+            loss_pin = torch.empty(self.w.rows, dtype=torch.float32).pin_memory()
+        def step():
+            xd.copy_(x_pin, non_blocking=True)
+            if vld is not None:
+                vld.copy_(vl_pin, non_blocking=True)
+            for h, dv in extra_in:
+                dv.copy_(h, non_blocking=True)
+            if op == "softmax":
+                smx.softmax_rows(xd, out=yd, valid_len=vld)
+            elif op == "log_softmax":
+                smx.log_softmax_rows(xd, out=yd, valid_len=vld)
+            elif op == "lse":
+                smx.softmax_lse(xd, valid_len=vld, out=yd)
+            elif op == "apply_stats":
+                smx.softmax_apply_stats(xd, extra_in[0][1], extra_in[1][1], out=yd, valid_len=vld)
+            elif op == "backward":
+                smx.softmax_backward(xd, extra_in[0][1], out=yd, valid_len=vld)
+            else:
+                smx.cross_entropy(xd, extra_in[0][1], valid_len=vld, grad=yd, loss=self.loss[0])
+                loss_pin.copy_(self.loss[0], non_blocking=True)
+            y_pin.copy_(yd, non_blocking=True)
+        h2d = x_pin.numel() * x_pin.element_size() + (0 if vl_pin is None else vl_pin.numel() * 4)
+        h2d += sum(h.numel() * h.element_size() for h, _ in extra_in)
+        d2h = y_pin.numel() * y_pin.element_size() + (self.w.rows * 4 if op == "cross_entropy" else 0)
+        return step, h2d, d2h
+
 
 def run_ours(args, w):
     import torch
@@ -277,35 +442,18 @@ def run_ours(args, w):
     smx.library()
 
     x_host, vl_host = wl.host_input(w.name)
-    in_size = 4 if w.in_dtype == "f32" else 2
-    out_size = 4 if w.out_dtype == "f32" else 2
-    bytes_step = wl.algorithmic_bytes(w.rows, w.cols, in_size, out_size, vl_host)
-    set_bytes = w.rows * w.cols * (in_size + out_size)
-    nsets = rotation_sets(set_bytes)
-    x_cpu = wl.storage_to_torch(x_host, w.in_dtype).reshape(w.rows, w.cols)
-    xs = [x_cpu.to(dev) for _ in range(nsets)]
-    ys = [torch.empty((w.rows, w.cols), dtype=wl.torch_dtype(w.out_dtype), device=dev)
-          for _ in range(nsets)]
-    vl = None if vl_host is None else torch.from_numpy(vl_host).to(dev)
     stream = torch.cuda.current_stream(dev)
     lib = smx.library()
-    P = lambda t: t.data_ptr()
-    in_code, out_code = smx.DTYPES[xs[0].dtype], smx.DTYPES[ys[0].dtype]
-    vl_ptr = None if vl is None else vl.data_ptr()
-    sptr = stream.cuda_stream
     lib.smx_debug_force_path(PATHS[args.path])
-
-    def step(i):
-        st = lib.smx_softmax_rows(P(xs[i % nsets]), P(ys[i % nsets]), w.rows, w.cols, vl_ptr,
-                                  in_code, out_code, sptr)
-        if st != 0:
-            raise smx.SmxError(st, "smx_softmax_rows")
+    g = GpuOp(args.op, w, x_host, vl_host, dev, torch, smx, stream)
+    bytes_step, nsets = g.bytes_step, g.nsets
 
     for i in range(args.warmup):
-        step(i)
+        g.launch(i)
+    used_path = lib.smx_debug_last_path()
+    launches_per_call = lib.smx_debug_last_launches()
     torch.cuda.synchronize(dev)
     assert smx.last_device_status() == 0
-    used_path = lib.smx_debug_last_path()
 
     sampler = ClockSampler(local)
     if rank == 0 or world > 1:
@@ -325,10 +473,10 @@ def run_ours(args, w):
     for i in range(args.steps):
         if i in sampled:
             ev[i][0].record(stream)
-            step(i)
+            g.launch(i)
             ev[i][1].record(stream)
         else:
-            step(i)
+            g.launch(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -343,19 +491,9 @@ def run_ours(args, w):
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     agg = aggregate(bytes_step, w.rows, args.steps, world, elapsed_ms / 1e3)
 
-    # end to end through the public call: pinned host input in, output back
-    x_pin = x_cpu.pin_memory()
-    y_pin = torch.empty((w.rows, w.cols), dtype=ys[0].dtype).pin_memory()
-    vl_pin = None if vl_host is None else torch.from_numpy(vl_host).pin_memory()
+    # end to end through the public call: pinned host inputs in, outputs back
+    e2e_step, h2d, d2h = g.e2e()
     e2e_steps = max(3, min(args.steps, 30))
-    xd, yd = xs[0], ys[0]
-    vld = None if vl_host is None else torch.empty_like(vl)
-    def e2e_step():
-        xd.copy_(x_pin, non_blocking=True)
-        if vld is not None:
-            vld.copy_(vl_pin, non_blocking=True)
-        smx.softmax_rows(xd, out=yd, valid_len=vld)
-        y_pin.copy_(yd, non_blocking=True)
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize(dev)
@@ -370,8 +508,6 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e = aggregate(bytes_step, w.rows, e2e_steps, world, e2e_ms / 1e3)
-    h2d = x_pin.numel() * x_pin.element_size() + (0 if vl_pin is None else vl_pin.numel() * 4)
-    d2h = y_pin.numel() * y_pin.element_size()
 
     if rank != 0:
         if world > 1:
@@ -381,13 +517,15 @@ def run_ours(args, w):
     peak, peak_kind = measured_peak()
     mean_launch_ms = statistics.fmean(launch_ms)
     achieved = bytes_step / (mean_launch_ms / 1e3) / 1e9
-    traffic, kernel_name = profile_traffic(w.name)
-    cpu_gbs, cpu_rows, cpu_s, cpu_rps = oracle_throughput(x_host, vl_host, w, args.cpu_budget)
+    traffic, kernel_name = profile_traffic(w.name, args.op)
+    cpu_gbs, cpu_rows, cpu_s, cpu_rps = oracle_throughput(x_host, vl_host, w, args.cpu_budget,
+                                                          op=args.op)
     line = {
-        "metric": METRIC, "value": agg["gbs"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_of(w, nsets), path=PATH_NAMES.get(used_path, used_path)),
+        "metric": metric_of(args.op), "value": agg["gbs"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": dict(config_of(w, nsets, args.op), path=PATH_NAMES.get(used_path, used_path)),
         "rows_per_s": agg["rows_per_s"],
         "pct_of_hbm_peak": 100.0 * agg["gbs"] / world / peak,
         "bytes_per_step": bytes_step,
@@ -402,7 +540,8 @@ def run_ours(args, w):
                                    f"thread, {cpu_s:.1f} s"},
         "e2e": {"value": e2e["gbs"], "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call,
+        "kernels_per_step": launches_per_call,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -424,6 +563,8 @@ def main(argv=None):
                     help="kernel family (diagnostics; the library chooses with auto)")
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds the reference arm spends over all its steps")
+    ap.add_argument("--op", choices=list(wl.OPS), default="softmax",
+                    help="entry point to time (default: the softmax)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -268,6 +268,7 @@ int smx_version(void);
  *   works normally -- a deterministic probe of the error path.
  * smx_debug_last_path(): the path (1..5) the last softmax/stats call on this
  *   thread used, 0 if none.
+ * smx_debug_last_launches(): kernels the last call on this thread launched.
  * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of
  *   `threads` threads per row (32 = one warp per row, path 1 only) holding `vpt`
  *   16-byte vectors each, when that shape covers the row (0, 0 = automatic).
@@ -276,6 +277,9 @@ int smx_version(void);
  * smx_debug_set_stream_ctas(n): n resident CTAs per SM on path 4, at most as
  *   many as fit (0 = automatic; also path 5).
  * smx_debug_set_split_slab(bytes): slab size of path 5 (0 = half the L2).
+ * smx_debug_set_inflight(read_only, backward): bytes of reads to keep in flight
+ *   per SM (which sets the persistent CTAs per SM) for the read-only
+ *   statistics / LSE rows and for the backward (0 = default).
  * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
  *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
  *   first; -1 = automatic (1 and 2).
@@ -287,12 +291,14 @@ void smx_debug_force_path(int path);
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes);
 void smx_debug_set_wait_limit(int64_t polls);
 int smx_debug_last_path(void);
+int smx_debug_last_launches(void);
 void smx_debug_set_regs_shape(int threads, int vpt);
 void smx_debug_set_stream_depth(int depth);
 void smx_debug_set_stream_ctas(int per_sm);
 void smx_debug_set_cluster_staging(int mode);
 void smx_debug_set_split_slab(int64_t bytes);
 void smx_debug_set_split_hints(int stats, int apply);
+void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 
 #ifdef __cplusplus
 }

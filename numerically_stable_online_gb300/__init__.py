@@ -89,6 +89,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_wait_limit.restype = None
         lib.smx_debug_last_path.argtypes = []
         lib.smx_debug_last_path.restype = I32
+        lib.smx_debug_last_launches.argtypes = []
+        lib.smx_debug_last_launches.restype = I32
         lib.smx_debug_set_regs_shape.argtypes = [I32, I32]
         lib.smx_debug_set_regs_shape.restype = None
         lib.smx_debug_set_stream_depth.argtypes = [I32]
@@ -101,6 +103,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_split_slab.restype = None
         lib.smx_debug_set_split_hints.argtypes = [I32, I32]
         lib.smx_debug_set_split_hints.restype = None
+        lib.smx_debug_set_inflight.argtypes = [I64, I64]
+        lib.smx_debug_set_inflight.restype = None
         _lib = lib
         return lib
 

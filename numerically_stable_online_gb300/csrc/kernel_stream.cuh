@@ -52,6 +52,41 @@ enum : int { MODE_APPLY = 2, MODE_LOG = 3, MODE_APPLY_LOG = 4, MODE_CE = 5, MODE
 // Cross-entropy epilogue of one item, elements [begin, begin + len) of its row
 // with L of them valid; v holds x (-inf in masked lanes).  The thread holding
 // x_t writes the row's loss; y (nullable) receives p - onehot(t).
+// Cross-entropy gradient of a whole row held in v as the exponentials
+// exp_and_sum<OutT, MODE_SOFTMAX> left there: p = e rD - [j == tl]; zeros on
+// ignored rows (and masked lanes), NaN in the valid lanes of bad rows.
+template <typename OutT, int VPT, int V>
+__device__ __forceinline__ void store_ce(OutT* yr, int G, int g, int ncols, int L, const float (&v)[VPT][V],
+                                         bool ignored, bool bad_row, float rD, int tl) {
+  const unsigned long long r2 = pk(rD, rD);
+  const bool own = tl >= 0 && (tl / V) % G == g;
+  const int jo = own ? tl / V / G : -1, io = tl % V;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int e0 = (j * G + g) * V;
+    if (e0 < ncols) {
+      float q[V];
+      if (!ignored && !bad_row) {
+#pragma unroll
+        for (int i = 0; i < V; i += 2) {
+          const unsigned long long t = mul2(pk(v[j][i], v[j][i + 1]), r2);
+          q[i] = pk_lo(t);
+          q[i + 1] = pk_hi(t);
+        }
+        if (j == jo) {
+#pragma unroll
+          for (int i = 0; i < V; ++i)
+            if (i == io) q[i] = __fsub_rn(q[i], 1.0f);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) q[i] = (!ignored && e0 + i < L) ? qnan() : 0.0f;
+      }
+      store_vec<OutT, V>(yr + e0, q);
+    }
+  }
+}
+
 template <typename OutT, int VPT, int V>
 __device__ __forceinline__ void ce_item(OutT* yr, float* loss, int64_t row, int G, int g, int len,
                                         int L, const float (&v)[VPT][V], float M, float D, float ld,
@@ -208,6 +243,21 @@ __global__ void SMX_STREAM_REGS
   };
   const uint64_t pol = (CHUNKED && it.l2_hint != 0) ? l2_policy(it.l2_hint) : 0;
   // copy this thread's vectors of item q into ring slot d; always one group
+  // per-row values the item needs after its reductions (the target; the given
+  // statistics) are loaded with the prefetch, DEPTH items ahead, so that their
+  // latency never sits on an item's critical path
+  constexpr bool HAS_TARGET = (MODE == MODE_CE || MODE == MODE_APPLY_CE);
+  int64_t Ts[DEPTH];
+  float Ms[DEPTH], Ds[DEPTH];
+  auto prefetch_row_values = [&](const Cursor& q, int slot) {
+    if constexpr (HAS_TARGET) Ts[slot] = q.k < k_end ? __ldg(target + it.row0 + q.r) : -1;
+    if constexpr (APPLY) {
+      if (it.row_stats && q.k < k_end) {
+        Ms[slot] = __ldg(m_in + q.r);
+        Ds[slot] = __ldg(d_in + q.r);
+      }
+    }
+  };
   auto prefetch = [&](const Cursor& q, int d) -> int {
     int Lk = 0;
     if (q.k < k_end) {
@@ -234,6 +284,7 @@ __global__ void SMX_STREAM_REGS
 #pragma unroll
   for (int d = 0; d < DEPTH; ++d) {
     Ls[d] = prefetch(pf, d);
+    prefetch_row_values(pf, d);
     advance(pf);
   }
 
@@ -259,13 +310,25 @@ __global__ void SMX_STREAM_REGS
 #pragma unroll
     for (int i = 0; i + 1 < DEPTH; ++i) Ls[i] = Ls[i + 1];
     Ls[DEPTH - 1] = prefetch(pf, d);
+    // this item's per-row values, then the ring moves on
+    const int64_t t_item = HAS_TARGET ? Ts[0] : -1;
+    const float m_item = APPLY ? Ms[0] : 0.0f, d_item = APPLY ? Ds[0] : 0.0f;
+#pragma unroll
+    for (int i = 0; i + 1 < DEPTH; ++i) {
+      if constexpr (HAS_TARGET) Ts[i] = Ts[i + 1];
+      if constexpr (APPLY) {
+        Ms[i] = Ms[i + 1];
+        Ds[i] = Ds[i + 1];
+      }
+    }
+    prefetch_row_values(pf, DEPTH - 1);
     advance(pf);
     d = d + 1 == DEPTH ? 0 : d + 1;
 
     if constexpr (APPLY) {
       if (cur.r != have_row) {  // uniform: every thread walks the same items
         if (it.row_stats) {
-          row_md = MD{__ldg(m_in + cur.r), __ldg(d_in + cur.r)};
+          row_md = MD{m_item, d_item};
         } else {
           MD acc{neg_inf(), 0.0f};
           const int64_t k0 = cur.r * it.nchunks;
@@ -291,8 +354,7 @@ __global__ void SMX_STREAM_REGS
         store_log<OutT, VPT, V>(yr, G, g, len, L, v, zero_row, nan_row, M, row_ld);
       } else if constexpr (MODE == MODE_APPLY_CE) {
         ce_item<OutT, VPT, V>(y == nullptr ? nullptr : yr, loss, row, G, g, len, L, v, M, Dr, row_ld,
-                              zero_row || nan_row, __ldg(target + row), row_valid(row),
-                              (int64_t)cur.c * ncols);
+                              zero_row || nan_row, t_item, row_valid(row), (int64_t)cur.c * ncols);
       } else {
         const OutConst kc = make_out_const<OutT>(M, Dr);
 #pragma unroll
@@ -312,6 +374,25 @@ __global__ void SMX_STREAM_REGS
         }
       }
     } else {
+      // cross-entropy: the thread holding x_t keeps it before v turns into
+      // exponentials
+      int64_t t_row = -1;
+      int tl = -1;
+      float xt = 0.0f;
+      bool ce_ignored = true;
+      if constexpr (MODE == MODE_CE) {
+        t_row = t_item;
+        ce_ignored = t_row < 0 || t_row >= L;  // a whole row: its valid length is the item's
+        tl = ce_ignored ? -1 : (int)t_row;
+        if (tl >= 0 && (tl / V) % G == g) {
+          const int jo = tl / V / G, io = tl % V;
+#pragma unroll
+          for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+              if (j == jo && i == io) xt = v[j][i];
+        }
+      }
       float mx = warp_max_nan(local_max(v));
       if (lane == 0) s_max[par][warp] = mx;
       __syncthreads();
@@ -319,8 +400,15 @@ __global__ void SMX_STREAM_REGS
       float Dsum = 0.0f;
       if (M != neg_inf()) {
         float sum;
-        if constexpr (MODE == MODE_LOG || MODE == MODE_CE) sum = warp_sum(sum_exp(v, M));  // v keeps x
-        else sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
+        if constexpr (MODE == MODE_LOG) {
+          sum = warp_sum(sum_exp(v, M));  // v keeps x
+        } else if constexpr (MODE == MODE_CE) {
+          // with a gradient, exponentials in place as the softmax forms them;
+          // the loss alone needs only their sum
+          sum = warp_sum(y != nullptr ? exp_and_sum<OutT, MODE_SOFTMAX>(v, M) : sum_exp(v, M));
+        } else {
+          sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
+        }
         if (lane == 0) s_sum[warp] = sum;
         __syncthreads();
         Dsum = warp_sum(lane < nw ? s_sum[lane] : 0.0f);
@@ -337,11 +425,19 @@ __global__ void SMX_STREAM_REGS
         }
       } else if constexpr (MODE == MODE_CE) {
         const bool zero_row = (M == neg_inf());
-        const bool nan_row = !zero_row && (Dsum != Dsum);
-        const float D = zero_row ? 0.0f : stats_correct(Dsum, M);
-        ce_item<OutT, VPT, V>(y == nullptr ? nullptr : y + row * it.cols, loss, row, G, g, len, L, v, M,
-                              D, zero_row ? 0.0f : logf(D), zero_row || nan_row, __ldg(target + row),
-                              row_valid(row), 0);
+        const bool bad_row = zero_row || (Dsum != Dsum);
+        if (tl >= 0 && (tl / V) % G == g) {
+          float ld;
+          if (y != nullptr)
+            ld = __fmaf_rn(-softmax_sum_offset_log2<OutT>(M), LN2, logf(Dsum));
+          else
+            ld = logf(stats_correct(Dsum, M));
+          loss[row] = bad_row ? qnan() : __fadd_rn(__fsub_rn(M, xt), ld);
+        }
+        if (ce_ignored && g == 0) loss[row] = 0.0f;
+        if (y != nullptr)
+          store_ce<OutT, VPT, V>(y + row * it.cols, G, g, len, L, v, ce_ignored, bad_row,
+                                 recip_refined(Dsum), tl);
       } else if constexpr (MODE == MODE_LOG) {
         const bool zero_row = (M == neg_inf());
         const bool nan_row = !zero_row && (Dsum != Dsum);

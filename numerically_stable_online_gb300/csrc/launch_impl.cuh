@@ -26,6 +26,7 @@ cudaError_t launch_regs_vpt(const Call& c, const Plan& p) {
     for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
       const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
       const unsigned grid = (unsigned)((n + rows_per_cta - 1) / rows_per_cta);
+      note_launch();
       k_rows_regs<InT, OutT, VPT, WR, MODE><<<grid, p.threads, 0, c.stream>>>(
           static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, r0 + n, c.cols,
           c.valid_len, r0);
@@ -86,6 +87,7 @@ cudaError_t launch_cluster_t(const Call& c, const Plan& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  note_launch();
   return cudaLaunchKernelEx(&cfg, k_rows_cluster<InT, OutT, CLUSTER_RV, MODE, TMA>,
                             static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out,
                             c.rows, c.cols, c.valid_len, p.chunk, p.smem_elems, c.max_polls,
@@ -106,7 +108,8 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
   // at most 16 elements per thread with the compensated exponential (fp32
   // outputs) or a per-element exponential after the sum, and 32 otherwise
   constexpr bool PER_ELEMENT_EXP = ExpPolicy<OutT, MODE>::ACCURATE || MODE == MODE_APPLY ||
-                                   MODE == MODE_CE || MODE == MODE_APPLY_CE;
+                                   MODE == MODE_APPLY_CE ||
+                                   (MODE == MODE_CE && ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE);
   if constexpr (VPT * V > (PER_ELEMENT_EXP ? 16 : 32)) {
     return cudaErrorInvalidValue;
   } else {
@@ -123,6 +126,7 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
       set_bytes[dev] = smem;
     }
     const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
+    note_launch();
     kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
         static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), m_out, d_out, m_in, d_in, it,
         c.valid_len, c.target, c.loss);
@@ -177,7 +181,11 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
     return launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, it, nullptr, nullptr, c.m_in,
                                                                c.d_in);
   } else {
-    const int64_t slab = p.slab_rows;
+    // the statistics-only calls (row statistics, LSE, the loss alone) read
+    // every element once: one slab of all rows
+    const bool read_once = (MODE == MODE_STATS || (MODE == MODE_CE && c.y == nullptr)) &&
+                           c.rows * p.nchunks <= ((int64_t)1 << 31) && p.scratch == nullptr;
+    const int64_t slab = read_once ? c.rows : p.slab_rows;
     const size_t part_n = (size_t)slab * p.nchunks;
     const size_t bytes = split_scratch_bytes(slab, p.nchunks);
     char* base = reinterpret_cast<char*>(p.scratch);
@@ -202,11 +210,13 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
         if (c.y != nullptr) {
           e = launch_stream_k<InT, OutT, MODE_APPLY_CE, SV, 2, true>(c, p, ap, nullptr, nullptr, pm, pd);
         } else {
+          note_launch();
           k_merge_chunk_ce<InT, 256><<<(unsigned)n, 256, 0, c.stream>>>(
               pm, pd, p.nchunks, static_cast<const InT*>(c.x), c.cols, c.target, c.valid_len, r0, c.loss);
           e = cudaGetLastError();
         }
       } else {
+        note_launch();
         k_merge_chunk_stats<256><<<(unsigned)n, 256, 0, c.stream>>>(
             pm, pd, p.nchunks, c.m_out + r0, c.d_out == nullptr ? nullptr : c.d_out + r0);
         e = cudaGetLastError();
@@ -224,6 +234,7 @@ template <typename InT, typename OutT, int MODE>
 cudaError_t launch_generic(const Call& c) {
   for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
     const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
+    note_launch();
     k_rows_generic<InT, OutT, MODE><<<(unsigned)n, GENERIC_THREADS, 0, c.stream>>>(
         static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), c.m_out, c.d_out, c.m_in, c.d_in,
         r0 + n, c.cols, c.valid_len, r0, c.target, c.loss);
@@ -251,6 +262,7 @@ cudaError_t launch_bwd_k(const Call& c, const Plan& p, const Items& it, float* p
     set_bytes[dev] = smem;
   }
   const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
+  note_launch();
   kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
       static_cast<const InT*>(c.x), static_cast<const InT*>(c.g), static_cast<OutT*>(c.y), part_out,
       part_in, it, c.valid_len);
@@ -264,6 +276,7 @@ cudaError_t launch_backward(const Call& c, const Plan& p) {
   if (p.path == PATH_GENERIC) {
     for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
       const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;
+      note_launch();
       k_backward_generic<InT, OutT><<<(unsigned)n, 256, 0, c.stream>>>(
           static_cast<const InT*>(c.x), static_cast<const InT*>(c.g), static_cast<OutT*>(c.y), c.cols,
           c.valid_len, r0);
@@ -381,7 +394,9 @@ cudaError_t launch_in(const Call& c, const Plan& p) {
     case MODE_APPLY: return launch_out<InT, MODE_APPLY>(c, p);
     case MODE_LOG: return launch_out<InT, MODE_LOG>(c, p);
     case MODE_CE:
-      return c.y == nullptr ? launch_typed<InT, float, MODE_CE>(c, p) : launch_out<InT, MODE_CE>(c, p);
+      // the loss alone: no output type; a half type keeps the 32-element shapes
+      return c.y == nullptr ? launch_typed<InT, __nv_bfloat16, MODE_CE>(c, p)
+                            : launch_out<InT, MODE_CE>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -410,9 +425,8 @@ int cluster_capacity(int cluster, int64_t smem_bytes) {
   return n;
 }
 
-template <typename InT>
-int stream_occupancy(int vpt, int threads, int depth) {
-  // the bf16-output softmax kernel stands for the family
+template <typename InT, typename OutT, int MODE>
+int stream_occupancy_mode(int vpt, int threads, int depth) {
   const int64_t smem = stream_smem_bytes(depth, vpt, threads);
   auto query = [&](auto kern) -> int {
     int n = 0;
@@ -425,29 +439,43 @@ int stream_occupancy(int vpt, int threads, int depth) {
     return n;
   };
   constexpr int V = Elem<InT>::V;
+  constexpr bool CH = (MODE == MODE_APPLY);  // the apply mode runs the chunked kernel, depth 2
   auto by_depth = [&](auto k2, auto k3, auto k4) {
+    if (CH) return query(k2);
     return depth == 3 ? query(k3) : (depth == 4 ? query(k4) : query(k2));
   };
   switch (vpt) {
     case 1:
-      return by_depth(k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 2, false>,
-                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 3, false>,
-                      k_rows_stream<InT, __nv_bfloat16, 1, MODE_SOFTMAX, 4, false>);
+      return by_depth(k_rows_stream<InT, OutT, 1, MODE, 2, CH>, k_rows_stream<InT, OutT, 1, MODE, CH ? 2 : 3, CH>,
+                      k_rows_stream<InT, OutT, 1, MODE, CH ? 2 : 4, CH>);
     case 2:
-      return by_depth(k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 2, false>,
-                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 3, false>,
-                      k_rows_stream<InT, __nv_bfloat16, 2, MODE_SOFTMAX, 4, false>);
+      return by_depth(k_rows_stream<InT, OutT, 2, MODE, 2, CH>, k_rows_stream<InT, OutT, 2, MODE, CH ? 2 : 3, CH>,
+                      k_rows_stream<InT, OutT, 2, MODE, CH ? 2 : 4, CH>);
     case 4:
-      return by_depth(k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 2, false>,
-                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 3, false>,
-                      k_rows_stream<InT, __nv_bfloat16, 4, MODE_SOFTMAX, 4, false>);
+      if constexpr (4 * V <= 16 || !CH)
+        return by_depth(k_rows_stream<InT, OutT, 4, MODE, 2, CH>,
+                        k_rows_stream<InT, OutT, 4, MODE, CH ? 2 : 3, CH>,
+                        k_rows_stream<InT, OutT, 4, MODE, CH ? 2 : 4, CH>);
+      return 0;
     case 8:
-      if constexpr (8 * V <= 32)
-        return by_depth(k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 2, false>,
-                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 3, false>,
-                        k_rows_stream<InT, __nv_bfloat16, 8, MODE_SOFTMAX, 4, false>);
+      if constexpr (8 * V <= 32 && !CH)
+        return by_depth(k_rows_stream<InT, OutT, 8, MODE, 2, CH>, k_rows_stream<InT, OutT, 8, MODE, 3, CH>,
+                        k_rows_stream<InT, OutT, 8, MODE, 4, CH>);
       return 0;
     default: return 0;
+  }
+}
+
+// Resident CTAs per SM of the streamed kernel of `mode` (a half-precision
+// output stands for the output types; statistics write fp32).
+template <typename InT>
+int stream_occupancy(int vpt, int threads, int depth, int mode) {
+  switch (mode) {
+    case MODE_STATS: return stream_occupancy_mode<InT, float, MODE_STATS>(vpt, threads, depth);
+    case MODE_LOG: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_LOG>(vpt, threads, depth);
+    case MODE_CE: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_CE>(vpt, threads, depth);
+    case MODE_APPLY: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_APPLY>(vpt, threads, depth);
+    default: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_SOFTMAX>(vpt, threads, depth);
   }
 }
 

@@ -134,22 +134,50 @@ __device__ __forceinline__ float exp_and_sum(float (&v)[VPT][V], float M) {
 // (to be corrected by stats_correct), leaving v unchanged.  Requires M != -inf.
 template <int VPT, int V>
 __device__ __forceinline__ float sum_exp(const float (&v)[VPT][V], float M) {
-  const bool huge = !(fabsf(M) < 1e38f);
-  const float c = huge ? 0.0f : __fmul_rn(-M, L2E_HI);
-  const float msub = huge ? M : 0.0f;
-  const unsigned long long k2 = pk(L2E_HI, L2E_HI), c2 = pk(c, c);
   unsigned long long acc = pk(0.0f, 0.0f);
+  const unsigned long long k2 = pk(L2E_HI, L2E_HI);
+  if (fabsf(M) < 1e38f) {
+    const float c = __fmul_rn(-M, L2E_HI);
+    const unsigned long long c2 = pk(c, c);
 #pragma unroll
-  for (int j = 0; j < VPT; ++j) {
+    for (int j = 0; j < VPT; ++j)
 #pragma unroll
-    for (int i = 0; i < V; i += 2) {
-      const float a = huge ? __fsub_rn(v[j][i], msub) : v[j][i];
-      const float b = huge ? __fsub_rn(v[j][i + 1], msub) : v[j][i + 1];
-      const unsigned long long u = fma2(pk(a, b), k2, c2);
-      acc = add2(acc, pk(ex2_ftz(pk_lo(u)), ex2_ftz(pk_hi(u))));
-    }
+      for (int i = 0; i < V; i += 2) {
+        const unsigned long long u = fma2(pk(v[j][i], v[j][i + 1]), k2, c2);
+        acc = add2(acc, pk(ex2_ftz(pk_lo(u)), ex2_ftz(pk_hi(u))));
+      }
+  } else {  // |M| near the top of the range: x - M first (see exp_and_sum)
+    const unsigned long long nm = pk(-M, -M);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+#pragma unroll
+      for (int i = 0; i < V; i += 2) {
+        const unsigned long long u = mul2(add2(pk(v[j][i], v[j][i + 1]), nm), k2);
+        acc = add2(acc, pk(ex2_ftz(pk_lo(u)), ex2_ftz(pk_hi(u))));
+      }
   }
   return __fadd_rn(pk_lo(acc), pk_hi(acc));
+}
+
+// The exponent offset, in log2 units, of the sum exp_and_sum<OutT,
+// MODE_SOFTMAX> forms: its terms are 2^(x L2E_HI + c) = 2^((x - M) L2E_HI) *
+// 2^delta with delta = c + M L2E_HI exactly, c = RN(-M L2E_HI + s).  With
+// a = RN(-M L2E_HI) and e1 its exact residual, delta = (c - a) - e1, where
+// c - a is exact (Sterbenz) unless |M| is small, when its rounding is far
+// below the error of the sum.  So log d = log(sum) - delta ln 2.  The
+// compensated exponential (fp32 outputs) has no offset.
+template <typename OutT>
+__device__ __forceinline__ float softmax_sum_offset_log2(float M) {
+  using P = ExpPolicy<OutT, MODE_SOFTMAX>;
+  if constexpr (P::ACCURATE) {
+    return 0.0f;
+  } else {
+    if (!(fabsf(M) < 1e38f)) return P::SCALE_LOG2;
+    const float a = __fmul_rn(-M, L2E_HI);
+    const float e1 = __fmaf_rn(-M, L2E_HI, -a);
+    const float c = __fmaf_rn(-M, L2E_HI, P::SCALE_LOG2);
+    return __fsub_rn(__fsub_rn(c, a), e1);
+  }
 }
 
 // Store log_softmax of the row held in v (inputs x): (x - M) - ld with

@@ -18,6 +18,7 @@ constexpr int64_t FIXED_SCRATCH_FLOATS = 65536;
 static __device__ __align__(256) float g_fixed_scratch[FIXED_SCRATCH_FLOATS];
 
 namespace smx {
+thread_local int t_kernel_launches = 0;
 namespace {
 
 constexpr int MAX_DEVICES = 64;
@@ -51,6 +52,8 @@ std::atomic<int> g_stream_ctas_per_sm{0};
 std::atomic<int> g_cluster_stage{0};  // 0 automatic, 1 bulk copies, 2 cp.async
 std::atomic<int64_t> g_split_slab_bytes{0};
 std::atomic<int> g_split_hint_stats{-1}, g_split_hint_apply{-1};
+std::atomic<int64_t> g_bwd_inflight{48 * 1024};  // backward: reads in flight per SM
+std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
@@ -178,11 +181,11 @@ bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
   return true;
 }
 
-int stream_occupancy(int in_dtype, int vpt, int threads, int depth) {
+int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode) {
   switch (in_dtype) {
-    case SMX_F32: return stream_occupancy_f32(vpt, threads, depth);
-    case SMX_F16: return stream_occupancy_f16(vpt, threads, depth);
-    default: return stream_occupancy_bf16(vpt, threads, depth);
+    case SMX_F32: return stream_occupancy_f32(vpt, threads, depth, mode);
+    case SMX_F16: return stream_occupancy_f16(vpt, threads, depth, mode);
+    default: return stream_occupancy_bf16(vpt, threads, depth, mode);
   }
 }
 
@@ -194,7 +197,8 @@ int stream_occupancy(int in_dtype, int vpt, int threads, int depth) {
 constexpr int64_t STREAM_INFLIGHT_BYTES = 48 * 1024;
 
 bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
-                 bool has_lengths, bool apply, Plan* p) {
+                 bool has_lengths, int mode, int64_t inflight, Plan* p) {
+  const bool apply = mode == MODE_APPLY;
   const int es = elem_size(in_dtype);
   if (cols * es > STREAM_MAX_ROW_BYTES) return false;
   Plan r;
@@ -208,12 +212,12 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
   }
   const int dd = g_stream_depth.load();
   const int depth = (!apply && (dd == 3 || dd == 4)) ? dd : 2;  // the apply kernel prefetches 2
-  const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth);
+  const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth, mode);
   if (occ_max <= 0) return false;
   int occ = occ_max;
   int64_t row_read = cols * es;
   if (has_lengths) row_read = (row_read + 1) / 2;
-  int64_t want = STREAM_INFLIGHT_BYTES / ((int64_t)depth * (row_read > 0 ? row_read : 1));
+  int64_t want = inflight / ((int64_t)depth * (row_read > 0 ? row_read : 1));
   if (want < 1) want = 1;
   if (want < occ) occ = (int)want;
   const int forced = g_stream_ctas_per_sm.load();
@@ -325,7 +329,8 @@ void plan_backward(DeviceInfo& d, const Call& c, bool vec_ok, Plan* p) {
       if (occ_max > 0) {
         int64_t read = 2 * row_bytes;
         if (c.valid_len != nullptr) read = (read + 1) / 2;
-        int64_t want = STREAM_INFLIGHT_BYTES / (2 * (read > 0 ? read : 1));
+        const int64_t per_cta = 2 * (read > 0 ? read : 1);  // two items prefetched
+        int64_t want = (g_bwd_inflight.load() + per_cta - 1) / per_cta;
         if (want < 1) want = 1;
         int occ = want < occ_max ? (int)want : occ_max;
         const int forced = g_stream_ctas_per_sm.load();
@@ -404,11 +409,13 @@ smx_status run(Call& c, DeviceInfo& dev) {
     } else if (force != PATH_GENERIC) {
       // the compensated exponential (fp32 softmax outputs, and every apply
       // output) holds 16 elements per thread at most
-      const bool acc = (c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32) || c.mode == MODE_APPLY ||
-                       c.mode == MODE_CE;
+      const bool acc = (c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32) ||
+                       (c.mode == MODE_CE && c.y != nullptr && c.out_dtype == SMX_F32) ||
+                       c.mode == MODE_APPLY;
       if (force != PATH_REGS || !classic)
-        planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr,
-                              c.mode == MODE_APPLY, &p);
+        planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, c.mode,
+                              c.mode == MODE_STATS ? g_read_only_inflight.load() : STREAM_INFLIGHT_BYTES,
+                              &p);
       if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       // rows longer than one CTA holds: a row per thread-block cluster when the
       // rows fill every resident cluster, else (a few very long rows) L2 slabs,
@@ -506,6 +513,7 @@ cudaError_t launch_merge(const float* m_a, const float* d_a, const float* m_b, c
                          float* m_o, float* d_o, int64_t n, cudaStream_t stream) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
+  note_launch();
   k_merge_stats<<<(unsigned)blocks, 256, 0, stream>>>(m_a, d_a, m_b, d_b, m_o, d_o, n);
   return cudaGetLastError();
 }
@@ -519,6 +527,7 @@ extern "C" {
 smx_status smx_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
                             const int32_t* valid_len, smx_dtype in_dtype, smx_dtype out_dtype,
                             smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
@@ -538,6 +547,7 @@ smx_status smx_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
 smx_status smx_softmax_rows_fixed_scratch(const void* x, void* y, int64_t rows, int64_t cols,
                                           const int32_t* valid_len, smx_dtype in_dtype,
                                           smx_dtype out_dtype, smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
@@ -582,6 +592,7 @@ smx_status smx_softmax_rows_fixed_scratch(const void* x, void* y, int64_t rows, 
 smx_status smx_softmax_row_stats(const void* x, float* m_out, float* d_out, int64_t rows,
                                  int64_t cols, const int32_t* valid_len, smx_dtype in_dtype,
                                  smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype)) return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
   if (rows == 0) return SMX_OK;
@@ -604,6 +615,7 @@ smx_status smx_softmax_row_stats(const void* x, float* m_out, float* d_out, int6
 smx_status smx_log_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
                                 const int32_t* valid_len, smx_dtype in_dtype, smx_dtype out_dtype,
                                 smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
@@ -622,6 +634,7 @@ smx_status smx_log_softmax_rows(const void* x, void* y, int64_t rows, int64_t co
 
 smx_status smx_softmax_lse(const void* x, float* lse_out, int64_t rows, int64_t cols,
                            const int32_t* valid_len, smx_dtype in_dtype, smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype)) return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
   if (rows == 0) return SMX_OK;
@@ -640,6 +653,7 @@ smx_status smx_softmax_lse(const void* x, float* lse_out, int64_t rows, int64_t 
 smx_status smx_softmax_apply_stats(const void* x, const float* m_in, const float* d_in, void* y,
                                    int64_t rows, int64_t cols, const int32_t* valid_len,
                                    smx_dtype in_dtype, smx_dtype out_dtype, smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
@@ -660,6 +674,7 @@ smx_status smx_softmax_apply_stats(const void* x, const float* m_in, const float
 smx_status smx_softmax_backward(const void* p, const void* g, void* dx, int64_t rows, int64_t cols,
                                 const int32_t* valid_len, smx_dtype dtype, smx_dtype dx_dtype,
                                 smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(dtype) || !valid_dtype(dx_dtype)) return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return SMX_OK;
@@ -679,6 +694,7 @@ smx_status smx_softmax_backward(const void* p, const void* g, void* dx, int64_t 
 smx_status smx_cross_entropy(const void* x, const int64_t* target, float* loss, void* grad,
                              int64_t rows, int64_t cols, const int32_t* valid_len, smx_dtype in_dtype,
                              smx_dtype grad_dtype, smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(grad_dtype))
     return SMX_ERR_INVALID_ARG;
   if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
@@ -705,6 +721,7 @@ smx_status smx_cross_entropy(const void* x, const int64_t* target, float* loss, 
 smx_status smx_softmax_merge_stats(const float* m_a, const float* d_a, const float* m_b,
                                    const float* d_b, float* m_out, float* d_out, int64_t n,
                                    smx_stream_t stream) {
+  t_kernel_launches = 0;
   if (n < 0) return SMX_ERR_INVALID_ARG;
   if (n == 0) return SMX_OK;
   if (!m_a || !d_a || !m_b || !d_b || !m_out || !d_out) return SMX_ERR_INVALID_ARG;
@@ -726,6 +743,7 @@ smx_status smx_softmax_merge_stats(const float* m_a, const float* d_a, const flo
 }
 
 smx_status smx_last_device_status(smx_stream_t stream) {
+  t_kernel_launches = 0;
   DeviceInfo* dev = nullptr;
   smx_status s = device_info(&dev);
   if (s != SMX_OK) return s;
@@ -769,9 +787,16 @@ void smx_debug_set_wait_limit(int64_t polls) { g_wait_limit.store(polls); }
 
 int smx_debug_last_path(void) { return t_last_path; }
 
+int smx_debug_last_launches(void) { return t_kernel_launches; }
+
 void smx_debug_set_stream_depth(int depth) { g_stream_depth.store(depth > 0 ? depth : 0); }
 
 void smx_debug_set_split_slab(int64_t bytes) { g_split_slab_bytes.store(bytes > 0 ? bytes : 0); }
+
+void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes) {
+  g_read_only_inflight.store(read_only_bytes > 0 ? read_only_bytes : 96 * 1024);
+  g_bwd_inflight.store(backward_bytes > 0 ? backward_bytes : 48 * 1024);
+}
 
 void smx_debug_set_split_hints(int stats, int apply) {
   g_split_hint_stats.store(stats >= 0 && stats <= 2 ? stats : -1);

@@ -58,6 +58,11 @@ struct Plan {
 constexpr int CLUSTER_RV = 2;  // register vectors per thread on the cluster path
 constexpr int CLUSTER_THREADS = 1024;
 
+// Kernels launched by the calling thread's current library call (a testing
+// and benchmarking count; reset by each entry point).
+extern thread_local int t_kernel_launches;
+inline void note_launch() { ++t_kernel_launches; }
+
 // Launch the planned kernel(s) for one input type; returns the first CUDA error.
 cudaError_t launch_in_f32(const Call& c, const Plan& p);
 cudaError_t launch_in_f16(const Call& c, const Plan& p);
@@ -70,9 +75,9 @@ int cluster_capacity_f16(int cluster, int64_t smem_bytes);
 int cluster_capacity_bf16(int cluster, int64_t smem_bytes);
 
 // Resident CTAs per SM of the streamed kernel for this input type and shape.
-int stream_occupancy_f32(int vpt, int threads, int depth);
-int stream_occupancy_f16(int vpt, int threads, int depth);
-int stream_occupancy_bf16(int vpt, int threads, int depth);
+int stream_occupancy_f32(int vpt, int threads, int depth, int mode);
+int stream_occupancy_f16(int vpt, int threads, int depth, int mode);
+int stream_occupancy_bf16(int vpt, int threads, int depth, int mode);
 int split_occupancy_f32(int threads);
 int split_occupancy_f16(int threads);
 int split_occupancy_bf16(int threads);

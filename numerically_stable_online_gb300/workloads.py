@@ -150,6 +150,34 @@ def causal_valid_len(rows: int) -> np.ndarray:
     return (np.arange(rows) % CAUSAL_SLICE_ROWS + 1).astype(np.int32)
 
 
+OPS = ("softmax", "log_softmax", "lse", "apply_stats", "backward", "cross_entropy")
+
+
+def op_bytes(op: str, rows: int, cols: int, in_size: int, out_size: int, valid_len=None) -> int:
+    """Bytes an operation must move over a [rows, cols] batch: the valid inputs
+    read once (the backward reads two arrays), each dense output written once,
+    and the per-row values (lengths 4 B, statistics 8 B, LSE 4 B, targets 8 B +
+    loss 4 B) once."""
+    if valid_len is None:
+        valid = rows * cols
+        lens = 0
+    else:
+        valid = int(np.clip(np.asarray(valid_len, dtype=np.int64), 0, cols).sum())
+        lens = rows * 4
+    dense_out = rows * cols * out_size
+    if op in ("softmax", "log_softmax"):
+        return valid * in_size + dense_out + lens
+    if op == "lse":
+        return valid * in_size + rows * 4 + lens
+    if op == "apply_stats":
+        return valid * in_size + dense_out + rows * 8 + lens
+    if op == "backward":
+        return 2 * valid * in_size + dense_out + lens
+    if op == "cross_entropy":
+        return valid * in_size + dense_out + rows * 12 + lens
+    raise ValueError(f"unknown op {op}")
+
+
 def algorithmic_bytes(rows: int, cols: int, in_size: int, out_size: int, valid_len=None) -> int:
     """Bytes the method must move: the valid input read once, every output written
     once, and the row lengths read once when given."""
