@@ -280,6 +280,8 @@ int smx_version(void);
  * smx_debug_set_inflight(read_only, backward): bytes of reads to keep in flight
  *   per SM (which sets the persistent CTAs per SM) for the read-only
  *   statistics / LSE rows and for the backward (0 = default).
+ * smx_debug_set_stream_warp(off): 1 = path 4 walks every row with a whole CTA;
+ *   0 = rows that fit one warp are walked a row per warp (default).
  * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
  *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
  *   first; -1 = automatic (1 and 2).
@@ -298,6 +300,7 @@ void smx_debug_set_stream_ctas(int per_sm);
 void smx_debug_set_cluster_staging(int mode);
 void smx_debug_set_split_slab(int64_t bytes);
 void smx_debug_set_split_hints(int stats, int apply);
+void smx_debug_set_stream_warp(int off);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 
 #ifdef __cplusplus

@@ -105,6 +105,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_split_hints.restype = None
         lib.smx_debug_set_inflight.argtypes = [I64, I64]
         lib.smx_debug_set_inflight.restype = None
+        lib.smx_debug_set_stream_warp.argtypes = [I32]
+        lib.smx_debug_set_stream_warp.restype = None
         _lib = lib
         return lib
 

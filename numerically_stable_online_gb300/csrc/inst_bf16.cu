@@ -6,8 +6,8 @@ cudaError_t launch_in_bf16(const Call& c, const Plan& p) { return launch_in<__nv
 int cluster_capacity_bf16(int cluster, int64_t smem_bytes) {
   return cluster_capacity<__nv_bfloat16>(cluster, smem_bytes);
 }
-int stream_occupancy_bf16(int vpt, int threads, int depth, int mode) {
-  return stream_occupancy<__nv_bfloat16>(vpt, threads, depth, mode);
+int stream_occupancy_bf16(int vpt, int threads, int depth, int mode, bool warp) {
+  return stream_occupancy<__nv_bfloat16>(vpt, threads, depth, mode, warp);
 }
 int split_occupancy_bf16(int threads) { return split_occupancy<__nv_bfloat16>(threads); }
 int backward_occupancy_bf16(int vpt, int threads) {

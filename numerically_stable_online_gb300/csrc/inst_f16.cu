@@ -6,8 +6,8 @@ cudaError_t launch_in_f16(const Call& c, const Plan& p) { return launch_in<__hal
 int cluster_capacity_f16(int cluster, int64_t smem_bytes) {
   return cluster_capacity<__half>(cluster, smem_bytes);
 }
-int stream_occupancy_f16(int vpt, int threads, int depth, int mode) {
-  return stream_occupancy<__half>(vpt, threads, depth, mode);
+int stream_occupancy_f16(int vpt, int threads, int depth, int mode, bool warp) {
+  return stream_occupancy<__half>(vpt, threads, depth, mode, warp);
 }
 int split_occupancy_f16(int threads) { return split_occupancy<__half>(threads); }
 int backward_occupancy_f16(int vpt, int threads) {

@@ -6,8 +6,8 @@ cudaError_t launch_in_f32(const Call& c, const Plan& p) { return launch_in<float
 int cluster_capacity_f32(int cluster, int64_t smem_bytes) {
   return cluster_capacity<float>(cluster, smem_bytes);
 }
-int stream_occupancy_f32(int vpt, int threads, int depth, int mode) {
-  return stream_occupancy<float>(vpt, threads, depth, mode);
+int stream_occupancy_f32(int vpt, int threads, int depth, int mode, bool warp) {
+  return stream_occupancy<float>(vpt, threads, depth, mode, warp);
 }
 int split_occupancy_f32(int threads) { return split_occupancy<float>(threads); }
 int backward_occupancy_f32(int vpt, int threads) {

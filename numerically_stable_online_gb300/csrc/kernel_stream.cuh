@@ -13,9 +13,11 @@
 // item's group is awaited with cp.async.wait_group just before the item is used.
 //
 // Whole rows (CHUNKED = false) are dealt round robin: CTA b takes rows
-// b, b + gridDim.x, ...  Chunks (CHUNKED = true) are dealt in contiguous runs:
-// CTA b takes items [b n / gridDim.x, (b + 1) n / gridDim.x), so a CTA meets
-// each of its rows in consecutive items.
+// b, b + gridDim.x, ...  With WARP = true each warp is such a walker on its own
+// (a row per warp, rows b NW + w, stepping by gridDim.x NW): short rows then
+// need no block barrier at all, only warp shuffles.  Chunks (CHUNKED = true)
+// are dealt in contiguous runs: CTA b takes items [b n / gridDim.x,
+// (b + 1) n / gridDim.x), so a CTA meets each of its rows in consecutive items.
 //
 // Modes (the same walk):
 //   MODE_SOFTMAX  whole rows: y = e^(x - m) / d.
@@ -38,8 +40,10 @@
 //   MODE_CE       whole rows: cross-entropy with logits (the same section and
 //                 "The Jacobian, and the backward pass that never divides"):
 //                 loss = LSE - x_t = (m - x_t) + log d, and, when y is given,
-//                 the fused gradient y = p - onehot(t).  A target outside the
-//                 valid prefix is ignored: loss 0 and a zero gradient row.
+//                 the fused gradient y = p - onehot(t): the row's p is stored,
+//                 then the thread that holds x_t stores p_t - 1 over its own
+//                 p_t.  A target outside the valid prefix is ignored: loss 0
+//                 and a zero gradient row.
 //   MODE_APPLY_CE   chunks: MODE_CE with the row's merged (M, D).
 #pragma once
 
@@ -48,87 +52,6 @@
 namespace smx {
 
 enum : int { MODE_APPLY = 2, MODE_LOG = 3, MODE_APPLY_LOG = 4, MODE_CE = 5, MODE_APPLY_CE = 6 };
-
-// Cross-entropy epilogue of one item, elements [begin, begin + len) of its row
-// with L of them valid; v holds x (-inf in masked lanes).  The thread holding
-// x_t writes the row's loss; y (nullable) receives p - onehot(t).
-// Cross-entropy gradient of a whole row held in v as the exponentials
-// exp_and_sum<OutT, MODE_SOFTMAX> left there: p = e rD - [j == tl]; zeros on
-// ignored rows (and masked lanes), NaN in the valid lanes of bad rows.
-template <typename OutT, int VPT, int V>
-__device__ __forceinline__ void store_ce(OutT* yr, int G, int g, int ncols, int L, const float (&v)[VPT][V],
-                                         bool ignored, bool bad_row, float rD, int tl) {
-  const unsigned long long r2 = pk(rD, rD);
-  const bool own = tl >= 0 && (tl / V) % G == g;
-  const int jo = own ? tl / V / G : -1, io = tl % V;
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int e0 = (j * G + g) * V;
-    if (e0 < ncols) {
-      float q[V];
-      if (!ignored && !bad_row) {
-#pragma unroll
-        for (int i = 0; i < V; i += 2) {
-          const unsigned long long t = mul2(pk(v[j][i], v[j][i + 1]), r2);
-          q[i] = pk_lo(t);
-          q[i + 1] = pk_hi(t);
-        }
-        if (j == jo) {
-#pragma unroll
-          for (int i = 0; i < V; ++i)
-            if (i == io) q[i] = __fsub_rn(q[i], 1.0f);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) q[i] = (!ignored && e0 + i < L) ? qnan() : 0.0f;
-      }
-      store_vec<OutT, V>(yr + e0, q);
-    }
-  }
-}
-
-template <typename OutT, int VPT, int V>
-__device__ __forceinline__ void ce_item(OutT* yr, float* loss, int64_t row, int G, int g, int len,
-                                        int L, const float (&v)[VPT][V], float M, float D, float ld,
-                                        bool bad_row, int64_t t, int64_t Lrow, int64_t begin) {
-  const bool ignored = t < 0 || t >= Lrow;
-  const int64_t tl64 = t - begin;
-  const int tl = (!ignored && tl64 >= 0 && tl64 < len) ? (int)tl64 : -1;
-  if (tl >= 0 && (tl / V) % G == g) {
-    const int jo = tl / V / G, io = tl % V;
-    float xt = 0.0f;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j)
-#pragma unroll
-      for (int i = 0; i < V; ++i)
-        if (j == jo && i == io) xt = v[j][i];
-    loss[row] = bad_row ? qnan() : __fadd_rn(__fsub_rn(M, xt), ld);
-  }
-  if (ignored && begin == 0 && g == 0) loss[row] = 0.0f;
-  if (yr == nullptr) return;
-  const OutConst kc = make_out_const<OutT>(M, D);
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int e0 = (j * G + g) * V;
-    if (e0 < len) {
-      float q[V];
-      if (ignored) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) q[i] = 0.0f;
-      } else if (bad_row) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) q[i] = e0 + i < L ? qnan() : 0.0f;
-      } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-          q[i] = out_value<OutT>(v[j][i], kc);
-          if (e0 + i == tl) q[i] = __fsub_rn(q[i], 1.0f);
-        }
-      }
-      store_vec<OutT, V>(yr + e0, q);
-    }
-  }
-}
 
 // The items of one launch: item k is chunk k % nchunks of row row0 + k / nchunks.
 struct Items {
@@ -149,6 +72,12 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t smem_dst, const void* g
                "l"(gsrc), "l"(pol)
                : "memory");
 }
+__device__ __forceinline__ void cp_async8(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -165,34 +94,45 @@ __device__ __forceinline__ uint64_t l2_policy(int hint) {
 
 // SMX_STREAM_MAXNREG (a build-time tuning knob) caps the registers per thread,
 // trading spills for resident CTAs.
+// The warp walkers run 128-thread CTAs, so their register budget is not the
+// 1024-thread one.
 #ifdef SMX_STREAM_MAXNREG
 #define SMX_STREAM_REGS __maxnreg__(SMX_STREAM_MAXNREG)
 #else
-#define SMX_STREAM_REGS __launch_bounds__(1024)
+#define SMX_STREAM_REGS __launch_bounds__(WARP ? 128 : 1024)
 #endif
 
-template <typename InT, typename OutT, int VPT, int MODE, int DEPTH, bool CHUNKED>
+template <typename InT, typename OutT, int VPT, int MODE, int DEPTH, bool CHUNKED, bool WARP = false>
 __global__ void SMX_STREAM_REGS
     k_rows_stream(const InT* __restrict__ x, OutT* __restrict__ y, float* __restrict__ m_out,
                   float* __restrict__ d_out, const float* __restrict__ m_in,
                   const float* __restrict__ d_in, Items it, const int32_t* __restrict__ valid_len,
                   const int64_t* __restrict__ target, float* __restrict__ loss) {
   constexpr bool APPLY = (MODE == MODE_APPLY || MODE == MODE_APPLY_LOG || MODE == MODE_APPLY_CE);
+  constexpr bool CE = (MODE == MODE_CE || MODE == MODE_APPLY_CE);
   static_assert(CHUNKED || !APPLY, "the apply modes walk chunks");
+  static_assert(!(WARP && CHUNKED), "a warp walks whole rows");
   constexpr int V = Elem<InT>::V;
-  extern __shared__ __align__(16) uint4 sbuf[];  // [DEPTH][VPT][G]: thread g owns column g
+  // [walkers][DEPTH][VPT][G] uint4: thread g of a walker owns column g; then
+  // [DEPTH][blockDim.x] 8-byte words: each thread's copy of its item's per-row
+  // value (the target, or the given (m, d))
+  extern __shared__ __align__(16) uint4 sbuf[];
   // s_max alternates between items: an item with no valid lane skips the sum's
   // barrier, so only the next item's max barrier separates reads from rewrites
   // (s_mm, s_dd alternate between row merges for the same reason)
   __shared__ float s_max[2][32], s_sum[32], s_mm[2][32], s_dd[2][32];
 
-  const int G = blockDim.x, g = threadIdx.x, lane = g & 31, warp = g >> 5, nw = G >> 5;
-  const uint32_t my_slot = static_cast<uint32_t>(__cvta_generic_to_shared(sbuf + g));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int G = WARP ? 32 : blockDim.x, g = WARP ? lane : threadIdx.x;
+  uint4* ring = sbuf + (WARP ? (size_t)warp * DEPTH * VPT * 32 : 0);
+  const uint32_t my_slot = static_cast<uint32_t>(__cvta_generic_to_shared(ring + g));
   const uint32_t slot_stride = (uint32_t)(VPT * G * 16);  // bytes between ring slots
+  uint2* aux = reinterpret_cast<uint2*>(sbuf + (size_t)DEPTH * VPT * blockDim.x);
+  const uint32_t my_aux = static_cast<uint32_t>(__cvta_generic_to_shared(aux + threadIdx.x));
   const int ncols = (int)(CHUNKED ? it.chunk : it.cols);
 
   // An item's place: k, its row r (from row0) and chunk c.  Two cursors walk
-  // the CTA's items without dividing: `cur` at the item being reduced, `pf`
+  // the walker's items without dividing: `cur` at the item being reduced, `pf`
   // DEPTH items ahead at the next one to prefetch.
   struct Cursor {
     int64_t k, r;
@@ -200,10 +140,16 @@ __global__ void SMX_STREAM_REGS
   };
   int64_t k_end;
   Cursor cur;
+  int64_t step = gridDim.x;
   if constexpr (CHUNKED) {
     const int64_t kb = (int64_t)blockIdx.x * it.n / gridDim.x;
     k_end = (int64_t)(blockIdx.x + 1) * it.n / gridDim.x;
     cur = Cursor{kb, kb / it.nchunks, (int)(kb % it.nchunks)};
+  } else if constexpr (WARP) {
+    k_end = it.n;
+    const int64_t k0 = (int64_t)blockIdx.x * nw + warp;
+    cur = Cursor{k0, k0, 0};
+    step = (int64_t)gridDim.x * nw;
   } else {
     k_end = it.n;
     cur = Cursor{(int64_t)blockIdx.x, (int64_t)blockIdx.x, 0};
@@ -216,7 +162,7 @@ __global__ void SMX_STREAM_REGS
         ++q.r;
       }
     } else {
-      q.k += gridDim.x;
+      q.k += step;
       q.r = q.k;
     }
   };
@@ -241,23 +187,48 @@ __global__ void SMX_STREAM_REGS
     const int64_t v = __ldg(valid_len + row);
     return v < 0 ? 0 : (v > it.cols ? it.cols : v);
   };
+  // reductions over the walker (the CTA, or one warp)
+  auto walker_max = [&](float m, int par) -> float {
+    m = warp_max_nan(m);
+    if constexpr (WARP) {
+      return m;
+    } else {
+      if (lane == 0) s_max[par][warp] = m;
+      __syncthreads();
+      return warp_max_nan(lane < nw ? s_max[par][lane] : neg_inf());
+    }
+  };
+  auto walker_sum = [&](float t) -> float {
+    t = warp_sum(t);
+    if constexpr (WARP) {
+      return t;
+    } else {
+      if (lane == 0) s_sum[warp] = t;
+      __syncthreads();
+      return warp_sum(lane < nw ? s_sum[lane] : 0.0f);
+    }
+  };
   const uint64_t pol = (CHUNKED && it.l2_hint != 0) ? l2_policy(it.l2_hint) : 0;
-  // copy this thread's vectors of item q into ring slot d; always one group
-  // per-row values the item needs after its reductions (the target; the given
-  // statistics) are loaded with the prefetch, DEPTH items ahead, so that their
-  // latency never sits on an item's critical path
-  constexpr bool HAS_TARGET = (MODE == MODE_CE || MODE == MODE_APPLY_CE);
-  int64_t Ts[DEPTH];
-  float Ms[DEPTH], Ds[DEPTH];
-  auto prefetch_row_values = [&](const Cursor& q, int slot) {
-    if constexpr (HAS_TARGET) Ts[slot] = q.k < k_end ? __ldg(target + it.row0 + q.r) : -1;
-    if constexpr (APPLY) {
-      if (it.row_stats && q.k < k_end) {
-        Ms[slot] = __ldg(m_in + q.r);
-        Ds[slot] = __ldg(d_in + q.r);
+  // per-row values the item needs (the target; the given statistics) travel
+  // with the item: lane 0 of each warp copies them into its own word of the
+  // slot in the same cp.async group (so no register waits on their loads) and
+  // hands them to the other lanes by shuffle once the group has landed
+  constexpr bool AUX = CE || APPLY;
+  auto prefetch_row_values = [&](const Cursor& q, int d) {
+    if constexpr (AUX) {
+      if (lane == 0 && q.k < k_end) {  // one copy per warp, shuffled to the lanes
+        const uint32_t dst = my_aux + d * blockDim.x * 8;
+        if constexpr (CE) cp_async8(dst, target + it.row0 + q.r);
+        if constexpr (APPLY) {
+          if (it.row_stats) {
+            cp_async4(dst, m_in + q.r);
+            cp_async4(dst + 4, d_in + q.r);
+          }
+        }
       }
     }
   };
+  // copy this thread's vectors of item q into ring slot d; always one group
   auto prefetch = [&](const Cursor& q, int d) -> int {
     int Lk = 0;
     if (q.k < k_end) {
@@ -275,6 +246,7 @@ __global__ void SMX_STREAM_REGS
         }
       }
     }
+    prefetch_row_values(q, d);
     cp_async_commit();
     return Lk;
   };
@@ -284,14 +256,13 @@ __global__ void SMX_STREAM_REGS
 #pragma unroll
   for (int d = 0; d < DEPTH; ++d) {
     Ls[d] = prefetch(pf, d);
-    prefetch_row_values(pf, d);
     advance(pf);
   }
 
-  // the apply mode's merged summary of the row it is in
+  // the apply modes' summary of the row they are in
   int64_t have_row = -1;
   MD row_md{neg_inf(), 0.0f};
-  float row_ld = 0.0f;  // log of row_md.d (the log modes)
+  float row_ld = 0.0f;  // log of row_md.d (the log and cross-entropy modes)
   int mpar = 0;
 
   for (int d = 0, par = 0; cur.k < k_end; advance(cur), par ^= 1) {
@@ -299,29 +270,41 @@ __global__ void SMX_STREAM_REGS
     const int L = Ls[0];
     const int len = item_len(cur);
     const int64_t row = it.row0 + cur.r;
+    const int64_t begin = (int64_t)cur.c * ncols;
     float v[VPT][V];
-    const InT* sx = reinterpret_cast<const InT*>(sbuf + (size_t)d * VPT * G);
+    const InT* sx = reinterpret_cast<const InT*>(ring + (size_t)d * VPT * G);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       const int e0 = (j * G + g) * V;
       load_masked<InT, true>(sx + e0, e0, L, v[j]);
     }
+    // cross-entropy: the target's place in this item, and x_t, read by the
+    // thread that copied it (the slot holds the item in element order) before
+    // the slot is refilled
+    int64_t t_item = -1;
+    float m_item = 0.0f, d_item = 0.0f;
+    if constexpr (AUX) {
+      const uint2 w0 = aux[d * blockDim.x + threadIdx.x];  // meaningful in lane 0
+      const uint2 w = make_uint2(__shfl_sync(0xffffffffu, w0.x, 0), __shfl_sync(0xffffffffu, w0.y, 0));
+      if constexpr (CE) t_item = (long long)(((unsigned long long)w.y << 32) | w.x);
+      if constexpr (APPLY) {
+        m_item = __uint_as_float(w.x);
+        d_item = __uint_as_float(w.y);
+      }
+    }
+    int tl = -1;
+    bool t_mine = false;
+    float xt = 0.0f;
+    if constexpr (CE) {
+      const int64_t tl64 = t_item - begin;
+      if (tl64 >= 0 && tl64 < L) tl = (int)tl64;
+      t_mine = tl >= 0 && (tl / V) % G == g;
+      if (t_mine) xt = Elem<InT>::to_f32(sx[tl]);
+    }
     // the slot's words are in registers now: refill it with the item DEPTH ahead
 #pragma unroll
     for (int i = 0; i + 1 < DEPTH; ++i) Ls[i] = Ls[i + 1];
     Ls[DEPTH - 1] = prefetch(pf, d);
-    // this item's per-row values, then the ring moves on
-    const int64_t t_item = HAS_TARGET ? Ts[0] : -1;
-    const float m_item = APPLY ? Ms[0] : 0.0f, d_item = APPLY ? Ds[0] : 0.0f;
-#pragma unroll
-    for (int i = 0; i + 1 < DEPTH; ++i) {
-      if constexpr (HAS_TARGET) Ts[i] = Ts[i + 1];
-      if constexpr (APPLY) {
-        Ms[i] = Ms[i + 1];
-        Ds[i] = Ds[i + 1];
-      }
-    }
-    prefetch_row_values(pf, DEPTH - 1);
     advance(pf);
     d = d + 1 == DEPTH ? 0 : d + 1;
 
@@ -349,103 +332,94 @@ __global__ void SMX_STREAM_REGS
       const float M = row_md.m, Dr = row_md.d;
       const bool zero_row = (M == neg_inf());
       const bool nan_row = !zero_row && (Dr != Dr || M != M || M == pos_inf());
-      OutT* yr = y + row * it.cols + (int64_t)cur.c * ncols;
+      OutT* yr = y + row * it.cols + begin;
       if constexpr (MODE == MODE_APPLY_LOG) {
         store_log<OutT, VPT, V>(yr, G, g, len, L, v, zero_row, nan_row, M, row_ld);
-      } else if constexpr (MODE == MODE_APPLY_CE) {
-        ce_item<OutT, VPT, V>(y == nullptr ? nullptr : yr, loss, row, G, g, len, L, v, M, Dr, row_ld,
-                              zero_row || nan_row, t_item, row_valid(row), (int64_t)cur.c * ncols);
       } else {
-        const OutConst kc = make_out_const<OutT>(M, Dr);
+        // cross-entropy: an ignored target zeroes the row, a bad row is NaN
+        // in its valid lanes; the owner of x_t writes the loss
+        bool zero_out = zero_row, nan_out = nan_row;
+        if constexpr (MODE == MODE_APPLY_CE) {
+          const bool ignored = t_item < 0 || t_item >= row_valid(row);
+          const bool bad = zero_row || nan_row;
+          zero_out = ignored;
+          nan_out = !ignored && bad;
+          if (t_mine) loss[row] = bad ? qnan() : __fadd_rn(__fsub_rn(M, xt), row_ld);
+          if (ignored && cur.c == 0 && g == 0) loss[row] = 0.0f;
+        }
+        if (MODE != MODE_APPLY_CE || y != nullptr) {
+          const OutConst kc = make_out_const<OutT>(M, Dr);
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-          const int e0 = (j * G + g) * V;
-          if (e0 < len) {
-            float p[V];
-            if (!zero_row && !nan_row) {
+          for (int j = 0; j < VPT; ++j) {
+            const int e0 = (j * G + g) * V;
+            if (e0 < len) {
+              float p[V];
+              if (!zero_out && !nan_out) {
 #pragma unroll
-              for (int i = 0; i < V; ++i) p[i] = out_value<OutT>(v[j][i], kc);
-            } else {
+                for (int i = 0; i < V; ++i) p[i] = out_value<OutT>(v[j][i], kc);
+              } else {
 #pragma unroll
-              for (int i = 0; i < V; ++i) p[i] = (nan_row && e0 + i < L) ? qnan() : 0.0f;
+                for (int i = 0; i < V; ++i) p[i] = (nan_out && e0 + i < L) ? qnan() : 0.0f;
+              }
+              store_vec<OutT, V>(yr + e0, p);
             }
-            store_vec<OutT, V>(yr + e0, p);
+          }
+          if constexpr (MODE == MODE_APPLY_CE) {
+            // p_t - 1 over the owner's own earlier store of p_t
+            if (t_mine && !zero_out && !nan_out)
+              yr[tl] = Elem<OutT>::from_f32(__fsub_rn(out_value<OutT>(xt, kc), 1.0f));
           }
         }
       }
     } else {
-      // cross-entropy: the thread holding x_t keeps it before v turns into
-      // exponentials
-      int64_t t_row = -1;
-      int tl = -1;
-      float xt = 0.0f;
-      bool ce_ignored = true;
-      if constexpr (MODE == MODE_CE) {
-        t_row = t_item;
-        ce_ignored = t_row < 0 || t_row >= L;  // a whole row: its valid length is the item's
-        tl = ce_ignored ? -1 : (int)t_row;
-        if (tl >= 0 && (tl / V) % G == g) {
-          const int jo = tl / V / G, io = tl % V;
-#pragma unroll
-          for (int j = 0; j < VPT; ++j)
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-              if (j == jo && i == io) xt = v[j][i];
-        }
-      }
-      float mx = warp_max_nan(local_max(v));
-      if (lane == 0) s_max[par][warp] = mx;
-      __syncthreads();
-      const float M = warp_max_nan(lane < nw ? s_max[par][lane] : neg_inf());
+      const float M = walker_max(local_max(v), par);
       float Dsum = 0.0f;
       if (M != neg_inf()) {
         float sum;
         if constexpr (MODE == MODE_LOG) {
-          sum = warp_sum(sum_exp(v, M));  // v keeps x
+          sum = sum_exp(v, M);  // v keeps x
         } else if constexpr (MODE == MODE_CE) {
           // with a gradient, exponentials in place as the softmax forms them;
           // the loss alone needs only their sum
-          sum = warp_sum(y != nullptr ? exp_and_sum<OutT, MODE_SOFTMAX>(v, M) : sum_exp(v, M));
+          sum = y != nullptr ? exp_and_sum<OutT, MODE_SOFTMAX>(v, M) : sum_exp(v, M);
         } else {
-          sum = warp_sum(exp_and_sum<OutT, MODE>(v, M));
+          sum = exp_and_sum<OutT, MODE>(v, M);
         }
-        if (lane == 0) s_sum[warp] = sum;
-        __syncthreads();
-        Dsum = warp_sum(lane < nw ? s_sum[lane] : 0.0f);
+        Dsum = walker_sum(sum);
       }
+      const bool zero_row = (M == neg_inf());
+      const bool nan_row = !zero_row && (Dsum != Dsum);
       if constexpr (MODE == MODE_STATS) {
         if (g == 0) {
-          const float dk = M == neg_inf() ? 0.0f : stats_correct(Dsum, M);
+          const float dk = zero_row ? 0.0f : stats_correct(Dsum, M);
           if (d_out != nullptr) {
             m_out[cur.k] = M;
             d_out[cur.k] = dk;
           } else {
-            m_out[cur.k] = M == neg_inf() ? neg_inf() : __fadd_rn(M, logf(dk));
+            m_out[cur.k] = zero_row ? neg_inf() : __fadd_rn(M, logf(dk));
           }
         }
       } else if constexpr (MODE == MODE_CE) {
-        const bool zero_row = (M == neg_inf());
-        const bool bad_row = zero_row || (Dsum != Dsum);
-        if (tl >= 0 && (tl / V) % G == g) {
-          float ld;
-          if (y != nullptr)
-            ld = __fmaf_rn(-softmax_sum_offset_log2<OutT>(M), LN2, logf(Dsum));
-          else
-            ld = logf(stats_correct(Dsum, M));
-          loss[row] = bad_row ? qnan() : __fadd_rn(__fsub_rn(M, xt), ld);
+        const bool ignored = tl < 0;  // a whole row: the item's valid length is the row's
+        const bool bad = zero_row || nan_row;
+        if (t_mine) {
+          const float ld = y != nullptr ? __fmaf_rn(-softmax_sum_offset_log2<OutT>(M), LN2, logf(Dsum))
+                                        : logf(stats_correct(Dsum, M));
+          loss[row] = bad ? qnan() : __fadd_rn(__fsub_rn(M, xt), ld);
         }
-        if (ce_ignored && g == 0) loss[row] = 0.0f;
-        if (y != nullptr)
-          store_ce<OutT, VPT, V>(y + row * it.cols, G, g, len, L, v, ce_ignored, bad_row,
-                                 recip_refined(Dsum), tl);
+        if (ignored && g == 0) loss[row] = 0.0f;
+        if (y != nullptr) {
+          OutT* yr = y + row * it.cols;
+          const float rD = recip_refined(Dsum);
+          store_row<OutT, VPT, V>(yr, G, g, len, L, v, ignored, !ignored && bad, rD);
+          // p_t - 1 over the owner's own earlier store of p_t
+          if (t_mine && !bad)
+            yr[tl] = Elem<OutT>::from_f32(__fsub_rn(__fmul_rn(exp_like_softmax<OutT>(xt, M), rD), 1.0f));
+        }
       } else if constexpr (MODE == MODE_LOG) {
-        const bool zero_row = (M == neg_inf());
-        const bool nan_row = !zero_row && (Dsum != Dsum);
         const float ld = zero_row ? 0.0f : logf(stats_correct(Dsum, M));
         store_log<OutT, VPT, V>(y + row * it.cols, G, g, len, L, v, zero_row, nan_row, M, ld);
       } else {
-        const bool zero_row = (M == neg_inf());
-        const bool nan_row = !zero_row && (Dsum != Dsum);
         store_row<OutT, VPT, V>(y + row * it.cols, G, g, len, L, v, zero_row, nan_row,
                                 recip_refined(Dsum));
       }

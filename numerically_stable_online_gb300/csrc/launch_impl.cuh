@@ -101,7 +101,7 @@ cudaError_t launch_cluster(const Call& c, const Plan& p) {
 }
 
 // One launch of the streamed kernel over the items `it`.
-template <typename InT, typename OutT, int MODE, int VPT, int DEPTH, bool CHUNKED>
+template <typename InT, typename OutT, int MODE, int VPT, int DEPTH, bool CHUNKED, bool WARP = false>
 cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float* m_out, float* d_out,
                             const float* m_in, const float* d_in) {
   constexpr int V = Elem<InT>::V;
@@ -113,8 +113,8 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
   if constexpr (VPT * V > (PER_ELEMENT_EXP ? 16 : 32)) {
     return cudaErrorInvalidValue;
   } else {
-    auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH, CHUNKED>;
-    const int64_t smem = stream_smem_bytes(DEPTH, VPT, p.threads);
+    auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH, CHUNKED, WARP>;
+    const int64_t smem = stream_smem_bytes(DEPTH, VPT, p.threads);  // walkers x their rings
     static int64_t set_bytes[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -125,7 +125,9 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
       if (e != cudaSuccess) return e;
       set_bytes[dev] = smem;
     }
-    const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
+    const int64_t walkers = WARP ? p.threads / 32 : 1;  // rows a CTA walks at once
+    const int64_t need = (it.n + walkers - 1) / walkers;
+    const int64_t grid = need < p.ctas ? need : p.ctas;
     note_launch();
     kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
         static_cast<const InT*>(c.x), static_cast<OutT*>(c.y), m_out, d_out, m_in, d_in, it,
@@ -136,6 +138,8 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
 
 template <typename InT, typename OutT, int MODE, int VPT>
 cudaError_t launch_stream_v(const Call& c, const Plan& p, const Items& it) {
+  if (p.warp_rows)  // a row per warp, two rows prefetched per warp
+    return launch_stream_k<InT, OutT, MODE, VPT, 2, false, true>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
   switch (p.stages) {
     case 3: return launch_stream_k<InT, OutT, MODE, VPT, 3, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
     case 4: return launch_stream_k<InT, OutT, MODE, VPT, 4, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
@@ -426,7 +430,7 @@ int cluster_capacity(int cluster, int64_t smem_bytes) {
 }
 
 template <typename InT, typename OutT, int MODE>
-int stream_occupancy_mode(int vpt, int threads, int depth) {
+int stream_occupancy_mode(int vpt, int threads, int depth, bool warp) {
   const int64_t smem = stream_smem_bytes(depth, vpt, threads);
   auto query = [&](auto kern) -> int {
     int n = 0;
@@ -444,6 +448,19 @@ int stream_occupancy_mode(int vpt, int threads, int depth) {
     if (CH) return query(k2);
     return depth == 3 ? query(k3) : (depth == 4 ? query(k4) : query(k2));
   };
+  if constexpr (!CH) {
+    if (warp) {
+      switch (vpt) {
+        case 1: return query(k_rows_stream<InT, OutT, 1, MODE, 2, false, true>);
+        case 2: return query(k_rows_stream<InT, OutT, 2, MODE, 2, false, true>);
+        case 4: return query(k_rows_stream<InT, OutT, 4, MODE, 2, false, true>);
+        case 8:
+          if constexpr (8 * V <= 32) return query(k_rows_stream<InT, OutT, 8, MODE, 2, false, true>);
+          return 0;
+        default: return 0;
+      }
+    }
+  }
   switch (vpt) {
     case 1:
       return by_depth(k_rows_stream<InT, OutT, 1, MODE, 2, CH>, k_rows_stream<InT, OutT, 1, MODE, CH ? 2 : 3, CH>,
@@ -469,13 +486,14 @@ int stream_occupancy_mode(int vpt, int threads, int depth) {
 // Resident CTAs per SM of the streamed kernel of `mode` (a half-precision
 // output stands for the output types; statistics write fp32).
 template <typename InT>
-int stream_occupancy(int vpt, int threads, int depth, int mode) {
+int stream_occupancy(int vpt, int threads, int depth, int mode, bool warp) {
   switch (mode) {
-    case MODE_STATS: return stream_occupancy_mode<InT, float, MODE_STATS>(vpt, threads, depth);
-    case MODE_LOG: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_LOG>(vpt, threads, depth);
-    case MODE_CE: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_CE>(vpt, threads, depth);
-    case MODE_APPLY: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_APPLY>(vpt, threads, depth);
-    default: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_SOFTMAX>(vpt, threads, depth);
+    case MODE_STATS: return stream_occupancy_mode<InT, float, MODE_STATS>(vpt, threads, depth, warp);
+    case MODE_LOG: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_LOG>(vpt, threads, depth, warp);
+    case MODE_CE: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_CE>(vpt, threads, depth, warp);
+    case MODE_APPLY:
+      return stream_occupancy_mode<InT, __nv_bfloat16, MODE_APPLY>(vpt, threads, depth, false);
+    default: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_SOFTMAX>(vpt, threads, depth, warp);
   }
 }
 

@@ -159,6 +159,20 @@ __device__ __forceinline__ float sum_exp(const float (&v)[VPT][V], float M) {
   return __fadd_rn(pk_lo(acc), pk_hi(acc));
 }
 
+// One element's exponential exactly as exp_and_sum<OutT, MODE_SOFTMAX> forms
+// it (same operations, same rounding): the compensated exponential for fp32
+// outputs, else 2^(fma(x, L2E_HI, c)) with its row constant c.
+template <typename OutT>
+__device__ __forceinline__ float exp_like_softmax(float x, float M) {
+  using P = ExpPolicy<OutT, MODE_SOFTMAX>;
+  if constexpr (P::ACCURATE) {
+    return exp_shift_accurate(x, M);
+  } else {
+    if (!(fabsf(M) < 1e38f)) return ex2_ftz(__fmaf_rn(__fsub_rn(x, M), L2E_HI, P::SCALE_LOG2));
+    return ex2_ftz(__fmaf_rn(x, L2E_HI, __fmaf_rn(-M, L2E_HI, P::SCALE_LOG2)));
+  }
+}
+
 // The exponent offset, in log2 units, of the sum exp_and_sum<OutT,
 // MODE_SOFTMAX> forms: its terms are 2^(x L2E_HI + c) = 2^((x - M) L2E_HI) *
 // 2^delta with delta = c + M L2E_HI exactly, c = RN(-M L2E_HI + s).  With

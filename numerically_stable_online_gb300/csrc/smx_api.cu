@@ -53,6 +53,7 @@ std::atomic<int> g_cluster_stage{0};  // 0 automatic, 1 bulk copies, 2 cp.async
 std::atomic<int64_t> g_split_slab_bytes{0};
 std::atomic<int> g_split_hint_stats{-1}, g_split_hint_apply{-1};
 std::atomic<int64_t> g_bwd_inflight{48 * 1024};  // backward: reads in flight per SM
+std::atomic<int> g_stream_warp{0};  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
 thread_local int t_last_cuda_error = 0;
@@ -181,11 +182,11 @@ bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
   return true;
 }
 
-int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode) {
+int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode, bool warp) {
   switch (in_dtype) {
-    case SMX_F32: return stream_occupancy_f32(vpt, threads, depth, mode);
-    case SMX_F16: return stream_occupancy_f16(vpt, threads, depth, mode);
-    default: return stream_occupancy_bf16(vpt, threads, depth, mode);
+    case SMX_F32: return stream_occupancy_f32(vpt, threads, depth, mode, warp);
+    case SMX_F16: return stream_occupancy_f16(vpt, threads, depth, mode, warp);
+    default: return stream_occupancy_bf16(vpt, threads, depth, mode, warp);
   }
 }
 
@@ -195,39 +196,54 @@ int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode) {
 // row reads in flight on every SM (measured on GB300: fewer CTAs starve HBM,
 // more only contend; with lengths given, rows are taken as half valid).
 constexpr int64_t STREAM_INFLIGHT_BYTES = 48 * 1024;
+constexpr int64_t CE_INFLIGHT_BYTES = 64 * 1024;
 
 bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
                  bool has_lengths, int mode, int64_t inflight, Plan* p) {
   const bool apply = mode == MODE_APPLY;
   const int es = elem_size(in_dtype);
   if (cols * es > STREAM_MAX_ROW_BYTES) return false;
+  const int V = 16 / es;
+  const int64_t nvec = cols / V;
+  const int max_vpt = (accurate_exp ? 16 : 32) / V;
   Plan r;
-  if (!plan_regs(cols, in_dtype, accurate_exp, &r) || r.warp_rows) {
-    const int V = 16 / es;
-    const int64_t nvec = cols / V;
+  // a row that fits one warp is walked by one warp (no block barrier), unless
+  // a CTA shape is forced or the warp walkers are switched off
+  bool warp = false;
+  if (!apply && g_stream_warp.load() == 0 && g_regs_threads.load() == 0 &&
+      nvec <= 32LL * max_vpt) {
+    r.vpt = 1;
+    while (32LL * r.vpt < nvec) r.vpt <<= 1;
+    r.threads = WARP_WALKER_THREADS;
+    warp = true;
+  } else if (!plan_regs(cols, in_dtype, accurate_exp, &r) || r.warp_rows) {
     r.threads = 64;
     r.vpt = 1;
     while (64LL * r.vpt < nvec) r.vpt <<= 1;
     if (r.vpt * V > (accurate_exp ? 16 : 32)) return false;
   }
   const int dd = g_stream_depth.load();
-  const int depth = (!apply && (dd == 3 || dd == 4)) ? dd : 2;  // the apply kernel prefetches 2
-  const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth, mode);
+  // the apply kernel and the warp walkers prefetch 2 items
+  const int depth = (!apply && !warp && (dd == 3 || dd == 4)) ? dd : 2;
+  const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth, mode, warp);
   if (occ_max <= 0) return false;
   int occ = occ_max;
   int64_t row_read = cols * es;
   if (has_lengths) row_read = (row_read + 1) / 2;
-  int64_t want = inflight / ((int64_t)depth * (row_read > 0 ? row_read : 1));
+  const int64_t walkers = warp ? r.threads / 32 : 1;
+  int64_t want = inflight / ((int64_t)depth * walkers * (row_read > 0 ? row_read : 1));
   if (want < 1) want = 1;
   if (want < occ) occ = (int)want;
   const int forced = g_stream_ctas_per_sm.load();
   if (forced > 0) occ = forced < occ_max ? forced : occ_max;
   const int64_t ctas = (int64_t)occ * d.sm_count;
+  const int64_t need = (rows + walkers - 1) / walkers;
   p->path = PATH_STREAM;
   p->threads = r.threads;
   p->vpt = r.vpt;
+  p->warp_rows = warp;
   p->stages = depth;
-  p->ctas = (int)(rows < ctas ? rows : ctas);
+  p->ctas = (int)(need < ctas ? need : ctas);
   return true;
 }
 
@@ -413,9 +429,13 @@ smx_status run(Call& c, DeviceInfo& dev) {
                        (c.mode == MODE_CE && c.y != nullptr && c.out_dtype == SMX_F32) ||
                        c.mode == MODE_APPLY;
       if (force != PATH_REGS || !classic)
+        // read-only rows (statistics, LSE) and the cross-entropy (longer per-row
+        // epilogue) keep more rows in flight (measured on GB300)
+        const int64_t inflight = c.mode == MODE_STATS ? g_read_only_inflight.load()
+                                 : c.mode == MODE_CE  ? CE_INFLIGHT_BYTES
+                                                      : STREAM_INFLIGHT_BYTES;
         planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, c.mode,
-                              c.mode == MODE_STATS ? g_read_only_inflight.load() : STREAM_INFLIGHT_BYTES,
-                              &p);
+                              inflight, &p);
       if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       // rows longer than one CTA holds: a row per thread-block cluster when the
       // rows fill every resident cluster, else (a few very long rows) L2 slabs,
@@ -797,6 +817,8 @@ void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes) {
   g_read_only_inflight.store(read_only_bytes > 0 ? read_only_bytes : 96 * 1024);
   g_bwd_inflight.store(backward_bytes > 0 ? backward_bytes : 48 * 1024);
 }
+
+void smx_debug_set_stream_warp(int off) { g_stream_warp.store(off ? 1 : 0); }
 
 void smx_debug_set_split_hints(int stats, int apply) {
   g_split_hint_stats.store(stats >= 0 && stats <= 2 ? stats : -1);

@@ -75,9 +75,9 @@ int cluster_capacity_f16(int cluster, int64_t smem_bytes);
 int cluster_capacity_bf16(int cluster, int64_t smem_bytes);
 
 // Resident CTAs per SM of the streamed kernel for this input type and shape.
-int stream_occupancy_f32(int vpt, int threads, int depth, int mode);
-int stream_occupancy_f16(int vpt, int threads, int depth, int mode);
-int stream_occupancy_bf16(int vpt, int threads, int depth, int mode);
+int stream_occupancy_f32(int vpt, int threads, int depth, int mode, bool warp);
+int stream_occupancy_f16(int vpt, int threads, int depth, int mode, bool warp);
+int stream_occupancy_bf16(int vpt, int threads, int depth, int mode, bool warp);
 int split_occupancy_f32(int threads);
 int split_occupancy_f16(int threads);
 int split_occupancy_bf16(int threads);
@@ -89,6 +89,7 @@ int backward_occupancy_bf16(int vpt, int threads);
 constexpr int BWD_MAX_ROW_BYTES = 16384;  // whole rows per CTA; longer rows in chunks
 
 constexpr int STREAM_MAX_ROW_BYTES = 32768;
+constexpr int WARP_WALKER_THREADS = 128;  // CTA of the warp walkers: 4 independent warps
 
 // Scratch of the long-row slab path for slabs of `slab` rows of `nchunks`
 // chunks: the chunk summaries (m, then d).
@@ -97,9 +98,10 @@ inline size_t split_scratch_bytes(int64_t slab, int64_t nchunks) {
 }
 
 // Dynamic shared memory of the streamed kernel: `depth` rows of vpt 16-byte
-// vectors for each of the CTA's threads.
+// vectors for each of the CTA's threads, and an 8-byte word per thread per row
+// for the row's own values (target, given statistics).
 inline int64_t stream_smem_bytes(int depth, int vpt, int threads) {
-  return (int64_t)depth * vpt * threads * 16;
+  return (int64_t)depth * vpt * threads * 16 + (int64_t)depth * threads * 8;
 }
 
 cudaError_t launch_merge(const float* m_a, const float* d_a, const float* m_b, const float* d_b,

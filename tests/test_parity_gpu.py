@@ -53,6 +53,7 @@ def lib(built):
     built.smx_debug_set_split_slab(0)
     built.smx_debug_set_split_hints(-1, -1)
     built.smx_debug_set_stream_ctas(0)
+    built.smx_debug_set_stream_warp(0)
 
 
 DEV = "cuda:0"
@@ -277,7 +278,9 @@ def test_stream_ring_many_rows(lib, in_dtype, out_dtype, cols, depth):
     lib.smx_debug_force_path(PATH_STREAM)
     lib.smx_debug_set_stream_depth(depth)
     run_and_compare(x, in_dtype, out_dtype, rows, cols, vl)
-    assert lib.smx_debug_last_path() == PATH_STREAM
+    es = 4 if in_dtype == "f32" else 2
+    # rows of a 16-byte multiple take path 4; others the scalar kernel
+    assert lib.smx_debug_last_path() == (PATH_STREAM if cols * es % 16 == 0 else PATH_GENERIC)
     m, d = gpu_stats(x, in_dtype, rows, cols, vl)
     m_ref, d_ref = oracle.row_stats(x, in_dtype, rows, cols, vl)
     check_stats(m, d, m_ref, d_ref)
@@ -478,3 +481,28 @@ def test_bounded_wait_reports_timeout(lib):
     y = smx.softmax_rows(x)
     assert smx.last_device_status() == 0
     parity.compare(y.cpu().numpy(), p, "f32")
+
+
+@pytest.mark.parametrize("cols", [8, 100, 256, 1000, 1024, 2048])
+@pytest.mark.parametrize("in_dtype,out_dtype", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f16"),
+                                                ("f16", "f32")])
+@pytest.mark.parametrize("warp_off", [0, 1])
+def test_stream_walkers(lib, cols, in_dtype, out_dtype, warp_off):
+    """Path 4 with a row per warp (rows that fit one warp) and with a CTA per
+    row, many rows per walker, lengths including 0, 1 and cols."""
+    rows = 3000
+    rng = np.random.default_rng(cols + 11)
+    x = stored(rng.normal(0, 6, rows * cols), in_dtype)
+    vl = rng.integers(0, cols + 1, size=rows).astype(np.int32)
+    vl[::101] = 0
+    vl[1::67] = 1
+    vl[2::53] = cols
+    lib.smx_debug_force_path(PATH_STREAM)
+    lib.smx_debug_set_stream_warp(warp_off)
+    run_and_compare(x, in_dtype, out_dtype, rows, cols, vl)
+    es = 4 if in_dtype == "f32" else 2
+    # rows of a 16-byte multiple take path 4; others the scalar kernel
+    assert lib.smx_debug_last_path() == (PATH_STREAM if cols * es % 16 == 0 else PATH_GENERIC)
+    m, d = gpu_stats(x, in_dtype, rows, cols, vl)
+    m_ref, d_ref = oracle.row_stats(x, in_dtype, rows, cols, vl)
+    check_stats(m, d, m_ref, d_ref)

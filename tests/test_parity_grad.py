@@ -43,6 +43,7 @@ def lib(built):
     yield built
     built.smx_debug_force_path(0)
     built.smx_debug_set_split_slab(0)
+    built.smx_debug_set_stream_warp(0)
 
 
 def lengths_t(valid_len):
@@ -242,3 +243,19 @@ def test_ce_bench_workload_full_size(lib):
     _, d = oracle.row_stats(xs, "bf16", len(sel), w.cols)
     parity.compare_ce(loss.cpu().numpy()[sel], wl.torch_to_storage(grad[sel].cpu()), ref_loss,
                       ref_grad, np.log(d), tt, "bf16")
+
+
+@pytest.mark.parametrize("cols", [8, 256, 1000, 1024])
+@pytest.mark.parametrize("in_dtype,grad_dtype", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f16")])
+@pytest.mark.parametrize("warp_off", [0, 1])
+@pytest.mark.parametrize("with_grad", [True, False])
+def test_ce_stream_walkers(lib, cols, in_dtype, grad_dtype, warp_off, with_grad):
+    rows = 1500
+    rng = np.random.default_rng(cols + 13)
+    x = stored(rng.normal(0, 6, rows * cols), in_dtype)
+    vl = rng.integers(0, cols + 1, size=rows).astype(np.int32)
+    vl[::97] = 0
+    t = rng.integers(-1, cols + 1, rows)
+    lib.smx_debug_force_path(PATH_STREAM)
+    lib.smx_debug_set_stream_warp(warp_off)
+    run_ce(x, in_dtype, grad_dtype, rows, cols, t, vl, with_grad=with_grad)

@@ -42,6 +42,7 @@ def lib(built):
     yield built
     built.smx_debug_force_path(0)
     built.smx_debug_set_split_slab(0)
+    built.smx_debug_set_stream_warp(0)
 
 
 def lengths_t(valid_len):
@@ -251,3 +252,17 @@ def test_column_split_softmax(lib, in_dtype, out_dtype, cols, cut):
     y = torch.cat([ya, yb], dim=1)
     p = oracle.softmax_rows(xs, in_dtype, rows, cols)
     parity.compare(wl.torch_to_storage(y.cpu()), p, out_dtype)
+
+
+@pytest.mark.parametrize("cols", [8, 256, 1000, 1024])
+@pytest.mark.parametrize("in_dtype,out_dtype", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f32")])
+@pytest.mark.parametrize("warp_off", [0, 1])
+def test_log_stream_walkers(lib, cols, in_dtype, out_dtype, warp_off):
+    rows = 1500
+    rng = np.random.default_rng(cols + 12)
+    x = stored(rng.normal(0, 6, rows * cols), in_dtype)
+    vl = rng.integers(0, cols + 1, size=rows).astype(np.int32)
+    vl[::97] = 0
+    lib.smx_debug_force_path(PATH_STREAM)
+    lib.smx_debug_set_stream_warp(warp_off)
+    run_log(x, in_dtype, out_dtype, rows, cols, vl)
