@@ -428,7 +428,7 @@ smx_status run(Call& c, DeviceInfo& dev) {
       const bool acc = (c.mode == MODE_SOFTMAX && c.out_dtype == SMX_F32) ||
                        (c.mode == MODE_CE && c.y != nullptr && c.out_dtype == SMX_F32) ||
                        c.mode == MODE_APPLY;
-      if (force != PATH_REGS || !classic)
+      if (force != PATH_REGS || !classic) {
         // read-only rows (statistics, LSE) and the cross-entropy (longer per-row
         // epilogue) keep more rows in flight (measured on GB300)
         const int64_t inflight = c.mode == MODE_STATS ? g_read_only_inflight.load()
@@ -436,6 +436,7 @@ smx_status run(Call& c, DeviceInfo& dev) {
                                                       : STREAM_INFLIGHT_BYTES;
         planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, c.mode,
                               inflight, &p);
+      }
       if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       // rows longer than one CTA holds: a row per thread-block cluster when the
       // rows fill every resident cluster, else (a few very long rows) L2 slabs,
