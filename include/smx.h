@@ -34,12 +34,13 @@
  *
  * Memory and ownership: every data pointer is a device pointer owned by the
  * caller; the library never frees or retains it.  It allocates one device
- * status word per device on first use, and the long-row path (rows too long for
- * one CTA) takes a small stream-ordered scratch allocation per call for its
- * chunk summaries (cudaMallocAsync / cudaFreeAsync on `stream`: 8 bytes per
- * chunk of 4096 elements of an L2-sized slab of rows); its variant
- * smx_softmax_rows_fixed_scratch uses a fixed array instead.  No other call
- * allocates.
+ * status word and creates one memory pool per device on first use.  The
+ * long-row paths (rows too long for one CTA) take a small stream-ordered
+ * scratch allocation per call from that pool for their chunk summaries
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`: 8 bytes per chunk of
+ * 4096 elements, plus 4 bytes per row); the pool keeps up to 64 MiB between
+ * calls so that later calls reuse it.  smx_softmax_rows_fixed_scratch uses a
+ * fixed array instead.  No other call allocates.
  * Every call is asynchronous on `stream` (NULL is the legacy default stream) and
  * returns after enqueueing its kernels.
  *
@@ -282,6 +283,9 @@ int smx_version(void);
  *   statistics / LSE rows and for the backward (0 = default).
  * smx_debug_set_stream_warp(off): 1 = path 4 walks every row with a whole CTA;
  *   0 = rows that fit one warp are walked a row per warp (default).
+ * smx_debug_set_split_fused(off): 1 = path 5 runs two launches per slab (the
+ *   statistics pass, then the normalising pass); 0 = one cooperative launch for
+ *   all slabs with per-row completion counts (default where supported).
  * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
  *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
  *   first; -1 = automatic (1 and 2).
@@ -301,6 +305,7 @@ void smx_debug_set_cluster_staging(int mode);
 void smx_debug_set_split_slab(int64_t bytes);
 void smx_debug_set_split_hints(int stats, int apply);
 void smx_debug_set_stream_warp(int off);
+void smx_debug_set_split_fused(int off);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 
 #ifdef __cplusplus

@@ -107,6 +107,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_inflight.restype = None
         lib.smx_debug_set_stream_warp.argtypes = [I32]
         lib.smx_debug_set_stream_warp.restype = None
+        lib.smx_debug_set_split_fused.argtypes = [I32]
+        lib.smx_debug_set_split_fused.restype = None
         _lib = lib
         return lib
 

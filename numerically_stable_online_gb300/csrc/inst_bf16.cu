@@ -10,6 +10,7 @@ int stream_occupancy_bf16(int vpt, int threads, int depth, int mode, bool warp) 
   return stream_occupancy<__nv_bfloat16>(vpt, threads, depth, mode, warp);
 }
 int split_occupancy_bf16(int threads) { return split_occupancy<__nv_bfloat16>(threads); }
+int split_fused_occupancy_bf16(int threads) { return split_fused_occupancy<__nv_bfloat16>(threads); }
 int backward_occupancy_bf16(int vpt, int threads) {
   return backward_occupancy<__nv_bfloat16>(vpt, threads);
 }

@@ -10,6 +10,7 @@ int stream_occupancy_f16(int vpt, int threads, int depth, int mode, bool warp) {
   return stream_occupancy<__half>(vpt, threads, depth, mode, warp);
 }
 int split_occupancy_f16(int threads) { return split_occupancy<__half>(threads); }
+int split_fused_occupancy_f16(int threads) { return split_fused_occupancy<__half>(threads); }
 int backward_occupancy_f16(int vpt, int threads) {
   return backward_occupancy<__half>(vpt, threads);
 }

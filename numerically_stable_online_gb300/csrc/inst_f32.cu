@@ -10,6 +10,7 @@ int stream_occupancy_f32(int vpt, int threads, int depth, int mode, bool warp) {
   return stream_occupancy<float>(vpt, threads, depth, mode, warp);
 }
 int split_occupancy_f32(int threads) { return split_occupancy<float>(threads); }
+int split_fused_occupancy_f32(int threads) { return split_fused_occupancy<float>(threads); }
 int backward_occupancy_f32(int vpt, int threads) {
   return backward_occupancy<float>(vpt, threads);
 }

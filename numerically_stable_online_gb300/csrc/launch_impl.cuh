@@ -3,17 +3,40 @@
 // compile in parallel) with SMX_IN_T and SMX_SUFFIX defined.
 #pragma once
 
+#include <mutex>
+#include <unordered_map>
+
 #include "kernel_backward.cuh"
 #include "kernel_cluster.cuh"
 #include "kernel_generic.cuh"
 #include "kernel_stream.cuh"
 #include "kernel_regs.cuh"
+#include "kernel_split_fused.cuh"
 #include "smx_launch.h"
 
 namespace smx {
 namespace {
 
 constexpr int64_t MAX_GRID_X_ROWS = int64_t(1) << 30;
+
+// The dynamic-shared-memory limit of a kernel is only ever raised: launches and
+// occupancy queries of one kernel with different sizes share the attribute, so
+// lowering it for one would make another's launch fail.  The largest value set
+// per (device, kernel) is kept here.
+inline cudaError_t smem_raise(const void* kern, int64_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int64_t> set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  int64_t& have = set[dev][kern];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 constexpr int64_t MAX_GRID_Y = 65535;
 
 template <typename InT, typename OutT, int MODE, int VPT, bool WR>
@@ -51,20 +74,17 @@ cudaError_t launch_regs_wr(const Call& c, const Plan& p) {
 template <typename InT, typename OutT, int MODE, bool TMA>
 cudaError_t prepare_cluster_kernel(int64_t smem_bytes) {
   auto kern = k_rows_cluster<InT, OutT, CLUSTER_RV, MODE, TMA>;
-  // per device: the largest dynamic shared memory size set so far
-  static int64_t set_bytes[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (set_bytes[dev] < smem_bytes) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
-    if (e != cudaSuccess) return e;
+  static bool nonportable[64] = {};
+  if (!nonportable[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    set_bytes[dev] = smem_bytes;
+    nonportable[dev] = true;
   }
-  return cudaSuccess;
+  return smem_raise(reinterpret_cast<const void*>(kern), smem_bytes);
 }
 
 template <typename InT, typename OutT, int MODE, bool TMA>
@@ -115,16 +135,12 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
   } else {
     auto kern = k_rows_stream<InT, OutT, VPT, MODE, DEPTH, CHUNKED, WARP>;
     const int64_t smem = stream_smem_bytes(DEPTH, VPT, p.threads);  // walkers x their rings
-    static int64_t set_bytes[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (set_bytes[dev] < smem) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      set_bytes[dev] = smem;
-    }
+    e = smem_raise(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
     const int64_t walkers = WARP ? p.threads / 32 : 1;  // rows a CTA walks at once
     const int64_t need = (it.n + walkers - 1) / walkers;
     const int64_t grid = need < p.ctas ? need : p.ctas;
@@ -171,6 +187,97 @@ cudaError_t launch_stream(const Call& c, const Plan& p) {
   }
 }
 
+// One cooperative launch over all slabs: chunk summaries, per-row completion
+// counts, merge and normalise (kernel_split_fused.cuh).  Scratch: the chunk
+// summaries of every row and one counter per row, zeroed on the stream first.
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_split_fused(const Call& c, const Plan& p) {
+  constexpr int SV = 16 / Elem<InT>::V;
+  auto kern = k_rows_split<InT, OutT, MODE, SV, 2>;
+  const int64_t smem = 2LL * SV * p.threads * 16;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  e = smem_raise(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  // every CTA of a cooperative grid must be resident: size it by this
+  // instantiation's own occupancy
+  static int resident[64][2] = {};  // per device: threads asked, CTAs resident (asked once)
+  if (resident[dev][0] != p.threads) {
+    int occ = 0, sms = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, p.threads, (size_t)smem)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    resident[dev][1] = occ * sms;
+    resident[dev][0] = p.threads;
+  }
+  const int grid = p.fused_ctas < resident[dev][1] ? p.fused_ctas : resident[dev][1];
+  const size_t n_sum = (size_t)c.rows * p.nchunks;
+  const size_t bytes = 2 * n_sum * sizeof(float) + (size_t)c.rows * sizeof(unsigned);
+  char* base = nullptr;
+  e = scratch_alloc(c, reinterpret_cast<void**>(&base), bytes);
+  if (e != cudaSuccess) return e;
+  SplitArgs a;
+  a.rows = c.rows;
+  a.cols = c.cols;
+  a.nchunks = p.nchunks;
+  a.slab = p.slab_rows;
+  a.ms = reinterpret_cast<float*>(base);
+  a.ds = a.ms + n_sum;
+  a.count = reinterpret_cast<unsigned*>(a.ds + n_sum);
+  a.target = c.target;
+  a.loss = c.loss;
+  a.max_polls = c.max_polls;
+  a.status = c.status;
+  e = cudaMemsetAsync(a.count, 0, (size_t)c.rows * sizeof(unsigned), c.stream);
+  if (e == cudaSuccess) {
+    const InT* xp = static_cast<const InT*>(c.x);
+    OutT* yp = static_cast<OutT*>(c.y);
+    const int32_t* vl = c.valid_len;
+    void* args[] = {(void*)&xp, (void*)&yp, (void*)&a, (void*)&vl};
+    note_launch();
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3((unsigned)grid),
+                                    dim3((unsigned)p.threads), args, (size_t)smem, c.stream);
+  }
+  const cudaError_t f = cudaFreeAsync(base, c.stream);
+  return e != cudaSuccess ? e : f;
+}
+
+// Resident CTAs per SM of the one-launch long-row kernel (the fp32-output
+// softmax stands for the family).
+template <typename InT>
+int split_fused_occupancy(int threads) {
+  constexpr int SV = 16 / Elem<InT>::V;
+  auto kern = k_rows_split<InT, float, MODE_SOFTMAX, SV, 2>;
+  const int64_t smem = 2LL * SV * threads * 16;
+  int n = 0;
+  if (smem_raise(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  // every output type must fit as many
+  auto kb = k_rows_split<InT, __nv_bfloat16, MODE_CE, SV, 2>;
+  int n2 = 0;
+  if (smem_raise(reinterpret_cast<const void*>(kb), smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n2, kb, threads, (size_t)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  auto kc = k_rows_split<InT, float, MODE_CE, SV, 2>;
+  int n3 = 0;
+  if (smem_raise(reinterpret_cast<const void*>(kc), smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n3, kc, threads, (size_t)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  n = n2 < n ? n2 : n;
+  return n3 < n ? n3 : n;
+}
+
 // Long rows in chunks of 16 elements per thread.  Softmax and log_softmax, in
 // slabs of rows: the streamed kernel computes every chunk's summary, then
 // normalises every chunk with its row's merged (M, D); row statistics (or LSE)
@@ -185,6 +292,13 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
     return launch_stream_k<InT, OutT, MODE_APPLY, SV, 2, true>(c, p, it, nullptr, nullptr, c.m_in,
                                                                c.d_in);
   } else {
+    // softmax, log_softmax and the cross-entropy with its gradient: one
+    // persistent cooperative launch (kernel_split_fused.cuh) unless switched
+    // off or the scratch is fixed
+    if constexpr (MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE) {
+      if (p.fused_split && p.scratch == nullptr && (MODE != MODE_CE || c.y != nullptr))
+        return launch_split_fused<InT, OutT, MODE>(c, p);
+    }
     // the statistics-only calls (row statistics, LSE, the loss alone) read
     // every element once: one slab of all rows
     const bool read_once = (MODE == MODE_STATS || (MODE == MODE_CE && c.y == nullptr)) &&
@@ -195,7 +309,7 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
     char* base = reinterpret_cast<char*>(p.scratch);
     cudaError_t e = cudaSuccess;
     if (base == nullptr) {
-      e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, c.stream);
+      e = scratch_alloc(c, reinterpret_cast<void**>(&base), bytes);
       if (e != cudaSuccess) return e;
     }
     float* pm = reinterpret_cast<float*>(base);
@@ -255,16 +369,12 @@ cudaError_t launch_bwd_k(const Call& c, const Plan& p, const Items& it, float* p
                          const float* part_in) {
   auto kern = k_backward<InT, OutT, VPT, MODE, 2>;
   const int64_t smem = 2 * stream_smem_bytes(2, VPT, p.threads);
-  static int64_t set_bytes[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (set_bytes[dev] < smem) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    set_bytes[dev] = smem;
-  }
+  e = smem_raise(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   const int64_t grid = it.n < p.ctas ? it.n : p.ctas;
   note_launch();
   kern<<<(unsigned)grid, p.threads, (size_t)smem, c.stream>>>(
@@ -307,7 +417,7 @@ cudaError_t launch_backward(const Call& c, const Plan& p) {
   char* base = reinterpret_cast<char*>(p.scratch);
   cudaError_t e = cudaSuccess;
   if (base == nullptr) {
-    e = cudaMallocAsync(reinterpret_cast<void**>(&base), bytes, c.stream);
+    e = scratch_alloc(c, reinterpret_cast<void**>(&base), bytes);
     if (e != cudaSuccess) return e;
   }
   float* part = reinterpret_cast<float*>(base);
@@ -330,8 +440,7 @@ int backward_occupancy(int vpt, int threads) {
   auto query = [&](auto kern, int v) -> int {
     const int64_t smem = 2 * stream_smem_bytes(2, v, threads);
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
+    if (smem_raise(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -434,8 +543,7 @@ int stream_occupancy_mode(int vpt, int threads, int depth, bool warp) {
   const int64_t smem = stream_smem_bytes(depth, vpt, threads);
   auto query = [&](auto kern) -> int {
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
+    if (smem_raise(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -505,8 +613,7 @@ int split_occupancy(int threads) {
   const int64_t smem = stream_smem_bytes(2, SV, threads);
   auto query = [&](auto kern) -> int {
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
+    if (smem_raise(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, (size_t)smem) != cudaSuccess) {
       cudaGetLastError();
       return 0;

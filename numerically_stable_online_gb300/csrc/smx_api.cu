@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "../../include/smx.h"
 #include "kernel_generic.cuh"
@@ -22,6 +23,7 @@ thread_local int t_kernel_launches = 0;
 namespace {
 
 constexpr int MAX_DEVICES = 64;
+constexpr uint64_t SCRATCH_POOL_KEEP_BYTES = 64ull << 20;  // scratch memory kept between calls
 constexpr int64_t DEFAULT_MAX_POLLS = int64_t(1) << 21;
 // shared memory kept back from the cluster kernel's staging area for its
 // static arrays (barriers, per-warp partials, the CTA summary)
@@ -34,7 +36,9 @@ struct DeviceInfo {
   int64_t smem_optin = 0;
   int64_t l2_bytes = 0;
   int* status = nullptr;   // device status word
+  cudaMemPool_t pool = nullptr;  // the long-row paths' scratch (keeps its memory between calls)
   int max_cluster[3] = {0, 0, 0};  // per input type, 0 = not queried yet
+  bool coop = false;                // cooperative launches supported
 };
 
 DeviceInfo g_dev[MAX_DEVICES];
@@ -53,7 +57,8 @@ std::atomic<int> g_cluster_stage{0};  // 0 automatic, 1 bulk copies, 2 cp.async
 std::atomic<int64_t> g_split_slab_bytes{0};
 std::atomic<int> g_split_hint_stats{-1}, g_split_hint_apply{-1};
 std::atomic<int64_t> g_bwd_inflight{48 * 1024};  // backward: reads in flight per SM
-std::atomic<int> g_stream_warp{0};  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
+std::atomic<int> g_stream_warp{0};
+std::atomic<int> g_split_fused{0};  // 0: long rows in one cooperative launch; 1: two launches per slab  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
 thread_local int t_last_cuda_error = 0;
@@ -95,11 +100,30 @@ smx_status device_info(DeviceInfo** out) {
       d.sm_count = sms;
       d.smem_optin = optin;
       d.l2_bytes = l2;
+      int coop = 0;
+      if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
+        return cuda_fail(e, SMX_ERR_DEVICE);
+      d.coop = coop != 0;
       if (d.supported) {
         int* s = nullptr;
         if ((e = cudaMalloc(&s, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
         if ((e = cudaMemset(s, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
         d.status = s;
+        // a pool of the library's own, so that the per-call scratch of the
+        // long-row paths reuses memory instead of mapping it anew after every
+        // synchronisation (the default pool returns its memory then)
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+        uint64_t keep = SCRATCH_POOL_KEEP_BYTES;
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+          return cuda_fail(e, SMX_ERR_DEVICE);
+        d.pool = pool;
       }
       d.ready = true;
     }
@@ -109,12 +133,43 @@ smx_status device_info(DeviceInfo** out) {
   return SMX_OK;
 }
 
-int cluster_capacity(int in_dtype, int cluster, int64_t smem_bytes) {
-  switch (in_dtype) {
-    case SMX_F32: return cluster_capacity_f32(cluster, smem_bytes);
-    case SMX_F16: return cluster_capacity_f16(cluster, smem_bytes);
-    default: return cluster_capacity_bf16(cluster, smem_bytes);
+// Residency answers (occupancy queries) are properties of the device and the
+// kernel's shape, so each is asked of the runtime once and kept: a query costs
+// microseconds of host time, more than a short call's kernel.
+std::mutex g_occ_mutex;
+std::unordered_map<uint64_t, int> g_occ_cache;
+
+template <typename F>
+int cached_query(uint64_t key, F&& query) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return query();
+  key = key * 64 + (uint64_t)(dev & 63);
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    const auto it = g_occ_cache.find(key);
+    if (it != g_occ_cache.end()) return it->second;
   }
+  const int v = query();
+  if (v > 0) {  // failures are not kept
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    g_occ_cache[key] = v;
+  }
+  return v;
+}
+
+// key fields: kind (4 bits), input type (2), then the query's own numbers
+uint64_t occ_key(int kind, int in_dtype, uint64_t a, uint64_t b = 0, uint64_t c = 0, uint64_t d = 0) {
+  return ((((((uint64_t)kind * 4 + (uint64_t)in_dtype) * 65536 + a) * 65536 + b) * 64 + c) * 16) + d;
+}
+
+int cluster_capacity(int in_dtype, int cluster, int64_t smem_bytes) {
+  return cached_query(occ_key(1, in_dtype, (uint64_t)cluster, (uint64_t)(smem_bytes / 16)), [&] {
+    switch (in_dtype) {
+      case SMX_F32: return cluster_capacity_f32(cluster, smem_bytes);
+      case SMX_F16: return cluster_capacity_f16(cluster, smem_bytes);
+      default: return cluster_capacity_bf16(cluster, smem_bytes);
+    }
+  });
 }
 
 int64_t cluster_smem_cap_bytes(const DeviceInfo& d) {
@@ -183,11 +238,15 @@ bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
 }
 
 int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode, bool warp) {
-  switch (in_dtype) {
-    case SMX_F32: return stream_occupancy_f32(vpt, threads, depth, mode, warp);
-    case SMX_F16: return stream_occupancy_f16(vpt, threads, depth, mode, warp);
-    default: return stream_occupancy_bf16(vpt, threads, depth, mode, warp);
-  }
+  return cached_query(occ_key(2, in_dtype, (uint64_t)vpt, (uint64_t)threads, (uint64_t)depth * 8 + mode,
+                              warp ? 1 : 0),
+                      [&] {
+                        switch (in_dtype) {
+                          case SMX_F32: return stream_occupancy_f32(vpt, threads, depth, mode, warp);
+                          case SMX_F16: return stream_occupancy_f16(vpt, threads, depth, mode, warp);
+                          default: return stream_occupancy_bf16(vpt, threads, depth, mode, warp);
+                        }
+                      });
 }
 
 // Streamed path for rows of at most 32 KiB: the CTA shape of the register path
@@ -197,6 +256,7 @@ int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode, bo
 // more only contend; with lengths given, rows are taken as half valid).
 constexpr int64_t STREAM_INFLIGHT_BYTES = 48 * 1024;
 constexpr int64_t CE_INFLIGHT_BYTES = 64 * 1024;
+constexpr int64_t CLUSTER_MAX_ROW_BYTES = 4 << 20;
 
 bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
                  bool has_lengths, int mode, int64_t inflight, Plan* p) {
@@ -264,12 +324,13 @@ bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
   int64_t slab = slab_bytes / (cols * es);
   if (slab < 1) slab = 1;
   if (slab * nchunks > ((int64_t)1 << 31)) slab = ((int64_t)1 << 31) / nchunks;
-  int occ_max = 0;
-  switch (in_dtype) {
-    case SMX_F32: occ_max = split_occupancy_f32(threads); break;
-    case SMX_F16: occ_max = split_occupancy_f16(threads); break;
-    default: occ_max = split_occupancy_bf16(threads); break;
-  }
+  const int occ_max = cached_query(occ_key(3, in_dtype, (uint64_t)threads), [&] {
+    switch (in_dtype) {
+      case SMX_F32: return split_occupancy_f32(threads);
+      case SMX_F16: return split_occupancy_f16(threads);
+      default: return split_occupancy_bf16(threads);
+    }
+  });
   if (occ_max <= 0) return false;
   int occ = occ_max;
   const int forced = g_stream_ctas_per_sm.load();
@@ -282,6 +343,22 @@ bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
   p->chunk = chunk;
   p->nchunks = (int)nchunks;
   p->slab_rows = slab;
+  // one cooperative launch when the device supports it: every CTA resident
+  if (g_split_fused.load() == 0 && d.coop) {
+    const int fo = cached_query(occ_key(4, in_dtype, (uint64_t)threads), [&] {
+      switch (in_dtype) {
+        case SMX_F32: return split_fused_occupancy_f32(threads);
+        case SMX_F16: return split_fused_occupancy_f16(threads);
+        default: return split_fused_occupancy_bf16(threads);
+      }
+    });
+    if (fo > 0) {
+      int fc = fo;
+      if (forced > 0) fc = forced < fo ? forced : fo;
+      p->fused_split = true;
+      p->fused_ctas = fc * d.sm_count;
+    }
+  }
   const int hs = g_split_hint_stats.load(), ha = g_split_hint_apply.load();
   p->l2_hint_stats = hs >= 0 ? hs : 1;  // the statistics pass's reads stay for the re-read
   p->l2_hint_apply = ha >= 0 ? ha : 2;  // the normalising pass's reads are the last
@@ -315,11 +392,13 @@ bool plan_cluster(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan*
 }
 
 int backward_occupancy(int in_dtype, int vpt, int threads) {
-  switch (in_dtype) {
-    case SMX_F32: return backward_occupancy_f32(vpt, threads);
-    case SMX_F16: return backward_occupancy_f16(vpt, threads);
-    default: return backward_occupancy_bf16(vpt, threads);
-  }
+  return cached_query(occ_key(5, in_dtype, (uint64_t)vpt, (uint64_t)threads), [&] {
+    switch (in_dtype) {
+      case SMX_F32: return backward_occupancy_f32(vpt, threads);
+      case SMX_F16: return backward_occupancy_f16(vpt, threads);
+      default: return backward_occupancy_bf16(vpt, threads);
+    }
+  });
 }
 
 // Softmax backward: rows of up to 16 KiB per CTA (at most 16 elements per
@@ -394,6 +473,7 @@ smx_status run_backward(Call& c, DeviceInfo& dev) {
                       (reinterpret_cast<uintptr_t>(c.y) % 16 == 0) && ((c.cols * es) % 16 == 0);
   Plan p;
   plan_backward(dev, c, vec_ok, &p);
+  c.pool = dev.pool;
   cudaError_t e;
   switch (c.in_dtype) {
     case SMX_F32: e = launch_in_f32(c, p); break;
@@ -439,9 +519,11 @@ smx_status run(Call& c, DeviceInfo& dev) {
       }
       if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       // rows longer than one CTA holds: a row per thread-block cluster when the
-      // rows fill every resident cluster, else (a few very long rows) L2 slabs,
-      // which spread every row over all SMs
-      if (!planned && classic) {
+      // rows fill every resident cluster and are shorter than 4 MiB, else
+      // chunks (path 5), which spread every row over all SMs (measured on
+      // GB300: from 4 MiB rows on, the cluster's on-chip copy no longer holds
+      // the row and the chunked path is faster)
+      if (!planned && classic && c.cols * es_in < CLUSTER_MAX_ROW_BYTES) {
         planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
         if (planned && c.rows < p.resident_clusters) planned = false;
       }
@@ -451,6 +533,7 @@ smx_status run(Call& c, DeviceInfo& dev) {
   }
   if (!planned) p.path = PATH_GENERIC;
   c.status = dev.status;
+  c.pool = dev.pool;
   const int64_t wl = g_wait_limit.load();
   c.max_polls = wl != 0 ? wl : DEFAULT_MAX_POLLS;
   cudaError_t e;
@@ -820,6 +903,8 @@ void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes) {
 }
 
 void smx_debug_set_stream_warp(int off) { g_stream_warp.store(off ? 1 : 0); }
+
+void smx_debug_set_split_fused(int off) { g_split_fused.store(off ? 1 : 0); }
 
 void smx_debug_set_split_hints(int stats, int apply) {
   g_split_hint_stats.store(stats >= 0 && stats <= 2 ? stats : -1);

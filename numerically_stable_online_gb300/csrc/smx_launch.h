@@ -28,7 +28,14 @@ struct Call {
   const void* g = nullptr;      // backward: the upstream gradient (x is the forward output p)
   const int64_t* target = nullptr;  // cross-entropy: target index per row
   float* loss = nullptr;            // cross-entropy: loss per row
+  cudaMemPool_t pool = nullptr;     // where the per-call scratch comes from (null: the default pool)
 };
+
+// Stream-ordered scratch of a call: from the library's pool when it has one.
+inline cudaError_t scratch_alloc(const Call& c, void** p, size_t bytes) {
+  return c.pool != nullptr ? cudaMallocFromPoolAsync(p, bytes, c.pool, c.stream)
+                           : cudaMallocAsync(p, bytes, c.stream);
+}
 
 // Call::mode of the softmax backward (past the kernels' MODE_* values).
 constexpr int CALL_BACKWARD = 8;
@@ -48,6 +55,8 @@ struct Plan {
   bool stage_tma = true;   // stage with bulk copies (TMA) or per-thread cp.async
   // split rows: slabs of slab_rows rows, chunks of `chunk` elements
   int64_t slab_rows = 0;
+  bool fused_split = false;  // long rows in one cooperative launch of fused_ctas (all resident)
+  int fused_ctas = 0;
   int l2_hint_stats = 0;  // L2 policies of the two passes' reads (Items::l2_hint)
   int l2_hint_apply = 0;
   int resident_clusters = 0;
@@ -81,6 +90,9 @@ int stream_occupancy_bf16(int vpt, int threads, int depth, int mode, bool warp);
 int split_occupancy_f32(int threads);
 int split_occupancy_f16(int threads);
 int split_occupancy_bf16(int threads);
+int split_fused_occupancy_f32(int threads);
+int split_fused_occupancy_f16(int threads);
+int split_fused_occupancy_bf16(int threads);
 // ... of the backward kernels: whole rows (vpt, threads) or chunks (vpt = 0).
 int backward_occupancy_f32(int vpt, int threads);
 int backward_occupancy_f16(int vpt, int threads);

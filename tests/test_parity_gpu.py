@@ -54,6 +54,7 @@ def lib(built):
     built.smx_debug_set_split_hints(-1, -1)
     built.smx_debug_set_stream_ctas(0)
     built.smx_debug_set_stream_warp(0)
+    built.smx_debug_set_split_fused(0)
 
 
 DEV = "cuda:0"
@@ -506,3 +507,28 @@ def test_stream_walkers(lib, cols, in_dtype, out_dtype, warp_off):
     m, d = gpu_stats(x, in_dtype, rows, cols, vl)
     m_ref, d_ref = oracle.row_stats(x, in_dtype, rows, cols, vl)
     check_stats(m, d, m_ref, d_ref)
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype,rows,cols,slab", [
+    ("f32", "f32", 7, 300_000, 2 << 20), ("bf16", "bf16", 9, 150_000, 1 << 20),
+    ("f16", "f32", 5, 40_000, 64 << 10), ("bf16", "f16", 33, 12_288, 96 << 10)])
+@pytest.mark.parametrize("fused_off", [0, 1])
+def test_long_rows_one_launch_and_two(lib, in_dtype, out_dtype, rows, cols, slab, fused_off):
+    """Path 5 as one cooperative launch over all slabs (per-row completion
+    counts) and as two launches per slab, with small slabs so that many slabs
+    and chunk ranges that straddle rows occur; lengths include 0 and 1."""
+    rng = np.random.default_rng(cols + rows)
+    x = stored(rng.normal(0, 5, rows * cols), in_dtype)
+    vl = rng.integers(0, cols + 1, size=rows).astype(np.int32)
+    vl[0], vl[1] = 0, 1
+    vl[-1] = cols
+    lib.smx_debug_force_path(PATH_SPLIT)
+    lib.smx_debug_set_split_slab(slab)
+    lib.smx_debug_set_split_fused(fused_off)
+    xt = to_device(x, in_dtype, rows, cols)
+    smx.softmax_rows(xt, valid_len=torch.from_numpy(vl).to(DEV), out_dtype=DT[out_dtype])
+    slab_rows = max(1, slab // (cols * (4 if in_dtype == "f32" else 2)))
+    assert lib.smx_debug_last_path() == PATH_SPLIT
+    assert lib.smx_debug_last_launches() == (1 if not fused_off else 2 * -(-rows // slab_rows))
+    assert smx.last_device_status() == 0
+    run_and_compare(x, in_dtype, out_dtype, rows, cols, vl)
