@@ -72,6 +72,8 @@ def _load():
         lib.orc_apply_stats.argtypes = [P, I32, I64, P, P, P, P, I64, P]
         lib.orc_softmax_backward.argtypes = [P, P, I32, I64, P, P, I64, P]
         lib.orc_cross_entropy.argtypes = [P, I32, I64, P, P, P, I64, P, P]
+        lib.orc_attention_rows.argtypes = [P, P, P, I32, I64, I64, I64, D, I32, P, I64, P, P, P, P]
+        lib.orc_attention_online.argtypes = [P, P, I64, I64, I64, I32, P, P, P]
         _lib = lib
         return lib
 
@@ -285,3 +287,41 @@ def cross_entropy(x, dtype, rows: int, cols: int, target, valid_len=None, rows_s
     lib.orc_cross_entropy(_ptr(a), code, cols, _ptr(vl), _ptr(t), _ptr(sel), n_sel, _ptr(loss),
                           _ptr(grad))
     return loss, grad
+
+
+def attention_rows(q, k, v, dtype, heads: int, sq: int, sk: int, d: int, scale: float,
+                   causal: bool = False, rows_sel=None):
+    """fp64 attention of the selected (head, row) pairs, index head * sq + row.
+
+    q: [heads, sq, d], k and v: [heads, sk, d] stored values of one type.
+    Returns (o [n, d], lse [n], oabs [n, d] = sum p |v|, smax [n] = max scale |q|.|k|).
+    """
+    lib = _load()
+    a, code = _as_storage(q, dtype)
+    b, _ = _as_storage(k, dtype)
+    c, _ = _as_storage(v, dtype)
+    if a.size != heads * sq * d or b.size != heads * sk * d or c.size != heads * sk * d:
+        raise ValueError("q, k, v have the wrong number of elements")
+    sel = None if rows_sel is None else np.ascontiguousarray(rows_sel, dtype=np.int64)
+    n = heads * sq if sel is None else sel.size
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    oabs = np.empty((n, d), dtype=np.float64)
+    smax = np.empty(n, dtype=np.float64)
+    lib.orc_attention_rows(_ptr(a), _ptr(b), _ptr(c), code, sq, sk, d, float(scale), 1 if causal else 0,
+                           _ptr(sel), n, _ptr(o), _ptr(lse), _ptr(oabs), _ptr(smax))
+    return o, lse, oabs, smax
+
+
+def attention_online(s, v, block: int, rescale_o: bool = True):
+    """The pages' (m, l, o) running state over blocks of scores s [n] and values v [n, d]."""
+    lib = _load()
+    sv = np.ascontiguousarray(s, dtype=np.float64)
+    vv = np.ascontiguousarray(v, dtype=np.float64)
+    n, d = vv.shape
+    o = np.empty(d)
+    m = np.empty(1)
+    l = np.empty(1)
+    lib.orc_attention_online(_ptr(sv), _ptr(vv), n, d, block, 1 if rescale_o else 0, _ptr(o), _ptr(m),
+                             _ptr(l))
+    return o, float(m[0]), float(l[0])

@@ -47,6 +47,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 
 enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
@@ -428,4 +429,110 @@ void orc_cross_entropy(const void *x, int dtype, int64_t cols, const int32_t *va
             for (int64_t j = 0; j < L; ++j)
                 gr[j] = exp(load_elem(x, dtype, base + j) - m) / d - (j == t ? 1.0 : 0.0);
     }
+}
+
+/* ---------------------------------------------------------------------------
+ * Attention with the weighted value numerator ("Online stable softmax",
+ * "Carry a weighted value numerator for attention" and "Reference summary";
+ * "Softmax numerics architecture...", "From online softmax to tiled
+ * attention").  For query row i of head h, with scores s_j = scale * q_i . k_j
+ * over the valid keys j (all Sk keys, or with the causal mask j <= i + Sk - Sq),
+ *   m = max s_j,  l = sum exp(s_j - m),  o = sum exp(s_j - m) v_j / l,
+ *   LSE = m + log l.
+ * A row with no valid key is the declared empty row: o = 0, LSE = -inf.
+ * q is [BH][Sq][D], k and v are [BH][Sk][D], all in `dtype`.  `sel` lists
+ * n_sel (head, row) pairs as head * Sq + row (NULL: every row in order).
+ * oabs receives sum p_j |v_j| per output element (the scale of the output's
+ * rounding errors), smax the largest |s_j| computed from |q| . |k| (the scale of
+ * the scores' rounding errors); either may be NULL.
+ * ------------------------------------------------------------------------- */
+void orc_attention_rows(const void *q, const void *k, const void *v, int dtype, int64_t Sq,
+                        int64_t Sk, int64_t D, double scale, int causal, const int64_t *sel,
+                        int64_t n_sel, double *o, double *lse, double *oabs, double *smax)
+{
+    double *s = (double *)malloc((size_t)(Sk > 0 ? Sk : 1) * sizeof(double));
+    for (int64_t n = 0; n < n_sel; ++n) {
+        int64_t idx = sel ? sel[n] : n;
+        int64_t h = idx / Sq, i = idx % Sq;
+        int64_t nk = Sk;
+        if (causal) {
+            nk = i + Sk - Sq + 1;
+            if (nk < 0) nk = 0;
+            if (nk > Sk) nk = Sk;
+        }
+        const int64_t qb = (h * Sq + i) * D, kb = h * Sk * D;
+        double m = -INFINITY, amax = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t d = 0; d < D; ++d) {
+                double qd = load_elem(q, dtype, qb + d), kd = load_elem(k, dtype, kb + j * D + d);
+                acc += qd * kd;
+                aabs += fabs(qd) * fabs(kd);
+            }
+            s[j] = scale * acc;
+            if (s[j] > m) m = s[j];
+            if (fabs(scale) * aabs > amax) amax = fabs(scale) * aabs;
+        }
+        if (smax) smax[n] = amax;
+        for (int64_t d = 0; d < D; ++d) {
+            o[n * D + d] = 0.0;
+            if (oabs) oabs[n * D + d] = 0.0;
+        }
+        if (nk == 0 || m == -INFINITY || isnan(m)) {
+            lse[n] = nk == 0 || m == -INFINITY ? -INFINITY : NAN;
+            if (nk > 0 && isnan(m))
+                for (int64_t d = 0; d < D; ++d) o[n * D + d] = NAN;
+            continue;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nk; ++j) l += exp(s[j] - m);
+        for (int64_t j = 0; j < nk; ++j) {
+            double p = exp(s[j] - m) / l;
+            for (int64_t d = 0; d < D; ++d) {
+                double vd = load_elem(v, dtype, kb + j * D + d);
+                o[n * D + d] += p * vd;
+                if (oabs) oabs[n * D + d] += p * fabs(vd);
+            }
+        }
+        lse[n] = m + log(l);
+    }
+    free(s);
+}
+
+/* The running state (m, l, o) over blocks of B scores, as the pages state it
+ * ("Reference summary"): from (-inf, 0, 0), each block with its own maximum
+ * m2, sum l2 = sum exp(s - m2) and numerator o2 = sum exp(s - m2) v merges as
+ *   m' = max(m, m2),  l' = exp(m - m') l + exp(m2 - m') l2,
+ *   o' = exp(m - m') o + exp(m2 - m') o2,
+ * and o / l at the end.  rescale_o == 0 is the pages' named error: the sum is
+ * rescaled but the numerator is not.  s: n scores; v: [n][D] doubles. */
+void orc_attention_online(const double *s, const double *v, int64_t n, int64_t D, int64_t B,
+                          int rescale_o, double *o_out, double *m_out, double *l_out)
+{
+    double m = -INFINITY, l = 0.0;
+    double *o = (double *)calloc((size_t)D, sizeof(double));
+    double *o2 = (double *)calloc((size_t)D, sizeof(double));
+    for (int64_t b0 = 0; b0 < n; b0 += B) {
+        int64_t b1 = b0 + B < n ? b0 + B : n;
+        double m2 = -INFINITY;
+        for (int64_t j = b0; j < b1; ++j) if (s[j] > m2) m2 = s[j];
+        double l2 = 0.0;
+        for (int64_t d = 0; d < D; ++d) o2[d] = 0.0;
+        for (int64_t j = b0; j < b1; ++j) {
+            double e = exp(s[j] - m2);
+            l2 += e;
+            for (int64_t d = 0; d < D; ++d) o2[d] += e * v[j * D + d];
+        }
+        double mn = m > m2 ? m : m2;
+        double fa = m == -INFINITY ? 0.0 : exp(m - mn);  /* the empty prefix: selected, not evaluated */
+        double fb = exp(m2 - mn);
+        l = fa * l + fb * l2;
+        for (int64_t d = 0; d < D; ++d) o[d] = (rescale_o ? fa : 1.0) * o[d] + fb * o2[d];
+        m = mn;
+    }
+    for (int64_t d = 0; d < D; ++d) o_out[d] = l > 0 ? o[d] / l : 0.0;
+    *m_out = m;
+    *l_out = l;
+    free(o);
+    free(o2);
 }
