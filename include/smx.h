@@ -223,6 +223,32 @@ smx_status smx_cross_entropy(const void *x, const int64_t *target, float *loss, 
                              smx_dtype grad_dtype, smx_stream_t stream);
 
 /*
+ * Attention forward with the online weighted numerator ("Online stable
+ * softmax", "Carry a weighted value numerator for attention" and "Reference
+ * summary"; "Softmax numerics architecture...", "From online softmax to tiled
+ * attention"): for each head h and query row i, with s_j = scale q_i . k_j over
+ * the valid keys,
+ *     o_i = sum_j e^(s_j - m) v_j / l,   l = sum_j e^(s_j - m),   m = max s_j,
+ *     lse_i = m + log l,
+ * computed block by block with the running state (m, l, o) so that the score
+ * matrix never leaves the chip.  Scores, m, l and o are fp32; the probabilities
+ * enter the second product rounded to the input type.
+ *   q        device [heads][seq_q][head_dim], dtype; k, v: [heads][seq_k][head_dim].
+ *            (heads = batch x heads, each head contiguous.)  16-byte aligned.
+ *   o        device, like q, written.  Must not overlap q, k, v or lse.
+ *   lse      device float[heads][seq_q], written; or NULL.
+ *   head_dim 64 or 128 (else SMX_ERR_UNSUPPORTED); heads <= 65535.
+ *   scale    > 0, e.g. 1/sqrt(head_dim).
+ *   causal   0: every key; 1: key j is valid for query i when
+ *            j <= i + seq_k - seq_q (bottom-right aligned).  A row with no
+ *            valid key is the declared empty row: o = 0, lse = -inf.
+ *   dtype    SMX_F16 or SMX_BF16 (the tensor-core input types).
+ */
+smx_status smx_attention_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 int64_t heads, int64_t seq_q, int64_t seq_k, int head_dim,
+                                 double scale, int causal, smx_dtype dtype, smx_stream_t stream);
+
+/*
  * Element-wise merge of two arrays of block summaries ("Online stable softmax",
  * "Derive the update for two blocks"):
  *   m' = max(m_a, m_b),  d' = d_a exp(m_a - m') + d_b exp(m_b - m').

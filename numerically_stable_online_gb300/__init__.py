@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "SmxError", "library", "softmax_rows", "softmax_rows_fixed_scratch", "softmax_row_stats",
     "softmax_merge_stats", "log_softmax_rows", "softmax_lse", "softmax_apply_stats",
-    "softmax_backward", "cross_entropy",
+    "softmax_backward", "cross_entropy", "attention_forward",
     "last_device_status", "status_string", "DTYPES",
 ]
 
@@ -73,6 +73,8 @@ def library() -> ctypes.CDLL:
         lib.smx_softmax_backward.restype = st
         lib.smx_cross_entropy.argtypes = [P, P, P, P, I64, I64, P, I32, I32, P]
         lib.smx_cross_entropy.restype = st
+        lib.smx_attention_forward.argtypes = [P, P, P, P, P, I64, I64, I64, I32, ctypes.c_double, I32, I32, P]
+        lib.smx_attention_forward.restype = st
         lib.smx_last_device_status.argtypes = [P]
         lib.smx_last_device_status.restype = st
         lib.smx_status_string.argtypes = [st]
@@ -332,6 +334,34 @@ def cross_entropy(x: torch.Tensor, target: torch.Tensor, valid_len: torch.Tensor
     if st != 0:
         raise SmxError(st, "smx_cross_entropy")
     return loss, grad
+
+
+def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                      causal: bool = False, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      with_lse: bool = True, stream=None):
+    """(o, lse) of attention over [..., seq, head_dim] fp16/bf16 tensors (leading dims = heads)."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() < 2:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [..., seq, head_dim]")
+    if k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+        raise ValueError("q, k, v shapes do not match")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    d = q.shape[-1]
+    heads = int(q.numel() // (q.shape[-2] * d)) if q.numel() else 0
+    sq, sk = q.shape[-2], k.shape[-2]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if with_lse and lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    st = library().smx_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         None if lse is None else lse.data_ptr(), heads, sq, sk, d,
+                                         float(scale), 1 if causal else 0, _dtype(q.dtype), _stream(stream))
+    if st != 0:
+        raise SmxError(st, "smx_attention_forward")
+    return out, lse
 
 
 def last_device_status(stream=None) -> int:

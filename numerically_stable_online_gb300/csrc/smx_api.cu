@@ -822,6 +822,37 @@ smx_status smx_cross_entropy(const void* x, const int64_t* target, float* loss, 
   return run(c, *dev);
 }
 
+smx_status smx_attention_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int64_t heads, int64_t seq_q, int64_t seq_k, int head_dim,
+                                 double scale, int causal, smx_dtype dtype, smx_stream_t stream) {
+  t_kernel_launches = 0;
+  if (heads < 0 || seq_q < 0 || seq_k < 0 || (dtype != SMX_F16 && dtype != SMX_BF16) ||
+      !(scale > 0.0) || !(scale < 1e30))
+    return SMX_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return SMX_ERR_UNSUPPORTED;
+  if (heads > 65535) return SMX_ERR_UNSUPPORTED;
+  if (heads > 0 && (seq_q > INT64_MAX / 4 / heads / head_dim || seq_k > INT64_MAX / 4 / heads / head_dim))
+    return SMX_ERR_INVALID_ARG;
+  if (heads == 0 || seq_q == 0) return SMX_OK;
+  if (q == nullptr || o == nullptr || (seq_k > 0 && (k == nullptr || v == nullptr)))
+    return SMX_ERR_INVALID_ARG;
+  const auto misaligned = [](const void* p) { return p != nullptr && reinterpret_cast<uintptr_t>(p) % 16 != 0; };
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o)) return SMX_ERR_INVALID_ARG;
+  const int64_t nq = heads * seq_q * head_dim * 2, nk = heads * seq_k * head_dim * 2;
+  if (overlaps(o, nq, q, nq) || overlaps(o, nq, k, nk) || overlaps(o, nq, v, nk) ||
+      (lse && (overlaps(lse, heads * seq_q * 4, o, nq) || overlaps(lse, heads * seq_q * 4, q, nq) ||
+               overlaps(lse, heads * seq_q * 4, k, nk) || overlaps(lse, heads * seq_q * 4, v, nk))))
+    return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  AttnCall c{q, k, v, o, lse, heads, seq_q, seq_k, head_dim, scale, causal ? 1 : 0, (int)dtype,
+             reinterpret_cast<cudaStream_t>(stream)};
+  const cudaError_t e = launch_attention(c);
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
+  return SMX_OK;
+}
+
 smx_status smx_softmax_merge_stats(const float* m_a, const float* d_a, const float* m_b,
                                    const float* d_b, float* m_out, float* d_out, int64_t n,
                                    smx_stream_t stream) {

@@ -72,6 +72,21 @@ constexpr int CLUSTER_THREADS = 1024;
 extern thread_local int t_kernel_launches;
 inline void note_launch() { ++t_kernel_launches; }
 
+// Attention forward (inst_attention.cu): q [heads][sq][d], k, v [heads][sk][d],
+// o like q, lse [heads][sq] fp32 or null; d 64 or 128; dtype fp16 (1) or bf16 (2).
+struct AttnCall {
+  const void *q, *k, *v;
+  void* o;
+  float* lse;
+  int64_t heads, sq, sk;
+  int d;
+  double scale;
+  int causal;
+  int dtype;
+  cudaStream_t stream;
+};
+cudaError_t launch_attention(const AttnCall& c);
+
 // Launch the planned kernel(s) for one input type; returns the first CUDA error.
 cudaError_t launch_in_f32(const Call& c, const Plan& p);
 cudaError_t launch_in_f16(const Call& c, const Plan& p);
