@@ -50,7 +50,8 @@ PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4, "split":
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_regs.cuh",
                   "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
-                  "kernel_backward.cuh", "launch_impl.cuh", "smx_api.cu"]
+                  "kernel_backward.cuh", "kernel_split_fused.cuh", "launch_impl.cuh", "smx_api.cu"]
+ATTN_SOURCES = ["smx_device.cuh", "kernel_attention.cuh", "inst_attention.cu", "smx_api.cu"]
 
 
 def metric_of(op: str) -> str:
@@ -94,9 +95,9 @@ def rotation_sets(bytes_per_set: int, l2_bytes: int = L2_BYTES) -> int:
     return max(2, min(16, -(-3 * l2_bytes // max(1, bytes_per_set)) + 1))
 
 
-def source_hash() -> str:
+def source_hash(files=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in files or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "numerically_stable_online_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -112,17 +113,18 @@ def profile_traffic(workload: str, op: str = "softmax"):
     mh = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     mt = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     mk = re.search(r"kernel:\s*(\S+)", text)
-    if not mh or not mt or mh.group(1) != source_hash():
+    if not mh or not mt or mh.group(1) != source_hash(ATTN_SOURCES if op == "attention" else None):
         return None, mk.group(1) if mk else None
     return int(mt.group(1)), mk.group(1) if mk else None
 
 
-def measured_peak():
+def measured_peak(kind: str = "hbm_gbs"):
+    """The measured peak (HBM copy GB/s, or bf16 TFLOP/s burst), else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as fh:
-            return float(json.load(fh)["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+            return float(json.load(fh)[kind]), "measured"
+    return (6800.0 if kind == "hbm_gbs" else 1900.0), "fallback"
 
 
 class ClockSampler:
@@ -550,13 +552,199 @@ def run_ours(args, w):
     return 0
 
 
+ATTN_METRIC = "attention forward TFLOP/s (4 heads sq sk d, halved when causal) on 1 GB300; % of bf16 tensor peak"
+
+
+def attention_oracle_sample(name, q, k, v, budget_s, min_rows=4):
+    """Time the fp64 reference attention on a bounded sample of rows of head 0."""
+    import oracle
+
+    heads, n, d, causal = wl.ATTN_WORKLOADS[name]
+    qs = wl.torch_to_storage(q[:1].cpu()).reshape(-1)
+    ks = wl.torch_to_storage(k[:1].cpu()).reshape(-1)
+    vs = wl.torch_to_storage(v[:1].cpu()).reshape(-1)
+    rows = np.arange(n - 4, n)  # the last rows see every key under either mask
+    t0 = time.perf_counter()
+    oracle.attention_rows(qs, ks, vs, "bf16", 1, n, n, d, d ** -0.5, causal, rows_sel=rows)
+    per_row = (time.perf_counter() - t0) / rows.size
+    m = int(max(min_rows, min(n, budget_s / max(per_row, 1e-9))))
+    rows = np.arange(n - m, n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qs, ks, vs, "bf16", 1, n, n, d, d ** -0.5, causal, rows_sel=rows)
+    dt = time.perf_counter() - t0
+    flops = sum(4.0 * ((r + 1) if causal else n) * d for r in rows)
+    return flops / dt / 1e12, m, dt
+
+
+def run_attention(args):
+    import torch
+
+    import numerically_stable_online_gb300 as smx
+    from numerically_stable_online_gb300 import build as smx_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        smx_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    lib = smx.library()
+    name = args.workload
+    heads, n, d, causal = wl.ATTN_WORKLOADS[name]
+    q, k, v = wl.attention_inputs(name, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(heads, n, dtype=torch.float32, device=dev)
+    flops = wl.attention_flops(heads, n, n, d, causal)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    code = smx.DTYPES[q.dtype]
+
+    def step():
+        st = lib.smx_attention_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       heads, n, n, d, d ** -0.5, 1 if causal else 0, code, sptr)
+        if st != 0:
+            raise smx.SmxError(st, "smx_attention_forward")
+
+    for _ in range(args.warmup):
+        step()
+    launches = lib.smx_debug_last_launches()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    value = flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    # end to end through the public call: q, k, v from pinned host memory, o and lse back
+    qp, kp, vp = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        smx.attention_forward(q, k, v, causal=causal, out=o, lse=lse)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    peak, peak_kind = measured_peak("bf16_tflops")
+    mean_launch_ms = statistics.fmean(launch_ms)
+    achieved = flops / (mean_launch_ms / 1e3) / 1e12
+    traffic, kernel_name = profile_traffic(name, "attention")
+    cpu_tf, cpu_rows, cpu_s = attention_oracle_sample(name, q, k, v, args.cpu_budget)
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "heads": heads, "seq": n, "head_dim": d, "causal": causal,
+                   "op": "attention", "l2": "inputs 3 x 128 MiB, larger than L2"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} cuBLAS bf16 GEMM throughput (burst)",
+                     "kernel": kernel_name or "k_attention<bf16,128> (mma.sync m16n8k16)",
+                     "flops_per_launch": flops, "mean_launch_us": mean_launch_ms * 1e3,
+                     "median_launch_us": statistics.median(launch_ms) * 1e3},
+        "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": f"last {cpu_rows} query rows of head 0, fp64 C reference, one thread, "
+                                   f"{cpu_s:.1f} s"},
+        "e2e": {"value": flops * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps * launches,
+        "kernels_per_step": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_attention_reference(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+
+    import oracle
+
+    oracle.build()
+    name = args.workload
+    heads, n, d, causal = wl.ATTN_WORKLOADS[name]
+    q, k, v = wl.attention_inputs(name, "cpu")
+    qs = wl.torch_to_storage(q[:1]).reshape(-1)
+    ks = wl.torch_to_storage(k[:1]).reshape(-1)
+    vs = wl.torch_to_storage(v[:1]).reshape(-1)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qs, ks, vs, "bf16", 1, n, n, d, d ** -0.5, causal, rows_sel=np.arange(n - 2, n))
+    per_row = (time.perf_counter() - t0) / 2
+    per_step = int(max(1, min(n, args.ref_budget / max(1, args.steps + args.warmup) / per_row)))
+    tot_flops = 0.0
+    for s_ in range(args.warmup):
+        oracle.attention_rows(qs, ks, vs, "bf16", 1, n, n, d, d ** -0.5, causal,
+                              rows_sel=np.arange(n - per_step, n))
+    t0 = time.perf_counter()
+    for s_ in range(args.steps):
+        rows = np.arange(n - per_step, n)
+        oracle.attention_rows(qs, ks, vs, "bf16", 1, n, n, d, d ** -0.5, causal, rows_sel=rows)
+        tot_flops += sum(4.0 * ((r + 1) if causal else n) * d for r in rows)
+    dt = time.perf_counter() - t0
+    value = tot_flops / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": name, "op": "attention"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} query rows of head 0 per step (fp64 C reference, one thread)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(wl.WORKLOADS) + sorted(wl.ATTN_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU reference work for cpu_baseline")
     ap.add_argument("--path", choices=sorted(PATHS), default="auto",
@@ -568,6 +756,16 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.op == "attention":
+        if args.workload is None:
+            args.workload = "attn_bf16_4x32x4096x128"
+        if args.workload not in wl.ATTN_WORKLOADS:
+            ap.error("--op attention takes an attention workload")
+        return run_attention_reference(args) if args.impl == "reference" else run_attention(args)
+    if args.workload is None:
+        args.workload = wl.BENCH_WORKLOAD
+    if args.workload not in wl.WORKLOADS:
+        ap.error("an attention workload needs --op attention")
     w = wl.WORKLOADS[args.workload]
     if w.name == "bf16_causal_8x32x4096x4096":
         ap.error("the causal batch is a parity case, not a benchmark workload")

@@ -150,7 +150,30 @@ def causal_valid_len(rows: int) -> np.ndarray:
     return (np.arange(rows) % CAUSAL_SLICE_ROWS + 1).astype(np.int32)
 
 
-OPS = ("softmax", "log_softmax", "lse", "apply_stats", "backward", "cross_entropy")
+OPS = ("softmax", "log_softmax", "lse", "apply_stats", "backward", "cross_entropy", "attention")
+
+# Attention workloads (name -> heads, sequence length, head dim, causal): the
+# pages' N = 4096 attention example ("Softmax numerics architecture...", "From
+# online softmax to tiled attention") as 4 x 32 heads of head dim 128, bf16,
+# q, k, v ~ N(0, 1) drawn on the device from one seeded generator.
+ATTN_WORKLOADS = {
+    "attn_bf16_4x32x4096x128": (128, 4096, 128, False),
+    "attn_bf16_4x32x4096x128_causal": (128, 4096, 128, True),
+}
+ATTN_SEED = 1006
+
+
+def attention_inputs(name: str, device):
+    """(q, k, v) bf16 [heads, seq, d] on `device`, seeded."""
+    heads, n, d, _ = ATTN_WORKLOADS[name]
+    g = torch.Generator(device=device).manual_seed(ATTN_SEED)
+    return tuple(torch.randn(heads, n, d, generator=g, device=device).to(torch.bfloat16) for _ in range(3))
+
+
+def attention_flops(heads: int, sq: int, sk: int, d: int, causal: bool) -> float:
+    """Multiply-adds of the two products (2 flops each): 4 heads sq sk d, half
+    of it under the causal mask (sq = sk)."""
+    return 4.0 * heads * sq * sk * d * (0.5 if causal else 1.0)
 
 
 def op_bytes(op: str, rows: int, cols: int, in_size: int, out_size: int, valid_len=None) -> int:
