@@ -312,6 +312,9 @@ int smx_version(void);
  * smx_debug_set_split_fused(off): 1 = path 5 runs two launches per slab (the
  *   statistics pass, then the normalising pass); 0 = one cooperative launch for
  *   all slabs with per-row completion counts (default where supported).
+ * smx_debug_set_attention_mma_sync(on): 1 = the attention forward runs on the
+ *   mma.sync kernel (warp-level tensor-core instructions) instead of the
+ *   tcgen05/TMEM kernel (default).
  * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
  *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
  *   first; -1 = automatic (1 and 2).
@@ -332,6 +335,7 @@ void smx_debug_set_split_slab(int64_t bytes);
 void smx_debug_set_split_hints(int stats, int apply);
 void smx_debug_set_stream_warp(int off);
 void smx_debug_set_split_fused(int off);
+void smx_debug_set_attention_mma_sync(int on);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 
 #ifdef __cplusplus

@@ -111,6 +111,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_stream_warp.restype = None
         lib.smx_debug_set_split_fused.argtypes = [I32]
         lib.smx_debug_set_split_fused.restype = None
+        lib.smx_debug_set_attention_mma_sync.argtypes = [I32]
+        lib.smx_debug_set_attention_mma_sync.restype = None
         _lib = lib
         return lib
 

@@ -58,7 +58,8 @@ std::atomic<int64_t> g_split_slab_bytes{0};
 std::atomic<int> g_split_hint_stats{-1}, g_split_hint_apply{-1};
 std::atomic<int64_t> g_bwd_inflight{48 * 1024};  // backward: reads in flight per SM
 std::atomic<int> g_stream_warp{0};
-std::atomic<int> g_split_fused{0};  // 0: long rows in one cooperative launch; 1: two launches per slab  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
+std::atomic<int> g_split_fused{0};
+std::atomic<int> g_attention_mma_sync{0};  // 1: the attention forward on mma.sync instead of tcgen05  // 0: long rows in one cooperative launch; 1: two launches per slab  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
 thread_local int t_last_cuda_error = 0;
@@ -257,6 +258,7 @@ int stream_occupancy(int in_dtype, int vpt, int threads, int depth, int mode, bo
 constexpr int64_t STREAM_INFLIGHT_BYTES = 48 * 1024;
 constexpr int64_t CE_INFLIGHT_BYTES = 64 * 1024;
 constexpr int64_t CLUSTER_MAX_ROW_BYTES = 4 << 20;
+constexpr int64_t ATTN_MAX_POLLS = int64_t(1) << 24;  // each tensor-core wait: tens of ms at most
 
 bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
                  bool has_lengths, int mode, int64_t inflight, Plan* p) {
@@ -848,6 +850,10 @@ smx_status smx_attention_forward(const void* q, const void* k, const void* v, vo
   if (s != SMX_OK) return s;
   AttnCall c{q, k, v, o, lse, heads, seq_q, seq_k, head_dim, scale, causal ? 1 : 0, (int)dtype,
              reinterpret_cast<cudaStream_t>(stream)};
+  c.status = dev->status;
+  const int64_t wl = g_wait_limit.load();
+  c.max_polls = wl > 0 ? wl : ATTN_MAX_POLLS;
+  c.tensor_memory = g_attention_mma_sync.load() == 0;
   const cudaError_t e = launch_attention(c);
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
   return SMX_OK;
@@ -936,6 +942,8 @@ void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes) {
 void smx_debug_set_stream_warp(int off) { g_stream_warp.store(off ? 1 : 0); }
 
 void smx_debug_set_split_fused(int off) { g_split_fused.store(off ? 1 : 0); }
+
+void smx_debug_set_attention_mma_sync(int on) { g_attention_mma_sync.store(on ? 1 : 0); }
 
 void smx_debug_set_split_hints(int stats, int apply) {
   g_split_hint_stats.store(stats >= 0 && stats <= 2 ? stats : -1);

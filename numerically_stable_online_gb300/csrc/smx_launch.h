@@ -84,6 +84,9 @@ struct AttnCall {
   int causal;
   int dtype;
   cudaStream_t stream;
+  int* status = nullptr;   // device status word (bounded waits of the tcgen05 kernel)
+  int64_t max_polls = 0;
+  bool tensor_memory = true;  // tcgen05/TMEM kernel; false: the mma.sync kernel
 };
 cudaError_t launch_attention(const AttnCall& c);
 

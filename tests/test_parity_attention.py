@@ -11,7 +11,8 @@ error carried through the same weights, plus the rounding of the output:
 LSE (fp32): |lse - ref| <= 2^-16 (|ref| + smax) + 2^-18.  Empty rows: o = +0 and
 lse = -inf exactly.
 
-Cases: head_dim 64 and 128; bf16 and fp16; causal and not; query and key
+Every case runs on both kernels (tcgen05/TMEM, and mma.sync).  Cases:
+head_dim 64 and 128; bf16 and fp16; causal and not; query and key
 counts that are not multiples of the 64-row blocks; more queries than keys
 under the causal mask (empty rows); no keys at all; large scores; and the
 4 x 32 heads x 4096 x 128 shape of the pages' attention example on sampled
@@ -39,6 +40,15 @@ def built():
     build.build()
     oracle.build()
     yield smx.library()
+
+
+@pytest.fixture(autouse=True, params=["tcgen05", "mma_sync"])
+def kernel(request, built):
+    """Every case on both kernels: tcgen05/TMEM (default) and mma.sync."""
+    built.smx_debug_set_attention_mma_sync(1 if request.param == "mma_sync" else 0)
+    yield request.param
+    built.smx_debug_set_attention_mma_sync(0)
+    assert smx.last_device_status() == 0
 
 
 def check(o_dev, lse_dev, q, k, v, dt, heads, sq, sk, d, scale, causal, rows_sel=None):
