@@ -44,8 +44,8 @@ cudaError_t launch_attention_t(const AttnCall& c) {
 template <typename T, int D>
 cudaError_t launch_attention_tc_t(const AttnCall& c) {
   auto kern = k_attention_tc<T, D>;
-  // Q, K x 2, V^T, P and the 1024-byte alignment slack
-  const int64_t smem = (int64_t)(ATT_TC_BM * D + 3 * ATT_TC_BN * D + ATT_TC_BM * ATT_TC_BN) * 2 + 1024;
+  // the operand tiles and 1024 bytes for their alignment and the barriers
+  const int64_t smem = (int64_t)att_tc_tile_bytes<D>() + 1024;
   static std::mutex mu;
   static bool set[64] = {};
   int dev = 0;
@@ -56,6 +56,10 @@ cudaError_t launch_attention_tc_t(const AttnCall& c) {
     std::lock_guard<std::mutex> lock(mu);
     if (!set[dev]) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      // two CTAs of (D = 128) 113 KiB each need the largest shared-memory carveout
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       set[dev] = true;
     }

@@ -4,28 +4,32 @@
 // summary"; "Softmax numerics architecture...", "From online softmax to tiled
 // attention"), with both products issued by one thread as tcgen05.mma and
 // accumulated in tensor memory:
-//   S  (128 x 64 fp32, TMEM columns [D, D + 64))  = Q K_B^T
-//   O  (128 x D fp32,  TMEM columns [0, D))      += P V_B
+//   S  (128 x 64 fp32, TMEM columns D + 64 (b & 1) onward) = Q K_b^T
+//   O  (128 x D fp32,  TMEM columns [0, D))              += P_b V_b
 // One CTA of 128 threads takes 128 query rows of one head; thread r owns query
 // row r, which is TMEM lane r, so the row's maximum and sum need no exchange.
-// Operands sit in shared memory K-major with the 128-byte swizzle (8-row atoms
-// of 1024 bytes; 16-byte chunks XOR-ed with the row): Q and K as stored, P
-// written by the row threads, V transposed while it is staged (V^T rows are
-// the head dimension, so the second product's B operand is K-major too).
+// Operands sit in shared memory with the 128-byte swizzle (8-row atoms of
+// 1024 bytes; 16-byte chunks XOR-ed with the row), all tiles in one layout:
+// rows of 64 16-bit elements.  Q, K and P (written by the row threads) are
+// K-major operands; V, staged as stored ([key][head dim]), is the second
+// product's B operand in MN-major form, so nothing is transposed.
 //
-// Per key block: one thread issues S = Q K^T and commits to an mbarrier (the
-// commit also covers the previous block's O += P V^T); the next block's K
-// (cp.async, second buffer) and V (registers) are fetched meanwhile; each row
-// thread reads its 64 scores from TMEM,
-// masks, updates (m, l), writes P (the input type) to shared memory and, when
-// its reference maximum has to move, rescales its O row in TMEM; one thread
-// issues O += P V^T and commits.  The reference maximum moves only when the
+// Pipeline, per key block b: S(b + 1) is issued (two S buffers in TMEM, two K
+// and two V buffers in shared memory) before the row threads take S(b), so
+// the tensor core computes the next scores and the previous O += P V while
+// the rows compute this block's exponentials.  Each row thread masks its 64
+// scores, updates (m, l), and only then waits for the previous O += P V
+// before it writes P (the input type) to shared memory and, when its
+// reference maximum has to move, rescales its O row in TMEM; one thread
+// issues O += P V.  K and V of later blocks are copied by cp.async as soon
+// as their buffers are free.  The reference maximum moves only when the
 // block's maximum exceeds it by more than 8 (base-2 units): the exponentials
 // then stay below 2^8, and l and o always share one reference, so the result
 // is the same quotient (the rescale is exact bookkeeping, not an
-// approximation).  Two CTAs share an SM (shared memory 97 KiB and up to 256
-// TMEM columns each) so that one's softmax overlaps the other's products.  Every mbarrier wait is bounded; running out records
-// SMX_ERR_TIMEOUT in the device status word.
+// approximation).  Two CTAs share an SM (shared memory 113 KiB and 256 TMEM
+// columns each) so that one's softmax overlaps the other's products.
+// Every mbarrier wait is bounded; running out records SMX_ERR_TIMEOUT in the
+// device status word.
 #pragma once
 
 #include <type_traits>
@@ -37,6 +41,13 @@ namespace smx {
 constexpr int ATT_TC_BM = 128;  // query rows per CTA (one per thread, one per TMEM lane)
 constexpr int ATT_TC_BN = 64;   // keys per block
 constexpr int ATT_TC_THREADS = 128;
+// shared memory of the operand tiles: Q [128][D], K [2][64][D], V [2][64][D],
+// P [128][64] (16-bit elements); the launch adds 1024 bytes so that the tiles
+// can start on a 1024-byte boundary, and the barriers live in that slack
+template <int D>
+__host__ __device__ constexpr int att_tc_tile_bytes() {
+  return (ATT_TC_BM * D + 4 * ATT_TC_BN * D + ATT_TC_BM * ATT_TC_BN) * 2;
+}
 
 struct AttnTcArgs {
   AttnArgs a;
@@ -63,12 +74,22 @@ __device__ __forceinline__ uint64_t tc_sdesc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// the same for an MN-major operand (each 128-byte row holds 64 consecutive
+// N-elements of one K index; 8 K-rows make a 1024-byte atom): 8-row groups
+// along K are 1024 bytes apart (stride offset), the 64-element halves along N
+// are `lbo` bytes apart (leading offset)
+__device__ __forceinline__ uint64_t tc_sdesc_mn(uint32_t saddr, uint32_t lbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // instruction descriptor of kind::f16: fp32 accumulator, A and B of type T,
-// both K-major, M x N
+// A K-major, B K-major or (b_mn) MN-major, M x N
 template <typename T>
-__device__ __forceinline__ uint32_t tc_idesc(int M, int N) {
+__device__ __forceinline__ uint32_t tc_idesc(int M, int N, bool b_mn = false) {
   const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
@@ -118,6 +139,30 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 64 consecutive columns of this warp's 32 lanes; the wait is part of the same
+// statement, so no use of the values can be scheduled before it
+__device__ __forceinline__ void tc_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -133,15 +178,13 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(ATT_TC_THREADS)
+__global__ void __launch_bounds__(ATT_TC_THREADS, 1)
     k_attention_tc(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    T* __restrict__ o, float* __restrict__ lse, AttnTcArgs args) {
   static_assert(D == 64 || D == 128, "head dimension");
   constexpr int BM = ATT_TC_BM, BN = ATT_TC_BN;
-  constexpr uint32_t TCOLS = D == 128 ? 256 : 128;  // O then S, a power of two
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t mbar[1];  // products done (S each block, then the last O)
-  __shared__ uint32_t tmem_base;
+  constexpr uint32_t TCOLS = 256;  // O (D columns) then two S buffers of 64: a power of two
+  extern __shared__ __align__(16) uint8_t smem_raw[];
 
   const AttnArgs& a = args.a;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -151,14 +194,21 @@ __global__ void __launch_bounds__(ATT_TC_THREADS)
   const T* kh = k + head * a.sk * D;
   const T* vh = v + head * a.sk * D;
 
-  // 1024-aligned operand tiles: Q [BM][D], K [2][BN][D], V^T [D][BN], P [BM][BN]
+  // 1024-aligned operand tiles: Q [BM][D], K [2][BN][D], V [2][BN][D], P [BM][BN]
   const uint32_t raw = tc_su32(smem_raw);
-  uint8_t* base = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const uint32_t pad = (1024 - (raw & 1023)) & 1023;
+  uint8_t* base = smem_raw + pad;
   uint8_t* sQ = base;
   uint8_t* sK0 = sQ + BM * D * 2;
-  constexpr int KT = BN * D * 2;  // bytes of one K or V^T tile
-  uint8_t* sVt = sK0 + 2 * KT;
-  uint8_t* sP = sVt + KT;
+  constexpr int KT = BN * D * 2;  // bytes of one K or V tile
+  uint8_t* sV0 = sK0 + 2 * KT;
+  uint8_t* sP = sV0 + 2 * KT;
+  // three mbarriers (S of even / odd key blocks; O += P V) and the TMEM
+  // address: in the alignment gap when it has room, else after the tiles
+  // (the launch's 1024 spare bytes hold the gap plus these 28 bytes)
+  uint8_t* aux = pad >= 32 ? smem_raw : base + att_tc_tile_bytes<D>();
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(aux);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 24);
 
   int64_t kv_end = a.sk;
   if (a.causal) {
@@ -181,150 +231,153 @@ __global__ void __launch_bounds__(ATT_TC_THREADS)
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_su32(&tmem_base)),
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc_su32(tmem_slot)),
                  "r"(TCOLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_su32(&mbar[0])) : "memory");
+#pragma unroll
+    for (int i = 0; i < 3; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_su32(mbar + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = tmem_base;
+  const uint32_t tmem = *tmem_slot;
   const uint32_t t_o = tmem, t_s = tmem + D;
   // this thread's TMEM lane (its query row) in the warp's 32-lane slice
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   const int64_t qi = q0 + tid;
   const int64_t lim = a.causal ? qi + a.sk - a.sq : a.sk - 1;  // keys j <= lim are valid
 
-  const uint32_t id_s = tc_idesc<T>(BM, BN), id_o = tc_idesc<T>(BM, D);
+  const uint32_t id_s = tc_idesc<T>(BM, BN), id_o = tc_idesc<T>(BM, D, true);
   bool ok = true;
   float m_ref = neg_inf(), l = 0.0f;
+  // keys j <= jmax are valid for this row
+  const int64_t jmax = lim < a.sk - 1 ? lim : a.sk - 1;
+  const float cs = a.scale_log2;  // > 0, so the raw maximum scales to the scaled one
 
-  // staging of key block b: K by cp.async into buffer (b & 1); V into
-  // registers (vr) one block ahead, then transposed into V^T with eight 2-byte
-  // stores per 16-byte chunk (lanes over consecutive keys, so a warp fills
-  // whole chunks)
-  constexpr int VCH = BN * (D / 8) / ATT_TC_THREADS;  // 16-byte V chunks per thread
-  uint4 vr[VCH];
-  auto stage_k = [&](int blk) {
-    const int64_t key0 = (int64_t)blk * BN;
-    uint8_t* sK = sK0 + (blk & 1) * KT;
-    for (int i = tid; i < BN * (D / 8); i += ATT_TC_THREADS) {
-      const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-      const uint32_t dst = tc_su32(sK + tc_off(r, c, BN));
-      if (key0 + r < a.sk)
-        att_cp16(dst, kh + (key0 + r) * D + c);
-      else
-        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+  // key block blk of K or V into tile buffer (blk & 1) by cp.async, rows past
+  // the keys zero; one commit group each, empty past the last block (so the
+  // group count per block is fixed).  V keeps its stored layout: it is the
+  // second product's B operand in MN-major form (N = head dimension).
+  auto stage = [&](const T* src, uint8_t* tiles, int blk) {
+    if (blk < nblocks) {
+      const int64_t key0 = (int64_t)blk * BN;
+      uint8_t* dst_tile = tiles + (blk & 1) * KT;
+      for (int i = tid; i < BN * (D / 8); i += ATT_TC_THREADS) {
+        const int r = i / (D / 8), c = (i % (D / 8)) * 8;
+        const uint32_t dst = tc_su32(dst_tile + tc_off(r, c, BN));
+        if (key0 + r < a.sk)
+          att_cp16(dst, src + (key0 + r) * D + c);
+        else
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+      }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  auto load_v = [&](int blk) {
-    const int64_t key0 = (int64_t)blk * BN;
+  // S(blk) = Q K(blk)^T into TMEM buffer (blk & 1): D / 16 steps of K = 16
+  // (two per 32 bytes of a 128-byte row); committed to mbar[blk & 1]
+  auto issue_s = [&](int blk) {
+    const uint32_t kbase = tc_su32(sK0 + (blk & 1) * KT);
 #pragma unroll
-    for (int u = 0; u < VCH; ++u) {
-      const int i = tid + u * ATT_TC_THREADS;
-      const int j = i % BN, c = (i / BN) * 8;
-      vr[u] = make_uint4(0, 0, 0, 0);
-      if (key0 + j < a.sk) vr[u] = __ldg(reinterpret_cast<const uint4*>(vh + (key0 + j) * D + c));
+    for (int st = 0; st < D / 16; ++st) {
+      const uint32_t koff = (uint32_t)((st & 3) * 32);
+      const uint64_t da = tc_sdesc(tc_su32(sQ) + (uint32_t)((st >> 2) * BM * 128) + koff);
+      const uint64_t db = tc_sdesc(kbase + (uint32_t)((st >> 2) * BN * 128) + koff);
+      tc_mma(t_s + (uint32_t)((blk & 1) * BN), da, db, id_s, st > 0 ? 1u : 0u);
     }
+    tc_commit(tc_su32(&mbar[blk & 1]));
   };
-  auto store_vt = [&]() {
-#pragma unroll
-    for (int u = 0; u < VCH; ++u) {
-      const int i = tid + u * ATT_TC_THREADS;
-      const int j = i % BN, c = (i / BN) * 8;
-      const uint16_t* e = reinterpret_cast<const uint16_t*>(&vr[u]);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) *reinterpret_cast<uint16_t*>(sVt + tc_off(c + t, j, D)) = e[t];
-    }
+  // cp.async (all but the newest N groups) and generic stores visible to the
+  // tensor core
+  auto sync_async = [&](auto pending) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(decltype(pending)::value) : "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   };
-  // block 0's K and V before the loop
-  if (nblocks > 0) {
-    stage_k(0);
-    load_v(0);
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+  // blocks 0 and 1's K and block 0's V before the loop; S(0) issued
+  stage(kh, sK0, 0);
+  stage(vh, sV0, 0);
+  stage(kh, sK0, 1);
+  sync_async(std::integral_constant<int, 0>());
+  if (tid == 0 && nblocks > 0) issue_s(0);
 
   for (int b = 0; b < nblocks; ++b) {
     const int64_t key0 = (int64_t)b * BN;
-    // S = Q K^T: D / 16 steps of K = 16 (two per 32 bytes of a 128-byte row)
-    if (tid == 0) {
-      const uint32_t kbase = tc_su32(sK0 + (b & 1) * KT);
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const uint32_t koff = (uint32_t)((s & 3) * 32);
-        const uint64_t da = tc_sdesc(tc_su32(sQ) + (uint32_t)((s >> 2) * BM * 128) + koff);
-        const uint64_t db = tc_sdesc(kbase + (uint32_t)((s >> 2) * BN * 128) + koff);
-        tc_mma(t_s, da, db, id_s, s > 0 ? 1u : 0u);
-      }
-      tc_commit(tc_su32(&mbar[0]));
-    }
-    // the next block's K in flight while this one runs (its buffer's last
-    // reader, the previous S, has finished)
-    const bool more = b + 1 < nblocks;
-    if (more) stage_k(b + 1);
-    // S done; its commit covers every earlier product of the issuing thread,
-    // so O += P V^T of the previous block has finished too: P, O and V^T may
-    // be rewritten
-    if (!tc_wait(tc_su32(&mbar[0]), (uint32_t)(b & 1), args.max_polls, args.status)) {
+    // S(b + 1) behind S(b) and O += P(b - 1) V(b - 1): its K landed before the last
+    // barrier, and its TMEM buffer's last reader (the softmax of b - 1) passed it
+    if (tid == 0 && b + 1 < nblocks) issue_s(b + 1);
+    // S(b) done.  mbar[x] takes every other block's commit, and no commit of
+    // block b + 2 can come before all threads passed this wait (it follows the
+    // barrier at the end of this block), so the phase parity is unambiguous
+    if (!tc_wait(tc_su32(&mbar[b & 1]), (uint32_t)((b >> 1) & 1), args.max_polls, args.status)) {
       ok = false;
       atomicOr(args.status, DEV_TIMEOUT);
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // this block's V^T from the registers, then the next block's V into them
-    store_vt();
-    if (more) load_v(b + 1);
-    // this row's 64 scores: mask, block maximum in scaled base-2 units
-    float s[BN];
+    // the K buffer S(b) read is free: block b + 2's K into it
+    stage(kh, sK0, b + 2);
+
+    // this row's 64 scores; the valid prefix of the block for this row
+    float sc[BN];
+    tc_ld64(t_s + lane_off + (uint32_t)((b & 1) * BN), sc);
+    const int64_t nv64 = jmax - key0 + 1;
+    const int nv = nv64 < 0 ? 0 : (nv64 > BN ? BN : (int)nv64);
+    if (nv < BN) {
 #pragma unroll
-    for (int c = 0; c < BN; c += 16) {
-      float t16[16];
-      tc_ld16(t_s + lane_off + (uint32_t)c, t16);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) s[c + i] = t16[i];
+      for (int i = 0; i < BN; ++i)
+        if (i >= nv) sc[i] = neg_inf();
     }
-    float mx = neg_inf();
+    // block maximum (eight independent chains), in scaled base-2 units
+    float mx8[8];
 #pragma unroll
-    for (int i = 0; i < BN; ++i) {
-      const int64_t j = key0 + i;
-      s[i] = (j > lim || j >= a.sk) ? neg_inf() : s[i] * a.scale_log2;
-      mx = fmaxf(mx, s[i]);
-    }
+    for (int i = 0; i < 8; ++i) mx8[i] = sc[i];
+#pragma unroll
+    for (int i = 8; i < BN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sc[i]);
+    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * cs;
     // move the reference only when needed (see the header); alpha rescales l and O
     float alpha = 1.0f;
     if (mx > m_ref + 8.0f) {
       alpha = m_ref == neg_inf() ? 0.0f : ex2_full(m_ref - mx);
       m_ref = mx;
     }
-    const float sub = m_ref == neg_inf() ? 0.0f : m_ref;
-    float ps = 0.0f;
+    const float nsub = m_ref == neg_inf() ? 0.0f : -m_ref;
+    // p = 2^(s cs - m_ref), packed to the input type; four partial sums
+    uint32_t pk[BN / 2];
+    float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < BN; i += 2) {
+      const float p0 = ex2_ftz(__fmaf_rn(sc[i], cs, nsub));
+      const float p1 = ex2_ftz(__fmaf_rn(sc[i + 1], cs, nsub));
+      ps4[(i >> 1) & 3] += p0 + p1;
+      pk[i / 2] = pack2<T>(p0, p1);
+    }
+    l = __fmaf_rn(l, alpha, (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+
+    // O += P(b - 1) V(b - 1) finished: P, O and that V buffer may be
+    // rewritten; block b + 1's V into the buffer
+    if (b > 0) {
+      if (!tc_wait(tc_su32(&mbar[2]), (uint32_t)((b - 1) & 1), args.max_polls, args.status)) {
+        ok = false;
+        atomicOr(args.status, DEV_TIMEOUT);
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    }
+    stage(vh, sV0, b + 1);
     // P row into shared memory, 8 keys (16 bytes) at a time
 #pragma unroll
-    for (int c = 0; c < BN; c += 8) {
-      float p8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        p8[i] = ex2_full(s[c + i] - sub);
-        ps += p8[i];
-      }
-      const uint4 w = make_uint4(pack2<T>(p8[0], p8[1]), pack2<T>(p8[2], p8[3]), pack2<T>(p8[4], p8[5]),
-                                 pack2<T>(p8[6], p8[7]));
-      *reinterpret_cast<uint4*>(sP + tc_off(tid, c, BM)) = w;
-    }
-    l = __fmaf_rn(l, alpha, ps);
+    for (int c = 0; c < BN; c += 8)
+      *reinterpret_cast<uint4*>(sP + tc_off(tid, c, BM)) =
+          make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
     // TMEM loads and stores are warp-collective: a warp rescales when any of
     // its rows must (the others multiply by 1, exactly)
     if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-      // O row *= alpha (the previous product has finished: waited above)
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
         float t16[16];
@@ -334,30 +387,27 @@ __global__ void __launch_bounds__(ATT_TC_THREADS)
         tc_st16(t_o + lane_off + (uint32_t)c, t16);
       }
     }
-    // P and V^T written, the next block's K landed
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // P written; block b + 2's K and block b's V landed (block b + 1's V, the
+    // newest group, may still be in flight)
+    sync_async(std::integral_constant<int, 1>());
 
-    // O += P V^T: BN / 16 steps of K = 16 over the block's keys
+    // O += P V: BN / 16 steps of K = 16 over the block's keys (two 8-key
+    // groups of V, 2048 bytes, a step); committed to mbar[2]
     if (tid == 0) {
+      const uint32_t vbase = tc_su32(sV0 + (b & 1) * KT);
 #pragma unroll
       for (int s2 = 0; s2 < BN / 16; ++s2) {
         const uint32_t koff = (uint32_t)((s2 & 3) * 32);
         const uint64_t da = tc_sdesc(tc_su32(sP) + (uint32_t)((s2 >> 2) * BM * 128) + koff);
-        const uint64_t db = tc_sdesc(tc_su32(sVt) + (uint32_t)((s2 >> 2) * D * 128) + koff);
+        const uint64_t db = tc_sdesc_mn(vbase + (uint32_t)(s2 * 2048), (uint32_t)(BN * 128));
         tc_mma(t_o, da, db, id_o, (b > 0 || s2 > 0) ? 1u : 0u);
       }
+      tc_commit(tc_su32(&mbar[2]));
     }
   }
-  // the last O += P V^T: one more commit on the same barrier (every earlier
-  // phase has been waited, so the parity names this one)
-  if (nblocks > 0) {
-    if (tid == 0) tc_commit(tc_su32(&mbar[0]));
-    if (!tc_wait(tc_su32(&mbar[0]), (uint32_t)(nblocks & 1), args.max_polls, args.status)) ok = false;
-  }
+  // the last O += P V
+  if (nblocks > 0 && !tc_wait(tc_su32(&mbar[2]), (uint32_t)((nblocks - 1) & 1), args.max_polls, args.status))
+    ok = false;
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (!ok) atomicOr(args.status, DEV_TIMEOUT);
