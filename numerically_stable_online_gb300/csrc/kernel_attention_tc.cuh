@@ -163,6 +163,12 @@ __device__ __forceinline__ void tc_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
+// three-input maximum (one instruction on this architecture)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -262,17 +268,31 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
   // the keys zero; one commit group each, empty past the last block (so the
   // group count per block is fixed).  V keeps its stored layout: it is the
   // second product's B operand in MN-major form (N = head dimension).
+  // this thread's chunks of a tile: column c0 of rows r0 + RS u (RS a
+  // multiple of 8, so the swizzle phase is fixed and the shared offset
+  // advances by whole atoms)
+  constexpr int CPR = D / 8;                   // 16-byte chunks a row
+  constexpr int RS = ATT_TC_THREADS / CPR;    // rows a pass
+  constexpr int NU = BN / RS;                  // passes a tile
+  const int r0 = tid / CPR, c0 = (tid % CPR) * 8;
+  const uint32_t soff = tc_off(r0, c0, BN);
   auto stage = [&](const T* src, uint8_t* tiles, int blk) {
     if (blk < nblocks) {
       const int64_t key0 = (int64_t)blk * BN;
-      uint8_t* dst_tile = tiles + (blk & 1) * KT;
-      for (int i = tid; i < BN * (D / 8); i += ATT_TC_THREADS) {
-        const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-        const uint32_t dst = tc_su32(dst_tile + tc_off(r, c, BN));
-        if (key0 + r < a.sk)
-          att_cp16(dst, src + (key0 + r) * D + c);
-        else
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+      const uint32_t dst = tc_su32(tiles + (blk & 1) * KT) + soff;
+      const T* g = src + (key0 + r0) * D + c0;
+      if (key0 + BN <= a.sk) {
+#pragma unroll
+        for (int u = 0; u < NU; ++u) att_cp16(dst + (uint32_t)(u * RS * 128), g + (int64_t)u * RS * D);
+      } else {
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          if (key0 + r0 + u * RS < a.sk)
+            att_cp16(dst + (uint32_t)(u * RS * 128), g + (int64_t)u * RS * D);
+          else
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst + (uint32_t)(u * RS * 128)), "r"(0)
+                         : "memory");
+        }
       }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -333,14 +353,15 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       for (int i = 0; i < BN; ++i)
         if (i >= nv) sc[i] = neg_inf();
     }
-    // block maximum (eight independent chains), in scaled base-2 units
-    float mx8[8];
+    // block maximum (four chains of three-input max), in scaled base-2 units
+    float mx4[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx8[i] = sc[i];
+    for (int j = 0; j < 4; ++j) mx4[j] = fmaxf(sc[2 * j], sc[2 * j + 1]);
 #pragma unroll
-    for (int i = 8; i < BN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sc[i]);
-    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * cs;
+    for (int i = 8; i < BN; i += 8)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx4[j] = max3(mx4[j], sc[i + 2 * j], sc[i + 2 * j + 1]);
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
     // move the reference only when needed (see the header); alpha rescales l and O
     float alpha = 1.0f;
     if (mx > m_ref + 8.0f) {
@@ -348,17 +369,20 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
       m_ref = mx;
     }
     const float nsub = m_ref == neg_inf() ? 0.0f : -m_ref;
-    // p = 2^(s cs - m_ref), packed to the input type; four partial sums
-    uint32_t pk[BN / 2];
-    float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // p = 2^(s cs - m_ref) (pairs by one f32x2 FMA), packed to the input type;
+    // two f32x2 partial sums
+    uint32_t pk2[BN / 2];
+    const unsigned long long cs2 = pk(cs, cs), ns2 = pk(nsub, nsub);
+    unsigned long long acc2[2] = {0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < BN; i += 2) {
-      const float p0 = ex2_ftz(__fmaf_rn(sc[i], cs, nsub));
-      const float p1 = ex2_ftz(__fmaf_rn(sc[i + 1], cs, nsub));
-      ps4[(i >> 1) & 3] += p0 + p1;
-      pk[i / 2] = pack2<T>(p0, p1);
+      const unsigned long long e = fma2(pk(sc[i], sc[i + 1]), cs2, ns2);
+      const float p0 = ex2_ftz(pk_lo(e)), p1 = ex2_ftz(pk_hi(e));
+      acc2[(i >> 1) & 1] = add2(acc2[(i >> 1) & 1], pk(p0, p1));
+      pk2[i / 2] = pack2<T>(p0, p1);
     }
-    l = __fmaf_rn(l, alpha, (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+    const float ps = (pk_lo(acc2[0]) + pk_hi(acc2[0])) + (pk_lo(acc2[1]) + pk_hi(acc2[1]));
+    l = __fmaf_rn(l, alpha, ps);
 
     // O += P(b - 1) V(b - 1) finished: P, O and that V buffer may be
     // rewritten; block b + 1's V into the buffer
@@ -374,7 +398,7 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
 #pragma unroll
     for (int c = 0; c < BN; c += 8)
       *reinterpret_cast<uint4*>(sP + tc_off(tid, c, BM)) =
-          make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
+          make_uint4(pk2[c / 2], pk2[c / 2 + 1], pk2[c / 2 + 2], pk2[c / 2 + 3]);
     // TMEM loads and stores are warp-collective: a warp rescales when any of
     // its rows must (the others multiply by 1, exactly)
     if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
