@@ -51,7 +51,8 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_regs.cuh",
                   "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
                   "kernel_backward.cuh", "kernel_split_fused.cuh", "launch_impl.cuh", "smx_api.cu"]
-ATTN_SOURCES = ["smx_device.cuh", "kernel_attention.cuh", "inst_attention.cu", "smx_api.cu"]
+ATTN_SOURCES = ["smx_device.cuh", "kernel_attention.cuh", "kernel_attention_tc.cuh", "inst_attention.cu",
+                "smx_api.cu"]
 
 
 def metric_of(op: str) -> str:
@@ -552,7 +553,8 @@ def run_ours(args, w):
     return 0
 
 
-ATTN_METRIC = "attention forward TFLOP/s (4 heads sq sk d, halved when causal) on 1 GB300; % of bf16 tensor peak"
+ATTN_METRIC = ("attention forward TFLOP/s (4 head_dim FLOPs per valid query-key pair) on 1 GB300; "
+               "% of bf16 tensor peak")
 
 
 def attention_oracle_sample(name, q, k, v, budget_s, min_rows=4):
@@ -677,7 +679,7 @@ def run_attention(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} cuBLAS bf16 GEMM throughput (burst)",
-                     "kernel": kernel_name or "k_attention<bf16,128> (mma.sync m16n8k16)",
+                     "kernel": kernel_name or "k_attention_tc<bf16,128> (tcgen05.mma, TMEM accumulators)",
                      "flops_per_launch": flops, "mean_launch_us": mean_launch_ms * 1e3,
                      "median_launch_us": statistics.median(launch_ms) * 1e3},
         "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",

@@ -170,10 +170,20 @@ def attention_inputs(name: str, device):
     return tuple(torch.randn(heads, n, d, generator=g, device=device).to(torch.bfloat16) for _ in range(3))
 
 
+def attention_pairs(sq: int, sk: int, causal: bool) -> int:
+    """Valid (query, key) pairs of one head: all of them, or under the
+    bottom-right aligned causal mask (key j valid for query i when
+    j <= i + sk - sq) sum_i clamp(i + sk - sq + 1, 0, sk)."""
+    if not causal:
+        return sq * sk
+    i = np.arange(sq, dtype=np.int64)
+    return int(np.clip(i + sk - sq + 1, 0, sk).sum())
+
+
 def attention_flops(heads: int, sq: int, sk: int, d: int, causal: bool) -> float:
-    """Multiply-adds of the two products (2 flops each): 4 heads sq sk d, half
-    of it under the causal mask (sq = sk)."""
-    return 4.0 * heads * sq * sk * d * (0.5 if causal else 1.0)
+    """Multiply-adds of the two products over the valid pairs, 2 flops each:
+    4 d per pair."""
+    return 4.0 * heads * d * attention_pairs(sq, sk, causal)
 
 
 def op_bytes(op: str, rows: int, cols: int, in_size: int, out_size: int, valid_len=None) -> int:

@@ -79,3 +79,15 @@ def test_reference_arm_other_ranks_exit_quietly():
 def test_bench_rejects_too_few_warmups():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_attention_flops_count_valid_pairs():
+    """4 head_dim FLOPs per valid (query, key) pair, the pairs counted by brute
+    force over the mask the attention entry point documents."""
+    from numerically_stable_online_gb300 import workloads as wl
+
+    for sq, sk in [(1, 1), (3, 5), (5, 3), (7, 7), (4, 0)]:
+        for causal in (False, True):
+            brute = sum(1 for i in range(sq) for j in range(sk) if not causal or j <= i + sk - sq)
+            assert wl.attention_pairs(sq, sk, causal) == brute
+            assert wl.attention_flops(2, sq, sk, 64, causal) == 4.0 * 2 * 64 * brute
