@@ -74,7 +74,7 @@ cudaError_t launch_attention_tc_t(const AttnCall& c) {
   a.max_polls = c.max_polls;
   const dim3 grid((unsigned)((c.sq + ATT_TC_BM - 1) / ATT_TC_BM), (unsigned)c.heads);
   note_launch();
-  kern<<<grid, ATT_TC_THREADS, (size_t)smem, c.stream>>>(static_cast<const T*>(c.q), static_cast<const T*>(c.k),
+  kern<<<grid, ATT_TC_BLOCK, (size_t)smem, c.stream>>>(static_cast<const T*>(c.q), static_cast<const T*>(c.k),
                                                           static_cast<const T*>(c.v), static_cast<T*>(c.o), c.lse,
                                                           a);
   return cudaGetLastError();

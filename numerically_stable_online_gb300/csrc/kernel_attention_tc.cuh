@@ -6,8 +6,9 @@
 // accumulated in tensor memory:
 //   S  (128 x 64 fp32, TMEM columns D + 64 (b & 1) onward) = Q K_b^T
 //   O  (128 x D fp32,  TMEM columns [0, D))              += P_b V_b
-// One CTA of 128 threads takes 128 query rows of one head; thread r owns query
-// row r, which is TMEM lane r, so the row's maximum and sum need no exchange.
+// One CTA takes 128 query rows of one head: row thread r (warps 0-3) owns
+// query row r, which is TMEM lane r, so the row's maximum and sum need no
+// exchange; a fifth warp issues the products.
 // Operands sit in shared memory with the 128-byte swizzle (8-row atoms of
 // 1024 bytes; 16-byte chunks XOR-ed with the row), all tiles in one layout:
 // rows of 64 16-bit elements.  Q, K and P (written by the row threads) are
@@ -20,14 +21,16 @@
 // the rows compute this block's exponentials.  Each row thread masks its 64
 // scores, updates (m, l), and only then waits for the previous O += P V
 // before it writes P (the input type) to shared memory and, when its
-// reference maximum has to move, rescales its O row in TMEM; one thread
-// issues O += P V.  K and V of later blocks are copied by cp.async as soon
-// as their buffers are free.  The reference maximum moves only when the
-// block's maximum exceeds it by more than 8 (base-2 units): the exponentials
-// then stay below 2^8, and l and o always share one reference, so the result
-// is the same quotient (the rescale is exact bookkeeping, not an
-// approximation).  Two CTAs share an SM (shared memory 113 KiB and 256 TMEM
-// columns each) so that one's softmax overlaps the other's products.
+// reference maximum has to move, rescales its O row in TMEM; it then arrives
+// (without waiting) on a named barrier, on which the issuing warp waits
+// before it issues O += P V and the scores two blocks ahead.  K and V of
+// later blocks are copied by cp.async as soon as their buffers are free.
+// The reference maximum moves only when the block's maximum exceeds it by
+// more than 8 (base-2 units): the exponentials then stay below 2^8, and l and
+// o always share one reference, so the result is the same quotient (the
+// rescale is exact bookkeeping, not an approximation).  Two CTAs share an SM
+// (shared memory 113 KiB and 256 TMEM columns each) so that one's softmax
+// overlaps the other's products.
 // Every mbarrier wait is bounded; running out records SMX_ERR_TIMEOUT in the
 // device status word.
 #pragma once
@@ -40,7 +43,8 @@ namespace smx {
 
 constexpr int ATT_TC_BM = 128;  // query rows per CTA (one per thread, one per TMEM lane)
 constexpr int ATT_TC_BN = 64;   // keys per block
-constexpr int ATT_TC_THREADS = 128;
+constexpr int ATT_TC_THREADS = 128;                 // row threads (warps 0-3)
+constexpr int ATT_TC_BLOCK = ATT_TC_THREADS + 32;   // plus one warp that issues the products
 // shared memory of the operand tiles: Q [128][D], K [2][64][D], V [2][64][D],
 // P [128][64] (16-bit elements); the launch adds 1024 bytes so that the tiles
 // can start on a 1024-byte boundary, and the barriers live in that slack
@@ -184,7 +188,7 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(ATT_TC_THREADS, 1)
+__global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
     k_attention_tc(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    T* __restrict__ o, float* __restrict__ lse, AttnTcArgs args) {
   static_assert(D == 64 || D == 128, "head dimension");
@@ -193,7 +197,8 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
   extern __shared__ __align__(16) uint8_t smem_raw[];
 
   const AttnArgs& a = args.a;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool row_thread = tid < ATT_TC_THREADS;
   const int64_t head = blockIdx.y;
   const int64_t q0 = (int64_t)blockIdx.x * BM;
   const T* qh = q + head * a.sq * D;
@@ -226,13 +231,15 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
   const int nblocks = (int)((kv_end + BN - 1) / BN);
 
   // Q: 16-byte chunks straight into the swizzled layout; rows past sq zero
-  for (int i = tid; i < BM * (D / 8); i += ATT_TC_THREADS) {
-    const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-    const uint32_t dst = tc_su32(sQ + tc_off(r, c, BM));
-    if (q0 + r < a.sq)
-      att_cp16(dst, qh + (q0 + r) * D + c);
-    else
-      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+  if (row_thread) {
+    for (int i = tid; i < BM * (D / 8); i += ATT_TC_THREADS) {
+      const int r = i / (D / 8), c = (i % (D / 8)) * 8;
+      const uint32_t dst = tc_su32(sQ + tc_off(r, c, BM));
+      if (q0 + r < a.sq)
+        att_cp16(dst, qh + (q0 + r) * D + c);
+      else
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
@@ -310,161 +317,181 @@ __global__ void __launch_bounds__(ATT_TC_THREADS, 1)
     }
     tc_commit(tc_su32(&mbar[blk & 1]));
   };
-  // cp.async (all but the newest N groups) and generic stores visible to the
-  // tensor core
-  auto sync_async = [&](auto pending) {
-    asm volatile("cp.async.wait_group %0;" ::"n"(decltype(pending)::value) : "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  // O += P(blk) V(blk): BN / 16 steps of K = 16 over the block's keys (two
+  // 8-key groups of V, 2048 bytes, a step); committed to mbar[2]
+  auto issue_pv = [&](int blk) {
+    const uint32_t vbase = tc_su32(sV0 + (blk & 1) * KT);
+#pragma unroll
+    for (int s2 = 0; s2 < BN / 16; ++s2) {
+      const uint32_t koff = (uint32_t)((s2 & 3) * 32);
+      const uint64_t da = tc_sdesc(tc_su32(sP) + (uint32_t)((s2 >> 2) * BM * 128) + koff);
+      const uint64_t db = tc_sdesc_mn(vbase + (uint32_t)(s2 * 2048), (uint32_t)(BN * 128));
+      tc_mma(t_o, da, db, id_o, (blk > 0 || s2 > 0) ? 1u : 0u);
+    }
+    tc_commit(tc_su32(&mbar[2]));
   };
 
-  // blocks 0 and 1's K and block 0's V before the loop; S(0) issued
-  stage(kh, sK0, 0);
-  stage(vh, sV0, 0);
-  stage(kh, sK0, 1);
-  sync_async(std::integral_constant<int, 0>());
-  if (tid == 0 && nblocks > 0) issue_s(0);
+  // blocks 0 and 1's K and block 0's V before the loop
+  if (row_thread) {
+    stage(kh, sK0, 0);
+    stage(vh, sV0, 0);
+    stage(kh, sK0, 1);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-  for (int b = 0; b < nblocks; ++b) {
-    const int64_t key0 = (int64_t)b * BN;
-    // S(b + 1) behind S(b) and O += P(b - 1) V(b - 1): its K landed before the last
-    // barrier, and its TMEM buffer's last reader (the softmax of b - 1) passed it
-    if (tid == 0 && b + 1 < nblocks) issue_s(b + 1);
-    // S(b) done.  mbar[x] takes every other block's commit, and no commit of
-    // block b + 2 can come before all threads passed this wait (it follows the
-    // barrier at the end of this block), so the phase parity is unambiguous
-    if (!tc_wait(tc_su32(&mbar[b & 1]), (uint32_t)((b >> 1) & 1), args.max_polls, args.status)) {
-      ok = false;
-      atomicOr(args.status, DEV_TIMEOUT);
+  if (!row_thread) {
+    // The issuing warp.  Tensor-core order: S(0), S(1), then per block b,
+    // once the row threads have finished it (named barrier 1: P(b) written,
+    // S(b) read, O rescaled, V(b) and K(b + 2) landed), O += P(b) V(b) and
+    // S(b + 2) into the score buffer S(b) used.
+    if (lane == 0 && nblocks > 0) {
+      issue_s(0);
+      if (nblocks > 1) issue_s(1);
     }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // the K buffer S(b) read is free: block b + 2's K into it
-    stage(kh, sK0, b + 2);
-
-    // this row's 64 scores; the valid prefix of the block for this row
-    float sc[BN];
-    tc_ld64(t_s + lane_off + (uint32_t)((b & 1) * BN), sc);
-    const int64_t nv64 = jmax - key0 + 1;
-    const int nv = nv64 < 0 ? 0 : (nv64 > BN ? BN : (int)nv64);
-    if (nv < BN) {
-#pragma unroll
-      for (int i = 0; i < BN; ++i)
-        if (i >= nv) sc[i] = neg_inf();
+    __syncwarp();
+    for (int b = 0; b < nblocks; ++b) {
+      asm volatile("barrier.sync.aligned 1, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (lane == 0) {
+        issue_pv(b);
+        if (b + 2 < nblocks) issue_s(b + 2);
+      }
+      __syncwarp();
     }
-    // block maximum (four chains of three-input max), in scaled base-2 units
-    float mx4[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) mx4[j] = fmaxf(sc[2 * j], sc[2 * j + 1]);
-#pragma unroll
-    for (int i = 8; i < BN; i += 8)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mx4[j] = max3(mx4[j], sc[i + 2 * j], sc[i + 2 * j + 1]);
-    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
-    // move the reference only when needed (see the header); alpha rescales l and O
-    float alpha = 1.0f;
-    if (mx > m_ref + 8.0f) {
-      alpha = m_ref == neg_inf() ? 0.0f : ex2_full(m_ref - mx);
-      m_ref = mx;
-    }
-    const float nsub = m_ref == neg_inf() ? 0.0f : -m_ref;
-    // p = 2^(s cs - m_ref) (pairs by one f32x2 FMA), packed to the input type;
-    // two f32x2 partial sums
-    uint32_t pk2[BN / 2];
-    const unsigned long long cs2 = pk(cs, cs), ns2 = pk(nsub, nsub);
-    unsigned long long acc2[2] = {0ull, 0ull};
-#pragma unroll
-    for (int i = 0; i < BN; i += 2) {
-      const unsigned long long e = fma2(pk(sc[i], sc[i + 1]), cs2, ns2);
-      const float p0 = ex2_ftz(pk_lo(e)), p1 = ex2_ftz(pk_hi(e));
-      acc2[(i >> 1) & 1] = add2(acc2[(i >> 1) & 1], pk(p0, p1));
-      pk2[i / 2] = pack2<T>(p0, p1);
-    }
-    const float ps = (pk_lo(acc2[0]) + pk_hi(acc2[0])) + (pk_lo(acc2[1]) + pk_hi(acc2[1]));
-    l = __fmaf_rn(l, alpha, ps);
-
-    // O += P(b - 1) V(b - 1) finished: P, O and that V buffer may be
-    // rewritten; block b + 1's V into the buffer
-    if (b > 0) {
-      if (!tc_wait(tc_su32(&mbar[2]), (uint32_t)((b - 1) & 1), args.max_polls, args.status)) {
+  } else {
+    for (int b = 0; b < nblocks; ++b) {
+      const int64_t key0 = (int64_t)b * BN;
+      // S(b) done.  mbar[x] takes every other block's commit, and S(b + 2)
+      // is issued only after every row thread finished block b (so after
+      // this wait): the phase parity is unambiguous
+      if (!tc_wait(tc_su32(&mbar[b & 1]), (uint32_t)((b >> 1) & 1), args.max_polls, args.status)) {
         ok = false;
         atomicOr(args.status, DEV_TIMEOUT);
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    }
-    stage(vh, sV0, b + 1);
-    // P row into shared memory, 8 keys (16 bytes) at a time
-#pragma unroll
-    for (int c = 0; c < BN; c += 8)
-      *reinterpret_cast<uint4*>(sP + tc_off(tid, c, BM)) =
-          make_uint4(pk2[c / 2], pk2[c / 2 + 1], pk2[c / 2 + 2], pk2[c / 2 + 3]);
-    // TMEM loads and stores are warp-collective: a warp rescales when any of
-    // its rows must (the others multiply by 1, exactly)
-    if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        float t16[16];
-        tc_ld16(t_o + lane_off + (uint32_t)c, t16);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) t16[i] *= alpha;
-        tc_st16(t_o + lane_off + (uint32_t)c, t16);
-      }
-    }
-    // P written; block b + 2's K and block b's V landed (block b + 1's V, the
-    // newest group, may still be in flight)
-    sync_async(std::integral_constant<int, 1>());
+      // the K buffer S(b) read is free: block b + 2's K into it
+      stage(kh, sK0, b + 2);
 
-    // O += P V: BN / 16 steps of K = 16 over the block's keys (two 8-key
-    // groups of V, 2048 bytes, a step); committed to mbar[2]
-    if (tid == 0) {
-      const uint32_t vbase = tc_su32(sV0 + (b & 1) * KT);
+      // this row's 64 scores; the valid prefix of the block for this row
+      float sc[BN];
+      tc_ld64(t_s + lane_off + (uint32_t)((b & 1) * BN), sc);
+      const int64_t nv64 = jmax - key0 + 1;
+      const int nv = nv64 < 0 ? 0 : (nv64 > BN ? BN : (int)nv64);
+      if (nv < BN) {
 #pragma unroll
-      for (int s2 = 0; s2 < BN / 16; ++s2) {
-        const uint32_t koff = (uint32_t)((s2 & 3) * 32);
-        const uint64_t da = tc_sdesc(tc_su32(sP) + (uint32_t)((s2 >> 2) * BM * 128) + koff);
-        const uint64_t db = tc_sdesc_mn(vbase + (uint32_t)(s2 * 2048), (uint32_t)(BN * 128));
-        tc_mma(t_o, da, db, id_o, (b > 0 || s2 > 0) ? 1u : 0u);
+        for (int i = 0; i < BN; ++i)
+          if (i >= nv) sc[i] = neg_inf();
       }
-      tc_commit(tc_su32(&mbar[2]));
+      // block maximum (four chains of three-input max), in scaled base-2 units
+      float mx4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx4[j] = fmaxf(sc[2 * j], sc[2 * j + 1]);
+#pragma unroll
+      for (int i = 8; i < BN; i += 8)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx4[j] = max3(mx4[j], sc[i + 2 * j], sc[i + 2 * j + 1]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
+      // move the reference only when needed (see the header); alpha rescales l and O
+      float alpha = 1.0f;
+      if (mx > m_ref + 8.0f) {
+        alpha = m_ref == neg_inf() ? 0.0f : ex2_full(m_ref - mx);
+        m_ref = mx;
+      }
+      const float nsub = m_ref == neg_inf() ? 0.0f : -m_ref;
+      // p = 2^(s cs - m_ref) (pairs by one f32x2 FMA), packed to the input type;
+      // two f32x2 partial sums
+      uint32_t pk2[BN / 2];
+      const unsigned long long cs2 = pk(cs, cs), ns2 = pk(nsub, nsub);
+      unsigned long long acc2[2] = {0ull, 0ull};
+#pragma unroll
+      for (int i = 0; i < BN; i += 2) {
+        const unsigned long long e = fma2(pk(sc[i], sc[i + 1]), cs2, ns2);
+        const float p0 = ex2_ftz(pk_lo(e)), p1 = ex2_ftz(pk_hi(e));
+        acc2[(i >> 1) & 1] = add2(acc2[(i >> 1) & 1], pk(p0, p1));
+        pk2[i / 2] = pack2<T>(p0, p1);
+      }
+      const float ps = (pk_lo(acc2[0]) + pk_hi(acc2[0])) + (pk_lo(acc2[1]) + pk_hi(acc2[1]));
+      l = __fmaf_rn(l, alpha, ps);
+
+      // O += P(b - 1) V(b - 1) finished: P, O and that V buffer may be
+      // rewritten; block b + 1's V into the buffer
+      if (b > 0) {
+        if (!tc_wait(tc_su32(&mbar[2]), (uint32_t)((b - 1) & 1), args.max_polls, args.status)) {
+          ok = false;
+          atomicOr(args.status, DEV_TIMEOUT);
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      }
+      stage(vh, sV0, b + 1);
+      // P row into shared memory, 8 keys (16 bytes) at a time
+#pragma unroll
+      for (int c = 0; c < BN; c += 8)
+        *reinterpret_cast<uint4*>(sP + tc_off(tid, c, BM)) =
+            make_uint4(pk2[c / 2], pk2[c / 2 + 1], pk2[c / 2 + 2], pk2[c / 2 + 3]);
+      // TMEM loads and stores are warp-collective: a warp rescales when any of
+      // its rows must (the others multiply by 1, exactly)
+      if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float t16[16];
+          tc_ld16(t_o + lane_off + (uint32_t)c, t16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t16[i] *= alpha;
+          tc_st16(t_o + lane_off + (uint32_t)c, t16);
+        }
+      }
+      // P written; block b + 2's K and block b's V landed (block b + 1's V,
+      // the newest group, may still be in flight); hand the block to the
+      // issuing warp without waiting for it
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      asm volatile("barrier.arrive.aligned 1, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
     }
+    // the last O += P V (mbar[2] is at most one phase ahead of any row's wait)
+    if (nblocks > 0 && !tc_wait(tc_su32(&mbar[2]), (uint32_t)((nblocks - 1) & 1), args.max_polls, args.status))
+      ok = false;
   }
-  // the last O += P V
-  if (nblocks > 0 && !tc_wait(tc_su32(&mbar[2]), (uint32_t)((nblocks - 1) & 1), args.max_polls, args.status))
-    ok = false;
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (!ok) atomicOr(args.status, DEV_TIMEOUT);
 
   // o = O / l in the input type; LSE = m ln 2 + log l; the empty row: 0, -inf.
-  // The TMEM loads are warp-collective, so every thread loads; rows past the
-  // end store nothing.
+  // The TMEM loads are warp-collective, so every row thread loads; rows past
+  // the end store nothing.
   const float inv = l > 0.0f ? recip_refined(l) : 0.0f;
   T* orow = o + (head * a.sq + (qi < a.sq ? qi : 0)) * D;
+  if (row_thread) {
 #pragma unroll
-  for (int c = 0; c < D; c += 16) {
-    float t16[16];
-    if (nblocks > 0) {
-      tc_ld16(t_o + lane_off + (uint32_t)c, t16);
-    } else {
+    for (int c = 0; c < D; c += 16) {
+      float t16[16];
+      if (nblocks > 0) {
+        tc_ld16(t_o + lane_off + (uint32_t)c, t16);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) t16[i] = 0.0f;
-    }
-    if (qi < a.sq) {
-      uint4 w0, w1;
-      w0.x = pack2<T>(t16[0] * inv, t16[1] * inv);
-      w0.y = pack2<T>(t16[2] * inv, t16[3] * inv);
-      w0.z = pack2<T>(t16[4] * inv, t16[5] * inv);
-      w0.w = pack2<T>(t16[6] * inv, t16[7] * inv);
-      w1.x = pack2<T>(t16[8] * inv, t16[9] * inv);
-      w1.y = pack2<T>(t16[10] * inv, t16[11] * inv);
-      w1.z = pack2<T>(t16[12] * inv, t16[13] * inv);
-      w1.w = pack2<T>(t16[14] * inv, t16[15] * inv);
-      *reinterpret_cast<uint4*>(orow + c) = w0;
-      *reinterpret_cast<uint4*>(orow + c + 8) = w1;
+        for (int i = 0; i < 16; ++i) t16[i] = 0.0f;
+      }
+      if (qi < a.sq) {
+        uint4 w0, w1;
+        w0.x = pack2<T>(t16[0] * inv, t16[1] * inv);
+        w0.y = pack2<T>(t16[2] * inv, t16[3] * inv);
+        w0.z = pack2<T>(t16[4] * inv, t16[5] * inv);
+        w0.w = pack2<T>(t16[6] * inv, t16[7] * inv);
+        w1.x = pack2<T>(t16[8] * inv, t16[9] * inv);
+        w1.y = pack2<T>(t16[10] * inv, t16[11] * inv);
+        w1.z = pack2<T>(t16[12] * inv, t16[13] * inv);
+        w1.w = pack2<T>(t16[14] * inv, t16[15] * inv);
+        *reinterpret_cast<uint4*>(orow + c) = w0;
+        *reinterpret_cast<uint4*>(orow + c + 8) = w1;
+      }
     }
   }
-  if (qi < a.sq && lse != nullptr) lse[head * a.sq + qi] = l > 0.0f ? __fmaf_rn(m_ref, LN2, logf(l)) : neg_inf();
+  if (row_thread && qi < a.sq && lse != nullptr)
+    lse[head * a.sq + qi] = l > 0.0f ? __fmaf_rn(m_ref, LN2, logf(l)) : neg_inf();
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0) {
