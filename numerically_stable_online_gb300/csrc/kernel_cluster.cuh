@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
           float f[V];
           staged_vec<InT, V>(sx, vi, v_full, c0 + (int64_t)vi * V, L, f);
 #pragma unroll
-          for (int i = 0; i < V; ++i) f[i] = exp_shift_accurate(f[i], m_c);
+          for (int i = 0; i < V; i += 2) exp_shift_accurate2(f[i], f[i + 1], m_c, f[i], f[i + 1]);
           *reinterpret_cast<float4*>(se + (int64_t)vi * V) = make_float4(f[0], f[1], f[2], f[3]);
           sum = __fadd_rn(sum, __fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])));
         }
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
 #pragma unroll
       for (int k = 0; k < RV; ++k) {
 #pragma unroll
-        for (int i = 0; i < V; ++i) r[k][i] = exp_shift_accurate(r[k][i], m_c);
+        for (int i = 0; i < V; i += 2) exp_shift_accurate2(r[k][i], r[k][i + 1], m_c, r[k][i], r[k][i + 1]);
         sum = __fadd_rn(sum, __fadd_rn(__fadd_rn(r[k][0], r[k][1]), __fadd_rn(r[k][2], r[k][3])));
       }
     } else if (m_c != neg_inf()) {
@@ -370,8 +370,9 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < V; ++i) pv[i] = valid_vec ? __fmul_rn(f[i], scale_c) : 0.0f;
           } else {
+            out_values<OutT, V>(f, kc, pv);
 #pragma unroll
-            for (int i = 0; i < V; ++i) pv[i] = valid_vec ? out_value<OutT>(f[i], kc) : 0.0f;
+            for (int i = 0; i < V; ++i) pv[i] = valid_vec ? pv[i] : 0.0f;
           }
         } else {
           const int64_t e0 = c0 + (int64_t)vi * V;

@@ -45,7 +45,7 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 }
 
 template <typename InT, typename OutT, int MODE, int VPT, int DEPTH>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
     k_rows_split(const InT* __restrict__ x, OutT* __restrict__ y, SplitArgs a,
                  const int32_t* __restrict__ valid_len) {
   static_assert(MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE, "modes of the split");
@@ -266,8 +266,7 @@ __global__ void __launch_bounds__(256)
           if (e0 < len) {
             float q[V];
             if (!zero_out && !nan_out) {
-#pragma unroll
-              for (int i = 0; i < V; ++i) q[i] = out_value<OutT>(v[j][i], kc);
+              out_values<OutT, V>(v[j], kc, q);
             } else {
 #pragma unroll
               for (int i = 0; i < V; ++i) q[i] = (nan_out && e0 + i < L) ? qnan() : 0.0f;

@@ -355,8 +355,7 @@ __global__ void SMX_STREAM_REGS
             if (e0 < len) {
               float p[V];
               if (!zero_out && !nan_out) {
-#pragma unroll
-                for (int i = 0; i < V; ++i) p[i] = out_value<OutT>(v[j][i], kc);
+                out_values<OutT, V>(v[j], kc, p);
               } else {
 #pragma unroll
                 for (int i = 0; i < V; ++i) p[i] = (nan_out && e0 + i < L) ? qnan() : 0.0f;

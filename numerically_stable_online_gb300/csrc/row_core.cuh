@@ -84,7 +84,11 @@ __device__ __forceinline__ float exp_and_sum(float (&v)[VPT][V], float M) {
     for (int j = 0; j < VPT; ++j) {
       float sk[V];
 #pragma unroll
-      for (int i = 0; i < V; ++i) sk[i] = v[j][i] = exp_shift_accurate(v[j][i], M);
+      for (int i = 0; i < V; i += 2) {
+        exp_shift_accurate2(v[j][i], v[j][i + 1], M, v[j][i], v[j][i + 1]);
+        sk[i] = v[j][i];
+        sk[i + 1] = v[j][i + 1];
+      }
 #pragma unroll
       for (int w = V / 2; w > 0; w >>= 1)
 #pragma unroll
@@ -307,6 +311,25 @@ __device__ __forceinline__ float out_value(float x, const OutConst& k) {
   } else {
     const float u = k.huge ? __fmaf_rn(__fsub_rn(x, k.M), L2E_HI, k.c2) : __fmaf_rn(x, L2E_HI, k.c2);
     return __fmul_rn(ex2_ftz(u), k.rD2);
+  }
+}
+
+// out_value of a vector's lanes, two at a time where the arithmetic packs
+// (identical results to the scalar form).
+template <typename OutT, int V>
+__device__ __forceinline__ void out_values(const float (&x)[V], const OutConst& k, float (&q)[V]) {
+  if constexpr (ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE) {
+#pragma unroll
+    for (int i = 0; i < V; i += 2) {
+      float e0, e1;
+      exp_shift_accurate2(x[i], x[i + 1], k.M, e0, e1);
+      const unsigned long long r = mul2(pk(e0, e1), pk(k.rD, k.rD));
+      q[i] = pk_lo(r);
+      q[i + 1] = pk_hi(r);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) q[i] = out_value<OutT>(x[i], k);
   }
 }
 

@@ -188,6 +188,26 @@ __device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigne
   return d;
 }
 
+// exp_shift_accurate for two lanes at once in f32x2 arithmetic.  Every step is
+// the scalar step with each half rounded the same way (a - b as fma(b, -1, a),
+// -u as t * (-L2E_HI): both exact rewrites), so the results are bit-identical
+// to two scalar calls, in about half the instructions.
+__device__ __forceinline__ void exp_shift_accurate2(float x0, float x1, float m, float& e0, float& e1) {
+  const unsigned long long X = pk(x0, x1), NM = pk(-m, -m), N1 = pk(-1.0f, -1.0f);
+  const unsigned long long T = add2(X, NM);          // t = x - m
+  const unsigned long long Z = fma2(X, N1, T);       // z = t - x
+  const unsigned long long TZ = fma2(Z, N1, T);      // t - z
+  const unsigned long long TLO = add2(fma2(TZ, N1, X), fma2(Z, N1, NM));  // (x - (t - z)) + (-m - z)
+  const unsigned long long UN = mul2(T, pk(-L2E_HI, -L2E_HI));           // -u
+  const unsigned long long R = fma2(T, pk(L2E_HI, L2E_HI), UN);          // t L2E_HI - u, exact
+  const unsigned long long C =
+      fma2(R, pk(LN2, LN2), fma2(T, pk(L2E_LO_LN2, L2E_LO_LN2), TLO));
+  const unsigned long long E = pk(ex2_ftz(-pk_lo(UN)), ex2_ftz(-pk_hi(UN)));
+  const unsigned long long RES = fma2(E, C, E);
+  e0 = pk_lo(T) < -110.0f ? 0.0f : pk_lo(RES);
+  e1 = pk_hi(T) < -110.0f ? 0.0f : pk_hi(RES);
+}
+
 // ---------------------------------------------------------------------------
 // Storage types.  A 16-byte vector holds V = 16 / sizeof(T) elements.
 // ---------------------------------------------------------------------------
