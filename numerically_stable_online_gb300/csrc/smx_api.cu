@@ -201,7 +201,9 @@ int max_cluster_size(DeviceInfo& d, int in_dtype) {
   return c;
 }
 
-bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
+// read_heavy: the statistics / LSE and cross-entropy rows, whose per-row
+// reductions dominate; the others write a row per row read.
+bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p, bool read_heavy = false) {
   const int V = 16 / elem_size(in_dtype);
   const int64_t nvec = cols / V;
   // the compensated exponential (fp32 outputs) keeps more live registers per
@@ -215,14 +217,20 @@ bool plan_regs(int64_t cols, int in_dtype, bool accurate_exp, Plan* p) {
     vpt = dbg_v;
     G = dbg_t;
   } else {
-    // measured on GB300: two vectors per thread and 64..256 threads per row
-    // are best; then four, one, eight vectors
-    const int order[4] = {2, 4, 1, 8};
+    // measured on GB300 (CTA shapes per mode over bf16/f16/f32 rows of 1K-8K
+    // elements): rows that write an output are fastest with two vectors per
+    // thread and 64..512 threads, then four, one, eight vectors; the
+    // read-heavy rows with four vectors per thread and 64..256 threads (fewer
+    // threads per row: cheaper reductions), then two, eight, one
+    const int order_w[4] = {2, 4, 1, 8}, order_r[4] = {4, 2, 8, 1};
+    const int* order = read_heavy ? order_r : order_w;
+    const int64_t g_hi = read_heavy ? 256 : 512;
     for (int pass = 0; pass < 2 && vpt == 0; ++pass) {
-      for (int v : order) {
+      for (int k = 0; k < 4; ++k) {
+        const int v = order[k];
         if (v > max_vpt) continue;
         const int64_t g = ((nvec + v - 1) / v + 31) / 32 * 32;
-        if (pass == 0 ? (g >= 64 && g <= 256) : g <= 1024) {
+        if (pass == 0 ? (g >= 64 && g <= g_hi) : g <= 1024) {
           vpt = v;
           G = g;
           break;
@@ -278,7 +286,8 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
     while (32LL * r.vpt < nvec) r.vpt <<= 1;
     r.threads = WARP_WALKER_THREADS;
     warp = true;
-  } else if (!plan_regs(cols, in_dtype, accurate_exp, &r) || r.warp_rows) {
+  } else if (!plan_regs(cols, in_dtype, accurate_exp, &r, mode == MODE_STATS || mode == MODE_CE) ||
+             r.warp_rows) {
     r.threads = 64;
     r.vpt = 1;
     while (64LL * r.vpt < nvec) r.vpt <<= 1;
