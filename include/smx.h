@@ -303,15 +303,16 @@ int smx_version(void);
  *   4; 0 = automatic).
  * smx_debug_set_stream_ctas(n): n resident CTAs per SM on path 4, at most as
  *   many as fit (0 = automatic; also path 5).
- * smx_debug_set_split_slab(bytes): slab size of path 5 (0 = half the L2).
+ * smx_debug_set_split_slab(bytes): slab size of path 5 (0 = one slab of all rows).
  * smx_debug_set_inflight(read_only, backward): bytes of reads to keep in flight
  *   per SM (which sets the persistent CTAs per SM) for the read-only
  *   statistics / LSE rows and for the backward (0 = default).
  * smx_debug_set_stream_warp(off): 1 = path 4 walks every row with a whole CTA;
  *   0 = rows that fit one warp are walked a row per warp (default).
- * smx_debug_set_split_fused(off): 1 = path 5 runs two launches per slab (the
- *   statistics pass, then the normalising pass); 0 = one cooperative launch for
- *   all slabs with per-row completion counts (default where supported).
+ * smx_debug_set_split_fused(on): 1 = path 5 runs one cooperative launch for
+ *   all slabs with per-row completion counts (where supported); 0 = two
+ *   launches per slab, the statistics pass and then the normalising pass
+ *   (default).
  * smx_debug_set_attention_mma_sync(on): 1 = the attention forward runs on the
  *   mma.sync kernel (warp-level tensor-core instructions) instead of the
  *   tcgen05/TMEM kernel (default).
@@ -334,7 +335,7 @@ void smx_debug_set_cluster_staging(int mode);
 void smx_debug_set_split_slab(int64_t bytes);
 void smx_debug_set_split_hints(int stats, int apply);
 void smx_debug_set_stream_warp(int off);
-void smx_debug_set_split_fused(int off);
+void smx_debug_set_split_fused(int on);
 void smx_debug_set_attention_mma_sync(int on);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 

@@ -12,8 +12,8 @@
 //      (release: a device fence, then the atomics);
 //   B  for each row it meets, thread 0 waits (acquire, bounded) until the row's
 //      count reaches the number of chunks, the CTA merges the row's summaries
-//      and normalises its chunks of the row, re-reading them from L2 (a slab
-//      is about half the L2).
+//      and normalises its chunks of the row, re-reading them (from L2 when
+//      the slab fits there).
 // The cp.async prefetch ring (kernel_stream.cuh) runs straight through the
 // phase and slab changes, so phase B's first chunks are in flight while the
 // CTA waits.  Phase A never waits, so with every CTA resident (a cooperative

@@ -224,7 +224,7 @@ cudaError_t launch_split_fused(const Call& c, const Plan& p) {
   a.rows = c.rows;
   a.cols = c.cols;
   a.nchunks = p.nchunks;
-  a.slab = p.slab_rows;
+  a.slab = p.slab_rows < c.rows ? p.slab_rows : c.rows;
   a.ms = reinterpret_cast<float*>(base);
   a.ds = a.ms + n_sum;
   a.count = reinterpret_cast<unsigned*>(a.ds + n_sum);
@@ -303,7 +303,8 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
     // every element once: one slab of all rows
     const bool read_once = (MODE == MODE_STATS || (MODE == MODE_CE && c.y == nullptr)) &&
                            c.rows * p.nchunks <= ((int64_t)1 << 31) && p.scratch == nullptr;
-    const int64_t slab = read_once ? c.rows : p.slab_rows;
+    // a slab is never more rows than the call has (the scratch is sized by it)
+    const int64_t slab = (read_once || p.slab_rows > c.rows) ? c.rows : p.slab_rows;
     const size_t part_n = (size_t)slab * p.nchunks;
     const size_t bytes = split_scratch_bytes(slab, p.nchunks);
     char* base = reinterpret_cast<char*>(p.scratch);
@@ -412,7 +413,7 @@ cudaError_t launch_backward(const Call& c, const Plan& p) {
   }
   if (p.path != PATH_SPLIT) return cudaErrorInvalidValue;
   // long rows: per slab, the chunks' partial dots, then dx per chunk
-  const int64_t slab = p.slab_rows;
+  const int64_t slab = p.slab_rows < c.rows ? p.slab_rows : c.rows;  // sizes the scratch
   const size_t bytes = (size_t)slab * p.nchunks * sizeof(float);
   char* base = reinterpret_cast<char*>(p.scratch);
   cudaError_t e = cudaSuccess;

@@ -13,8 +13,8 @@
 #include "smx_launch.h"
 
 // Scratch of smx_softmax_rows_fixed_scratch: 2 floats per chunk, 32768 chunks
-// of one slab (256 KiB).  A default slab (half the L2) holds well under 8192
-// chunks of 4096 elements.
+// of one slab (256 KiB); larger slabs are cut to fit (a 4 MiB fp32 row is 256
+// chunks, so a slab holds 128 such rows).
 constexpr int64_t FIXED_SCRATCH_FLOATS = 65536;
 static __device__ __align__(256) float g_fixed_scratch[FIXED_SCRATCH_FLOATS];
 
@@ -318,9 +318,9 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
   return true;
 }
 
-// Long rows in slabs of about half the L2 (the statistics pass leaves the slab
-// in L2 for the normalising pass's re-read), chunks of 16 elements per thread of
-// 256-thread CTAs, on the streamed kernel.
+// Long rows: chunks of 16 elements per thread of 256-thread CTAs on the
+// streamed kernel, the statistics of every chunk of a slab of rows, then the
+// merge and the normalising pass over the same slab.
 bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
   const int es = elem_size(in_dtype);
   const int V = 16 / es;
@@ -329,12 +329,17 @@ bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
   const int64_t chunk = (int64_t)threads * vpt * V;
   const int64_t nchunks = (cols + chunk - 1) / chunk;
   if (nchunks > ((int64_t)1 << 30)) return false;
-  int64_t slab_bytes = d.l2_bytes / 2;
+  // one slab of all rows by default: the normalising pass re-reads the input
+  // from DRAM.  Measured on GB300 (64 rows of 4 MiB): slabs of up to half the
+  // L2, which the second pass re-reads from L2, were slower (160 us against
+  // 142 us) -- every slab costs a drain of both passes, more than the re-read
+  // from DRAM saves
+  int64_t slab_bytes = INT64_MAX;
   const int64_t dbg = g_split_slab_bytes.load();
   if (dbg > 0) slab_bytes = dbg;
   int64_t slab = slab_bytes / (cols * es);
   if (slab < 1) slab = 1;
-  if (slab * nchunks > ((int64_t)1 << 31)) slab = ((int64_t)1 << 31) / nchunks;
+  if (slab > ((int64_t)1 << 31) / nchunks) slab = ((int64_t)1 << 31) / nchunks;
   const int occ_max = cached_query(occ_key(3, in_dtype, (uint64_t)threads), [&] {
     switch (in_dtype) {
       case SMX_F32: return split_occupancy_f32(threads);
@@ -354,8 +359,10 @@ bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
   p->chunk = chunk;
   p->nchunks = (int)nchunks;
   p->slab_rows = slab;
-  // one cooperative launch when the device supports it: every CTA resident
-  if (g_split_fused.load() == 0 && d.coop) {
+  // one cooperative launch (every CTA resident; per-row completion counts
+  // between the passes) when asked for and supported: measured on GB300 it
+  // is not faster than two launches over one slab (153 us against 142 us)
+  if (g_split_fused.load() != 0 && d.coop) {
     const int fo = cached_query(occ_key(4, in_dtype, (uint64_t)threads), [&] {
       switch (in_dtype) {
         case SMX_F32: return split_fused_occupancy_f32(threads);
@@ -461,12 +468,14 @@ void plan_backward(DeviceInfo& d, const Call& c, bool vec_ok, Plan* p) {
   int occ = occ_max;
   const int forced = g_stream_ctas_per_sm.load();
   if (forced > 0) occ = forced < occ_max ? forced : occ_max;
-  int64_t slab_bytes = d.l2_bytes / 2;
+  // one slab of all rows by default, as for the softmax (measured on GB300,
+  // 64 rows of 4 MiB: 215 us against 232 us with slabs of half the L2)
+  int64_t slab_bytes = INT64_MAX;
   const int64_t dbg = g_split_slab_bytes.load();
   if (dbg > 0) slab_bytes = dbg;
   int64_t slab = slab_bytes / (2 * row_bytes);
   if (slab < 1) slab = 1;
-  if (slab * nchunks > ((int64_t)1 << 31)) slab = ((int64_t)1 << 31) / nchunks;
+  if (slab > ((int64_t)1 << 31) / nchunks) slab = ((int64_t)1 << 31) / nchunks;
   p->path = PATH_SPLIT;
   p->threads = threads;
   p->vpt = vpt;
@@ -950,7 +959,7 @@ void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes) {
 
 void smx_debug_set_stream_warp(int off) { g_stream_warp.store(off ? 1 : 0); }
 
-void smx_debug_set_split_fused(int off) { g_split_fused.store(off ? 1 : 0); }
+void smx_debug_set_split_fused(int on) { g_split_fused.store(on ? 1 : 0); }
 
 void smx_debug_set_attention_mma_sync(int on) { g_attention_mma_sync.store(on ? 1 : 0); }
 

@@ -512,8 +512,8 @@ def test_stream_walkers(lib, cols, in_dtype, out_dtype, warp_off):
 @pytest.mark.parametrize("in_dtype,out_dtype,rows,cols,slab", [
     ("f32", "f32", 7, 300_000, 2 << 20), ("bf16", "bf16", 9, 150_000, 1 << 20),
     ("f16", "f32", 5, 40_000, 64 << 10), ("bf16", "f16", 33, 12_288, 96 << 10)])
-@pytest.mark.parametrize("fused_off", [0, 1])
-def test_long_rows_one_launch_and_two(lib, in_dtype, out_dtype, rows, cols, slab, fused_off):
+@pytest.mark.parametrize("fused", [1, 0])
+def test_long_rows_one_launch_and_two(lib, in_dtype, out_dtype, rows, cols, slab, fused):
     """Path 5 as one cooperative launch over all slabs (per-row completion
     counts) and as two launches per slab, with small slabs so that many slabs
     and chunk ranges that straddle rows occur; lengths include 0 and 1."""
@@ -524,11 +524,11 @@ def test_long_rows_one_launch_and_two(lib, in_dtype, out_dtype, rows, cols, slab
     vl[-1] = cols
     lib.smx_debug_force_path(PATH_SPLIT)
     lib.smx_debug_set_split_slab(slab)
-    lib.smx_debug_set_split_fused(fused_off)
+    lib.smx_debug_set_split_fused(fused)
     xt = to_device(x, in_dtype, rows, cols)
     smx.softmax_rows(xt, valid_len=torch.from_numpy(vl).to(DEV), out_dtype=DT[out_dtype])
     slab_rows = max(1, slab // (cols * (4 if in_dtype == "f32" else 2)))
     assert lib.smx_debug_last_path() == PATH_SPLIT
-    assert lib.smx_debug_last_launches() == (1 if not fused_off else 2 * -(-rows // slab_rows))
+    assert lib.smx_debug_last_launches() == (1 if fused else 2 * -(-rows // slab_rows))
     assert smx.last_device_status() == 0
     run_and_compare(x, in_dtype, out_dtype, rows, cols, vl)
