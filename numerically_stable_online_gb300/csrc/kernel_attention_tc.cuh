@@ -11,26 +11,28 @@
 // exchange; a fifth warp issues the products.
 // Operands sit in shared memory with the 128-byte swizzle (8-row atoms of
 // 1024 bytes; 16-byte chunks XOR-ed with the row), all tiles in one layout:
-// rows of 64 16-bit elements.  Q, K and P (written by the row threads) are
-// K-major operands; V, staged as stored ([key][head dim]), is the second
-// product's B operand in MN-major form, so nothing is transposed.
+// rows of 64 16-bit elements.  Q and K are K-major operands; V, staged as
+// stored ([key][head dim]), is the second product's B operand in MN-major
+// form, so nothing is transposed.  P (the input type) stays in tensor memory:
+// each row thread writes its packed row over the first 32 columns of the
+// score tile it has just read, and the second product takes A from there.
 //
-// Pipeline, per key block b: S(b + 1) is issued (two S buffers in TMEM, two K
-// and two V buffers in shared memory) before the row threads take S(b), so
-// the tensor core computes the next scores and the previous O += P V while
-// the rows compute this block's exponentials.  Each row thread masks its 64
-// scores, updates (m, l), and only then waits for the previous O += P V
-// before it writes P (the input type) to shared memory and, when its
-// reference maximum has to move, rescales its O row in TMEM; it then arrives
-// (without waiting) on a named barrier, on which the issuing warp waits
-// before it issues O += P V and the scores two blocks ahead.  K and V of
-// later blocks are copied by cp.async as soon as their buffers are free.
-// The reference maximum moves only when the block's maximum exceeds it by
-// more than 8 (base-2 units): the exponentials then stay below 2^8, and l and
-// o always share one reference, so the result is the same quotient (the
-// rescale is exact bookkeeping, not an approximation).  Two CTAs share an SM
-// (shared memory 113 KiB and 256 TMEM columns each) so that one's softmax
-// overlaps the other's products.
+// Pipeline, per key block b: S(b + 1) is already issued (two S tiles in TMEM,
+// two K and three V buffers in shared memory) when the row threads take
+// S(b), so the tensor core computes the next scores and the previous
+// O += P V while the rows compute this block's exponentials.  Each row thread
+// masks its 64 scores, updates (m, l), writes P, and -- only when its
+// reference maximum has to move -- waits for the previous O += P V and
+// rescales its O row in TMEM; it then arrives (without waiting) on a named
+// barrier, on which the issuing warp waits before it issues O += P V and the
+// scores two blocks ahead.  K and V of later blocks are copied by cp.async as
+// soon as their buffers are free (known from S(b): one thread's products
+// finish in issue order).  The reference maximum moves only when the block's
+// maximum exceeds it by more than 8 (base-2 units): the exponentials then
+// stay below 2^8, and l and o always share one reference, so the result is
+// the same quotient (the rescale is exact bookkeeping, not an
+// approximation).  Two CTAs share an SM (shared memory 113 KiB and 256 TMEM
+// columns each) so that one's softmax overlaps the other's products.
 // Every mbarrier wait is bounded; running out records SMX_ERR_TIMEOUT in the
 // device status word.
 #pragma once
@@ -45,12 +47,12 @@ constexpr int ATT_TC_BM = 128;  // query rows per CTA (one per thread, one per T
 constexpr int ATT_TC_BN = 64;   // keys per block
 constexpr int ATT_TC_THREADS = 128;                 // row threads (warps 0-3)
 constexpr int ATT_TC_BLOCK = ATT_TC_THREADS + 32;   // plus one warp that issues the products
-// shared memory of the operand tiles: Q [128][D], K [2][64][D], V [2][64][D],
-// P [128][64] (16-bit elements); the launch adds 1024 bytes so that the tiles
-// can start on a 1024-byte boundary, and the barriers live in that slack
+// shared memory of the operand tiles: Q [128][D], K [2][64][D], V [3][64][D]
+// (16-bit elements); the launch adds 1024 bytes so that the tiles can start on
+// a 1024-byte boundary, and the barriers live in that slack
 template <int D>
 __host__ __device__ constexpr int att_tc_tile_bytes() {
-  return (ATT_TC_BM * D + 4 * ATT_TC_BN * D + ATT_TC_BM * ATT_TC_BN) * 2;
+  return (ATT_TC_BM * D + 5 * ATT_TC_BN * D) * 2;
 }
 
 struct AttnTcArgs {
@@ -101,6 +103,16 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t da, uint64_t db
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(da), "l"(db), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// the same with the A operand in tensor memory: M rows in the lanes, K
+// 16-bit elements packed two to a 32-bit column (element 2c in the low half)
+__device__ __forceinline__ void tc_mma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t db, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(db), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint32_t mbar) {
@@ -173,6 +185,20 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// 32 consecutive columns of this warp's 32 lanes from registers; the wait is
+// part of the same statement
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
+      "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -205,7 +231,7 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   const T* kh = k + head * a.sk * D;
   const T* vh = v + head * a.sk * D;
 
-  // 1024-aligned operand tiles: Q [BM][D], K [2][BN][D], V [2][BN][D], P [BM][BN]
+  // 1024-aligned operand tiles: Q [BM][D], K [2][BN][D], V [3][BN][D]
   const uint32_t raw = tc_su32(smem_raw);
   const uint32_t pad = (1024 - (raw & 1023)) & 1023;
   uint8_t* base = smem_raw + pad;
@@ -213,13 +239,12 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   uint8_t* sK0 = sQ + BM * D * 2;
   constexpr int KT = BN * D * 2;  // bytes of one K or V tile
   uint8_t* sV0 = sK0 + 2 * KT;
-  uint8_t* sP = sV0 + 2 * KT;
-  // three mbarriers (S of even / odd key blocks; O += P V) and the TMEM
-  // address: in the alignment gap when it has room, else after the tiles
-  // (the launch's 1024 spare bytes hold the gap plus these 28 bytes)
-  uint8_t* aux = pad >= 32 ? smem_raw : base + att_tc_tile_bytes<D>();
+  // four mbarriers (S of even / odd key blocks; O += P V; the last O += P V)
+  // and the TMEM address: in the alignment gap when it has room, else after
+  // the tiles (the launch's 1024 spare bytes hold the gap plus these 36 bytes)
+  uint8_t* aux = pad >= 48 ? smem_raw : base + att_tc_tile_bytes<D>();
   uint64_t* mbar = reinterpret_cast<uint64_t*>(aux);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 24);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 32);
 
   int64_t kv_end = a.sk;
   if (a.causal) {
@@ -251,7 +276,7 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   }
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 3; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_su32(mbar + i)) : "memory");
+    for (int i = 0; i < 4; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_su32(mbar + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -271,7 +296,7 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   const int64_t jmax = lim < a.sk - 1 ? lim : a.sk - 1;
   const float cs = a.scale_log2;  // > 0, so the raw maximum scales to the scaled one
 
-  // key block blk of K or V into tile buffer (blk & 1) by cp.async, rows past
+  // key block blk of K or V into tile buffer (blk % nbuf) by cp.async, rows past
   // the keys zero; one commit group each, empty past the last block (so the
   // group count per block is fixed).  V keeps its stored layout: it is the
   // second product's B operand in MN-major form (N = head dimension).
@@ -283,10 +308,10 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   constexpr int NU = BN / RS;                  // passes a tile
   const int r0 = tid / CPR, c0 = (tid % CPR) * 8;
   const uint32_t soff = tc_off(r0, c0, BN);
-  auto stage = [&](const T* src, uint8_t* tiles, int blk) {
+  auto stage = [&](const T* src, uint8_t* tiles, int nbuf, int blk) {
     if (blk < nblocks) {
       const int64_t key0 = (int64_t)blk * BN;
-      const uint32_t dst = tc_su32(tiles + (blk & 1) * KT) + soff;
+      const uint32_t dst = tc_su32(tiles + (blk % nbuf) * KT) + soff;
       const T* g = src + (key0 + r0) * D + c0;
       if (key0 + BN <= a.sk) {
 #pragma unroll
@@ -317,25 +342,27 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
     }
     tc_commit(tc_su32(&mbar[blk & 1]));
   };
-  // O += P(blk) V(blk): BN / 16 steps of K = 16 over the block's keys (two
-  // 8-key groups of V, 2048 bytes, a step); committed to mbar[2]
+  // O += P(blk) V(blk): BN / 16 steps of K = 16 over the block's keys, P from
+  // the first BN / 2 columns of the block's TMEM score tile (8 columns a
+  // step), V (buffer blk % 3) two 8-key groups, 2048 bytes, a step; committed
+  // to mbar[2], and the last block's also to mbar[3]
   auto issue_pv = [&](int blk) {
-    const uint32_t vbase = tc_su32(sV0 + (blk & 1) * KT);
+    const uint32_t vbase = tc_su32(sV0 + (blk % 3) * KT);
+    const uint32_t pbase = t_s + (uint32_t)((blk & 1) * BN);
 #pragma unroll
     for (int s2 = 0; s2 < BN / 16; ++s2) {
-      const uint32_t koff = (uint32_t)((s2 & 3) * 32);
-      const uint64_t da = tc_sdesc(tc_su32(sP) + (uint32_t)((s2 >> 2) * BM * 128) + koff);
       const uint64_t db = tc_sdesc_mn(vbase + (uint32_t)(s2 * 2048), (uint32_t)(BN * 128));
-      tc_mma(t_o, da, db, id_o, (blk > 0 || s2 > 0) ? 1u : 0u);
+      tc_mma_ta(t_o, pbase + (uint32_t)(s2 * 8), db, id_o, (blk > 0 || s2 > 0) ? 1u : 0u);
     }
     tc_commit(tc_su32(&mbar[2]));
+    if (blk == nblocks - 1) tc_commit(tc_su32(&mbar[3]));
   };
 
   // blocks 0 and 1's K and block 0's V before the loop
   if (row_thread) {
-    stage(kh, sK0, 0);
-    stage(vh, sV0, 0);
-    stage(kh, sK0, 1);
+    stage(kh, sK0, 2, 0);
+    stage(vh, sV0, 3, 0);
+    stage(kh, sK0, 2, 1);
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -345,16 +372,24 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
 
   if (!row_thread) {
     // The issuing warp.  Tensor-core order: S(0), S(1), then per block b,
-    // once the row threads have finished it (named barrier 1: P(b) written,
-    // S(b) read, O rescaled, V(b) and K(b + 2) landed), O += P(b) V(b) and
-    // S(b + 2) into the score buffer S(b) used.
+    // once the row threads have finished it (named barrier 1 + (b & 1): P(b)
+    // in TMEM, O rescaled, V(b) and K(b + 2) landed), O += P(b) V(b) and
+    // S(b + 2) into the score tile that holds P(b).  One thread's products
+    // run in issue order, so S(b + 2) overwrites P(b) only after O += P(b) V(b)
+    // has read it.
     if (lane == 0 && nblocks > 0) {
       issue_s(0);
       if (nblocks > 1) issue_s(1);
     }
     __syncwarp();
     for (int b = 0; b < nblocks; ++b) {
-      asm volatile("barrier.sync.aligned 1, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
+      // named barrier 1 + (b & 1): the row threads can be at most one block
+      // ahead of this warp (they need S(b + 1), issued after the previous
+      // barrier), so two barriers never mix generations
+      if (b & 1)
+        asm volatile("barrier.sync.aligned 2, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
+      else
+        asm volatile("barrier.sync.aligned 1, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (lane == 0) {
         issue_pv(b);
@@ -373,8 +408,11 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
         atomicOr(args.status, DEV_TIMEOUT);
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      // the K buffer S(b) read is free: block b + 2's K into it
-      stage(kh, sK0, b + 2);
+      // S(b) finished, so did every product issued before it: the K buffer
+      // S(b) read takes block b + 2, the V buffer O += P(b - 2) V(b - 2) read
+      // takes block b + 1
+      stage(kh, sK0, 2, b + 2);
+      stage(vh, sV0, 3, b + 1);
 
       // this row's 64 scores; the valid prefix of the block for this row
       float sc[BN];
@@ -416,25 +454,18 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
       }
       const float ps = (pk_lo(acc2[0]) + pk_hi(acc2[0])) + (pk_lo(acc2[1]) + pk_hi(acc2[1]));
       l = __fmaf_rn(l, alpha, ps);
-
-      // O += P(b - 1) V(b - 1) finished: P, O and that V buffer may be
-      // rewritten; block b + 1's V into the buffer
-      if (b > 0) {
+      // TMEM loads and stores are warp-collective: a warp rescales when any of
+      // its rows must (the others multiply by 1, exactly)
+      if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        // O += P(b - 1) V(b - 1) finished first (mbar[2]: S(b) finished, so
+        // every product before it did, O += P(b - 2) V(b - 2) included, and
+        // O += P(b) V(b) waits for this block: its completed phases are b - 1
+        // or b, and the parity names b - 1 alone)
         if (!tc_wait(tc_su32(&mbar[2]), (uint32_t)((b - 1) & 1), args.max_polls, args.status)) {
           ok = false;
           atomicOr(args.status, DEV_TIMEOUT);
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      }
-      stage(vh, sV0, b + 1);
-      // P row into shared memory, 8 keys (16 bytes) at a time
-#pragma unroll
-      for (int c = 0; c < BN; c += 8)
-        *reinterpret_cast<uint4*>(sP + tc_off(tid, c, BM)) =
-            make_uint4(pk2[c / 2], pk2[c / 2 + 1], pk2[c / 2 + 2], pk2[c / 2 + 3]);
-      // TMEM loads and stores are warp-collective: a warp rescales when any of
-      // its rows must (the others multiply by 1, exactly)
-      if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
         for (int c = 0; c < D; c += 16) {
           float t16[16];
@@ -444,17 +475,22 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
           tc_st16(t_o + lane_off + (uint32_t)c, t16);
         }
       }
+      // P(b) over the first columns of the score tile it came from (this
+      // thread's lane; the scores are in registers already)
+      tc_st32(t_s + lane_off + (uint32_t)((b & 1) * BN), pk2);
       // P written; block b + 2's K and block b's V landed (block b + 1's V,
       // the newest group, may still be in flight); hand the block to the
       // issuing warp without waiting for it
       asm volatile("cp.async.wait_group 1;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      asm volatile("barrier.arrive.aligned 1, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
+      if (b & 1)
+        asm volatile("barrier.arrive.aligned 2, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
+      else
+        asm volatile("barrier.arrive.aligned 1, %0;" ::"n"(ATT_TC_BLOCK) : "memory");
     }
-    // the last O += P V (mbar[2] is at most one phase ahead of any row's wait)
-    if (nblocks > 0 && !tc_wait(tc_su32(&mbar[2]), (uint32_t)((nblocks - 1) & 1), args.max_polls, args.status))
-      ok = false;
+    // the last O += P V (its own barrier: mbar[2]'s phases are not all waited)
+    if (nblocks > 0 && !tc_wait(tc_su32(&mbar[3]), 0u, args.max_polls, args.status)) ok = false;
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
