@@ -289,10 +289,12 @@ int smx_version(void);
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
  * smx_debug_set_wait_limit(n): n > 0: polls of a staging barrier (path 2)
- *   before the kernel gives up and records SMX_ERR_TIMEOUT; 0 = default; n < 0:
- *   each CTA of path 2 first waits -n polls on a barrier that nothing signals,
- *   records SMX_ERR_TIMEOUT when that wait runs out (it always does), then
- *   works normally -- a deterministic probe of the error path.
+ *   or of a tensor-core barrier (the tcgen05 attention kernel) before the
+ *   kernel gives up and records SMX_ERR_TIMEOUT; 0 = default; n < 0: each CTA
+ *   of path 2, and of the tcgen05 attention kernel, first waits -n polls on a
+ *   barrier that nothing signals, records SMX_ERR_TIMEOUT when that wait runs
+ *   out (it always does), then works normally -- a deterministic probe of the
+ *   error path.
  * smx_debug_last_path(): the path (1..5) the last softmax/stats call on this
  *   thread used, 0 if none.
  * smx_debug_last_launches(): kernels the last call on this thread launched.

@@ -72,6 +72,7 @@ cudaError_t launch_attention_tc_t(const AttnCall& c) {
   a.a.causal = c.causal;
   a.status = c.status;
   a.max_polls = c.max_polls;
+  a.probe_polls = c.probe_polls;
   const dim3 grid((unsigned)((c.sq + ATT_TC_BM - 1) / ATT_TC_BM), (unsigned)c.heads);
   note_launch();
   kern<<<grid, ATT_TC_BLOCK, (size_t)smem, c.stream>>>(static_cast<const T*>(c.q), static_cast<const T*>(c.k),

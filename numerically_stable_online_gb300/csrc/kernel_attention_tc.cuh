@@ -59,6 +59,8 @@ struct AttnTcArgs {
   AttnArgs a;
   int* status;
   int64_t max_polls;
+  int64_t probe_polls;  // > 0: thread 0 first waits this many polls on a barrier nothing
+                        // signals and records SMX_ERR_TIMEOUT (a probe of the error path)
 };
 
 __device__ __forceinline__ uint32_t tc_su32(const void* p) {
@@ -142,6 +144,25 @@ __device__ __forceinline__ bool tc_wait(uint32_t mbar, uint32_t parity, int64_t 
     }
   }
   return false;
+}
+// Wait for an mbarrier phase bounded by wall time only (200 ms): the drain of
+// the kernel's own asynchronous work before it frees tensor memory, which
+// must end also after another wait has run out.
+__device__ __forceinline__ bool tc_wait_drain(uint32_t mbar, uint32_t parity) {
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 200000000ull) return false;
+  }
 }
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -239,12 +260,13 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   uint8_t* sK0 = sQ + BM * D * 2;
   constexpr int KT = BN * D * 2;  // bytes of one K or V tile
   uint8_t* sV0 = sK0 + 2 * KT;
-  // four mbarriers (S of even / odd key blocks; O += P V; the last O += P V)
-  // and the TMEM address: in the alignment gap when it has room, else after
-  // the tiles (the launch's 1024 spare bytes hold the gap plus these 36 bytes)
-  uint8_t* aux = pad >= 48 ? smem_raw : base + att_tc_tile_bytes<D>();
+  // six mbarriers (S of even / odd key blocks; O += P V; the last O += P V;
+  // the probe's, never signalled; the issuing lane's drain) and the TMEM
+  // address: in the alignment gap when it has room, else after the tiles (the
+  // launch's 1024 spare bytes hold the gap plus these 52 bytes)
+  uint8_t* aux = pad >= 64 ? smem_raw : base + att_tc_tile_bytes<D>();
   uint64_t* mbar = reinterpret_cast<uint64_t*>(aux);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 32);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 48);
 
   int64_t kv_end = a.sk;
   if (a.causal) {
@@ -276,13 +298,17 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
   }
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_su32(mbar + i)) : "memory");
+    for (int i = 0; i < 6; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_su32(mbar + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
+  // the error-path probe: a wait on a barrier nothing signals runs out
+  if (args.probe_polls > 0 && tid == 0 &&
+      !tc_wait(tc_su32(&mbar[4]), 0u, args.probe_polls, args.status))
+    atomicOr(args.status, DEV_TIMEOUT);
   const uint32_t t_o = tmem, t_s = tmem + D;
   // this thread's TMEM lane (its query row) in the warp's 32-lane slice
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -397,6 +423,14 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
       }
       __syncwarp();
     }
+    // every product this lane issued has finished before the tensor memory is
+    // freed (the row threads' waits cover them on the normal path; after a
+    // wait ran out they may not): one more commit, waited by wall time only
+    if (lane == 0 && nblocks > 0) {
+      tc_commit(tc_su32(&mbar[5]));
+      tc_wait_drain(tc_su32(&mbar[5]), 0u);
+    }
+    __syncwarp();
   } else {
     for (int b = 0; b < nblocks; ++b) {
       const int64_t key0 = (int64_t)b * BN;

@@ -871,6 +871,7 @@ smx_status smx_attention_forward(const void* q, const void* k, const void* v, vo
   c.status = dev->status;
   const int64_t wl = g_wait_limit.load();
   c.max_polls = wl > 0 ? wl : ATTN_MAX_POLLS;
+  c.probe_polls = wl < 0 ? -wl : 0;
   c.tensor_memory = g_attention_mma_sync.load() == 0;
   const cudaError_t e = launch_attention(c);
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);

@@ -86,6 +86,7 @@ struct AttnCall {
   cudaStream_t stream;
   int* status = nullptr;   // device status word (bounded waits of the tcgen05 kernel)
   int64_t max_polls = 0;
+  int64_t probe_polls = 0;    // > 0: the tcgen05 kernel's error-path probe (a wait that runs out)
   bool tensor_memory = true;  // tcgen05/TMEM kernel; false: the mma.sync kernel
 };
 cudaError_t launch_attention(const AttnCall& c);

@@ -131,3 +131,26 @@ def test_attention_pages_shape_sampled(causal):
     sel = np.array([remap[int(r // n)] * n + int(r % n) for r in rows])
     check(o[sub], lse[sub], q[sub], k[sub], v[sub], "bf16", len(sub), n, n, d, d ** -0.5, causal,
           rows_sel=sel)
+
+
+def test_attention_timeout_reported_and_context_usable(kernel):
+    """The error path of the tcgen05 kernel: with a negative wait limit one
+    thread per CTA waits on a barrier that nothing signals, the wait runs out
+    and SMX_ERR_TIMEOUT is recorded; every other wait of the launch then stops
+    early (its output is not meaningful), the kernel still lets its own
+    products finish before it frees tensor memory, and the next call on the
+    same context is correct and clean."""
+    if kernel != "tcgen05":
+        pytest.skip("the probe is in the tcgen05 kernel")
+    lib = smx.library()
+    g = torch.Generator(device=DEV).manual_seed(93)
+    q, k, v = (torch.randn(4, n, 128, generator=g, device=DEV).to(torch.bfloat16) for n in (256, 320, 320))
+    lib.smx_debug_set_wait_limit(-2000)
+    try:
+        smx.attention_forward(q, k, v, causal=True)
+        torch.cuda.synchronize()
+    finally:
+        lib.smx_debug_set_wait_limit(0)
+    assert smx.last_device_status() == 5  # SMX_ERR_TIMEOUT
+    run(3, 200, 260, 128, True, "bf16", seed=94)
+    assert smx.last_device_status() == 0
