@@ -284,7 +284,8 @@ int smx_version(void);
  * smx_debug_force_path(p): 0 = automatic choice; 1 = register-resident rows;
  *   2 = thread-block-cluster rows; 3 = generic (scalar, two-pass) rows;
  *   4 = persistent rows with the next rows prefetched (cp.async); 5 = long
- *   rows in L2-sized slabs (chunk summaries, then merge and normalise).  A
+ *   rows in chunks, in slabs of rows (chunk summaries, then merge and
+ *   normalise; one slab of all rows unless smx_debug_set_split_slab).  A
  *   forced path that cannot run the shape falls back to the automatic choice.
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).

@@ -421,8 +421,8 @@ int backward_occupancy(int in_dtype, int vpt, int threads) {
 
 // Softmax backward: rows of up to 16 KiB per CTA (at most 16 elements per
 // thread: two inputs held), with enough persistent CTAs for about 48 KiB of
-// reads in flight per SM; longer rows in chunks of 4096 elements (two passes
-// per L2-sized slab); the scalar kernel for unaligned shapes.
+// reads in flight per SM; longer rows in chunks of 4096 elements (two passes,
+// by default over one slab of all rows); the scalar kernel for unaligned shapes.
 void plan_backward(DeviceInfo& d, const Call& c, bool vec_ok, Plan* p) {
   p->path = PATH_GENERIC;
   if (!vec_ok) return;
