@@ -253,6 +253,41 @@ def oracle_throughput(x_host, vl, w, budget_s: float, min_rows: int = 1, op: str
     return sample_bytes(op, w, vl, sel) / dt / 1e9, n, dt, n / dt
 
 
+def _oracle_slice(job):
+    """Process-pool worker: the reference on one contiguous slice of rows;
+    returns its compute time (the slice's data arrives before the clock starts)."""
+    import dataclasses
+
+    op, w, x_part, vl_part, extra_part, n = job
+    ws = dataclasses.replace(w, rows=n)
+    t0 = time.perf_counter()
+    oracle_call(op, ws, x_part, vl_part, extra_part, np.arange(n))
+    return time.perf_counter() - t0
+
+
+def oracle_all_cores(x_host, vl, w, n: int, op: str = "softmax"):
+    """The same reference on the first n rows, split into one contiguous slice
+    per core of this process's CPU affinity (a spawn-context process pool: no
+    state of this process, GPU or otherwise, is inherited).  Returns
+    (GB/s over the slowest worker's compute time, cores)."""
+    import multiprocessing as mp
+
+    cores = max(1, len(os.sched_getaffinity(0)))
+    extra = oracle_inputs(op, w, x_host, vl)
+    bounds = np.linspace(0, n, min(cores, n) + 1).astype(np.int64)
+    jobs = []
+    for r0, r1 in zip(bounds[:-1], bounds[1:]):
+        r0, r1 = int(r0), int(r1)
+        part = {k: (v[r0:r1] if isinstance(v, np.ndarray) and v.shape[:1] == (w.rows,)
+                    else v[r0 * w.cols:r1 * w.cols] if isinstance(v, np.ndarray) else v)
+                for k, v in extra.items()}
+        jobs.append((op, w, x_host[r0 * w.cols:r1 * w.cols], None if vl is None else vl[r0:r1], part, r1 - r0))
+    with mp.get_context("spawn").Pool(len(jobs)) as pool:
+        pool.map(_oracle_slice, jobs[:1] * len(jobs), chunksize=1)  # start the workers, load the reference
+        dt = max(pool.map(_oracle_slice, jobs, chunksize=1))
+    return sample_bytes(op, w, vl, np.arange(n)) / dt / 1e9, len(jobs)
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -529,6 +564,7 @@ def run_ours(args, w):
     traffic, kernel_name = profile_traffic(w.name, args.op)
     cpu_gbs, cpu_rows, cpu_s, cpu_rps = oracle_throughput(x_host, vl_host, w, args.cpu_budget,
                                                           op=args.op)
+    cpu_all = oracle_all_cores(x_host, vl_host, w, cpu_rows, args.op) if args.cpu_all_cores else None
     line = {
         "metric": metric_of(args.op), "value": agg["gbs"], "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
@@ -545,9 +581,14 @@ def run_ours(args, w):
                      "mean_launch_us": mean_launch_ms * 1e3, "launch_timing": launch_timing,
                      "sampled_launches": len(launch_ms),
                      "sampled_median_launch_us": statistics.median(launch_ms) * 1e3},
-        "cpu_baseline": {"value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"first {cpu_rows} of {w.rows} rows, fp64 C reference, one "
-                                   f"thread, {cpu_s:.1f} s"},
+        "cpu_baseline": dict({"value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                              "sample": f"first {cpu_rows} of {w.rows} rows, fp64 C reference, one "
+                                        f"thread, {cpu_s:.1f} s"},
+                             **({} if cpu_all is None else {
+                                 "value_all_cores": cpu_all[0], "cores_all": cpu_all[1],
+                                 "all_cores_sample": "the same rows in one contiguous slice per core of the "
+                                                     "process's CPU affinity (spawned worker processes); "
+                                                     "the slowest worker's compute time"})),
         "e2e": {"value": e2e["gbs"], "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps * launches_per_call,
@@ -758,6 +799,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=None, choices=sorted(wl.WORKLOADS) + sorted(wl.ATTN_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU reference work for cpu_baseline")
+    ap.add_argument("--cpu-all-cores", type=int, default=1,
+                    help="also time the CPU reference on all cores of the affinity (1) or not (0)")
     ap.add_argument("--path", choices=sorted(PATHS), default="auto",
                     help="kernel family (diagnostics; the library chooses with auto)")
     ap.add_argument("--ref-budget", type=float, default=60.0,

@@ -91,3 +91,18 @@ def test_attention_flops_count_valid_pairs():
             brute = sum(1 for i in range(sq) for j in range(sk) if not causal or j <= i + sk - sq)
             assert wl.attention_pairs(sq, sk, causal) == brute
             assert wl.attention_flops(2, sq, sk, 64, causal) == 4.0 * 2 * 64 * brute
+
+
+@pytest.mark.parametrize("op", ["softmax", "apply_stats", "backward", "cross_entropy"])
+def test_cpu_reference_on_all_cores(op):
+    """The all-cores CPU baseline: one contiguous slice of rows per core of the
+    affinity, in spawned workers; every op's extra inputs are sliced with the rows."""
+    from numerically_stable_online_gb300 import workloads as wl
+
+    w = wl.WORKLOADS["f16_32768x1024_len"]
+    x, vl = wl.host_input(w.name, rows=64)
+    import dataclasses
+
+    w = dataclasses.replace(w, rows=64)
+    gbs, cores = bench.oracle_all_cores(x, vl, w, 48, op)
+    assert gbs > 0 and 1 <= cores <= min(48, len(os.sched_getaffinity(0)))
