@@ -81,3 +81,16 @@ def test_binding_refuses_cpu_tensors():
 
     with pytest.raises(ValueError):
         smx.softmax_rows(torch.zeros(2, 4))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: with the CUDA library absent the binding raises instead of
+    computing anything another way."""
+    import numerically_stable_online_gb300 as smx
+
+    monkeypatch.setattr(smx, "_lib", None)
+    monkeypatch.setattr(smx, "LIB_PATH", str(tmp_path / "libsmx.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        smx.library()
+    with pytest.raises(RuntimeError, match="not built"):
+        smx.last_device_status()  # a public call that reaches the library without a GPU tensor
