@@ -94,6 +94,26 @@ smx_status smx_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
                             smx_dtype out_dtype, smx_stream_t stream);
 
 /*
+ * smx_softmax_rows with the input, the output and valid_len in HOST memory:
+ * the same result, for callers whose rows live on the host.  The rows pass
+ * through two device staging slots (taken from the library's memory pool) in
+ * chunks of about 16 MiB of input: chunk i's copy to the device and its
+ * softmax run on `stream`, its copy back on a second stream the library owns,
+ * so both directions of the host link and the kernels run at once.  The host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the
+ * copies to overlap; pageable memory gives the same result, serialised.
+ *   x, y      host, [rows][cols] row-major, in_dtype / out_dtype; must not overlap.
+ *   valid_len host int32[rows] or NULL.
+ * Asynchronous on `stream`: y holds the result once `stream` has completed
+ * (for instance after smx_last_device_status(stream)); the host buffers must
+ * stay valid and untouched until then.  Argument errors are returned before
+ * anything is enqueued.
+ */
+smx_status smx_softmax_rows_host(const void *x, void *y, int64_t rows, int64_t cols,
+                                 const int32_t *valid_len, smx_dtype in_dtype,
+                                 smx_dtype out_dtype, smx_stream_t stream);
+
+/*
  * smx_softmax_rows, computed without allocating any device memory.
  *
  * The method's pages have no counterpart to this call; it exists for callers
@@ -316,6 +336,9 @@ int smx_version(void);
  *   all slabs with per-row completion counts (where supported); 0 = two
  *   launches per slab, the statistics pass and then the normalising pass
  *   (default).
+ * smx_debug_set_host_chunk(bytes, slots): smx_softmax_rows_host's chunk size
+ *   in input bytes and its number of device staging slots (2 to 4); 0 =
+ *   default for either.
  * smx_debug_set_attention_mma_sync(on): 1 = the attention forward runs on the
  *   mma.sync kernel (warp-level tensor-core instructions) instead of the
  *   tcgen05/TMEM kernel (default).
@@ -340,6 +363,7 @@ void smx_debug_set_split_hints(int stats, int apply);
 void smx_debug_set_stream_warp(int off);
 void smx_debug_set_split_fused(int on);
 void smx_debug_set_attention_mma_sync(int on);
+void smx_debug_set_host_chunk(int64_t bytes, int slots);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 
 #ifdef __cplusplus

@@ -16,7 +16,7 @@ import threading
 import torch
 
 __all__ = [
-    "SmxError", "library", "softmax_rows", "softmax_rows_fixed_scratch", "softmax_row_stats",
+    "SmxError", "library", "softmax_rows", "softmax_rows_fixed_scratch", "softmax_rows_host", "softmax_row_stats",
     "softmax_merge_stats", "log_softmax_rows", "softmax_lse", "softmax_apply_stats",
     "softmax_backward", "cross_entropy", "attention_forward",
     "last_device_status", "status_string", "DTYPES",
@@ -57,6 +57,8 @@ def library() -> ctypes.CDLL:
         st = ctypes.c_int
         lib.smx_softmax_rows.argtypes = [P, P, I64, I64, P, I32, I32, P]
         lib.smx_softmax_rows.restype = st
+        lib.smx_softmax_rows_host.argtypes = [P, P, I64, I64, P, I32, I32, P]
+        lib.smx_softmax_rows_host.restype = st
         lib.smx_softmax_rows_fixed_scratch.argtypes = [P, P, I64, I64, P, I32, I32, P]
         lib.smx_softmax_rows_fixed_scratch.restype = st
         lib.smx_softmax_row_stats.argtypes = [P, P, P, I64, I64, P, I32, P]
@@ -111,6 +113,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_stream_warp.restype = None
         lib.smx_debug_set_split_fused.argtypes = [I32]
         lib.smx_debug_set_split_fused.restype = None
+        lib.smx_debug_set_host_chunk.argtypes = [I64, I32]
+        lib.smx_debug_set_host_chunk.restype = None
         lib.smx_debug_set_attention_mma_sync.argtypes = [I32]
         lib.smx_debug_set_attention_mma_sync.restype = None
         _lib = lib
@@ -161,6 +165,43 @@ def softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None, valid_len: to
                                     _dtype(out.dtype), _stream(stream))
     if st != 0:
         raise SmxError(st, "smx_softmax_rows")
+    return out
+
+
+def softmax_rows_host(x: torch.Tensor, out: torch.Tensor | None = None, valid_len: torch.Tensor | None = None,
+                      out_dtype: torch.dtype | None = None, stream=None, wait: bool = True) -> torch.Tensor:
+    """softmax_rows of a HOST matrix into a host matrix, through the current device.
+
+    The library moves the rows through two device staging buffers in chunks,
+    overlapping each chunk's copy in, softmax and copy back.  Pinned tensors
+    (``x.pin_memory()``) let the copies run asynchronously; ``out=None``
+    allocates a pinned output when ``x`` is pinned.  With ``wait`` the call
+    returns after the stream has finished; otherwise ``out`` is ready once the
+    stream reaches this point.
+    """
+    for t, name in ((x, "x"), (out, "out")):
+        if t is not None and (t.is_cuda or t.dim() != 2 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 2-D [rows, cols] host tensor")
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype or x.dtype, pin_memory=x.is_pinned())
+    if out.shape != x.shape:
+        raise ValueError("out must match x's shape")
+    vl = None
+    if valid_len is not None:
+        if valid_len.is_cuda or valid_len.dtype != torch.int32 or not valid_len.is_contiguous() \
+                or valid_len.numel() != rows:
+            raise ValueError("valid_len must be a contiguous int32 host tensor with one entry per row")
+        vl = valid_len.data_ptr()
+    sp = _stream(stream)
+    st = library().smx_softmax_rows_host(x.data_ptr(), out.data_ptr(), rows, cols, vl, _dtype(x.dtype),
+                                         _dtype(out.dtype), sp)
+    if st != 0:
+        raise SmxError(st, "smx_softmax_rows_host")
+    if wait:
+        s = stream if hasattr(stream, "synchronize") else (
+            torch.cuda.current_stream() if stream is None else torch.cuda.ExternalStream(sp))
+        s.synchronize()
     return out
 
 

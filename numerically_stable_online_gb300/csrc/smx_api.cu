@@ -39,6 +39,7 @@ struct DeviceInfo {
   cudaMemPool_t pool = nullptr;  // the long-row paths' scratch (keeps its memory between calls)
   int max_cluster[3] = {0, 0, 0};  // per input type, 0 = not queried yet
   bool coop = false;                // cooperative launches supported
+  cudaStream_t copy_stream = nullptr;  // the host-buffer call's copies back (created on first use)
 };
 
 DeviceInfo g_dev[MAX_DEVICES];
@@ -59,6 +60,8 @@ std::atomic<int> g_split_hint_stats{-1}, g_split_hint_apply{-1};
 std::atomic<int64_t> g_bwd_inflight{48 * 1024};  // backward: reads in flight per SM
 std::atomic<int> g_stream_warp{0};
 std::atomic<int> g_split_fused{0};
+std::atomic<int64_t> g_host_chunk{0};  // host-buffer call: input bytes a chunk (0 = default)
+std::atomic<int> g_host_slots{0};      // host-buffer call: device staging slots (0 = default)
 std::atomic<int> g_attention_mma_sync{0};  // 1: the attention forward on mma.sync instead of tcgen05  // 0: long rows in one cooperative launch; 1: two launches per slab  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
@@ -668,6 +671,106 @@ smx_status smx_softmax_rows(const void* x, void* y, int64_t rows, int64_t cols,
   return run(c, *dev);
 }
 
+// The host-buffer call stages rows through device slots of about this much
+// input each (enough rows per launch; several chunks to overlap).
+constexpr int64_t HOST_CHUNK_BYTES = int64_t(16) << 20;
+constexpr int HOST_SLOTS = 2, HOST_MAX_SLOTS = 4;
+
+smx_status smx_softmax_rows_host(const void* x, void* y, int64_t rows, int64_t cols,
+                                 const int32_t* valid_len, smx_dtype in_dtype, smx_dtype out_dtype,
+                                 smx_stream_t stream) {
+  t_kernel_launches = 0;
+  if (rows < 0 || cols < 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+    return SMX_ERR_INVALID_ARG;
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return SMX_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return SMX_OK;
+  if (x == nullptr || y == nullptr) return SMX_ERR_INVALID_ARG;
+  const int64_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+  const int64_t nx = rows * cols * ies, ny = rows * cols * oes;
+  if (overlaps(x, nx, y, ny)) return SMX_ERR_ALIAS;
+  if (valid_len && overlaps(valid_len, rows * 4, y, ny)) return SMX_ERR_ALIAS;
+  DeviceInfo* dev = nullptr;
+  smx_status s = device_info(&dev);
+  if (s != SMX_OK) return s;
+  cudaError_t e;
+  cudaStream_t B = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (dev->copy_stream == nullptr &&
+        (e = cudaStreamCreateWithFlags(&dev->copy_stream, cudaStreamNonBlocking)) != cudaSuccess) {
+      dev->copy_stream = nullptr;
+      return cuda_fail(e, SMX_ERR_DEVICE);
+    }
+    B = dev->copy_stream;
+  }
+  const cudaStream_t A = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t chunk_bytes = g_host_chunk.load() > 0 ? g_host_chunk.load() : HOST_CHUNK_BYTES;
+  const int gs = g_host_slots.load();
+  const int nslots = gs >= 2 && gs <= HOST_MAX_SLOTS ? gs : HOST_SLOTS;
+  int64_t cr = chunk_bytes / (cols * ies);  // rows a chunk
+  if (cr < 1) cr = 1;
+  if (cr > rows) cr = rows;
+  auto up16 = [](int64_t b) { return (b + 15) / 16 * 16; };
+  const int64_t in_b = up16(cr * cols * ies), out_b = up16(cr * cols * oes);
+  const int64_t slot = in_b + out_b + (valid_len ? up16(cr * 4) : 0);
+  char* base = nullptr;
+  if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), (size_t)(nslots * slot), dev->pool, A)) !=
+      cudaSuccess)
+    return cuda_fail(e, SMX_ERR_DEVICE);
+  // per slot: its chunk computed (on A), its output copied back (on B)
+  cudaEvent_t computed[HOST_MAX_SLOTS] = {}, copied[HOST_MAX_SLOTS] = {}, done = nullptr;
+  for (int i = 0; i < nslots && e == cudaSuccess; ++i) {
+    if ((e = cudaEventCreateWithFlags(&computed[i], cudaEventDisableTiming)) == cudaSuccess)
+      e = cudaEventCreateWithFlags(&copied[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming);
+  int launches = 0;
+  for (int64_t i = 0, r0 = 0; e == cudaSuccess && r0 < rows; ++i, r0 += cr) {
+    const int sl = (int)(i % nslots);
+    const int64_t n = rows - r0 < cr ? rows - r0 : cr;
+    char* dx = base + sl * slot;
+    char* dy = dx + in_b;
+    int32_t* dvl = valid_len ? reinterpret_cast<int32_t*>(dy + out_b) : nullptr;
+    // in on A (the slot's previous chunk was computed earlier on A)
+    if ((e = cudaMemcpyAsync(dx, static_cast<const char*>(x) + r0 * cols * ies, (size_t)(n * cols * ies),
+                             cudaMemcpyHostToDevice, A)) != cudaSuccess)
+      break;
+    if (dvl && (e = cudaMemcpyAsync(dvl, valid_len + r0, (size_t)(n * 4), cudaMemcpyHostToDevice, A)) !=
+                   cudaSuccess)
+      break;
+    // the slot's output buffer is free once its previous chunk's copy back is done
+    if (i >= nslots && (e = cudaStreamWaitEvent(A, copied[sl], 0)) != cudaSuccess) break;
+    Call c{dx, dy, nullptr, nullptr, n, cols, dvl, (int)in_dtype, (int)out_dtype, MODE_SOFTMAX, A, nullptr, 0};
+    t_kernel_launches = 0;
+    s = run(c, *dev);
+    launches += t_kernel_launches;
+    if (s != SMX_OK) break;
+    // out on B, after the chunk's softmax
+    if ((e = cudaEventRecord(computed[sl], A)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(B, computed[sl], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(static_cast<char*>(y) + r0 * cols * oes, dy, (size_t)(n * cols * oes),
+                             cudaMemcpyDeviceToHost, B)) != cudaSuccess ||
+        (e = cudaEventRecord(copied[sl], B)) != cudaSuccess)
+      break;
+  }
+  // the call completes on the caller's stream: A waits for B's last copy,
+  // then the slots go back to the pool
+  cudaError_t f = cudaSuccess;
+  if (done != nullptr && (f = cudaEventRecord(done, B)) == cudaSuccess) f = cudaStreamWaitEvent(A, done, 0);
+  const cudaError_t g = cudaFreeAsync(base, A);
+  for (int i = 0; i < nslots; ++i) {
+    if (computed[i]) cudaEventDestroy(computed[i]);
+    if (copied[i]) cudaEventDestroy(copied[i]);
+  }
+  if (done) cudaEventDestroy(done);
+  t_kernel_launches = launches;
+  if (s != SMX_OK) return s;
+  if (e == cudaSuccess) e = f;
+  if (e == cudaSuccess) e = g;
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+  return SMX_OK;
+}
+
 smx_status smx_softmax_rows_fixed_scratch(const void* x, void* y, int64_t rows, int64_t cols,
                                           const int32_t* valid_len, smx_dtype in_dtype,
                                           smx_dtype out_dtype, smx_stream_t stream) {
@@ -961,6 +1064,10 @@ void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes) {
 void smx_debug_set_stream_warp(int off) { g_stream_warp.store(off ? 1 : 0); }
 
 void smx_debug_set_split_fused(int on) { g_split_fused.store(on ? 1 : 0); }
+void smx_debug_set_host_chunk(int64_t bytes, int slots) {
+  g_host_chunk.store(bytes > 0 ? bytes : 0);
+  g_host_slots.store(slots >= 2 && slots <= HOST_MAX_SLOTS ? slots : 0);
+}
 
 void smx_debug_set_attention_mma_sync(int on) { g_attention_mma_sync.store(on ? 1 : 0); }
 

@@ -94,3 +94,44 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         smx.library()
     with pytest.raises(RuntimeError, match="not built"):
         smx.last_device_status()  # a public call that reaches the library without a GPU tensor
+
+
+def test_host_buffer_call_checks_need_no_gpu(lib):
+    """smx_softmax_rows_host validates like smx_softmax_rows, on host
+    buffers, before it needs a device; with valid arguments and no device it
+    reports SMX_ERR_UNSUPPORTED and enqueues nothing."""
+    import numpy as np
+
+    x = np.zeros((4, 8), np.float32)
+    y = np.zeros((4, 8), np.float32)
+    vl = np.full(4, 8, np.int32)
+    px, py, pv = (ctypes.c_void_p(a.ctypes.data) for a in (x, y, vl))
+    f = lib.smx_softmax_rows_host
+    assert f(px, py, -1, 8, None, 0, 0, None) == 1
+    assert f(px, py, 4, -1, None, 0, 0, None) == 1
+    assert f(px, py, 4, 8, None, 5, 0, None) == 1
+    assert f(None, py, 4, 8, None, 0, 0, None) == 1
+    assert f(px, None, 4, 8, None, 0, 0, None) == 1
+    assert f(None, None, 0, 8, None, 0, 0, None) == 0
+    assert f(None, None, 4, 0, None, 0, 0, None) == 0
+    assert f(px, ctypes.c_void_p(x.ctypes.data + 4), 4, 8, None, 0, 0, None) == 3
+    assert f(px, py, 4, 8, ctypes.c_void_p(y.ctypes.data + 8), 0, 0, None) == 3
+    st = f(px, py, 4, 8, pv, 0, 0, None)
+    assert st in (0, 2)
+    if st == 2:
+        assert not y.any()  # nothing written without a device
+
+
+def test_host_buffer_binding_checks_arguments():
+    import torch
+
+    import numerically_stable_online_gb300 as smx
+
+    with pytest.raises(ValueError):
+        smx.softmax_rows_host(torch.zeros(8))
+    with pytest.raises(ValueError):
+        smx.softmax_rows_host(torch.zeros(2, 8), out=torch.zeros(2, 8).t())
+    with pytest.raises(ValueError):
+        smx.softmax_rows_host(torch.zeros(2, 8), valid_len=torch.zeros(2, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        smx.softmax_rows_host(torch.zeros(2, 8), out=torch.zeros(3, 8))
