@@ -10,9 +10,9 @@ Prints one JSON line on rank 0:
   value        algorithmic bytes (valid input read once + output written once
                + row lengths) of all ranks' steps / max-over-ranks timed region
   e2e          the same metric end to end from pinned host memory: the softmax
-               through its host-buffer call (copies in and back pipelined with
-               the chunks' softmax inside the call), the other ops through the
-               device call with the copies around it, every step
+               through its host-buffer call (the kernel reads and writes the
+               mapped pinned buffers in place over the host link), the other
+               ops through the device call with the copies around it, every step
   roofline     the softmax kernel's achieved bandwidth (CUDA events around every
                launch in the timed region) against the measured HBM copy peak
   cpu_baseline the fp64 CPU reference timed on this host on a bounded sample
@@ -437,8 +437,8 @@ class GpuOp:
             extra_in.append((self.t_cpu.pin_memory(), torch.empty_like(self.t)))
             loss_pin = torch.empty(self.w.rows, dtype=torch.float32).pin_memory()
         if op == "softmax":
-            # the host-buffer entry point: it pipelines the copies in and back
-            # with the chunks' softmax inside the call
+            # the host-buffer entry point (pinned buffers: read and written in
+            # place by the kernel over the host link)
             def host_step():
                 smx.softmax_rows_host(x_pin, out=y_pin, valid_len=vl_pin, wait=False)
             h2d = x_pin.numel() * x_pin.element_size() + (0 if vl_pin is None else vl_pin.numel() * 4)

@@ -95,13 +95,19 @@ smx_status smx_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
 
 /*
  * smx_softmax_rows with the input, the output and valid_len in HOST memory:
- * the same result, for callers whose rows live on the host.  The rows pass
- * through two device staging slots (taken from the library's memory pool) in
- * chunks of about 16 MiB of input: chunk i's copy to the device and its
- * softmax run on `stream`, its copy back on a second stream the library owns,
- * so both directions of the host link and the kernels run at once.  The host
- * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the
- * copies to overlap; pageable memory gives the same result, serialised.
+ * the same result, for callers whose rows live on the host.  Two ways, the
+ * same arithmetic:
+ *  - In place: when x, y (and valid_len, if given) are page-locked buffers
+ *    mapped into the device's address space (cudaHostAlloc / cudaHostRegister
+ *    memory on a unified-addressing system) and the rows take a kernel that
+ *    reads each element once (rows up to a few MiB), one launch reads x and
+ *    writes y in host memory over the host link.
+ *  - Staged, otherwise (pageable buffers, long rows): the rows pass through
+ *    two device staging slots (taken from the library's memory pool) in
+ *    chunks of about 16 MiB of input: chunk i's copy to the device and its
+ *    softmax run on `stream`, its copy back on a second stream the library
+ *    owns, so both directions of the host link and the kernels run at once.
+ *    Pageable memory gives the same result with the copies serialised.
  *   x, y      host, [rows][cols] row-major, in_dtype / out_dtype; must not overlap.
  *   valid_len host int32[rows] or NULL.
  * Asynchronous on `stream`: y holds the result once `stream` has completed
@@ -336,9 +342,10 @@ int smx_version(void);
  *   all slabs with per-row completion counts (where supported); 0 = two
  *   launches per slab, the statistics pass and then the normalising pass
  *   (default).
- * smx_debug_set_host_chunk(bytes, slots): smx_softmax_rows_host's chunk size
- *   in input bytes and its number of device staging slots (2 to 4); 0 =
- *   default for either.
+ * smx_debug_set_host_chunk(bytes, slots, staged): smx_softmax_rows_host's
+ *   chunk size in input bytes and its number of device staging slots (2 to
+ *   4), 0 = default for either; staged = 1 sends mapped page-locked buffers
+ *   through the staging slots too (0 = in place where possible).
  * smx_debug_set_attention_mma_sync(on): 1 = the attention forward runs on the
  *   mma.sync kernel (warp-level tensor-core instructions) instead of the
  *   tcgen05/TMEM kernel (default).
@@ -363,7 +370,7 @@ void smx_debug_set_split_hints(int stats, int apply);
 void smx_debug_set_stream_warp(int off);
 void smx_debug_set_split_fused(int on);
 void smx_debug_set_attention_mma_sync(int on);
-void smx_debug_set_host_chunk(int64_t bytes, int slots);
+void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 
 #ifdef __cplusplus

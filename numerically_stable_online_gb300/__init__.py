@@ -113,7 +113,7 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_stream_warp.restype = None
         lib.smx_debug_set_split_fused.argtypes = [I32]
         lib.smx_debug_set_split_fused.restype = None
-        lib.smx_debug_set_host_chunk.argtypes = [I64, I32]
+        lib.smx_debug_set_host_chunk.argtypes = [I64, I32, I32]
         lib.smx_debug_set_host_chunk.restype = None
         lib.smx_debug_set_attention_mma_sync.argtypes = [I32]
         lib.smx_debug_set_attention_mma_sync.restype = None
@@ -172,12 +172,14 @@ def softmax_rows_host(x: torch.Tensor, out: torch.Tensor | None = None, valid_le
                       out_dtype: torch.dtype | None = None, stream=None, wait: bool = True) -> torch.Tensor:
     """softmax_rows of a HOST matrix into a host matrix, through the current device.
 
-    The library moves the rows through two device staging buffers in chunks,
-    overlapping each chunk's copy in, softmax and copy back.  Pinned tensors
-    (``x.pin_memory()``) let the copies run asynchronously; ``out=None``
-    allocates a pinned output when ``x`` is pinned.  With ``wait`` the call
-    returns after the stream has finished; otherwise ``out`` is ready once the
-    stream reaches this point.
+    Pinned tensors (``x.pin_memory()``; ``out=None`` allocates a pinned output
+    when ``x`` is pinned, and ``valid_len`` must be pinned too) are read and
+    written in place by the kernel over the host link, except for rows long
+    enough to take the two-pass long-row kernels.  Otherwise the library moves
+    the rows through two device staging buffers in chunks, overlapping each
+    chunk's copy in, softmax and copy back.  With ``wait`` the call returns
+    after the stream has finished; otherwise ``out`` is ready once the stream
+    reaches this point.
     """
     for t, name in ((x, "x"), (out, "out")):
         if t is not None and (t.is_cuda or t.dim() != 2 or not t.is_contiguous()):

@@ -32,7 +32,7 @@ def built():
     oracle.build()
     lib = smx.library()
     yield lib
-    lib.smx_debug_set_host_chunk(0, 0)
+    lib.smx_debug_set_host_chunk(0, 0, 0)
 
 
 def host_tensor(x_store, in_dtype, rows, cols, pinned):
@@ -53,23 +53,53 @@ def chunks(rows, cols, in_dtype):
     return -(-rows // cr)
 
 
+PATH_REGS, PATH_STREAM, PATH_SPLIT = 1, 4, 5
+
+
 @pytest.mark.parametrize("name,rows,out_dtype,pinned", [
-    ("bf16_16384x4096", 3 * 2048 + 77, "bf16", True),     # 4 chunks, ragged last
+    ("bf16_16384x4096", 3 * 2048 + 77, "bf16", True),     # 4 chunks staged, ragged last
     ("bf16_16384x4096", 2 * 2048 + 1, "f32", False),      # pageable, wider output
     ("f16_32768x1024_len", 2 * 8192 + 5, "f16", True),    # lengths from host memory
-    ("f32_64x1000", 64, "bf16", True),                    # unaligned rows, one chunk
-    ("f32_64x1048576_rise", 7, "f32", True),              # 4 MiB rows, 4 a chunk
+    ("f32_64x1000", 64, "bf16", True),                    # one chunk
+    ("f32_64x1048576_rise", 7, "f32", True),              # 4 MiB rows, 4 a chunk; always staged
 ])
-def test_host_call_workloads(built, name, rows, out_dtype, pinned):
+@pytest.mark.parametrize("staged", [0, 1])
+def test_host_call_workloads(built, name, rows, out_dtype, pinned, staged):
+    """Page-locked buffers are read and written in place by the streamed
+    kernel (one launch) unless staging is forced or the rows take the
+    long-row kernels; pageable buffers always go through the staging slots."""
+    built.smx_debug_set_host_chunk(0, 0, staged)
     w = wl.WORKLOADS[name]
     x_store, vl = wl.host_input(name, rows=rows)
     x = host_tensor(x_store, w.in_dtype, rows, w.cols, pinned)
     vlt = None if vl is None else torch.from_numpy(np.asarray(vl, np.int32))
+    if pinned and vlt is not None:
+        vlt = vlt.pin_memory()
     y = smx.softmax_rows_host(x, valid_len=vlt, out_dtype=DT[out_dtype])
     assert not y.is_cuda and y.is_pinned() == pinned and y.dtype == DT[out_dtype]
-    assert built.smx_debug_last_launches() >= chunks(rows, w.cols, w.in_dtype)
+    in_place = pinned and not staged and built.smx_debug_last_path() != PATH_SPLIT
+    if in_place:
+        assert built.smx_debug_last_launches() == 1
+        assert built.smx_debug_last_path() in (PATH_REGS, PATH_STREAM)
+    else:
+        assert built.smx_debug_last_launches() >= chunks(rows, w.cols, w.in_dtype)
     assert smx.last_device_status() == 0
     compare_all(y, x_store, w.in_dtype, out_dtype, rows, w.cols, vl)
+    if name == "f32_64x1048576_rise":
+        assert built.smx_debug_last_path() == PATH_SPLIT
+
+
+def test_lengths_in_pageable_memory_stage(built):
+    """In place needs every buffer mapped: pinned rows with pageable lengths
+    go through the staging slots."""
+    name, rows = "f16_32768x1024_len", 8192 + 3
+    w = wl.WORKLOADS[name]
+    x_store, vl = wl.host_input(name, rows=rows)
+    x = host_tensor(x_store, w.in_dtype, rows, w.cols, True)
+    y = smx.softmax_rows_host(x, valid_len=torch.from_numpy(np.asarray(vl, np.int32)))
+    assert built.smx_debug_last_launches() >= 2
+    assert smx.last_device_status() == 0
+    compare_all(y, x_store, w.in_dtype, w.out_dtype, rows, w.cols, vl)
 
 
 def test_rows_longer_than_a_chunk(built):
@@ -83,9 +113,12 @@ def test_rows_longer_than_a_chunk(built):
     compare_all(y, x_store, "f32", "f32", rows, cols, None, block_rows=1)
 
 
-def test_caller_stream_and_output_buffer(built):
-    """On a side stream, into a given output: the result is complete once that
-    stream is synchronised, and matches the device call on the same rows."""
+@pytest.mark.parametrize("staged", [0, 1])
+def test_caller_stream_and_output_buffer(built, staged):
+    """On a side stream, into a given output, in place and staged: the result
+    is complete once that stream is synchronised, and repeated calls give the
+    same bits."""
+    built.smx_debug_set_host_chunk(0, 0, staged)
     name, rows = "bf16_16384x4096", 2048 + 513
     w = wl.WORKLOADS[name]
     x_store, _ = wl.host_input(name, rows=rows)
@@ -120,7 +153,7 @@ def test_many_chunks_and_slots(built, chunk_bytes, slots, pinned):
     """Small chunks (tens to hundreds of them, a ragged last one; 5000 bytes is
     less than one 8000-byte row, so one row a chunk) through 2, 3 and 4 staging
     slots, so every slot is reused many times while copies are in flight."""
-    built.smx_debug_set_host_chunk(chunk_bytes, slots)
+    built.smx_debug_set_host_chunk(chunk_bytes, slots, 1)
     try:
         name, rows = "f16_32768x1024_len", 1000
         w = wl.WORKLOADS[name]
@@ -137,4 +170,4 @@ def test_many_chunks_and_slots(built, chunk_bytes, slots, pinned):
         assert smx.last_device_status() == 0
         compare_all(y, x_store, "f32", "bf16", rows, cols, None)
     finally:
-        built.smx_debug_set_host_chunk(0, 0)
+        built.smx_debug_set_host_chunk(0, 0, 0)
