@@ -5,8 +5,11 @@ with the tolerances the library states:
                 |1 - sum_j y_j| <= 1e-5 (summed in fp64) on every normal row.
   fp16 / bf16:  the output's bit pattern is within 1 of the correctly rounded
                 fp64 result's (covers subnormals and binade edges).
-  everywhere:   masked lanes and empty / all -inf rows are +0 bit for bit; rows
-                the policy makes NaN are NaN in every valid lane.
+  everywhere:   masked lanes, and valid lanes whose reference probability is
+                exactly 0 (a -inf lane, every lane of an all -inf row, an
+                exponential below the fp64 range), are +0 bit for bit; no
+                output is -0; rows the policy makes NaN are NaN in every
+                valid lane.
 """
 import numpy as np
 
@@ -35,13 +38,16 @@ def compare(y, p, out_dtype, valid_len=None, rows_sel=None):
     masked = j >= L[:, None]
     nan_rows = np.isnan(p).any(axis=1)
     stats = {}
+    zero_lanes = ~nan_rows[:, None] & ~masked & (p == 0)
     if out_dtype == "f32":
         y = np.asarray(y, dtype=np.float32).reshape(n, cols)
         bits = y.view(np.uint32)
         assert np.all(bits[masked] == 0), "masked lanes must be +0"
+        assert np.all(bits[zero_lanes] == 0), "lanes of probability 0 must be +0"
         yv = y.astype(np.float64)
         pv = p
         nn = ~nan_rows[:, None] & ~masked
+        assert np.all(bits[nn] >> 31 == 0), "outputs must be non-negative (no -0)"
         assert np.all(np.isnan(yv[nan_rows[:, None] & ~masked])), "NaN rows must be NaN"
         big = nn & (pv >= F32_TINY)
         small = nn & (pv < F32_TINY)
@@ -57,6 +63,7 @@ def compare(y, p, out_dtype, valid_len=None, rows_sel=None):
     else:
         yb = np.asarray(y).view(np.uint16).reshape(n, cols).astype(np.int64)
         assert np.all(yb[masked] == 0), "masked lanes must be +0"
+        assert np.all(yb[zero_lanes] == 0), "lanes of probability 0 must be +0"
         exp_all = 0x7C00 if out_dtype == "f16" else 0x7F80
         isnan = ((yb & exp_all) == exp_all) & ((yb & ~exp_all & 0x7FFF) != 0)
         nv = nan_rows[:, None] & ~masked
