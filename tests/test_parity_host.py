@@ -35,6 +35,14 @@ def built():
     lib.smx_debug_set_host_chunk(0, 0, 0)
 
 
+@pytest.fixture(autouse=True)
+def default_host_path(built):
+    """Every test starts and ends with the default chunk, slots and path."""
+    built.smx_debug_set_host_chunk(0, 0, 0)
+    yield
+    built.smx_debug_set_host_chunk(0, 0, 0)
+
+
 def host_tensor(x_store, in_dtype, rows, cols, pinned):
     t = wl.storage_to_torch(np.ascontiguousarray(x_store).reshape(-1), in_dtype).reshape(rows, cols)
     return t.pin_memory() if pinned else t.contiguous()
