@@ -599,7 +599,11 @@ def run_ours(args, w):
                                                      "process's CPU affinity (spawned worker processes); "
                                                      "the slowest worker's compute time"})),
         "e2e": {"value": e2e["gbs"], "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "how": ("smx_softmax_rows_host on pinned host buffers: the kernel reads x and writes y "
+                        "in place over the host link when they are mapped (else staged copies on two "
+                        "streams)" if args.op == "softmax" else
+                        "pinned host copies in, the device call, the outputs copied back, one stream")},
         "gpu_launches": args.steps * launches_per_call,
         "kernels_per_step": launches_per_call,
         "clocks": clocks,
@@ -746,7 +750,8 @@ def run_attention(args):
                                    f"{cpu_s:.1f} s"},
         "e2e": {"value": flops * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "how": "pinned host copies of q, k and v in, the device call, o and lse copied back, one stream"},
         "gpu_launches": args.steps * launches,
         "kernels_per_step": launches,
         "clocks": clocks,
