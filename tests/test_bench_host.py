@@ -1,6 +1,8 @@
 """Host-side logic of bench.py, on CPU: the whole-job aggregation, the
-max-over-ranks timing with two gloo ranks, the L2 rotation, and the reference
-arm's JSON line (fp64 CPU reference only, no GPU)."""
+max-over-ranks timing with two gloo ranks, the L2 rotation, the reference
+arm's JSON line (fp64 CPU reference only, no GPU), the clock sampler's
+parsing and throttle reasons, the profile lookup's source-hash gate and the
+measured-peak fallback."""
 import json
 import os
 import subprocess
@@ -106,3 +108,69 @@ def test_cpu_reference_on_all_cores(op):
     w = dataclasses.replace(w, rows=64)
     gbs, cores = bench.oracle_all_cores(x, vl, w, 48, op)
     assert gbs > 0 and 1 <= cores <= min(48, len(os.sched_getaffinity(0)))
+
+
+class _FakeSmi:
+    """Stands in for the nvidia-smi process: canned CSV samples."""
+
+    def __init__(self, lines):
+        self.lines = lines
+        self.terminated = False
+
+    def terminate(self):
+        self.terminated = True
+
+    def communicate(self, timeout=None):
+        return "\n".join(self.lines) + "\n", None
+
+
+def _sample(sm, reasons=("Not Active",) * 4):
+    return ", ".join(["0", str(sm), "2070", "900.5", "0x0000000000000000", *reasons])
+
+
+def test_clock_sampler_median_and_reasons():
+    import time
+
+    cs = bench.ClockSampler(0)
+    cs.t0 = time.time() - 1.0
+    lines = [_sample(2070), _sample(2055), _sample(1980, ("Not Active", "Not Active", "Not Active", "Active")),
+             "garbage line", _sample(2070)]
+    cs.proc = _FakeSmi(lines)
+    rec = cs.stop(t_begin=cs.t0 - 1, t_end=time.time() + 1)
+    assert cs.proc.terminated
+    assert rec["sm_mhz"] == 2062.5 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] == 4
+    cs = bench.ClockSampler(0)
+    cs.t0 = time.time() - 1.0
+    cs.proc = _FakeSmi([_sample(1500, ("Active", "Not Active", "Active", "Not Active"))])
+    rec = cs.stop(cs.t0 - 1, time.time() + 1)
+    assert rec["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_sampler_without_nvidia_smi():
+    cs = bench.ClockSampler(0)
+    rec = cs.stop(0.0, 1.0)
+    assert rec["sm_mhz"] is None and rec["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_profile_traffic_follows_the_source_hash(monkeypatch, tmp_path):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "softmax_wl_a.md").write_text(
+        "# ncu\n\nkernel: k_rows_stream<bf16,bf16>\nsource_hash: 0123456789abcdef\n"
+        "dram_bytes_per_launch: 212694912\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda files=None: "0123456789abcdef")
+    assert bench.profile_traffic("wl_a", "softmax") == (212694912, "k_rows_stream<bf16,bf16>")
+    monkeypatch.setattr(bench, "source_hash", lambda files=None: "fedcba9876543210")
+    # taken on other sources: the kernel is named, the traffic is not reported
+    assert bench.profile_traffic("wl_a", "softmax") == (None, "k_rows_stream<bf16,bf16>")
+    assert bench.profile_traffic("no_such_workload", "softmax") == (None, None)
+
+
+def test_measured_peak_and_fallback(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peak("hbm_gbs") == (6800.0, "fallback")
+    assert bench.measured_peak("bf16_tflops") == (1900.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6689.1, "bf16_tflops": 1939.3}))
+    assert bench.measured_peak("hbm_gbs") == (6689.1, "measured")
+    assert bench.measured_peak("bf16_tflops") == (1939.3, "measured")
