@@ -1,5 +1,6 @@
 """The ncu summaries under profiles/ are short text named for an operation and
-a workload that exist, each giving its kernel, the source hash it was taken
+a workload that exist (besides the compiler's resource summary of every
+kernel), each giving its kernel, the source hash it was taken
 on and the DRAM bytes per launch the bench line reads, and the full commands
 that made it: commands that run committed files only, with every ncu call
 leaving the GPU clocks alone (--clock-control none)."""
@@ -23,7 +24,24 @@ def test_profiles_exist_for_the_bench_workload():
     assert "attention_attn_bf16_4x32x4096x128.md" in names
 
 
-@pytest.mark.parametrize("path", FILES, ids=[os.path.basename(f) for f in FILES])
+NCU_FILES = [f for f in FILES if not os.path.basename(f).startswith("resources_")]
+RESOURCE_FILES = [f for f in FILES if os.path.basename(f).startswith("resources_")]
+
+
+@pytest.mark.parametrize("path", RESOURCE_FILES, ids=[os.path.basename(f) for f in RESOURCE_FILES])
+def test_resource_summary(path):
+    """The ptxas summary: the compile commands of committed sources with -Xptxas -v."""
+    text = open(path).read()
+    assert os.path.getsize(path) < 16 * 1024
+    cmds = [line.strip() for line in text.splitlines() if line.startswith("    nvcc ")]
+    assert cmds
+    for c in cmds:
+        assert "-Xptxas -v" in c and "arch=compute_103a,code=sm_103a" in c, c
+        src = c.split(" -c ")[1].split()[0]
+        assert os.path.exists(os.path.join(ROOT, src)), src
+
+
+@pytest.mark.parametrize("path", NCU_FILES, ids=[os.path.basename(f) for f in NCU_FILES])
 def test_profile_summary(path):
     base = os.path.basename(path)
     assert base.endswith((".md", ".txt")), "text summaries only"
