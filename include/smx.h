@@ -100,9 +100,12 @@ smx_status smx_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
  *  - In place: when x, y (and valid_len, if given) are page-locked buffers
  *    mapped into the device's address space (cudaHostAlloc / cudaHostRegister
  *    memory on a unified-addressing system) and the rows take a kernel that
- *    reads each element once (rows up to a few MiB), one launch reads x and
- *    writes y in host memory over the host link.
- *  - Staged, otherwise (pageable buffers, long rows): the rows pass through
+ *    reads each element once with plain loads (the streamed and
+ *    register-resident rows: at most 32,768 elements, 16,384 for fp32
+ *    outputs), one launch reads x and writes y in host memory over the host
+ *    link.
+ *  - Staged, otherwise (pageable buffers; longer rows, which the cluster and
+ *    long-row kernels take; unaligned rows): the rows pass through
  *    two device staging slots (taken from the library's memory pool) in
  *    chunks of about 16 MiB of input: chunk i's copy to the device and its
  *    softmax run on `stream`, its copy back on a second stream the library

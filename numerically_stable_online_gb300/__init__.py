@@ -174,8 +174,9 @@ def softmax_rows_host(x: torch.Tensor, out: torch.Tensor | None = None, valid_le
 
     Pinned tensors (``x.pin_memory()``; ``out=None`` allocates a pinned output
     when ``x`` is pinned, and ``valid_len`` must be pinned too) are read and
-    written in place by the kernel over the host link, except for rows long
-    enough to take the two-pass long-row kernels.  Otherwise the library moves
+    written in place by the kernel over the host link when the rows take the
+    streamed or register-resident kernels (up to 32,768 elements, 16,384 for
+    float32 outputs; 16-byte aligned rows).  Otherwise the library moves
     the rows through two device staging buffers in chunks, overlapping each
     chunk's copy in, softmax and copy back.  With ``wait`` the call returns
     after the stream has finished; otherwise ``out`` is ready once the stream
