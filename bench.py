@@ -16,6 +16,14 @@ Prints one JSON line on rank 0:
   roofline     the softmax kernel's achieved bandwidth (CUDA events around every
                launch in the timed region) against the measured HBM copy peak
   cpu_baseline the fp64 CPU reference timed on this host on a bounded sample
+  parity       the timed output buffer against the fp64 reference, all rows:
+               max relative error (fp32) or max ulp (fp16/bf16), max |1 - sum|,
+               masked lanes +0, and whether the bars are met
+  per_config   (softmax, one GPU) the same throughput, roofline and parity for
+               every workload of the bandwidth target, each timed over the same
+               --steps after the same --warmup
+  clocks       SM clock and clock-event reasons sampled through NVML every
+               100 us inside the timed region, from a child process
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME] [--op softmax|log_softmax|lse|apply_stats|
@@ -48,11 +56,12 @@ METRIC = "softmax GB/s (read+write) and rows/s on 1 GB300; % of HBM peak"
 UNIT = "GB/s"
 L2_BYTES = 129 * 10 ** 6
 LAUNCH_SAMPLE = 8
-PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4, "split": 5}
+PATHS = {"auto": 0, "regs": 1, "cluster": 2, "generic": 3, "stream": 4, "split": 5, "stripe": 6}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_regs.cuh",
                   "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
-                  "kernel_backward.cuh", "kernel_split_fused.cuh", "launch_impl.cuh", "smx_api.cu"]
+                  "kernel_backward.cuh", "kernel_split_fused.cuh", "kernel_stripe.cuh", "launch_impl.cuh",
+                  "smx_api.cu"]
 ATTN_SOURCES = ["smx_device.cuh", "kernel_attention.cuh", "kernel_attention_tc.cuh", "inst_attention.cu",
                 "smx_api.cu"]
 
@@ -187,6 +196,240 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# NVML clock-event reason bits (read only; nvmlDeviceGetCurrentClocksEventReasons)
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def nvml_sampler_main(device: str, path: str) -> int:
+    """Child process: poll the GPU's SM clock and clock-event reasons through
+    NVML (read-only queries) into `path`, one line per sample ("wall_time
+    sm_mhz max_mhz reasons_hex"): every 100 us after the parent writes "f" to
+    stdin (a timed region starts), every 20 ms after "s", until stdin closes.
+    A process of its own, so the polling never takes the launching thread's
+    interpreter lock."""
+    import ctypes
+    import select
+
+    try:
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+    except OSError:
+        print("error no-nvml", flush=True)
+        return 0
+    if nv.nvmlInit_v2() != 0:
+        print("error init", flush=True)
+        return 0
+    h = ctypes.c_void_p()
+    if device.startswith("GPU-"):
+        rc = nv.nvmlDeviceGetHandleByUUID(device.encode(), ctypes.byref(h))
+    else:
+        rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(device)), ctypes.byref(h))
+    if rc != 0:
+        print("error handle", flush=True)
+        return 0
+    reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+        getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+    mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+    interval = 0.02
+    with open(path, "w") as out:
+        print("ready", flush=True)
+        t_next = 0.0
+        while True:
+            if select.select([sys.stdin], [], [], 0)[0]:
+                c = sys.stdin.read(1)
+                if not c:
+                    break
+                interval = 1e-4 if c == "f" else 0.02
+                t_next = 0.0
+            t = time.time()
+            if t < t_next:
+                if interval > 1e-3:
+                    time.sleep(min(interval, t_next - t))
+                continue
+            t_next = t + interval
+            nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz))
+            reasons_fn(h, ctypes.byref(rs))
+            out.write(f"{t:.6f} {mhz.value} {mx.value} {rs.value:x}\n")
+    nv.nvmlShutdown()
+    return 0
+
+
+def summarize_clock_samples(lines, t_begin: float, t_end: float):
+    """Clock summary of the samples taken inside [t_begin, t_end] (wall time)."""
+    sm, smax, reasons = [], [], set()
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) != 4:
+            continue
+        try:
+            t, mhz, mx, bits = float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3], 16)
+        except ValueError:
+            continue
+        if not t_begin <= t <= t_end:
+            continue
+        sm.append(mhz)
+        smax.append(mx)
+        for bit, name in NVML_REASONS.items():
+            if bits & bit:
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm), "source": "NVML, polled in a child process",
+            "rejected": bool(reasons & set(REJECT_REASONS))}
+
+
+class NvmlSampler:
+    """Clocks sampled through NVML in a child process for the whole GPU leg,
+    every 100 us between fast() and slow(); window() summarises the samples
+    inside one timed region."""
+
+    def __init__(self, device: str):
+        import tempfile
+
+        self.device = device
+        self.proc = None
+        self.lines = None
+        fd, self.path = tempfile.mkstemp(prefix="smx_clocks_", suffix=".txt")
+        os.close(fd)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen([sys.executable, os.path.abspath(__file__), "--nvml-sampler",
+                                          self.device, self.path],
+                                         stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline().strip()
+        except OSError:
+            first = "error spawn"
+        if first != "ready":
+            if self.proc is not None:
+                self.proc.kill()
+                self.proc.wait()
+            self.proc = None
+        return self.proc is not None
+
+    def _send(self, c: str):
+        if self.proc is not None:
+            self.proc.stdin.write(c)
+            self.proc.stdin.flush()
+
+    def fast(self):
+        self._send("f")
+        time.sleep(0.002)  # the child has switched before the region starts
+
+    def slow(self):
+        self._send("s")
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.communicate(timeout=30)
+            self.proc = None
+        try:
+            with open(self.path) as fh:
+                self.lines = fh.read().splitlines()
+            os.unlink(self.path)
+        except OSError:
+            self.lines = self.lines or []
+
+    def window(self, t_begin: float, t_end: float):
+        return summarize_clock_samples(self.lines or [], t_begin, t_end)
+
+
+def nvml_device_id(torch, dev) -> str:
+    """NVML's name for the torch device: its UUID when torch reports one."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u and not u.startswith("GPU-"):
+            u = "GPU-" + u
+        return u
+    except Exception:  # noqa: BLE001 - older torch: fall back to the index
+        return str(dev.index or 0)
+
+
+# ---------------------------------------------------------------------------
+# Parity of a timed output with the fp64 reference (for the bench line).
+# ---------------------------------------------------------------------------
+F32_REL_TOL, F32_TINY, SUM_TOL, ULP_TOL = 2e-6, 1e-30, 1e-5, 1
+
+
+def parity_stats(y, p, out_dtype, valid_len=None):
+    """Error statistics of one softmax output against the fp64 reference p
+    [n, cols]: max relative error (fp32, where p >= 1e-30), max distance in
+    units in the last place from the correctly rounded value (fp16/bf16), max
+    |1 - sum(y)| over rows with a valid lane, and whether masked and
+    zero-probability lanes are +0 bit for bit and NaN rows NaN.
+    `within_tolerance` applies the bars: fp32 2e-6 relative and 1e-5 on the
+    sum, fp16/bf16 1 ulp."""
+    import oracle
+
+    n, cols = p.shape
+    L = np.full(n, cols, np.int64) if valid_len is None else np.clip(np.asarray(valid_len, np.int64), 0, cols)
+    masked = np.arange(cols)[None, :] >= L[:, None]
+    nan_rows = np.isnan(p).any(axis=1)
+    ok_lanes = ~nan_rows[:, None] & ~masked
+    zero_lanes = ok_lanes & (p == 0)
+    st = {"rows": int(n)}
+    if out_dtype == "f32":
+        y = np.asarray(y, np.float32).reshape(n, cols)
+        bits = y.view(np.uint32)
+        yv = y.astype(np.float64)
+        big = ok_lanes & (p >= F32_TINY)
+        rel = np.abs(yv[big] - p[big]) / p[big]
+        st["max_rel"] = float(rel.max()) if rel.size else 0.0
+        st["masked_zero_ok"] = bool(np.all(bits[masked] == 0) and np.all(bits[zero_lanes] == 0))
+        st["nan_rows_ok"] = bool(np.all(np.isnan(yv[nan_rows[:, None] & ~masked])))
+        small = ok_lanes & (p < F32_TINY)
+        tiny_ok = bool(np.all((yv[small] >= 0) & (yv[small] <= 2 * F32_TINY)))
+        normal = ~nan_rows & (L > 0) & (p.sum(axis=1) > 0)
+        s = np.where(masked, 0.0, yv)[normal].sum(axis=1)
+        st["max_sum_err"] = float(np.abs(s - 1.0).max()) if s.size else 0.0
+        st["within_tolerance"] = bool(st["max_rel"] <= F32_REL_TOL and st["max_sum_err"] <= SUM_TOL and tiny_ok
+                                      and st["masked_zero_ok"] and st["nan_rows_ok"]
+                                      and np.all(bits[ok_lanes] >> 31 == 0))
+    else:
+        yb = np.asarray(y).view(np.uint16).reshape(n, cols).astype(np.int64)
+        r = oracle.round_to(np.where(ok_lanes, p, 0.0), out_dtype).astype(np.int64)
+        diff = np.abs(yb - r)[ok_lanes]
+        st["max_ulp"] = int(diff.max()) if diff.size else 0
+        st["frac_exact"] = float((diff == 0).mean()) if diff.size else 1.0
+        st["masked_zero_ok"] = bool(np.all(yb[masked] == 0) and np.all(yb[zero_lanes] == 0))
+        exp_all = 0x7C00 if out_dtype == "f16" else 0x7F80
+        isnan = ((yb & exp_all) == exp_all) & ((yb & ~exp_all & 0x7FFF) != 0)
+        st["nan_rows_ok"] = bool(np.all(isnan[nan_rows[:, None] & ~masked]))
+        yv = oracle.decode(yb.astype(np.uint16), out_dtype).reshape(n, cols)
+        normal = ~nan_rows & (L > 0) & (p.sum(axis=1) > 0)
+        s = np.where(masked, 0.0, yv)[normal].sum(axis=1)
+        st["max_sum_err"] = float(np.abs(s - 1.0).max()) if s.size else 0.0
+        st["within_tolerance"] = bool(st["max_ulp"] <= ULP_TOL and st["masked_zero_ok"] and st["nan_rows_ok"]
+                                      and np.all(yb[ok_lanes] >> 15 == 0))
+    return st
+
+
+def parity_of_output(y_store, x_host, w, vl):
+    """parity_stats over all rows of the workload, in blocks of about 8M
+    elements; the statistics are the worst over the blocks."""
+    import oracle
+
+    block_rows = max(1, (8 << 20) // w.cols)
+    agg = {}
+    for r0 in range(0, w.rows, block_rows):
+        sel = np.arange(r0, min(w.rows, r0 + block_rows))
+        p = oracle.softmax_rows(x_host, w.in_dtype, w.rows, w.cols, vl, rows_sel=sel)
+        yb = y_store.reshape(w.rows, w.cols)[sel]
+        st = parity_stats(yb, p, w.out_dtype, None if vl is None else vl[sel])
+        for k, v in st.items():
+            if k == "rows":
+                agg[k] = agg.get(k, 0) + v
+            elif isinstance(v, bool):
+                agg[k] = agg.get(k, True) and v
+            elif k == "frac_exact":
+                agg[k] = min(agg.get(k, 1.0), v)
+            else:
+                agg[k] = max(agg.get(k, v), v)
+    return agg
 
 
 # ---------------------------------------------------------------------------
@@ -469,6 +712,91 @@ class GpuOp:
         return step, h2d, d2h
 
 
+# the workloads the HBM-bandwidth target is stated for (per_config entries)
+PER_CONFIG = ("f32_64x1000", "bf16_16384x4096", "f16_32768x1024_len", "f32_64x1048576_rise")
+
+
+def time_op(g, steps, warmup, stream, torch, dev, sampler=None, world=1, sample_launches=True):
+    """Warm up, then time `steps` launches of g between CUDA events on the
+    launching stream (synchronised on both sides).  Returns the region's ms,
+    sampled per-launch ms, the path and launches of a call, the wall-clock
+    bounds of the region and the index of the last launch."""
+    lib = g.lib
+    for i in range(warmup):
+        g.launch(i)
+    used_path = lib.smx_debug_last_path()
+    launches_per_call = lib.smx_debug_last_launches()
+    torch.cuda.synchronize(dev)
+    if g.smx.last_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    # per-launch durations from event pairs around every LAUNCH_SAMPLE-th step
+    # (an event pair around every launch would add its own gaps to the steps)
+    sampled = set(range(0, steps, LAUNCH_SAMPLE)) if sample_launches else set()
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.fast()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(steps):
+        if i in sampled:
+            ev[i][0].record(stream)
+            g.launch(i)
+            ev[i][1].record(stream)
+        else:
+            g.launch(i)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if sampler is not None:
+        sampler.slow()
+    if world > 1:
+        torch.distributed.barrier()
+    status = g.smx.last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    return (t_start.elapsed_time(t_end), [a.elapsed_time(b) for a, b in ev.values()], used_path,
+            launches_per_call, wall0, wall1, steps - 1)
+
+
+def timed_output_parity(g, last, x_host, vl_host, w):
+    """Parity statistics of the output buffer the last timed launch wrote."""
+    y = g.ys[last % g.nsets]
+    return parity_of_output(wl.torch_to_storage(y.cpu()).reshape(-1), x_host, w, vl_host)
+
+
+def per_config_entry(name, args, torch, smx, dev, stream, sampler, peak):
+    """The softmax on one workload: throughput over --steps after --warmup, the
+    roofline fraction, the committed profile's traffic, and parity statistics
+    of the timed output against the fp64 reference on all rows."""
+    w = wl.WORKLOADS[name]
+    x_host, vl_host = wl.host_input(name)
+    g = GpuOp("softmax", w, x_host, vl_host, dev, torch, smx, stream)
+    try:
+        ms, _, path, launches, wall0, wall1, last = time_op(g, args.steps, args.warmup, stream, torch, dev,
+                                                             sampler, sample_launches=False)
+        step_ms = ms / args.steps
+        achieved = g.bytes_step / (step_ms / 1e3) / 1e9
+        traffic, kernel = profile_traffic(name)
+        entry = {"workload": name, "value": achieved, "unit": UNIT, "ms_per_step": step_ms,
+                 "rows_per_s": w.rows / (step_ms / 1e3), "bytes_per_step": g.bytes_step,
+                 "path": PATH_NAMES.get(path, path), "kernels_per_step": launches,
+                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "frac": achieved / peak,
+                              "traffic": traffic, "kernel": kernel, "launch_timing": "timed region / steps"},
+                 "clocks": sampler.window(wall0, wall1) if sampler is not None and sampler.lines else None,
+                 "l2": f"rotating {g.nsets} input/output buffer sets, larger than L2 together"}
+        entry["_wall"] = (wall0, wall1)
+        entry["parity"] = timed_output_parity(g, last, x_host, vl_host, w)
+        return entry
+    finally:
+        del g
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, w):
     import torch
 
@@ -495,48 +823,20 @@ def run_ours(args, w):
     g = GpuOp(args.op, w, x_host, vl_host, dev, torch, smx, stream)
     bytes_step, nsets = g.bytes_step, g.nsets
 
-    for i in range(args.warmup):
-        g.launch(i)
-    used_path = lib.smx_debug_last_path()
-    launches_per_call = lib.smx_debug_last_launches()
-    torch.cuda.synchronize(dev)
-    assert smx.last_device_status() == 0
-
-    sampler = ClockSampler(local)
-    if rank == 0 or world > 1:
-        sampler.start()
-    # per-launch durations from event pairs around every LAUNCH_SAMPLE-th step
-    # (an event pair around every launch would add its own gaps to the steps)
-    sampled = set(range(0, args.steps, LAUNCH_SAMPLE))
-    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for i in sampled}
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    wall0 = time.time()
-    t_start.record(stream)
-    for i in range(args.steps):
-        if i in sampled:
-            ev[i][0].record(stream)
-            g.launch(i)
-            ev[i][1].record(stream)
-        else:
-            g.launch(i)
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop(wall0, wall1)
-    status = smx.last_device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
-    local_ms = t_start.elapsed_time(t_end)
-    launch_ms = [a.elapsed_time(b) for a, b in ev.values()]
+    # clocks: NVML polled every 100 us inside each timed region (a child
+    # process); nvidia-smi every 100 ms as the fallback
+    sampler = NvmlSampler(nvml_device_id(torch, dev))
+    if not sampler.start():
+        sampler = None
+    smi = None
+    if sampler is None:
+        smi = ClockSampler(local)
+        smi.start()
+    local_ms, launch_ms, used_path, launches_per_call, wall0, wall1, last = time_op(
+        g, args.steps, args.warmup, stream, torch, dev, sampler, world)
     elapsed_ms = max_over_ranks(local_ms, world)
     agg = aggregate(bytes_step, w.rows, args.steps, world, elapsed_ms / 1e3)
+    parity_main = timed_output_parity(g, last, x_host, vl_host, w) if args.op == "softmax" and rank == 0 else None
 
     # end to end through the public call: pinned host inputs in, outputs back
     e2e_step, h2d, d2h = g.e2e()
@@ -555,13 +855,32 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e = aggregate(bytes_step, w.rows, e2e_steps, world, e2e_ms / 1e3)
+    del g
+    torch.cuda.empty_cache()
+
+    peak, peak_kind = measured_peak()
+    per_config = None
+    if world == 1 and args.per_config and args.op == "softmax" and args.path == "auto":
+        per_config = []
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            per_config.append(per_config_entry(name, args, torch, smx, dev, stream, sampler, peak))
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.window(wall0, wall1)
+        for e in per_config or []:
+            e["clocks"] = sampler.window(*e["_wall"])
+    else:
+        clocks = smi.stop(wall0, wall1)
+    for e in per_config or []:
+        e.pop("_wall", None)
 
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
 
-    peak, peak_kind = measured_peak()
     # the kernel's average launch duration: when a step is one launch, this
     # rank's timed region (CUDA events on the launching stream) over its
     # launches; otherwise the step's sampled event pairs
@@ -608,6 +927,10 @@ def run_ours(args, w):
         "kernels_per_step": launches_per_call,
         "clocks": clocks,
     }
+    if parity_main is not None:
+        line["parity"] = parity_main
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -805,6 +1128,9 @@ def run_attention_reference(args):
 
 
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
+    if argv[:1] == ["--nvml-sampler"]:
+        return nvml_sampler_main(argv[1], argv[2])
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
@@ -821,6 +1147,9 @@ def main(argv=None):
                     help="seconds the reference arm spends over all its steps")
     ap.add_argument("--op", choices=list(wl.OPS), default="softmax",
                     help="entry point to time (default: the softmax)")
+    ap.add_argument("--per-config", type=int, default=1,
+                    help="softmax only, one GPU: also time every workload of the bandwidth target with "
+                         "the same steps and report its parity against the reference (1) or not (0)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

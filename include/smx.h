@@ -33,14 +33,17 @@
  * fp32 even when the inputs are not"); the output type is chosen separately.
  *
  * Memory and ownership: every data pointer is a device pointer owned by the
- * caller; the library never frees or retains it.  It allocates one device
- * status word and creates one memory pool per device on first use.  The
- * long-row paths (rows too long for one CTA) take a small stream-ordered
- * scratch allocation per call from that pool for their chunk summaries
- * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`: 8 bytes per chunk of
- * 4096 elements, plus 4 bytes per row); the pool keeps up to 64 MiB between
- * calls so that later calls reuse it.  smx_softmax_rows_fixed_scratch uses a
- * fixed array instead.  No other call allocates.
+ * caller; the library never frees or retains it.  On first use of a device it
+ * allocates one status word and creates one memory pool.  The long-row paths
+ * (rows too long for one CTA) and the staged host-buffer call keep their
+ * scratch (stripe and chunk summaries: 8 bytes per stripe or 4096-element
+ * chunk; per-row counters; staging slots) in per-device buffers from that
+ * pool that only grow: a call that needs more than any call before reallocates
+ * the buffer (stream-ordered), every other call allocates nothing.  Calls that
+ * use the scratch are ordered on the device: a call on a stream other than
+ * the previous user's first waits (cudaStreamWaitEvent) for the event recorded
+ * after that user.  smx_softmax_rows_fixed_scratch uses a fixed array instead.
+ * No other call allocates.
  * Every call is asynchronous on `stream` (NULL is the legacy default stream) and
  * returns after enqueueing its kernels.
  *
@@ -106,7 +109,7 @@ smx_status smx_softmax_rows(const void *x, void *y, int64_t rows, int64_t cols,
  *    link.
  *  - Staged, otherwise (pageable buffers; longer rows, which the cluster and
  *    long-row kernels take; unaligned rows): the rows pass through
- *    two device staging slots (taken from the library's memory pool) in
+ *    two device staging slots (the library's per-device scratch) in
  *    chunks of about 16 MiB of input: chunk i's copy to the device and its
  *    softmax run on `stream`, its copy back on a second stream the library
  *    owns, so both directions of the host link and the kernels run at once.
@@ -314,8 +317,11 @@ int smx_version(void);
  *   2 = thread-block-cluster rows; 3 = generic (scalar, two-pass) rows;
  *   4 = persistent rows with the next rows prefetched (cp.async); 5 = long
  *   rows in chunks, in slabs of rows (chunk summaries, then merge and
- *   normalise; one slab of all rows unless smx_debug_set_split_slab).  A
- *   forced path that cannot run the shape falls back to the automatic choice.
+ *   normalise; one slab of all rows unless smx_debug_set_split_slab); 6 =
+ *   long rows read once, each row in column stripes held in the shared
+ *   memory of a cooperative grid (softmax, log_softmax, cross-entropy with a
+ *   gradient).  A forced path that cannot run the shape falls back to the
+ *   automatic choice.
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
  * smx_debug_set_wait_limit(n): n > 0: polls of a staging barrier (path 2)
@@ -325,7 +331,7 @@ int smx_version(void);
  *   barrier that nothing signals, records SMX_ERR_TIMEOUT when that wait runs
  *   out (it always does), then works normally -- a deterministic probe of the
  *   error path.
- * smx_debug_last_path(): the path (1..5) the last softmax/stats call on this
+ * smx_debug_last_path(): the path (1..6) the last softmax/stats call on this
  *   thread used, 0 if none.
  * smx_debug_last_launches(): kernels the last call on this thread launched.
  * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of
@@ -358,6 +364,20 @@ int smx_version(void);
  * smx_debug_set_cluster_staging(m): how path 2 stages its shared-memory part:
  *   1 = bulk asynchronous copies (TMA) with one mbarrier per piece, 2 = per-
  *   thread cp.async; 0 = automatic.
+ * smx_debug_alloc_count(): device allocations, events and streams the library
+ *   has created in this process (a steady loop of calls adds none).
+ * smx_debug_probe_math(a, b, out, n, which, stream): out[i] = the library's
+ *   device primitive `which` at a[i] (and b[i]), for measuring its error:
+ *   0 = ex2.approx.ftz.f32 2^a, 1 = ex2.approx.f32 2^a (keeps subnormal
+ *   results), 2 = rcp.approx.ftz.f32 1/a, 3 = the refined reciprocal the
+ *   kernels normalise with, 4 = the compensated e^(a - b) of fp32 outputs,
+ *   5 = one term e^(a - b) as the statistics path forms it.  a, b, out:
+ *   device float[n] (b only for 4 and 5).  The pages have no counterpart.
+ * smx_debug_set_count_probe(polls): polls > 0: the per-row count waits of
+ *   the cooperative long-row kernels (path 6, and path 5 in its single-launch
+ *   form) wait for one more stripe or chunk than the row has, give up after
+ *   `polls` polls and record SMX_ERR_TIMEOUT (the output is then undefined) --
+ *   a deterministic probe of that error path; 0 = off.
  */
 void smx_debug_force_path(int path);
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes);
@@ -375,6 +395,10 @@ void smx_debug_set_split_fused(int on);
 void smx_debug_set_attention_mma_sync(int on);
 void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
+int64_t smx_debug_alloc_count(void);
+void smx_debug_set_count_probe(int64_t polls);
+smx_status smx_debug_probe_math(const float *a, const float *b, float *out, int64_t n, int which,
+                                smx_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -14,4 +14,6 @@ int split_fused_occupancy_bf16(int threads) { return split_fused_occupancy<__nv_
 int backward_occupancy_bf16(int vpt, int threads) {
   return backward_occupancy<__nv_bfloat16>(vpt, threads);
 }
+int stripe_occupancy_bf16(int64_t smem) { return stripe_occupancy<__nv_bfloat16>(smem); }
+int stripe_static_smem_bf16() { return stripe_static_smem<__nv_bfloat16>(); }
 }  // namespace smx

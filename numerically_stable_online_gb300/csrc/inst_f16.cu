@@ -14,4 +14,6 @@ int split_fused_occupancy_f16(int threads) { return split_fused_occupancy<__half
 int backward_occupancy_f16(int vpt, int threads) {
   return backward_occupancy<__half>(vpt, threads);
 }
+int stripe_occupancy_f16(int64_t smem) { return stripe_occupancy<__half>(smem); }
+int stripe_static_smem_f16() { return stripe_static_smem<__half>(); }
 }  // namespace smx

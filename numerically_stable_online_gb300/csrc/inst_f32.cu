@@ -14,4 +14,6 @@ int split_fused_occupancy_f32(int threads) { return split_fused_occupancy<float>
 int backward_occupancy_f32(int vpt, int threads) {
   return backward_occupancy<float>(vpt, threads);
 }
+int stripe_occupancy_f32(int64_t smem) { return stripe_occupancy<float>(smem); }
+int stripe_static_smem_f32() { return stripe_static_smem<float>(); }
 }  // namespace smx

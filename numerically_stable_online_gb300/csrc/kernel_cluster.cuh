@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
     return vend > c0 ? (int)((vend - c0) / V) : 0;
   };
   auto piece_end = [&](int p, int lim) { return (p + 1) * P < lim ? (p + 1) * P : lim; };
+  // thread 0 (TMA): bit p = parity of the number of fills issued on piece p's
+  // barrier, so that the last issued fill's phase is known after a timeout
+  uint32_t fill_par = 0;
   // stage the valid part of piece p of `row` (s_nv staged-and-valid vectors)
   auto fill_piece = [&](int64_t row, int s_nv, int p) {
     const InT* src = x + row * cols + c0;
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
       } else {
         mbar_arrive(smem_addr(&bars[p]));
       }
+      fill_par ^= 1u << p;
     } else {
       const int p1 = piece_end(p, s_nv);
       for (int vi = p * P + t; vi < p1; vi += T)
@@ -423,9 +427,13 @@ __global__ void __launch_bounds__(CLUSTER_THREADS, 1)
   if constexpr (TMA) {
     if (timed_out) {
       atomicOr(status, DEV_TIMEOUT);
-      // let this CTA's own copies land before its shared memory is released
-      const int last = rows > row_first ? (int)(((rows - 1 - row_first) / gridDim.y) & 1) : 0;
-      for (int p = 0; p < NP; ++p) mbar_wait_bounded(smem_addr(&bars[p]), (uint32_t)last, int64_t(1) << 21);
+      // Thread 0 issued every copy.  After its own wait ran out it stopped
+      // refilling, so each piece has at most one phase still pending: the one
+      // its last issued fill completes (fill k completes phase k, parity k & 1).
+      // Let those copies land before this CTA's shared memory is released.
+      if (t == 0 && row_first < rows)
+        for (int p = 0; p < NP; ++p)
+          mbar_wait_bounded(smem_addr(&bars[p]), ((fill_par >> p) & 1u) ^ 1u, int64_t(1) << 21);
     }
   } else {
     asm volatile("cp.async.wait_group 0;" ::: "memory");

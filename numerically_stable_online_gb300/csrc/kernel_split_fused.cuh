@@ -35,6 +35,7 @@ struct SplitArgs {
   const int64_t* target;
   float* loss;
   int64_t max_polls;
+  int64_t probe;     // > 0: each count wait asks for one chunk more than the row has (error-path probe)
   int* status;
 };
 
@@ -192,9 +193,11 @@ __global__ void __launch_bounds__(256, 3)
       // ---- phase B: the row's merged (M, D), then the chunk's outputs
       if (row != have_row) {
         if (g == 0) {
+          const unsigned need = (unsigned)nch + (a.probe > 0 ? 1u : 0u);
+          const int64_t limit = a.probe > 0 ? a.probe : a.max_polls;
           int64_t polls = 0;
-          while (ld_acquire_u32(a.count + row) < (unsigned)nch) {
-            if (++polls > a.max_polls) {
+          while (ld_acquire_u32(a.count + row) < need) {
+            if (++polls > limit) {
               atomicOr(a.status, DEV_TIMEOUT);
               break;
             }

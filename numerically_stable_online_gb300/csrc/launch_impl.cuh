@@ -12,6 +12,7 @@
 #include "kernel_stream.cuh"
 #include "kernel_regs.cuh"
 #include "kernel_split_fused.cuh"
+#include "kernel_stripe.cuh"
 #include "smx_launch.h"
 
 namespace smx {
@@ -216,10 +217,8 @@ cudaError_t launch_split_fused(const Call& c, const Plan& p) {
   }
   const int grid = p.fused_ctas < resident[dev][1] ? p.fused_ctas : resident[dev][1];
   const size_t n_sum = (size_t)c.rows * p.nchunks;
-  const size_t bytes = 2 * n_sum * sizeof(float) + (size_t)c.rows * sizeof(unsigned);
-  char* base = nullptr;
-  e = scratch_alloc(c, reinterpret_cast<void**>(&base), bytes);
-  if (e != cudaSuccess) return e;
+  char* base = reinterpret_cast<char*>(p.scratch);  // the library's per-device scratch
+  if (base == nullptr) return cudaErrorInvalidValue;
   SplitArgs a;
   a.rows = c.rows;
   a.cols = c.cols;
@@ -231,19 +230,89 @@ cudaError_t launch_split_fused(const Call& c, const Plan& p) {
   a.target = c.target;
   a.loss = c.loss;
   a.max_polls = c.max_polls;
+  a.probe = p.stripe_probe;
   a.status = c.status;
   e = cudaMemsetAsync(a.count, 0, (size_t)c.rows * sizeof(unsigned), c.stream);
-  if (e == cudaSuccess) {
-    const InT* xp = static_cast<const InT*>(c.x);
-    OutT* yp = static_cast<OutT*>(c.y);
-    const int32_t* vl = c.valid_len;
-    void* args[] = {(void*)&xp, (void*)&yp, (void*)&a, (void*)&vl};
-    note_launch();
-    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3((unsigned)grid),
-                                    dim3((unsigned)p.threads), args, (size_t)smem, c.stream);
+  if (e != cudaSuccess) return e;
+  const InT* xp = static_cast<const InT*>(c.x);
+  OutT* yp = static_cast<OutT*>(c.y);
+  const int32_t* vl = c.valid_len;
+  void* args[] = {(void*)&xp, (void*)&yp, (void*)&a, (void*)&vl};
+  note_launch();
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3((unsigned)grid),
+                                     dim3((unsigned)p.threads), args, (size_t)smem, c.stream);
+}
+
+// Long rows read once (kernel_stripe.cuh): one cooperative launch of
+// groups x Q CTAs, each row's stripes kept in shared memory from their
+// summary to their normalisation.  p.scratch holds the stripe summaries;
+// p.stripe_count / p.stripe_count_next the two counter arrays (this call's,
+// zero; the next call's, zeroed by the kernel).
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_stripe(const Call& c, const Plan& p) {
+  auto kern = k_rows_stripe<InT, OutT, MODE>;
+  const int64_t smem = (int64_t)p.stripe_slots * p.stripe_slot_vecs * 16;
+  cudaError_t e = smem_raise(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  if (p.scratch == nullptr || p.stripe_count == nullptr) return cudaErrorInvalidValue;
+  StripeArgs a;
+  a.rows = c.rows;
+  a.cols = c.cols;
+  a.Q = p.stripe_q;
+  a.groups = p.stripe_groups;
+  a.nslots = p.stripe_slots;
+  a.slot_vecs = p.stripe_slot_vecs;
+  a.sums = reinterpret_cast<float2*>(p.scratch);
+  a.count = p.stripe_count;
+  a.count_next = p.stripe_count_next;
+  a.count_next_n = p.stripe_count_next_n;
+  a.target = c.target;
+  a.loss = c.loss;
+  a.max_polls = c.max_polls;
+  a.probe = p.stripe_probe;
+  a.status = c.status;
+  const InT* xp = static_cast<const InT*>(c.x);
+  OutT* yp = static_cast<OutT*>(c.y);
+  const int32_t* vl = c.valid_len;
+  void* args[] = {(void*)&xp, (void*)&yp, (void*)&a, (void*)&vl};
+  note_launch();
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern),
+                                     dim3((unsigned)(p.stripe_q * p.stripe_groups)), dim3(STRIPE_THREADS),
+                                     args, (size_t)smem, c.stream);
+}
+
+// Resident CTAs per SM of the stripe kernel with `smem` bytes of ring (every
+// mode and output type must fit as many; the fp32 softmax, the bf16 and fp32
+// cross-entropy and the log_softmax stand for them).
+template <typename InT>
+int stripe_occupancy(int64_t smem) {
+  auto query = [&](auto kern) -> int {
+    int n = 0;
+    if (smem_raise(reinterpret_cast<const void*>(kern), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, STRIPE_THREADS, (size_t)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  };
+  int n = query(k_rows_stripe<InT, float, MODE_SOFTMAX>);
+  const int n2 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_CE>);
+  const int n3 = query(k_rows_stripe<InT, float, MODE_CE>);
+  const int n4 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_LOG>);
+  n = n2 < n ? n2 : n;
+  n = n3 < n ? n3 : n;
+  return n4 < n ? n4 : n;
+}
+
+// Static shared memory of the stripe kernel (the ring is dynamic).
+template <typename InT>
+int stripe_static_smem() {
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, k_rows_stripe<InT, float, MODE_CE>) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
   }
-  const cudaError_t f = cudaFreeAsync(base, c.stream);
-  return e != cudaSuccess ? e : f;
+  return (int)fa.sharedSizeBytes;
 }
 
 // Resident CTAs per SM of the one-launch long-row kernel (the fp32-output
@@ -293,26 +362,20 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
                                                                c.d_in);
   } else {
     // softmax, log_softmax and the cross-entropy with its gradient: one
-    // persistent cooperative launch (kernel_split_fused.cuh) unless switched
-    // off or the scratch is fixed
-    if constexpr (MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE) {
-      if (p.fused_split && p.scratch == nullptr && (MODE != MODE_CE || c.y != nullptr))
+    // persistent cooperative launch (kernel_split_fused.cuh) when planned
+    if (split_uses_fused(c, p)) {
+      if constexpr (MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE)
         return launch_split_fused<InT, OutT, MODE>(c, p);
     }
     // the statistics-only calls (row statistics, LSE, the loss alone) read
     // every element once: one slab of all rows
-    const bool read_once = (MODE == MODE_STATS || (MODE == MODE_CE && c.y == nullptr)) &&
-                           c.rows * p.nchunks <= ((int64_t)1 << 31) && p.scratch == nullptr;
+    const bool read_once = split_read_once(c, p);
     // a slab is never more rows than the call has (the scratch is sized by it)
     const int64_t slab = (read_once || p.slab_rows > c.rows) ? c.rows : p.slab_rows;
     const size_t part_n = (size_t)slab * p.nchunks;
-    const size_t bytes = split_scratch_bytes(slab, p.nchunks);
-    char* base = reinterpret_cast<char*>(p.scratch);
+    char* base = reinterpret_cast<char*>(p.scratch);  // the library's or the caller's scratch
+    if (base == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaSuccess;
-    if (base == nullptr) {
-      e = scratch_alloc(c, reinterpret_cast<void**>(&base), bytes);
-      if (e != cudaSuccess) return e;
-    }
     float* pm = reinterpret_cast<float*>(base);
     float* pd = pm + part_n;
     for (int64_t r0 = 0; r0 < c.rows && e == cudaSuccess; r0 += slab) {
@@ -340,10 +403,6 @@ cudaError_t launch_split(const Call& c, const Plan& p) {
             pm, pd, p.nchunks, c.m_out + r0, c.d_out == nullptr ? nullptr : c.d_out + r0);
         e = cudaGetLastError();
       }
-    }
-    if (p.scratch == nullptr) {
-      const cudaError_t f = cudaFreeAsync(base, c.stream);
-      if (e == cudaSuccess) e = f;
     }
     return e;
   }
@@ -414,23 +473,14 @@ cudaError_t launch_backward(const Call& c, const Plan& p) {
   if (p.path != PATH_SPLIT) return cudaErrorInvalidValue;
   // long rows: per slab, the chunks' partial dots, then dx per chunk
   const int64_t slab = p.slab_rows < c.rows ? p.slab_rows : c.rows;  // sizes the scratch
-  const size_t bytes = (size_t)slab * p.nchunks * sizeof(float);
-  char* base = reinterpret_cast<char*>(p.scratch);
+  float* part = p.scratch;  // the library's per-device scratch
+  if (part == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
-  if (base == nullptr) {
-    e = scratch_alloc(c, reinterpret_cast<void**>(&base), bytes);
-    if (e != cudaSuccess) return e;
-  }
-  float* part = reinterpret_cast<float*>(base);
   for (int64_t r0 = 0; r0 < c.rows && e == cudaSuccess; r0 += slab) {
     const int64_t n = c.rows - r0 < slab ? c.rows - r0 : slab;
     const Items it{n * p.nchunks, r0, c.cols, (int)p.chunk, p.nchunks, 0, 0};
     e = launch_bwd_k<InT, float, SV, BWD_DOT>(c, p, it, part, nullptr);
     if (e == cudaSuccess) e = launch_bwd_k<InT, OutT, SV, BWD_APPLY>(c, p, it, nullptr, part);
-  }
-  if (p.scratch == nullptr) {
-    const cudaError_t f = cudaFreeAsync(base, c.stream);
-    if (e == cudaSuccess) e = f;
   }
   return e;
 }
@@ -478,6 +528,11 @@ cudaError_t launch_typed(const Call& c, const Plan& p) {
     case PATH_GENERIC: return launch_generic<InT, OutT, MODE>(c);
     case PATH_STREAM: return launch_stream<InT, OutT, MODE>(c, p);
     case PATH_SPLIT: return launch_split<InT, OutT, MODE>(c, p);
+    case PATH_STRIPE:
+      if constexpr (MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE) {
+        if (MODE != MODE_CE || c.y != nullptr) return launch_stripe<InT, OutT, MODE>(c, p);
+      }
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

@@ -29,17 +29,44 @@ constexpr int64_t DEFAULT_MAX_POLLS = int64_t(1) << 21;
 // static arrays (barriers, per-warp partials, the CTA summary)
 constexpr int64_t CLUSTER_STATIC_SMEM = 1024;
 
+// A device buffer of the library's that only grows: reserved at the first call
+// that needs it and reallocated only when a call needs more than any before.
+struct ScratchBuf {
+  char* base = nullptr;
+  size_t bytes = 0;
+};
+
+// The per-device scratch of the long-row paths and of the staged host-buffer
+// call.  Calls that use it are ordered on the device: a call on another stream
+// than the previous user's first waits for the event recorded after it, so
+// calls on different streams never share the buffers at once.  Held (mutex)
+// from the reservation to the event record.
+struct ScratchState {
+  std::mutex mu;
+  cudaEvent_t done = nullptr;       // recorded after the last call that used the scratch
+  cudaStream_t last = nullptr;      // that call's stream
+  bool used = false;
+  ScratchBuf work;                  // chunk / stripe summaries, backward partial dots
+  ScratchBuf counts;                // the stripe kernel's two per-row counter arrays, zeroed at growth
+  int64_t count_cap = 0;            // rows each counter array holds
+  int count_parity = 0;             // which array the next stripe call counts in
+  ScratchBuf staging;               // the host-buffer call's device slots
+  cudaEvent_t computed[4] = {}, copied[4] = {}, host_done = nullptr;  // the host-buffer call's events
+};
+
 struct DeviceInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   bool supported = false;
   int sm_count = 0;
   int64_t smem_optin = 0;
   int64_t l2_bytes = 0;
   int* status = nullptr;   // device status word
   cudaMemPool_t pool = nullptr;  // the long-row paths' scratch (keeps its memory between calls)
-  int max_cluster[3] = {0, 0, 0};  // per input type, 0 = not queried yet
+  std::atomic<int> max_cluster[3] = {0, 0, 0};  // per input type, 0 = not queried yet
   bool coop = false;                // cooperative launches supported
   cudaStream_t copy_stream = nullptr;  // the host-buffer call's copies back (created on first use)
+  ScratchState scratch;
+  int stripe_smem_static[3] = {-1, -1, -1};  // per input type, queried once
 };
 
 DeviceInfo g_dev[MAX_DEVICES];
@@ -66,6 +93,11 @@ std::atomic<int> g_host_staged{0};     // host-buffer call: 1 = always through t
 std::atomic<int> g_attention_mma_sync{0};  // 1: the attention forward on mma.sync instead of tcgen05  // 0: long rows in one cooperative launch; 1: two launches per slab  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
+// Device allocations, events and streams the library has created (a testing
+// count: a steady loop of calls adds none).
+std::atomic<int64_t> g_alloc_calls{0};
+std::atomic<int64_t> g_count_probe{0};  // > 0: the cooperative long-row kernels' error-path probe (polls)
+
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
 
@@ -90,9 +122,9 @@ smx_status device_info(DeviceInfo** out) {
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_UNSUPPORTED);
   if (dev < 0 || dev >= MAX_DEVICES) return SMX_ERR_UNSUPPORTED;
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       int major = 0, minor = 0, sms = 0, optin = 0, l2 = 0;
       if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
@@ -112,6 +144,7 @@ smx_status device_info(DeviceInfo** out) {
       if (d.supported) {
         int* s = nullptr;
         if ((e = cudaMalloc(&s, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+        ++g_alloc_calls;
         if ((e = cudaMemset(s, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
         d.status = s;
         // a pool of the library's own, so that the per-call scratch of the
@@ -129,13 +162,59 @@ smx_status device_info(DeviceInfo** out) {
         if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
           return cuda_fail(e, SMX_ERR_DEVICE);
         d.pool = pool;
+        ++g_alloc_calls;
       }
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   if (!d.supported) return SMX_ERR_UNSUPPORTED;
   *out = &d;
   return SMX_OK;
+}
+
+// Make `b` hold at least `bytes` for a call on `stream` (caller holds st.mu).
+// Orders the call after the scratch's previous user when that ran on another
+// stream; grows the buffer (stream-ordered, zeroed when asked) only when the
+// call needs more than any call before.
+cudaError_t scratch_reserve(DeviceInfo& d, ScratchBuf& b, size_t bytes, cudaStream_t stream, bool zero) {
+  ScratchState& st = d.scratch;
+  cudaError_t e;
+  if (st.done == nullptr) {
+    if ((e = cudaEventCreateWithFlags(&st.done, cudaEventDisableTiming)) != cudaSuccess) return e;
+    ++g_alloc_calls;
+  }
+  if (st.used && st.last != stream) {
+    if ((e = cudaStreamWaitEvent(stream, st.done, 0)) != cudaSuccess) return e;
+    st.last = stream;  // later reservations of this call need no second wait
+  }
+  if (bytes <= b.bytes) return cudaSuccess;
+  size_t nb = b.bytes + b.bytes / 2;
+  if (nb < bytes) nb = bytes;
+  nb = (nb + 4095) / 4096 * 4096;
+  if (b.base != nullptr) {
+    if ((e = cudaFreeAsync(b.base, stream)) != cudaSuccess) return e;
+    b.base = nullptr;
+    b.bytes = 0;
+  }
+  if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&b.base), nb, d.pool, stream)) != cudaSuccess) {
+    b.base = nullptr;
+    return e;
+  }
+  ++g_alloc_calls;
+  b.bytes = nb;
+  if (zero && (e = cudaMemsetAsync(b.base, 0, nb, stream)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+// The call on `stream` has enqueued its last use of the scratch (caller holds st.mu).
+cudaError_t scratch_release(DeviceInfo& d, cudaStream_t stream) {
+  ScratchState& st = d.scratch;
+  const cudaError_t e = cudaEventRecord(st.done, stream);
+  if (e == cudaSuccess) {
+    st.last = stream;
+    st.used = true;
+  }
+  return e;
 }
 
 // Residency answers (occupancy queries) are properties of the device and the
@@ -379,12 +458,75 @@ bool plan_split(DeviceInfo& d, int64_t cols, int in_dtype, Plan* p) {
       if (forced > 0) fc = forced < fo ? forced : fo;
       p->fused_split = true;
       p->fused_ctas = fc * d.sm_count;
+      p->stripe_probe = g_count_probe.load();
     }
   }
   const int hs = g_split_hint_stats.load(), ha = g_split_hint_apply.load();
   p->l2_hint_stats = hs >= 0 ? hs : 1;  // the statistics pass's reads stay for the re-read
   p->l2_hint_apply = ha >= 0 ? ha : 2;  // the normalising pass's reads are the last
   return true;
+}
+
+int stripe_occupancy(int in_dtype, int64_t smem) {
+  return cached_query(occ_key(6, in_dtype, (uint64_t)(smem / 16)), [&] {
+    switch (in_dtype) {
+      case SMX_F32: return stripe_occupancy_f32(smem);
+      case SMX_F16: return stripe_occupancy_f16(smem);
+      default: return stripe_occupancy_bf16(smem);
+    }
+  });
+}
+
+// Long rows read once (kernel_stripe.cuh), for the softmax, log_softmax and
+// the cross-entropy with a gradient: Q CTAs per row, each holding one column
+// stripe of every row of its group in a ring of shared-memory slots.  The
+// stripes are as short as the CTAs allow, so that the ring holds as many as
+// possible (at least LAG + 2: LAG rows held between summary and
+// normalisation, plus copies in flight); the preferred ring is 8 slots, then
+// 6, then 4.  Not planned when a row needs more CTAs than the device holds or
+// the device cannot launch cooperatively.
+bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
+  if (!d.coop) return false;
+  const int es = elem_size(in_dtype);
+  const int V = 16 / es;
+  const int64_t nvec = cols / V;
+  if (nvec <= 0) return false;
+  int& st = d.stripe_smem_static[in_dtype];
+  if (st < 0) {
+    st = in_dtype == SMX_F32 ? stripe_static_smem_f32()
+                             : (in_dtype == SMX_F16 ? stripe_static_smem_f16() : stripe_static_smem_bf16());
+    if (st < 0) return false;
+  }
+  const int64_t ring_bytes = (d.smem_optin - st - 256) / 16 * 16;  // (256: the runtime's own reserve)
+  const int64_t ring_vecs = ring_bytes / 16;
+  const int64_t cap = d.sm_count < STRIPE_MAX_Q ? d.sm_count : STRIPE_MAX_Q;  // one CTA per SM
+  for (const int target : {8, 6, STRIPE_LAG + 2}) {
+    const int64_t slot_cap = ring_vecs / target;
+    if (slot_cap <= 0) continue;
+    const int64_t q_min = (nvec + slot_cap - 1) / slot_cap;
+    if (q_min > cap) continue;
+    int64_t groups = d.sm_count / q_min;
+    if (groups > rows) groups = rows;
+    if (groups < 1) groups = 1;
+    int64_t Q = d.sm_count / groups;
+    if (Q > STRIPE_MAX_Q) Q = STRIPE_MAX_Q;
+    if (Q > nvec) Q = nvec;
+    const int64_t slot_vecs = (nvec + Q - 1) / Q;
+    int64_t nslots = ring_vecs / slot_vecs;
+    if (nslots > STRIPE_MAX_SLOTS) nslots = STRIPE_MAX_SLOTS;
+    if (nslots < STRIPE_LAG + 2) continue;
+    const int64_t smem = nslots * slot_vecs * 16;
+    if (stripe_occupancy(in_dtype, smem) < 1) return false;
+    p->path = PATH_STRIPE;
+    p->stripe_q = (int)Q;
+    p->stripe_groups = (int)groups;
+    p->stripe_slots = (int)nslots;
+    p->stripe_slot_vecs = (int)slot_vecs;
+    p->ctas = (int)(Q * groups);
+    p->stripe_probe = g_count_probe.load();
+    return true;
+  }
+  return false;
 }
 
 bool plan_cluster(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
@@ -490,6 +632,8 @@ void plan_backward(DeviceInfo& d, const Call& c, bool vec_ok, Plan* p) {
   p->slab_rows = slab;
 }
 
+smx_status launch_planned(Call& c, DeviceInfo& dev, Plan p);
+
 smx_status run_backward(Call& c, DeviceInfo& dev) {
   const int es = elem_size(c.in_dtype);
   const bool vec_ok = (reinterpret_cast<uintptr_t>(c.x) % 16 == 0) &&
@@ -497,16 +641,7 @@ smx_status run_backward(Call& c, DeviceInfo& dev) {
                       (reinterpret_cast<uintptr_t>(c.y) % 16 == 0) && ((c.cols * es) % 16 == 0);
   Plan p;
   plan_backward(dev, c, vec_ok, &p);
-  c.pool = dev.pool;
-  cudaError_t e;
-  switch (c.in_dtype) {
-    case SMX_F32: e = launch_in_f32(c, p); break;
-    case SMX_F16: e = launch_in_f16(c, p); break;
-    default: e = launch_in_bf16(c, p); break;
-  }
-  t_last_path = p.path;
-  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
-  return SMX_OK;
+  return launch_planned(c, dev, p);
 }
 
 // The kernel family and launch shape for a call (no launch).
@@ -519,12 +654,15 @@ Plan plan_call(const Call& c, DeviceInfo& dev) {
   // softmax and (m, d) statistics run on every kernel; LSE, log_softmax and
   // the apply mode on the streamed, long-row and generic ones
   const bool classic = c.mode == MODE_SOFTMAX || (c.mode == MODE_STATS && c.d_out != nullptr);
+  const bool stripe_mode = c.mode == MODE_SOFTMAX || c.mode == MODE_LOG || (c.mode == MODE_CE && c.y != nullptr);
   Plan p;
   const int force = g_force_path.load();
   bool planned = false;
   if (vec_ok) {
     if (force == PATH_CLUSTER && classic) {
       planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
+    } else if (force == PATH_STRIPE && stripe_mode) {
+      planned = plan_stripe(dev, c.rows, c.cols, c.in_dtype, &p);
     } else if (force == PATH_SPLIT) {
       planned = plan_split(dev, c.cols, c.in_dtype, &p);
     } else if (force != PATH_GENERIC) {
@@ -552,6 +690,10 @@ Plan plan_call(const Call& c, DeviceInfo& dev) {
         planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
         if (planned && c.rows < p.resident_clusters) planned = false;
       }
+      // longer rows, or too few to fill the clusters: read once in column
+      // stripes over all SMs when the stripes fit the SMs' shared memory
+      // (softmax, log_softmax, cross-entropy with a gradient)
+      if (!planned && stripe_mode) planned = plan_stripe(dev, c.rows, c.cols, c.in_dtype, &p);
       if (!planned) planned = plan_split(dev, c.cols, c.in_dtype, &p);
       if (!planned && classic) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     }
@@ -560,16 +702,51 @@ Plan plan_call(const Call& c, DeviceInfo& dev) {
   return p;
 }
 
-smx_status launch_planned(Call& c, DeviceInfo& dev, const Plan& p) {
+cudaError_t launch_typed_in(const Call& c, const Plan& p) {
+  switch (c.in_dtype) {
+    case SMX_F32: return launch_in_f32(c, p);
+    case SMX_F16: return launch_in_f16(c, p);
+    default: return launch_in_bf16(c, p);
+  }
+}
+
+// Launch a planned call.  The long-row paths take their summaries (and the
+// stripe kernel its counters) from the device's scratch, which grows only when
+// a call needs more than any before: a steady loop of calls allocates nothing.
+smx_status launch_planned(Call& c, DeviceInfo& dev, Plan p) {
   c.status = dev.status;
-  c.pool = dev.pool;
   const int64_t wl = g_wait_limit.load();
   c.max_polls = wl != 0 ? wl : DEFAULT_MAX_POLLS;
-  cudaError_t e;
-  switch (c.in_dtype) {
-    case SMX_F32: e = launch_in_f32(c, p); break;
-    case SMX_F16: e = launch_in_f16(c, p); break;
-    default: e = launch_in_bf16(c, p); break;
+  const size_t need = plan_scratch_bytes(c, p);
+  cudaError_t e = cudaSuccess;
+  if (need == 0 || p.scratch != nullptr) {
+    e = launch_typed_in(c, p);
+  } else {
+    ScratchState& st = dev.scratch;
+    std::lock_guard<std::mutex> lock(st.mu);
+    e = scratch_reserve(dev, st.work, need, c.stream, false);
+    if (e == cudaSuccess && p.path == PATH_STRIPE && c.rows > st.count_cap) {
+      // both counter arrays (this call's and the next's), zero
+      e = scratch_reserve(dev, st.counts, (size_t)2 * c.rows * sizeof(unsigned), c.stream, true);
+      if (e == cudaSuccess) {
+        st.count_cap = (int64_t)(st.counts.bytes / (2 * sizeof(unsigned)));
+        st.count_parity = 0;
+      }
+    }
+    if (e == cudaSuccess) {
+      p.scratch = reinterpret_cast<float*>(st.work.base);
+      if (p.path == PATH_STRIPE) {
+        unsigned* cb = reinterpret_cast<unsigned*>(st.counts.base);
+        p.stripe_count = cb + (size_t)st.count_parity * st.count_cap;
+        p.stripe_count_next = cb + (size_t)(1 - st.count_parity) * st.count_cap;
+        p.stripe_count_next_n = st.count_cap;
+      }
+      e = launch_typed_in(c, p);
+      // the next stripe call counts in the array this one zeroed
+      if (e == cudaSuccess && p.path == PATH_STRIPE) st.count_parity ^= 1;
+      const cudaError_t f = scratch_release(dev, c.stream);
+      if (e == cudaSuccess) e = f;
+    }
   }
   t_last_path = p.path;
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
@@ -585,10 +762,11 @@ smx_status run(Call& c, DeviceInfo& dev) { return launch_planned(c, dev, plan_ca
 
 
 struct FixedSetup {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   bool supported = false;
   int sm_count = 0;
   int64_t l2_bytes = 0;
+  int64_t smem_optin = 0;
   float* scratch = nullptr;  // this device's copy of g_fixed_scratch
 };
 FixedSetup g_fixed[MAX_DEVICES];
@@ -600,25 +778,27 @@ smx_status fixed_setup(FixedSetup** out) {
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_UNSUPPORTED);
   if (dev < 0 || dev >= MAX_DEVICES) return SMX_ERR_UNSUPPORTED;
   FixedSetup& f = g_fixed[dev];
-  if (!f.ready) {
+  if (!f.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!f.ready) {
-      int major = 0, minor = 0, sms = 0, l2 = 0;
+    if (!f.ready.load(std::memory_order_relaxed)) {
+      int major = 0, minor = 0, sms = 0, l2 = 0, optin = 0;
       if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
           (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
-          (e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess)
+          (e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return cuda_fail(e, SMX_ERR_DEVICE);
       f.supported = (major == 10 && minor == 3);
       f.sm_count = sms;
       f.l2_bytes = l2;
+      f.smem_optin = optin;
       if (f.supported) {
         void* a = nullptr;
         if ((e = cudaGetSymbolAddress(&a, g_fixed_scratch)) != cudaSuccess)
           return cuda_fail(e, SMX_ERR_DEVICE);
         f.scratch = static_cast<float*>(a);
       }
-      f.ready = true;
+      f.ready.store(true, std::memory_order_release);
     }
   }
   if (!f.supported) return SMX_ERR_UNSUPPORTED;
@@ -715,10 +895,12 @@ smx_status smx_softmax_rows_host(const void* x, void* y, int64_t rows, int64_t c
   cudaStream_t B = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (dev->copy_stream == nullptr &&
-        (e = cudaStreamCreateWithFlags(&dev->copy_stream, cudaStreamNonBlocking)) != cudaSuccess) {
-      dev->copy_stream = nullptr;
-      return cuda_fail(e, SMX_ERR_DEVICE);
+    if (dev->copy_stream == nullptr) {
+      if ((e = cudaStreamCreateWithFlags(&dev->copy_stream, cudaStreamNonBlocking)) != cudaSuccess) {
+        dev->copy_stream = nullptr;
+        return cuda_fail(e, SMX_ERR_DEVICE);
+      }
+      ++g_alloc_calls;
     }
     B = dev->copy_stream;
   }
@@ -750,17 +932,27 @@ smx_status smx_softmax_rows_host(const void* x, void* y, int64_t rows, int64_t c
   auto up16 = [](int64_t b) { return (b + 15) / 16 * 16; };
   const int64_t in_b = up16(cr * cols * ies), out_b = up16(cr * cols * oes);
   const int64_t slot = in_b + out_b + (valid_len ? up16(cr * 4) : 0);
-  char* base = nullptr;
-  if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), (size_t)(nslots * slot), dev->pool, A)) !=
-      cudaSuccess)
+  // The staging slots and the events live in the device's scratch (grown only
+  // when a call needs more; events created once); the whole call holds it.
+  ScratchState& sst = dev->scratch;
+  std::lock_guard<std::mutex> lock(sst.mu);
+  if ((e = scratch_reserve(*dev, sst.staging, (size_t)(nslots * slot), A, false)) != cudaSuccess)
     return cuda_fail(e, SMX_ERR_DEVICE);
-  // per slot: its chunk computed (on A), its output copied back (on B)
-  cudaEvent_t computed[HOST_MAX_SLOTS] = {}, copied[HOST_MAX_SLOTS] = {}, done = nullptr;
-  for (int i = 0; i < nslots && e == cudaSuccess; ++i) {
-    if ((e = cudaEventCreateWithFlags(&computed[i], cudaEventDisableTiming)) == cudaSuccess)
-      e = cudaEventCreateWithFlags(&copied[i], cudaEventDisableTiming);
+  for (int i = 0; i < HOST_MAX_SLOTS && e == cudaSuccess; ++i) {
+    if (sst.computed[i] == nullptr && (e = cudaEventCreateWithFlags(&sst.computed[i], cudaEventDisableTiming)) == cudaSuccess)
+      ++g_alloc_calls;
+    if (e == cudaSuccess && sst.copied[i] == nullptr &&
+        (e = cudaEventCreateWithFlags(&sst.copied[i], cudaEventDisableTiming)) == cudaSuccess)
+      ++g_alloc_calls;
   }
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming);
+  if (e == cudaSuccess && sst.host_done == nullptr &&
+      (e = cudaEventCreateWithFlags(&sst.host_done, cudaEventDisableTiming)) == cudaSuccess)
+    ++g_alloc_calls;
+  if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_DEVICE);
+  char* base = sst.staging.base;
+  // per slot: its chunk computed (on A), its output copied back (on B)
+  cudaEvent_t* computed = sst.computed;
+  cudaEvent_t* copied = sst.copied;
   int launches = 0;
   for (int64_t i = 0, r0 = 0; e == cudaSuccess && r0 < rows; ++i, r0 += cr) {
     const int sl = (int)(i % nslots);
@@ -778,10 +970,29 @@ smx_status smx_softmax_rows_host(const void* x, void* y, int64_t rows, int64_t c
     // the slot's output buffer is free once its previous chunk's copy back is done
     if (i >= nslots && (e = cudaStreamWaitEvent(A, copied[sl], 0)) != cudaSuccess) break;
     Call c{dx, dy, nullptr, nullptr, n, cols, dvl, (int)in_dtype, (int)out_dtype, MODE_SOFTMAX, A, nullptr, 0};
+    Plan p = plan_call(c, *dev);
+    if (plan_scratch_bytes(c, p) > 0) {
+      // the long-row kernels' summaries: the work buffer of the scratch held here
+      if ((e = scratch_reserve(*dev, sst.work, plan_scratch_bytes(c, p), A, false)) != cudaSuccess) break;
+      p.scratch = reinterpret_cast<float*>(sst.work.base);
+      if (p.path == PATH_STRIPE) {
+        if (c.rows > sst.count_cap) {
+          if ((e = scratch_reserve(*dev, sst.counts, (size_t)2 * c.rows * sizeof(unsigned), A, true)) != cudaSuccess)
+            break;
+          sst.count_cap = (int64_t)(sst.counts.bytes / (2 * sizeof(unsigned)));
+          sst.count_parity = 0;
+        }
+        unsigned* cb = reinterpret_cast<unsigned*>(sst.counts.base);
+        p.stripe_count = cb + (size_t)sst.count_parity * sst.count_cap;
+        p.stripe_count_next = cb + (size_t)(1 - sst.count_parity) * sst.count_cap;
+        p.stripe_count_next_n = sst.count_cap;
+      }
+    }
     t_kernel_launches = 0;
-    s = run(c, *dev);
+    s = launch_planned(c, *dev, p);
     launches += t_kernel_launches;
     if (s != SMX_OK) break;
+    if (p.path == PATH_STRIPE) sst.count_parity ^= 1;
     // out on B, after the chunk's softmax
     if ((e = cudaEventRecord(computed[sl], A)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(B, computed[sl], 0)) != cudaSuccess ||
@@ -790,16 +1001,11 @@ smx_status smx_softmax_rows_host(const void* x, void* y, int64_t rows, int64_t c
         (e = cudaEventRecord(copied[sl], B)) != cudaSuccess)
       break;
   }
-  // the call completes on the caller's stream: A waits for B's last copy,
-  // then the slots go back to the pool
-  cudaError_t f = cudaSuccess;
-  if (done != nullptr && (f = cudaEventRecord(done, B)) == cudaSuccess) f = cudaStreamWaitEvent(A, done, 0);
-  const cudaError_t g = cudaFreeAsync(base, A);
-  for (int i = 0; i < nslots; ++i) {
-    if (computed[i]) cudaEventDestroy(computed[i]);
-    if (copied[i]) cudaEventDestroy(copied[i]);
-  }
-  if (done) cudaEventDestroy(done);
+  // the call completes on the caller's stream: A waits for B's last copy; the
+  // scratch's next user is ordered after that point of A
+  cudaError_t f = cudaEventRecord(sst.host_done, B);
+  if (f == cudaSuccess) f = cudaStreamWaitEvent(A, sst.host_done, 0);
+  const cudaError_t g = scratch_release(*dev, A);
   t_kernel_launches = launches;
   if (s != SMX_OK) return s;
   if (e == cudaSuccess) e = f;
@@ -830,15 +1036,30 @@ smx_status smx_softmax_rows_fixed_scratch(const void* x, void* y, int64_t rows, 
   if (s != SMX_OK) return s;
   Call c{x, y, nullptr, nullptr, rows, cols, valid_len, (int)in_dtype, (int)out_dtype,
          MODE_SOFTMAX, reinterpret_cast<cudaStream_t>(stream), nullptr, 0};
+  // The streamed and register-resident kernels need no scratch: rows they
+  // take run exactly as smx_softmax_rows runs them.  Longer rows take the
+  // chunked long-row kernels (never the cooperative ones, nor the cluster
+  // kernel, whose bounded waits report through the library's status word)
+  // with their summaries in the fixed array, in slabs cut to fit it.  No
+  // kernel launched here writes the status word, so c.status stays null.
   Plan p;
   if (vec_ok) {
     DeviceInfo d;
     d.sm_count = f->sm_count;
     d.l2_bytes = f->l2_bytes;
-    if (!plan_split(d, cols, in_dtype, &p)) return SMX_ERR_UNSUPPORTED;
-    const int64_t cap = FIXED_SCRATCH_FLOATS / (2 * (int64_t)p.nchunks);
-    if (p.slab_rows > cap) p.slab_rows = cap;
-    p.scratch = f->scratch;
+    d.smem_optin = f->smem_optin;
+    d.coop = false;
+    const bool acc = out_dtype == SMX_F32;
+    bool planned = plan_stream(d, rows, cols, in_dtype, acc, valid_len != nullptr, MODE_SOFTMAX,
+                               STREAM_INFLIGHT_BYTES, &p);
+    if (!planned) planned = plan_regs(cols, in_dtype, acc, &p);
+    if (!planned) {
+      if (!plan_split(d, cols, in_dtype, &p)) return SMX_ERR_UNSUPPORTED;
+      const int64_t cap = FIXED_SCRATCH_FLOATS / (2 * (int64_t)p.nchunks);
+      if (p.slab_rows > cap) p.slab_rows = cap;
+      p.scratch = f->scratch;
+      p.fixed_scratch = true;
+    }
   } else {
     p.path = PATH_GENERIC;  // the scalar kernel takes no scratch
   }
@@ -1076,7 +1297,11 @@ int smx_last_cuda_error(void) { return t_last_cuda_error; }
 
 int smx_version(void) { return 100; }
 
-void smx_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 5 ? path : 0); }
+void smx_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 6 ? path : 0); }
+
+int64_t smx_debug_alloc_count(void) { return g_alloc_calls.load(); }
+
+void smx_debug_set_count_probe(int64_t polls) { g_count_probe.store(polls > 0 ? polls : 0); }
 
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
   g_max_cluster.store(max_cluster > 0 ? max_cluster : 0);

@@ -7,7 +7,10 @@
 
 namespace smx {
 
-enum Path : int { PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_STREAM = 4, PATH_SPLIT = 5 };
+enum Path : int {
+  PATH_AUTO = 0, PATH_REGS = 1, PATH_CLUSTER = 2, PATH_GENERIC = 3, PATH_STREAM = 4, PATH_SPLIT = 5,
+  PATH_STRIPE = 6
+};
 
 struct Call {
   const void* x;
@@ -28,14 +31,7 @@ struct Call {
   const void* g = nullptr;      // backward: the upstream gradient (x is the forward output p)
   const int64_t* target = nullptr;  // cross-entropy: target index per row
   float* loss = nullptr;            // cross-entropy: loss per row
-  cudaMemPool_t pool = nullptr;     // where the per-call scratch comes from (null: the default pool)
 };
-
-// Stream-ordered scratch of a call: from the library's pool when it has one.
-inline cudaError_t scratch_alloc(const Call& c, void** p, size_t bytes) {
-  return c.pool != nullptr ? cudaMallocFromPoolAsync(p, bytes, c.pool, c.stream)
-                           : cudaMallocAsync(p, bytes, c.stream);
-}
 
 // Call::mode of the softmax backward (past the kernels' MODE_* values).
 constexpr int CALL_BACKWARD = 8;
@@ -61,8 +57,25 @@ struct Plan {
   int l2_hint_apply = 0;
   int resident_clusters = 0;
   int nchunks = 0;
-  float* scratch = nullptr;  // caller-provided summaries (else allocated per call)
+  float* scratch = nullptr;  // the long-row paths' summaries (the library's per-device scratch)
+  bool fixed_scratch = false;  // scratch is the fixed array of smx_softmax_rows_fixed_scratch
+  // read-once long rows (kernel_stripe.cuh): Q stripes per row, row groups,
+  // shared-memory ring slots of slot_vecs 16-byte vectors; the per-row
+  // counter arrays (this call's and the next call's)
+  int stripe_q = 0, stripe_groups = 0, stripe_slots = 0, stripe_slot_vecs = 0;
+  unsigned* stripe_count = nullptr;
+  unsigned* stripe_count_next = nullptr;
+  int64_t stripe_count_next_n = 0;
+  int64_t stripe_probe = 0;  // > 0: the count waits' error-path probe (paths 5 fused and 6)
 };
+
+// The read-once long-row kernel (kernel_stripe.cuh).
+constexpr int STRIPE_SYNC_WARPS = 2;   // sync warps per CTA (alternate rows)
+constexpr int STRIPE_LAG = 2;          // rows between a stripe's summary and its normalisation
+constexpr int STRIPE_RING = 4;         // summary / row-constant ring entries (>= LAG + 1)
+constexpr int STRIPE_MAX_SLOTS = 16;   // shared-memory ring slots (>= LAG + 2)
+constexpr int STRIPE_MAX_Q = 256;      // stripes per row (at most 8 summaries per sync lane)
+constexpr int STRIPE_THREADS = 1024;   // 30 compute warps + 2 sync warps
 
 constexpr int CLUSTER_RV = 2;  // register vectors per thread on the cluster path
 constexpr int CLUSTER_THREADS = 1024;
@@ -112,6 +125,14 @@ int split_occupancy_bf16(int threads);
 int split_fused_occupancy_f32(int threads);
 int split_fused_occupancy_f16(int threads);
 int split_fused_occupancy_bf16(int threads);
+// ... of the read-once long-row kernel with `smem` bytes of ring, and its
+// static shared memory (-1 if the query failed).
+int stripe_occupancy_f32(int64_t smem);
+int stripe_occupancy_f16(int64_t smem);
+int stripe_occupancy_bf16(int64_t smem);
+int stripe_static_smem_f32();
+int stripe_static_smem_f16();
+int stripe_static_smem_bf16();
 // ... of the backward kernels: whole rows (vpt, threads) or chunks (vpt = 0).
 int backward_occupancy_f32(int vpt, int threads);
 int backward_occupancy_f16(int vpt, int threads);
@@ -126,6 +147,31 @@ constexpr int WARP_WALKER_THREADS = 128;  // CTA of the warp walkers: 4 independ
 // chunks: the chunk summaries (m, then d).
 inline size_t split_scratch_bytes(int64_t slab, int64_t nchunks) {
   return (size_t)(2 * slab * nchunks) * sizeof(float);
+}
+
+// The split path's single cooperative launch (kernel_split_fused.cuh): when
+// planned, for the softmax, log_softmax and the cross-entropy with a gradient.
+inline bool split_uses_fused(const Call& c, const Plan& p) {
+  return p.fused_split && !p.fixed_scratch &&
+         (c.mode == 0 || c.mode == 3 || (c.mode == 5 && c.y != nullptr));
+}
+// The split path's statistics-only calls (row statistics, LSE, the loss
+// alone) read every element once, in one slab of all rows.
+inline bool split_read_once(const Call& c, const Plan& p) {
+  return (c.mode == 1 || (c.mode == 5 && c.y == nullptr)) &&
+         c.rows * p.nchunks <= ((int64_t)1 << 31) && !p.fixed_scratch;
+}
+
+// Device scratch (bytes) a planned call needs: the long-row paths' summaries.
+inline size_t plan_scratch_bytes(const Call& c, const Plan& p) {
+  if (p.path == PATH_STRIPE) return (size_t)c.rows * p.stripe_q * 2 * sizeof(float);
+  if (p.path != PATH_SPLIT) return 0;
+  const int64_t slab = p.slab_rows < c.rows ? p.slab_rows : c.rows;
+  if (c.mode == CALL_BACKWARD) return (size_t)slab * p.nchunks * sizeof(float);
+  if (c.mode == 2) return 0;  // the apply mode has its statistics
+  if (split_uses_fused(c, p))
+    return split_scratch_bytes(c.rows, p.nchunks) + (size_t)c.rows * sizeof(unsigned);
+  return split_scratch_bytes(split_read_once(c, p) ? c.rows : slab, p.nchunks);
 }
 
 // Dynamic shared memory of the streamed kernel: `depth` rows of vpt 16-byte

@@ -53,6 +53,28 @@ def test_default_bench_line():
     traffic, _ = bench.profile_traffic("bf16_16384x4096", "softmax")
     assert line["roofline"]["traffic"] == traffic
     assert line["gpu_launches"] == 200
+    # the timed output against the reference, all rows
+    assert line["parity"]["within_tolerance"] and line["parity"]["rows"] == 16384
+    assert line["parity"]["max_ulp"] <= 1 and line["parity"]["masked_zero_ok"]
+    # every other workload of the bandwidth target, same steps, with its parity
+    per = {e["workload"]: e for e in line["per_config"]}
+    assert set(per) == {"f32_64x1000", "f16_32768x1024_len", "f32_64x1048576_rise"}
+    for name, e in per.items():
+        w = bench.wl.WORKLOADS[name]
+        assert e["value"] > 0 and e["ms_per_step"] > 0 and 0 < e["roofline"]["frac"] < 1.2
+        assert e["parity"]["within_tolerance"], (name, e["parity"])
+        assert e["parity"]["rows"] == w.rows
+        assert "max_rel" in e["parity"] if w.out_dtype == "f32" else "max_ulp" in e["parity"]
+    assert per["f32_64x1048576_rise"]["path"] == "stripe"
+    assert per["f32_64x1048576_rise"]["kernels_per_step"] == 1
+
+
+def test_clocks_sampled_inside_a_short_region():
+    """A 20-step region lasts about a millisecond: the NVML sampler still sees it."""
+    line = bench_line("--steps", "20", "--warmup", "3", "--cpu-budget", "0.2", "--per-config", "0",
+                      "--cpu-all-cores", "0")
+    c = line["clocks"]
+    assert c["samples"] >= 5 and c["sm_mhz"] > 0 and c["source"].startswith("NVML")
 
 
 def test_attention_bench_line():

@@ -174,3 +174,61 @@ def test_measured_peak_and_fallback(monkeypatch, tmp_path):
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6689.1, "bf16_tflops": 1939.3}))
     assert bench.measured_peak("hbm_gbs") == (6689.1, "measured")
     assert bench.measured_peak("bf16_tflops") == (1939.3, "measured")
+
+
+# ---------------------------------------------------------------------------
+# The bench line's parity statistics and in-region clock summary.
+# ---------------------------------------------------------------------------
+
+def _reference_rows(in_dtype, rows, cols, seed, masked=False):
+    import numpy as np
+
+    import oracle
+    from numerically_stable_online_gb300 import workloads as wl
+
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    x = wl.to_storage(rng.normal(0, 5, rows * cols).astype(np.float32), in_dtype)
+    vl = rng.integers(0, cols + 1, rows).astype(np.int32) if masked else None
+    return x, vl, oracle.softmax_rows(x, in_dtype, rows, cols, vl)
+
+
+def test_parity_stats_pass_the_reference_and_catch_planted_mistakes():
+    import numpy as np
+
+    import oracle
+
+    rows, cols = 12, 64
+    x, vl, p = _reference_rows("f32", rows, cols, 3, masked=True)
+    y = p.astype(np.float32)
+    st = bench.parity_stats(y, p, "f32", vl)
+    assert st["within_tolerance"] and st["masked_zero_ok"] and st["max_rel"] <= 6e-8
+    bad = y.copy()
+    bad[0, 0] *= 1 + 4e-6  # one element 4e-6 off
+    assert not bench.parity_stats(bad, p, "f32", vl)["within_tolerance"]
+    bad = y.copy()
+    L = np.clip(vl, 0, cols)
+    r = int(np.argmax(L < cols))
+    bad[r, cols - 1] = 1e-9  # a masked lane written
+    st = bench.parity_stats(bad, p, "f32", vl)
+    assert not st["masked_zero_ok"] and not st["within_tolerance"]
+    # 16-bit outputs: correctly rounded bits pass, two units off fail
+    x16, _, p16 = _reference_rows("bf16", rows, cols, 4)
+    bits = oracle.round_to(p16, "bf16")
+    st = bench.parity_stats(bits, p16, "bf16")
+    assert st["within_tolerance"] and st["max_ulp"] == 0 and st["frac_exact"] == 1.0
+    bits2 = bits.copy()
+    bits2[3, 5] += 2
+    st = bench.parity_stats(bits2, p16, "bf16")
+    assert st["max_ulp"] == 2 and not st["within_tolerance"]
+
+
+def test_clock_samples_summarised_inside_the_region_only():
+    lines = ["100.000100 1980 2070 0", "100.000300 2070 2070 4", "100.000500 2070 2070 0",
+             "100.000900 1200 2070 8", "garbage", "101.5 500 2070 40"]
+    c = bench.summarize_clock_samples(lines, 100.0, 100.0006)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2070 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"] and not c["rejected"]
+    c = bench.summarize_clock_samples(lines, 100.0, 100.001)
+    assert "hw_slowdown" in c["reasons"] and c["rejected"]
+    assert bench.summarize_clock_samples(lines, 200.0, 201.0)["samples"] == 0

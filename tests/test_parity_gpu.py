@@ -22,8 +22,8 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 PAIRS = [(a, b) for a in DT for b in DT]
-PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM, PATH_SPLIT = 1, 2, 3, 4, 5
-ALL_PATHS = [PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM, PATH_SPLIT]
+PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM, PATH_SPLIT, PATH_STRIPE = 1, 2, 3, 4, 5, 6
+ALL_PATHS = [PATH_REGS, PATH_CLUSTER, PATH_GENERIC, PATH_STREAM, PATH_SPLIT, PATH_STRIPE]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,6 +55,7 @@ def lib(built):
     built.smx_debug_set_stream_ctas(0)
     built.smx_debug_set_stream_warp(0)
     built.smx_debug_set_split_fused(0)
+    built.smx_debug_set_count_probe(0)
 
 
 DEV = "cuda:0"
@@ -482,6 +483,32 @@ def test_bounded_wait_reports_timeout(lib):
     y = smx.softmax_rows(x)
     assert smx.last_device_status() == 0
     parity.compare(y.cpu().numpy(), p, "f32")
+
+
+def test_bounded_wait_runs_out_while_walking_rows(lib):
+    """More rows than resident clusters, so every cluster walks several rows,
+    with one poll per staging wait: waits run out on whichever row of the walk
+    they happen to, and the CTA stops refilling there.  Before it exits it must
+    still let every copy it issued land (each piece's last issued phase, not
+    the walk's last row).  The call's output is undefined; the next call on the
+    same context must be correct and report nothing."""
+    rows, cols = 48, 1 << 20
+    g = torch.Generator(device=DEV).manual_seed(48)
+    x = torch.randn(rows, cols, generator=g, device=DEV) * 3
+    lib.smx_debug_force_path(PATH_CLUSTER)
+    for staging in (1, 2):
+        lib.smx_debug_set_cluster_staging(staging)
+        lib.smx_debug_set_wait_limit(1)
+        smx.softmax_rows(x)
+        smx.last_device_status()  # a timeout may or may not have been recorded
+        lib.smx_debug_set_wait_limit(0)
+        y = smx.softmax_rows(x)
+        assert lib.smx_debug_last_path() == PATH_CLUSTER
+        assert smx.last_device_status() == 0
+        sel = [0, 17, 47]
+        xs = x[sel].cpu().numpy().reshape(-1)
+        p = oracle.softmax_rows(xs, "f32", len(sel), cols)
+        parity.compare(y[sel].cpu().numpy(), p, "f32")
 
 
 @pytest.mark.parametrize("cols", [8, 100, 256, 1000, 1024, 2048])

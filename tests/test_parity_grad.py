@@ -26,6 +26,7 @@ DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 PAIRS = [(a, b) for a in DT for b in DT]
 PATH_GENERIC, PATH_STREAM, PATH_SPLIT = 3, 4, 5
 PATHS = [PATH_GENERIC, PATH_STREAM, PATH_SPLIT]
+CE_PATHS = PATHS + [6]  # and the read-once long-row kernel
 DEV = "cuda:0"
 
 
@@ -160,7 +161,7 @@ def run_ce(x_store, in_dtype, grad_dtype, rows, cols, target, valid_len=None, of
 
 
 @pytest.mark.parametrize("in_dtype,grad_dtype", PAIRS)
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", CE_PATHS)
 def test_ce_worked_rows(lib, in_dtype, grad_dtype, path):
     lib.smx_debug_force_path(path)
     for row in list(wl.WORKED_ROWS.values()) + [[1000.0, 0.0]]:
@@ -179,7 +180,7 @@ def test_ce_confidently_wrong_is_finite(lib):
     assert torch.all((grad.cpu() - torch.tensor([[1.0, -1.0, 0.0, 0.0]])).abs() <= 6.1e-6)
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", CE_PATHS)
 @pytest.mark.parametrize("with_grad", [True, False])
 def test_ce_policy_rows(lib, path, with_grad):
     from tests.test_parity_gpu import POLICY_ROWS

@@ -61,7 +61,7 @@ def chunks(rows, cols, in_dtype):
     return -(-rows // cr)
 
 
-PATH_REGS, PATH_STREAM, PATH_SPLIT = 1, 4, 5
+PATH_REGS, PATH_STREAM, PATH_SPLIT, PATH_STRIPE = 1, 4, 5, 6
 
 
 @pytest.mark.parametrize("name,rows,out_dtype,pinned", [
@@ -70,6 +70,7 @@ PATH_REGS, PATH_STREAM, PATH_SPLIT = 1, 4, 5
     ("f16_32768x1024_len", 2 * 8192 + 5, "f16", True),    # lengths from host memory
     ("f32_64x1000", 64, "bf16", True),                    # one chunk
     ("f32_64x1048576_rise", 7, "f32", True),              # 4 MiB rows, 4 a chunk; always staged
+                                                          # (the read-once kernel's bulk copies stay in HBM)
 ])
 @pytest.mark.parametrize("staged", [0, 1])
 def test_host_call_workloads(built, name, rows, out_dtype, pinned, staged):
@@ -85,7 +86,7 @@ def test_host_call_workloads(built, name, rows, out_dtype, pinned, staged):
         vlt = vlt.pin_memory()
     y = smx.softmax_rows_host(x, valid_len=vlt, out_dtype=DT[out_dtype])
     assert not y.is_cuda and y.is_pinned() == pinned and y.dtype == DT[out_dtype]
-    in_place = pinned and not staged and built.smx_debug_last_path() != PATH_SPLIT
+    in_place = pinned and not staged and built.smx_debug_last_path() not in (PATH_SPLIT, PATH_STRIPE)
     if in_place:
         assert built.smx_debug_last_launches() == 1
         assert built.smx_debug_last_path() in (PATH_REGS, PATH_STREAM)
@@ -94,7 +95,7 @@ def test_host_call_workloads(built, name, rows, out_dtype, pinned, staged):
     assert smx.last_device_status() == 0
     compare_all(y, x_store, w.in_dtype, out_dtype, rows, w.cols, vl)
     if name == "f32_64x1048576_rise":
-        assert built.smx_debug_last_path() == PATH_SPLIT
+        assert built.smx_debug_last_path() == PATH_STRIPE
 
 
 def test_lengths_in_pageable_memory_stage(built):

@@ -25,6 +25,7 @@ DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 PAIRS = [(a, b) for a in DT for b in DT]
 PATH_GENERIC, PATH_STREAM, PATH_SPLIT = 3, 4, 5
 PATHS = [PATH_GENERIC, PATH_STREAM, PATH_SPLIT]
+LOG_PATHS = PATHS + [6]  # and the read-once long-row kernel
 DEV = "cuda:0"
 
 
@@ -79,7 +80,7 @@ def run_log(x_store, in_dtype, out_dtype, rows, cols, valid_len=None, offset=0, 
 # ------------------------------------------------------------------ log space
 
 @pytest.mark.parametrize("in_dtype,out_dtype", PAIRS)
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", LOG_PATHS)
 def test_log_worked_rows(lib, in_dtype, out_dtype, path):
     lib.smx_debug_force_path(path)
     for row in wl.WORKED_ROWS.values():
@@ -99,7 +100,7 @@ def test_log_worked_row_printed_values(lib):
 
 @pytest.mark.parametrize("in_dtype,out_dtype", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f32"),
                                                 ("f32", "f16")])
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", LOG_PATHS)
 def test_log_policy_rows(lib, in_dtype, out_dtype, path):
     lib.smx_debug_force_path(path)
     rows = np.array(POLICY_ROWS, np.float32)

@@ -59,9 +59,15 @@ def close(a: torch.Tensor, b: torch.Tensor, valid_len):
 
 
 def run_pair(x, out_dtype, valid_len):
+    lib = smx.library()
     y0 = smx.softmax_rows(x, valid_len=valid_len, out_dtype=out_dtype)
-    y1 = smx.softmax_rows_fixed_scratch(x, valid_len=valid_len, out_dtype=out_dtype)
-    y2 = smx.softmax_rows_fixed_scratch(x, valid_len=valid_len, out_dtype=out_dtype)
+    y1 = torch.empty_like(y0)
+    y2 = torch.empty_like(y0)
+    # the library allocates nothing in these two calls (outputs come from torch above)
+    before = lib.smx_debug_alloc_count()
+    smx.softmax_rows_fixed_scratch(x, out=y1, valid_len=valid_len)
+    smx.softmax_rows_fixed_scratch(x, out=y2, valid_len=valid_len)
+    assert lib.smx_debug_alloc_count() == before
     torch.cuda.synchronize()
     close(y1, y0, valid_len)
     close(y2, y0, valid_len)
