@@ -239,7 +239,10 @@ def nvml_sampler_main(device: str, path: str) -> int:
         print("ready", flush=True)
         t_next = 0.0
         while True:
-            if select.select([sys.stdin], [], [], 0)[0]:
+            # slow mode blocks on stdin until the next sample is due, so a
+            # switch to fast mode is seen at once; fast mode only peeks
+            wait = 0.0 if interval < 1e-3 else max(0.0, t_next - time.time())
+            if select.select([sys.stdin], [], [], wait)[0]:
                 c = sys.stdin.read(1)
                 if not c:
                     break
@@ -247,8 +250,6 @@ def nvml_sampler_main(device: str, path: str) -> int:
                 t_next = 0.0
             t = time.time()
             if t < t_next:
-                if interval > 1e-3:
-                    time.sleep(min(interval, t_next - t))
                 continue
             t_next = t + interval
             nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz))

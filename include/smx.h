@@ -337,7 +337,7 @@ int smx_version(void);
  * smx_debug_set_regs_shape(threads, vpt): on paths 1 and 4, use CTAs of
  *   `threads` threads per row (32 = one warp per row, path 1 only) holding `vpt`
  *   16-byte vectors each, when that shape covers the row (0, 0 = automatic).
- * smx_debug_set_stream_depth(n): rows prefetched per CTA on path 4 (2, 3 or
+ * smx_debug_set_stream_depth(n): rows prefetched per walker (CTA or warp) on path 4 (2, 3 or
  *   4; 0 = automatic).
  * smx_debug_set_stream_ctas(n): n resident CTAs per SM on path 4, at most as
  *   many as fit (0 = automatic; also path 5).
@@ -373,6 +373,9 @@ int smx_version(void);
  *   kernels normalise with, 4 = the compensated e^(a - b) of fp32 outputs,
  *   5 = one term e^(a - b) as the statistics path forms it.  a, b, out:
  *   device float[n] (b only for 4 and 5).  The pages have no counterpart.
+ * smx_debug_set_stripe_wait(ns): path 6's compute warps sleep about ns
+ *   nanoseconds between polls of a wait (0 = poll again at once; -1 = the
+ *   default).
  * smx_debug_set_count_probe(polls): polls > 0: the per-row count waits of
  *   the cooperative long-row kernels (path 6, and path 5 in its single-launch
  *   form) wait for one more stripe or chunk than the row has, give up after
@@ -397,6 +400,7 @@ void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 int64_t smx_debug_alloc_count(void);
 void smx_debug_set_count_probe(int64_t polls);
+void smx_debug_set_stripe_wait(int ns);
 smx_status smx_debug_probe_math(const float *a, const float *b, float *out, int64_t n, int which,
                                 smx_stream_t stream);
 

@@ -22,6 +22,7 @@
 #pragma once
 
 #include "kernel_stream.cuh"
+#include "smx_async.cuh"
 
 namespace smx {
 
@@ -38,12 +39,6 @@ struct SplitArgs {
   int64_t probe;     // > 0: each count wait asks for one chunk more than the row has (error-path probe)
   int* status;
 };
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 template <typename InT, typename OutT, int MODE, int VPT, int DEPTH>
 __global__ void __launch_bounds__(256, 3)

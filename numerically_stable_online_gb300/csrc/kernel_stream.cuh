@@ -96,10 +96,18 @@ __device__ __forceinline__ uint64_t l2_policy(int hint) {
 // trading spills for resident CTAs.
 // The warp walkers run 128-thread CTAs, so their register budget is not the
 // 1024-thread one.
+// SMX_WARP_MIN_CTAS (a build-time tuning knob) asks the compiler to fit that
+// many 128-thread warp-walker CTAs per SM (a register budget).  Measured on
+// GB300 (masked fp16 rows of 1024): 6 (at most 85 registers) against no budget
+// (92): softmax 21.0 -> 20.5 us, log_softmax 23.0 -> 20.6 us, cross-entropy
+// 26.0 -> 25.2 us; 8 (64 registers) spills and is slower.
+#ifndef SMX_WARP_MIN_CTAS
+#define SMX_WARP_MIN_CTAS 6
+#endif
 #ifdef SMX_STREAM_MAXNREG
 #define SMX_STREAM_REGS __maxnreg__(SMX_STREAM_MAXNREG)
 #else
-#define SMX_STREAM_REGS __launch_bounds__(WARP ? 128 : 1024)
+#define SMX_STREAM_REGS __launch_bounds__(WARP ? 128 : 1024, WARP ? SMX_WARP_MIN_CTAS : 1)
 #endif
 
 template <typename InT, typename OutT, int VPT, int MODE, int DEPTH, bool CHUNKED, bool WARP = false>

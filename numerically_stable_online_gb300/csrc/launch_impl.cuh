@@ -155,8 +155,13 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
 
 template <typename InT, typename OutT, int MODE, int VPT>
 cudaError_t launch_stream_v(const Call& c, const Plan& p, const Items& it) {
-  if (p.warp_rows)  // a row per warp, two rows prefetched per warp
-    return launch_stream_k<InT, OutT, MODE, VPT, 2, false, true>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
+  if (p.warp_rows) {  // a row per warp, p.stages rows prefetched per warp
+    switch (p.stages) {
+      case 3: return launch_stream_k<InT, OutT, MODE, VPT, 3, false, true>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
+      case 4: return launch_stream_k<InT, OutT, MODE, VPT, 4, false, true>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
+      default: return launch_stream_k<InT, OutT, MODE, VPT, 2, false, true>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
+    }
+  }
   switch (p.stages) {
     case 3: return launch_stream_k<InT, OutT, MODE, VPT, 3, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
     case 4: return launch_stream_k<InT, OutT, MODE, VPT, 4, false>(c, p, it, c.m_out, c.d_out, nullptr, nullptr);
@@ -248,13 +253,14 @@ cudaError_t launch_split_fused(const Call& c, const Plan& p) {
 // summary to their normalisation.  p.scratch holds the stripe summaries;
 // p.stripe_count / p.stripe_count_next the two counter arrays (this call's,
 // zero; the next call's, zeroed by the kernel).
-template <typename InT, typename OutT, int MODE>
-cudaError_t launch_stripe(const Call& c, const Plan& p) {
-  auto kern = k_rows_stripe<InT, OutT, MODE>;
+template <typename InT, typename OutT, int MODE, int VPT>
+cudaError_t launch_stripe_v(const Call& c, const Plan& p) {
+  auto kern = k_rows_stripe<InT, OutT, MODE, VPT>;
   const int64_t smem = (int64_t)p.stripe_slots * p.stripe_slot_vecs * 16;
   cudaError_t e = smem_raise(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   if (p.scratch == nullptr || p.stripe_count == nullptr) return cudaErrorInvalidValue;
+  if (p.stripe_slot_vecs > VPT * STRIPE_COMPUTE_THREADS) return cudaErrorInvalidValue;  // registers hold a stripe
   StripeArgs a;
   a.rows = c.rows;
   a.cols = c.cols;
@@ -270,6 +276,7 @@ cudaError_t launch_stripe(const Call& c, const Plan& p) {
   a.loss = c.loss;
   a.max_polls = c.max_polls;
   a.probe = p.stripe_probe;
+  a.wait_ns = p.stripe_wait_ns;
   a.status = c.status;
   const InT* xp = static_cast<const InT*>(c.x);
   OutT* yp = static_cast<OutT*>(c.y);
@@ -279,6 +286,15 @@ cudaError_t launch_stripe(const Call& c, const Plan& p) {
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern),
                                      dim3((unsigned)(p.stripe_q * p.stripe_groups)), dim3(STRIPE_THREADS),
                                      args, (size_t)smem, c.stream);
+}
+
+template <typename InT, typename OutT, int MODE>
+cudaError_t launch_stripe(const Call& c, const Plan& p) {
+  switch (p.vpt) {
+    case 2: return launch_stripe_v<InT, OutT, MODE, 2>(c, p);
+    case 3: return launch_stripe_v<InT, OutT, MODE, 3>(c, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Resident CTAs per SM of the stripe kernel with `smem` bytes of ring (every
@@ -295,10 +311,10 @@ int stripe_occupancy(int64_t smem) {
     }
     return n;
   };
-  int n = query(k_rows_stripe<InT, float, MODE_SOFTMAX>);
-  const int n2 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_CE>);
-  const int n3 = query(k_rows_stripe<InT, float, MODE_CE>);
-  const int n4 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_LOG>);
+  int n = query(k_rows_stripe<InT, float, MODE_SOFTMAX, STRIPE_MAX_VPT>);
+  const int n2 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_CE, STRIPE_MAX_VPT>);
+  const int n3 = query(k_rows_stripe<InT, float, MODE_CE, STRIPE_MAX_VPT>);
+  const int n4 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_LOG, STRIPE_MAX_VPT>);
   n = n2 < n ? n2 : n;
   n = n3 < n ? n3 : n;
   return n4 < n ? n4 : n;
@@ -308,7 +324,7 @@ int stripe_occupancy(int64_t smem) {
 template <typename InT>
 int stripe_static_smem() {
   cudaFuncAttributes fa{};
-  if (cudaFuncGetAttributes(&fa, k_rows_stripe<InT, float, MODE_CE>) != cudaSuccess) {
+  if (cudaFuncGetAttributes(&fa, k_rows_stripe<InT, float, MODE_CE, STRIPE_MAX_VPT>) != cudaSuccess) {
     cudaGetLastError();
     return -1;
   }
@@ -614,12 +630,21 @@ int stream_occupancy_mode(int vpt, int threads, int depth, bool warp) {
   };
   if constexpr (!CH) {
     if (warp) {
+      auto wd = [&](auto k2, auto k3, auto k4) { return depth == 3 ? query(k3) : (depth == 4 ? query(k4) : query(k2)); };
       switch (vpt) {
-        case 1: return query(k_rows_stream<InT, OutT, 1, MODE, 2, false, true>);
-        case 2: return query(k_rows_stream<InT, OutT, 2, MODE, 2, false, true>);
-        case 4: return query(k_rows_stream<InT, OutT, 4, MODE, 2, false, true>);
+        case 1:
+          return wd(k_rows_stream<InT, OutT, 1, MODE, 2, false, true>, k_rows_stream<InT, OutT, 1, MODE, 3, false, true>,
+                    k_rows_stream<InT, OutT, 1, MODE, 4, false, true>);
+        case 2:
+          return wd(k_rows_stream<InT, OutT, 2, MODE, 2, false, true>, k_rows_stream<InT, OutT, 2, MODE, 3, false, true>,
+                    k_rows_stream<InT, OutT, 2, MODE, 4, false, true>);
+        case 4:
+          return wd(k_rows_stream<InT, OutT, 4, MODE, 2, false, true>, k_rows_stream<InT, OutT, 4, MODE, 3, false, true>,
+                    k_rows_stream<InT, OutT, 4, MODE, 4, false, true>);
         case 8:
-          if constexpr (8 * V <= 32) return query(k_rows_stream<InT, OutT, 8, MODE, 2, false, true>);
+          if constexpr (8 * V <= 32)
+            return wd(k_rows_stream<InT, OutT, 8, MODE, 2, false, true>, k_rows_stream<InT, OutT, 8, MODE, 3, false, true>,
+                      k_rows_stream<InT, OutT, 8, MODE, 4, false, true>);
           return 0;
         default: return 0;
       }

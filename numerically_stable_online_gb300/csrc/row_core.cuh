@@ -69,7 +69,7 @@ __device__ __forceinline__ float local_max(const float (&v)[VPT][V]) {
 #pragma unroll
   for (int j = 0; j < VPT; ++j)
 #pragma unroll
-    for (int i = 0; i < V; ++i) m = fmax_nan(m, v[j][i]);
+    for (int i = 0; i < V; i += 2) m = fmax3_nan(m, v[j][i], v[j][i + 1]);
   return m;
 }
 

@@ -96,7 +96,8 @@ std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: read
 // Device allocations, events and streams the library has created (a testing
 // count: a steady loop of calls adds none).
 std::atomic<int64_t> g_alloc_calls{0};
-std::atomic<int64_t> g_count_probe{0};  // > 0: the cooperative long-row kernels' error-path probe (polls)
+std::atomic<int64_t> g_count_probe{0};
+std::atomic<int> g_stripe_wait_ns{-1};  // path 6 compute warps' sleep between polls (-1: default)  // > 0: the cooperative long-row kernels' error-path probe (polls)
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
@@ -377,8 +378,8 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
     if (r.vpt * V > (accurate_exp ? 16 : 32)) return false;
   }
   const int dd = g_stream_depth.load();
-  // the apply kernel and the warp walkers prefetch 2 items
-  const int depth = (!apply && !warp && (dd == 3 || dd == 4)) ? dd : 2;
+  // the apply kernel prefetches 2 items; the other walkers 2 unless set
+  const int depth = (!apply && (dd == 3 || dd == 4)) ? dd : 2;
   const int occ_max = stream_occupancy(in_dtype, r.vpt, r.threads, depth, mode, warp);
   if (occ_max <= 0) return false;
   int occ = occ_max;
@@ -500,8 +501,11 @@ bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* 
   const int64_t ring_bytes = (d.smem_optin - st - 256) / 16 * 16;  // (256: the runtime's own reserve)
   const int64_t ring_vecs = ring_bytes / 16;
   const int64_t cap = d.sm_count < STRIPE_MAX_Q ? d.sm_count : STRIPE_MAX_Q;  // one CTA per SM
+  // a compute thread holds at most STRIPE_MAX_VPT vectors of a stripe
+  const int64_t vec_cap = (int64_t)STRIPE_MAX_VPT * STRIPE_COMPUTE_THREADS;
   for (const int target : {8, 6, STRIPE_LAG + 2}) {
-    const int64_t slot_cap = ring_vecs / target;
+    int64_t slot_cap = ring_vecs / target;
+    if (slot_cap > vec_cap) slot_cap = vec_cap;
     if (slot_cap <= 0) continue;
     const int64_t q_min = (nvec + slot_cap - 1) / slot_cap;
     if (q_min > cap) continue;
@@ -518,12 +522,15 @@ bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* 
     const int64_t smem = nslots * slot_vecs * 16;
     if (stripe_occupancy(in_dtype, smem) < 1) return false;
     p->path = PATH_STRIPE;
+    p->vpt = slot_vecs <= 2LL * STRIPE_COMPUTE_THREADS ? 2 : 3;
     p->stripe_q = (int)Q;
     p->stripe_groups = (int)groups;
     p->stripe_slots = (int)nslots;
     p->stripe_slot_vecs = (int)slot_vecs;
     p->ctas = (int)(Q * groups);
     p->stripe_probe = g_count_probe.load();
+    const int wn = g_stripe_wait_ns.load();
+    p->stripe_wait_ns = wn >= 0 ? (unsigned)wn : STRIPE_WAIT_NS;
     return true;
   }
   return false;
@@ -1302,6 +1309,8 @@ void smx_debug_force_path(int path) { g_force_path.store(path >= 0 && path <= 6 
 int64_t smx_debug_alloc_count(void) { return g_alloc_calls.load(); }
 
 void smx_debug_set_count_probe(int64_t polls) { g_count_probe.store(polls > 0 ? polls : 0); }
+
+void smx_debug_set_stripe_wait(int ns) { g_stripe_wait_ns.store(ns >= 0 && ns <= 100000 ? ns : -1); }
 
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
   g_max_cluster.store(max_cluster > 0 ? max_cluster : 0);

@@ -77,6 +77,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// Bounded wait that yields the issue slots while it waits: after a failed
+// blocking poll the thread sleeps about `sleep_ns` (0: poll again at once).
+// Warps that wait on data or on another warp here do not take issue slots
+// from the warps that work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, int64_t max_polls,
+                                                  unsigned sleep_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  for (int64_t i = 1; i < max_polls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
+  }
+  return false;
+}
+
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -89,6 +103,17 @@ __device__ __forceinline__ void st_peer_f32(float* local, uint32_t rank, float v
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(local)), "r"(rank));
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
 }
+// Per-row completion counters of the cooperative long-row kernels: an
+// acquire load (GPU scope) to poll one, a release add to count into one.
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

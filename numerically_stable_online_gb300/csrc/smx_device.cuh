@@ -59,6 +59,12 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+// The same over three operands in one instruction (sm_100 family).
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // e^(x - m), fast form: one rounding of x - m, one of the product by log2 e.
 // Relative error about (|x - m| + 1) * 2^-23 plus that of the exp2 unit; used

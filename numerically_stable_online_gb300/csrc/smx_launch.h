@@ -67,15 +67,20 @@ struct Plan {
   unsigned* stripe_count_next = nullptr;
   int64_t stripe_count_next_n = 0;
   int64_t stripe_probe = 0;  // > 0: the count waits' error-path probe (paths 5 fused and 6)
+  unsigned stripe_wait_ns = 0;  // path 6 compute warps: sleep between polls of a wait
 };
 
 // The read-once long-row kernel (kernel_stripe.cuh).
-constexpr int STRIPE_SYNC_WARPS = 2;   // sync warps per CTA (alternate rows)
-constexpr int STRIPE_LAG = 2;          // rows between a stripe's summary and its normalisation
-constexpr int STRIPE_RING = 4;         // summary / row-constant ring entries (>= LAG + 1)
+constexpr int STRIPE_COLLECT_WARPS = 3;                       // collector warps (rows round robin)
+constexpr int STRIPE_SYNC_WARPS = 2 + STRIPE_COLLECT_WARPS;   // + the producer and publisher warps
+constexpr int STRIPE_LAG = 4;          // rows between a stripe's summary and its normalisation
+constexpr int STRIPE_RING = 8;         // summary / row-constant ring entries (>= LAG + 1)
 constexpr int STRIPE_MAX_SLOTS = 16;   // shared-memory ring slots (>= LAG + 2)
-constexpr int STRIPE_MAX_Q = 256;      // stripes per row (at most 8 summaries per sync lane)
-constexpr int STRIPE_THREADS = 1024;   // 30 compute warps + 2 sync warps
+constexpr int STRIPE_MAX_Q = 256;      // stripes per row (at most 8 summaries per collector lane)
+constexpr int STRIPE_THREADS = 1024;   // 27 compute warps + producer + publisher + 3 collectors
+constexpr int STRIPE_COMPUTE_THREADS = STRIPE_THREADS - 32 * STRIPE_SYNC_WARPS;
+constexpr int STRIPE_MAX_VPT = 3;      // 16-byte vectors per compute thread (registers)
+constexpr unsigned STRIPE_WAIT_NS = 0;  // compute warps' sleep between polls of a wait
 
 constexpr int CLUSTER_RV = 2;  // register vectors per thread on the cluster path
 constexpr int CLUSTER_THREADS = 1024;

@@ -87,8 +87,10 @@ def test_steady_loop_allocates_nothing(lib):
         parity.compare(y[:4].cpu().numpy(), p, "f32")
         ph = oracle.softmax_rows(hx.numpy().reshape(-1), "f32", 4, 262_144)
         parity.compare(hy.numpy(), ph, "f32")
-        # a call with more rows than any before grows the scratch once
-        x2 = torch.randn(rows * 3, cols // 4, device=DEV)
+        # a call with more long rows than any before grows the scratch once
+        # (160 rows of 4 MiB: 160 x 152 stripe summaries, more than any
+        # buffer so far holds)
+        x2 = torch.randn(160, cols, device=DEV)
         y2 = torch.empty_like(x2)
         smx.softmax_rows(x2, out=y2)
         torch.cuda.synchronize()
