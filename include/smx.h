@@ -373,9 +373,13 @@ int smx_version(void);
  *   kernels normalise with, 4 = the compensated e^(a - b) of fp32 outputs,
  *   5 = one term e^(a - b) as the statistics path forms it.  a, b, out:
  *   device float[n] (b only for 4 and 5).  The pages have no counterpart.
- * smx_debug_set_stripe_wait(ns): path 6's compute warps sleep about ns
- *   nanoseconds between polls of a wait (0 = poll again at once; -1 = the
- *   default).
+ * smx_debug_set_stripe_tuning(lag, piece_bytes, l2_ahead): path 6's rows of
+ *   lag between a stripe's summary and its normalisation (1..6, at most the
+ *   ring's slots - 2; 0 =
+ *   default), the size of the bulk copies a stripe is fetched in (a multiple
+ *   of 16; 0 = one copy per stripe; -1 = default) and how many rows past
+ *   each fill the producer prefetches that row's stripe into L2 (0 = off;
+ *   -1 = default).
  * smx_debug_set_count_probe(polls): polls > 0: the per-row count waits of
  *   the cooperative long-row kernels (path 6, and path 5 in its single-launch
  *   form) wait for one more stripe or chunk than the row has, give up after
@@ -400,7 +404,7 @@ void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 int64_t smx_debug_alloc_count(void);
 void smx_debug_set_count_probe(int64_t polls);
-void smx_debug_set_stripe_wait(int ns);
+void smx_debug_set_stripe_tuning(int lag, int piece_bytes, int l2_ahead);
 smx_status smx_debug_probe_math(const float *a, const float *b, float *out, int64_t n, int which,
                                 smx_stream_t stream);
 

@@ -121,8 +121,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_alloc_count.restype = I64
         lib.smx_debug_set_count_probe.argtypes = [I64]
         lib.smx_debug_set_count_probe.restype = None
-        lib.smx_debug_set_stripe_wait.argtypes = [I32]
-        lib.smx_debug_set_stripe_wait.restype = None
+        lib.smx_debug_set_stripe_tuning.argtypes = [I32, I32, I32]
+        lib.smx_debug_set_stripe_tuning.restype = None
         lib.smx_debug_probe_math.argtypes = [P, P, P, I64, I32, P]
         lib.smx_debug_probe_math.restype = st
         _lib = lib

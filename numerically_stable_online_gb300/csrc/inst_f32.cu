@@ -17,3 +17,11 @@ int backward_occupancy_f32(int vpt, int threads) {
 int stripe_occupancy_f32(int64_t smem) { return stripe_occupancy<float>(smem); }
 int stripe_static_smem_f32() { return stripe_static_smem<float>(); }
 }  // namespace smx
+
+#ifdef SMX_STRIPE_TRACE
+// The stripe kernel's wait stamps (build-time diagnostic; see kernel_stripe.cuh).
+extern "C" int smx_debug_stripe_trace(void* host, int64_t bytes) {
+  const int64_t n = (int64_t)sizeof(smx::g_stripe_trace);
+  return cudaMemcpyFromSymbol(host, smx::g_stripe_trace, (size_t)(bytes < n ? bytes : n)) == cudaSuccess ? 0 : 1;
+}
+#endif

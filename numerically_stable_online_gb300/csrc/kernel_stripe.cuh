@@ -63,7 +63,9 @@ struct StripeArgs {
   float* loss;
   int64_t max_polls;  // bound of each wait
   int64_t probe;      // > 0: the collectors wait for one stripe more than exists (the error-path probe)
-  unsigned wait_ns;   // compute warps: sleep between polls of a wait (0: poll at once)
+  int lag;            // rows between a stripe's summary and its normalisation (1..STRIPE_LAG)
+  int piece_bytes;    // bulk copies of at most this many bytes per stripe (0: one copy)
+  int l2_ahead;       // the producer prefetches into L2 the stripe this many rows past each fill (0: off)
   int* status;
 };
 
@@ -72,6 +74,8 @@ struct StripeRow {
   float M, D, ld;  // merged maximum and sum, log D
   OutConst kc;     // constants of out_value (its rD is 1/D)
   int zero_row, nan_row;
+  float F[32];     // kept exponentials: compute warp w's factor e^(m_w - M) / D
+                   // (0 when the warp held no finite element, or on a zero / NaN row)
 };
 
 // The flat merge of up to 32 summaries, one per lane (lanes without one pass
@@ -93,6 +97,22 @@ __device__ __forceinline__ float2 ld_cg_f2(const float2* p) {
   return v;
 }
 
+// SMX_STRIPE_TRACE (a build-time diagnostic, off in the library build): the
+// kernel stamps %globaltimer at its waits, per CTA and row, into a device
+// array read back with smx_debug_stripe_trace().
+#ifdef SMX_STRIPE_TRACE
+constexpr int STRIPE_TRACE_CTAS = 160, STRIPE_TRACE_ROWS = 256, STRIPE_TRACE_EVENTS = 8;
+__device__ unsigned long long g_stripe_trace[STRIPE_TRACE_CTAS][STRIPE_TRACE_ROWS][STRIPE_TRACE_EVENTS];
+__device__ __forceinline__ void stripe_stamp(int64_t r, int ev) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (blockIdx.x < STRIPE_TRACE_CTAS && r < STRIPE_TRACE_ROWS) g_stripe_trace[blockIdx.x][r][ev] = t;
+}
+#define SMX_STAMP(r, ev) stripe_stamp((r), (ev))
+#else
+#define SMX_STAMP(r, ev) ((void)0)
+#endif
+
 template <typename InT, typename OutT, int MODE>
 struct StripePolicy {
   // fp32 in and out: the compensated exponentials of the sum pass are kept in
@@ -109,8 +129,9 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
   static_assert(MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE, "modes of the stripe kernel");
   constexpr int V = Elem<InT>::V;
   constexpr bool KEEP_E = StripePolicy<InT, OutT, MODE>::KEEP_E;
-  constexpr int LAG = STRIPE_LAG, RING = STRIPE_RING;
-  constexpr int NC = STRIPE_THREADS / 32 - STRIPE_SYNC_WARPS;  // compute warps
+  constexpr int RING = STRIPE_RING;
+  const int LAG = a.lag;
+  constexpr int NC = STRIPE_COMPUTE_WARPS;
   constexpr int TC = NC * 32;
   extern __shared__ __align__(128) uint4 slots[];  // [nslots][slot_vecs]
   __shared__ __align__(8) uint64_t full_bar[STRIPE_MAX_SLOTS], free_bar[STRIPE_MAX_SLOTS];
@@ -119,7 +140,9 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
   __shared__ long long slot_t[STRIPE_MAX_SLOTS];    // cross-entropy: the target, -1 if ignored
   __shared__ float slot_xt[STRIPE_MAX_SLOTS];       // cross-entropy: x_t when this stripe holds it
   __shared__ float2 warp_md[RING][32];              // each compute warp's (m_w, d_w) of a row
+  __shared__ int warp_fast[RING][32];               // ... and whether it kept fast exponentials
   __shared__ StripeRow rowc[RING];
+  __shared__ uint4 neg_vec;                         // a vector of -inf (read in place of vectors past the stripe)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = (int)(blockIdx.x / (unsigned)a.Q), q = (int)(blockIdx.x % (unsigned)a.Q);
@@ -142,6 +165,9 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
     a.count_next[i] = 0;
 
   if (tid == 0) {
+    const unsigned ninf = std::is_same<InT, float>::value ? 0xff800000u
+                          : (std::is_same<InT, __half>::value ? 0xfc00fc00u : 0xff80ff80u);
+    neg_vec = make_uint4(ninf, ninf, ninf, ninf);
     for (int s = 0; s < nslots; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&free_bar[s]), NC);
@@ -156,53 +182,99 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
 
   if (warp < NC) {
     // ------------------------------------------------------------ compute warps
+    // Thread c holds vectors c, c + TC, ... of the stripe; those at or past
+    // nvq are read clamped to the stripe's last vector and discarded.  The
+    // per-vector work is branch-free: the row-uniform cases (a stripe cut by
+    // the valid prefix, zero and NaN rows) are decided once per row.
     const int c = tid;
     bool timed_out = false;  // after one wait ran out, later waits poll once
     for (int64_t i = 0; i < nr + LAG; ++i) {
       if (i < nr) {
         // ---- row i: this warp's part of the stripe, its maximum, its sum
         const int s = (int)(i % nslots), kr = (int)(i % RING);
-        if (!mbar_wait_backoff(smem_addr(&full_bar[s]), (uint32_t)((i / nslots) & 1),
-                               timed_out ? 1 : a.max_polls, a.wait_ns))
+        if (c == 0) SMX_STAMP(i, 0);
+        if (!mbar_wait_bounded(smem_addr(&full_bar[s]), (uint32_t)((i / nslots) & 1),
+                               timed_out ? 1 : a.max_polls))
           timed_out = true;
+        if (c == 0) SMX_STAMP(i, 1);
         const int Lv = stripe_valid(slot_len[s]);
-        const InT* sx = reinterpret_cast<const InT*>(slots + (size_t)s * a.slot_vecs);
+        const bool cut = Lv != nvq * V;  // the valid prefix ends inside the stripe
+        uint4* sv = slots + (size_t)s * a.slot_vecs;
         float f[VPT][V];
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-          const int e0 = (j * TC + c) * V;
-          load_masked<InT, true>(sx + e0, e0, Lv, f[j]);
+          const int k = j * TC + c;
+          unpack16<InT>(*(k < nvq ? sv + k : &neg_vec), f[j]);
+        }
+        if (cut) {
+#pragma unroll
+          for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int u = 0; u < V; ++u) f[j][u] = (j * TC + c) * V + u < Lv ? f[j][u] : neg_inf();
         }
         if constexpr (MODE == MODE_CE) {
           // x_t, kept by the thread that holds it (the slot's x may be overwritten)
           const int64_t t = slot_t[s] - col0;
+          const InT* sx = reinterpret_cast<const InT*>(sv);
           if (t >= 0 && t < Lv && (int)(t / V) % TC == c) slot_xt[s] = Elem<InT>::to_f32(sx[t]);
         }
         const float mw = warp_max_nan(local_max(f));
         float dw = 0.0f;
+        int fast = 0;
         if (mw != neg_inf()) {
-          float sum;
           if constexpr (KEEP_E) {
-            sum = 0.0f;
+            // Kept exponentials.  When every element the warp holds lies
+            // within STRIPE_FAST_RANGE of m_w, the plain form 2^(fma(x,
+            // log2e_hi, c)) is accurate enough: its argument, below 16 in
+            // magnitude, rounds with an error under 2^-21 (the exponential's
+            // relative error stays near 3e-7 plus the unit's own 1.4e-7, and
+            // log2e_hi's representation adds at most 11 * 2^-25.7), and the
+            // rounding of c = RN(-m_w log2e_hi) is common to the warp: its
+            // exact residual is applied to d_w here and to the warp's factor
+            // by the collector.  Otherwise (a wider range, masked or special
+            // values) the compensated exponential.
+            float mn = f[0][0];
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-              const int k = j * TC + c;
-              if (k * V < Lv) {
+            for (int j = 0; j < VPT; ++j)
+#pragma unroll
+              for (int u = 0; u < V; u += 2) mn = fmin3(mn, f[j][u], f[j][u + 1]);
+            mn = warp_min(mn);
+            fast = (fabsf(mw) < 1e38f && mn >= __fsub_rn(mw, STRIPE_FAST_RANGE)) ? 1 : 0;
+            unsigned long long acc = pk(0.0f, 0.0f);
+            if (fast) {
+              const float cw = __fmul_rn(-mw, L2E_HI);
+              const unsigned long long k2 = pk(L2E_HI, L2E_HI), c2 = pk(cw, cw);
+#pragma unroll
+              for (int j = 0; j < VPT; ++j) {
+                const int k = j * TC + c;
+#pragma unroll
+                for (int u = 0; u < V; u += 2) {
+                  const unsigned long long uu = fma2(pk(f[j][u], f[j][u + 1]), k2, c2);
+                  f[j][u] = ex2_ftz(pk_lo(uu));
+                  f[j][u + 1] = ex2_ftz(pk_hi(uu));
+                }
+                if (k < nvq) *reinterpret_cast<float4*>(sv + k) = make_float4(f[j][0], f[j][1], f[j][2], f[j][3]);
+                acc = add2(acc, add2(pk(f[j][0], f[j][1]), pk(f[j][2], f[j][3])));
+              }
+              dw = stats_correct(warp_sum(__fadd_rn(pk_lo(acc), pk_hi(acc))), mw);
+            } else {
+#pragma unroll
+              for (int j = 0; j < VPT; ++j) {
+                const int k = j * TC + c;
 #pragma unroll
                 for (int u = 0; u < V; u += 2) exp_shift_accurate2(f[j][u], f[j][u + 1], mw, f[j][u], f[j][u + 1]);
-                *reinterpret_cast<float4*>(slots + (size_t)s * a.slot_vecs + k) =
-                    make_float4(f[j][0], f[j][1], f[j][2], f[j][3]);
-                sum = __fadd_rn(sum, __fadd_rn(__fadd_rn(f[j][0], f[j][1]), __fadd_rn(f[j][2], f[j][3])));
+                if (k < nvq) *reinterpret_cast<float4*>(sv + k) = make_float4(f[j][0], f[j][1], f[j][2], f[j][3]);
+                acc = add2(acc, add2(pk(f[j][0], f[j][1]), pk(f[j][2], f[j][3])));
               }
+              dw = warp_sum(__fadd_rn(pk_lo(acc), pk_hi(acc)));
             }
-            dw = warp_sum(sum);
           } else {
-            sum = sum_exp(f, mw);
-            dw = stats_correct(warp_sum(sum), mw);
+            dw = stats_correct(warp_sum(sum_exp(f, mw)), mw);
           }
         }
         if (lane == 0) {
           warp_md[kr][warp] = make_float2(mw, dw);
+          warp_fast[kr][warp] = fast;
           mbar_arrive(smem_addr(&summ_bar[kr]));
         }
       }
@@ -210,15 +282,17 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         // ---- normalise row r = i - LAG from its slot
         const int64_t r = i - LAG;
         const int s = (int)(r % nslots), kr = (int)(r % RING);
-        if (!mbar_wait_backoff(smem_addr(&row_bar[kr]), (uint32_t)((r / RING) & 1),
-                               timed_out ? 1 : a.max_polls, a.wait_ns))
+        if (c == 0) SMX_STAMP(r, 2);
+        if (!mbar_wait_bounded(smem_addr(&row_bar[kr]), (uint32_t)((r / RING) & 1),
+                               timed_out ? 1 : a.max_polls))
           timed_out = true;
-        const StripeRow rc = rowc[kr];
+        if (c == 0) SMX_STAMP(r, 3);
+        const StripeRow& rc = rowc[kr];
         const int Lv = stripe_valid(slot_len[s]);
+        const bool cut = Lv != nvq * V;
         const int64_t row = row_of(r);
         OutT* yr = y + row * a.cols + col0;
-        const InT* sx = reinterpret_cast<const InT*>(slots + (size_t)s * a.slot_vecs);
-        const float* se = reinterpret_cast<const float*>(slots + (size_t)s * a.slot_vecs);
+        const uint4* sv = slots + (size_t)s * a.slot_vecs;
         bool zero_out = rc.zero_row, nan_out = rc.nan_row;
         int64_t tl = -1;
         if constexpr (MODE == MODE_CE) {
@@ -228,58 +302,56 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           tl = ignored ? -1 : slot_t[s] - col0;
           if (tl >= Lv) tl = -1;  // the target lies in another stripe (or before this one: tl < 0)
         }
-        // kept exponentials: this warp's factor e^(m_w - M) / D (0 when the
-        // warp held no finite element: its part of the slot still holds x)
-        float F = 0.0f;
-        if constexpr (KEEP_E) {
-          const float mw = warp_md[kr][warp].x;
-          F = (mw == neg_inf() || zero_out || nan_out) ? 0.0f : __fmul_rn(rescale_factor(mw, rc.M), rc.kc.rD);
-        }
+        // kept exponentials: this warp's factor (0 also when it held no finite
+        // element: its part of the slot still holds x)
+        const float F = KEEP_E ? rc.F[warp] : 0.0f;
+        if (zero_out || nan_out || (KEEP_E && F == 0.0f)) {
+          // the policy's rows: +0 (log: -inf), NaN in the valid lanes of NaN rows
+          const float fill = (MODE == MODE_LOG) ? neg_inf() : 0.0f;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-          const int k = j * TC + c;
-          const int e0 = k * V;
-          if (k < nvq) {
+          for (int j = 0; j < VPT; ++j) {
+            const int k = j * TC + c;
             float o[V];
-            if constexpr (MODE == MODE_LOG) {
-              if (nan_out || zero_out) {
 #pragma unroll
-                for (int u = 0; u < V; ++u) o[u] = (nan_out && e0 + u < Lv) ? qnan() : neg_inf();
-              } else {
-                float fv[V];
-                load_masked<InT, true>(sx + e0, e0, Lv, fv);
-                const unsigned long long nm = pk(-rc.M, -rc.M), nl = pk(-rc.ld, -rc.ld);
+            for (int u = 0; u < V; ++u) o[u] = (nan_out && k * V + u < Lv) ? qnan() : fill;
+            if (k < nvq) store_vec<OutT, V>(yr + k * V, o);
+          }
+        } else {
+          const float M = rc.M;
+#pragma unroll
+          for (int j = 0; j < VPT; ++j) {
+            const int k = j * TC + c;
+            const uint4 raw = *(k < nvq ? sv + k : &neg_vec);  // (past the stripe: not stored)
+            float o[V];
+            if constexpr (KEEP_E) {
+              // past the valid prefix the slot holds kept zeros (exponentials of -inf)
+              const unsigned long long f2 = pk(F, F);
+              const unsigned long long p0 = mul2(pk(__uint_as_float(raw.x), __uint_as_float(raw.y)), f2);
+              const unsigned long long p1 = mul2(pk(__uint_as_float(raw.z), __uint_as_float(raw.w)), f2);
+              o[0] = pk_lo(p0);
+              o[1] = pk_hi(p0);
+              o[2] = pk_lo(p1);
+              o[3] = pk_hi(p1);
+            } else {
+              float fv[V];
+              unpack16<InT>(raw, fv);
+              if (cut) {
+#pragma unroll
+                for (int u = 0; u < V; ++u) fv[u] = k * V + u < Lv ? fv[u] : neg_inf();
+              }
+              if constexpr (MODE == MODE_LOG) {
+                const unsigned long long nm = pk(-M, -M), nl = pk(-rc.ld, -rc.ld);
 #pragma unroll
                 for (int u = 0; u < V; u += 2) {
                   const unsigned long long t2 = add2(add2(pk(fv[u], fv[u + 1]), nm), nl);
                   o[u] = pk_lo(t2);
                   o[u + 1] = pk_hi(t2);
                 }
-              }
-            } else {
-              if (nan_out || zero_out || e0 >= Lv || (KEEP_E && F == 0.0f)) {
-#pragma unroll
-                for (int u = 0; u < V; ++u) o[u] = (nan_out && e0 + u < Lv) ? qnan() : 0.0f;
-              } else if constexpr (KEEP_E) {
-                const float4 e4 = *reinterpret_cast<const float4*>(se + e0);
-                const unsigned long long f2 = pk(F, F);
-                const unsigned long long p0 = mul2(pk(e4.x, e4.y), f2), p1 = mul2(pk(e4.z, e4.w), f2);
-                o[0] = pk_lo(p0);
-                o[1] = pk_hi(p0);
-                o[2] = pk_lo(p1);
-                o[3] = pk_hi(p1);
-                if (e0 + V > Lv) {
-#pragma unroll
-                  for (int u = 0; u < V; ++u)
-                    if (e0 + u >= Lv) o[u] = 0.0f;
-                }
               } else {
-                float fv[V];
-                load_masked<InT, true>(sx + e0, e0, Lv, fv);
                 out_values<OutT, V>(fv, rc.kc, o);
               }
             }
-            store_vec<OutT, V>(yr + e0, o);
+            if (k < nvq) store_vec<OutT, V>(yr + k * V, o);
           }
         }
         if constexpr (MODE == MODE_CE) {
@@ -291,7 +363,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
             if (!bad) {
               float pt;
               if constexpr (KEEP_E) {
-                pt = __fmul_rn(se[tl], F);
+                pt = __fmul_rn(reinterpret_cast<const float*>(sv)[tl], F);
               } else {
                 pt = out_value<OutT>(xt, rc.kc);
               }
@@ -303,6 +375,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         // this warp is done with the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&free_bar[s]));
+        if (c == 0) SMX_STAMP(r, 4);
       }
     }
   } else if (warp == NC) {
@@ -335,13 +408,32 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const uint32_t bar = smem_addr(&full_bar[s]);
         if (nv > 0) {
-          mbar_arrive_expect_tx(bar, (uint32_t)nv * 16u);
-          bulk_load_g2s(smem_addr(slots + (size_t)s * a.slot_vecs), x + row * a.cols + col0, (uint32_t)nv * 16u,
-                        bar);
+          // one expect-tx for the stripe, then its bytes in pieces of at most
+          // piece_bytes (several copies in flight at once)
+          const uint32_t total = (uint32_t)nv * 16u;
+          const uint32_t piece = a.piece_bytes > 0 ? (uint32_t)a.piece_bytes : total;
+          mbar_arrive_expect_tx(bar, total);
+          const char* src = reinterpret_cast<const char*>(x + row * a.cols + col0);
+          const uint32_t dst = smem_addr(slots + (size_t)s * a.slot_vecs);
+          for (uint32_t off = 0; off < total; off += piece)
+            bulk_load_g2s(dst + off, src + off, total - off < piece ? total - off : piece, bar);
         } else {
           mbar_arrive(bar);  // an empty stripe: the phase completes with no bytes
         }
         filled = j;
+        SMX_STAMP(j, 5);
+        // the stripe of a row further ahead, into L2 only (no shared memory)
+        const int64_t jp = j + a.l2_ahead;
+        if (a.l2_ahead > 0 && jp < nr && jp >= nslots) {
+          const int64_t rp = row_of(jp);
+          int64_t Lp = a.cols;
+          if (valid_len != nullptr) {
+            const int64_t v = __ldg(valid_len + rp);
+            Lp = v < 0 ? 0 : (v > a.cols ? a.cols : v);
+          }
+          const int nvp = (stripe_valid(Lp) + V - 1) / V;
+          if (nvp > 0) bulk_prefetch_l2(x + rp * a.cols + col0, (uint32_t)nvp * 16u);
+        }
       }
       // no bulk copy may outlive the CTA: wait (bounded) for each slot's last
       // issued fill (normally long complete)
@@ -365,6 +457,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         const int64_t row = row_of(r);
         a.sums[row * a.Q + q] = make_float2(md.m, md.d);
         red_release_add(a.count + row, 1u);
+        SMX_STAMP(r, 6);
       }
       __syncwarp();
     }
@@ -389,6 +482,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           __nanosleep(64);
         }
         if (late) atomicOr(a.status, DEV_TIMEOUT);
+        SMX_STAMP(r, 7);
       }
       if (__shfl_sync(0xffffffffu, late, 0)) timed_out = true;
       __syncwarp();  // lane 0's acquire orders the summaries for the warp
@@ -409,17 +503,36 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           if (b[u].x != neg_inf()) dl = __fadd_rn(dl, __fmul_rn(b[u].y, rescale_factor(b[u].x, ml)));
       }
       const MD md = warp_flat_merge(ml, dl);
+      const bool zero_row = md.m == neg_inf();
+      const bool nan_row = !zero_row && (md.d != md.d || md.m != md.m || md.m == pos_inf());
+      const OutConst kc = make_out_const<OutT>(md.m, md.d);
+      StripeRow& rc = rowc[kr];
+      if constexpr (KEEP_E) {
+        // lane w: compute warp w's factor e^(m_w - M) / D (its m_w is in
+        // warp_md until the compute warps reach row r + RING, after row r)
+        if (lane < NC) {
+          const float mw = warp_md[kr][lane].x;
+          float F = (mw == neg_inf() || zero_row || nan_row) ? 0.0f : __fmul_rn(rescale_factor(mw, md.m), kc.rD);
+          if (warp_fast[kr][lane]) {
+            // the warp's fast exponentials carry 2^(-delta), delta the exact
+            // residual of RN(-m_w log2e_hi): the factor takes 2^(delta) back
+            const float cw = __fmul_rn(-mw, L2E_HI);
+            const float delta = __fmaf_rn(-mw, L2E_HI, -cw);
+            F = __fmaf_rn(F, __fmul_rn(delta, LN2), F);
+          }
+          rc.F[lane] = F;
+        }
+      }
       if (lane == 0) {
-        StripeRow rc;
         rc.M = md.m;
         rc.D = md.d;
-        rc.zero_row = md.m == neg_inf();
-        rc.nan_row = !rc.zero_row && (md.d != md.d || md.m != md.m || md.m == pos_inf());
-        rc.ld = rc.zero_row ? 0.0f : logf(md.d);
-        rc.kc = make_out_const<OutT>(md.m, md.d);
-        rowc[kr] = rc;
-        mbar_arrive(smem_addr(&row_bar[kr]));
+        rc.zero_row = zero_row;
+        rc.nan_row = nan_row;
+        rc.ld = zero_row ? 0.0f : logf(md.d);
+        rc.kc = kc;
       }
+      __syncwarp();  // every lane's fields are written before lane 0 releases the row
+      if (lane == 0) mbar_arrive(smem_addr(&row_bar[kr]));
       __syncwarp();
     }
   }

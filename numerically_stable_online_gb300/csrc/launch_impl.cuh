@@ -276,7 +276,9 @@ cudaError_t launch_stripe_v(const Call& c, const Plan& p) {
   a.loss = c.loss;
   a.max_polls = c.max_polls;
   a.probe = p.stripe_probe;
-  a.wait_ns = p.stripe_wait_ns;
+  a.lag = p.stripe_lag;
+  a.piece_bytes = p.stripe_piece;
+  a.l2_ahead = p.stripe_l2_ahead;
   a.status = c.status;
   const InT* xp = static_cast<const InT*>(c.x);
   OutT* yp = static_cast<OutT*>(c.y);
@@ -292,7 +294,7 @@ template <typename InT, typename OutT, int MODE>
 cudaError_t launch_stripe(const Call& c, const Plan& p) {
   switch (p.vpt) {
     case 2: return launch_stripe_v<InT, OutT, MODE, 2>(c, p);
-    case 3: return launch_stripe_v<InT, OutT, MODE, 3>(c, p);
+    case 4: return launch_stripe_v<InT, OutT, MODE, 4>(c, p);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -97,7 +97,9 @@ std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: read
 // count: a steady loop of calls adds none).
 std::atomic<int64_t> g_alloc_calls{0};
 std::atomic<int64_t> g_count_probe{0};
-std::atomic<int> g_stripe_wait_ns{-1};  // path 6 compute warps' sleep between polls (-1: default)  // > 0: the cooperative long-row kernels' error-path probe (polls)
+std::atomic<int> g_stripe_lag{0};    // path 6: rows of lag (0: default)
+std::atomic<int> g_stripe_piece{-1};  // path 6: bytes per bulk copy (-1: default)
+std::atomic<int> g_stripe_l2_ahead{-1};  // path 6: rows prefetched into L2 past a fill (-1: default)  // > 0: the cooperative long-row kernels' error-path probe (polls)
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_path = 0;
@@ -503,7 +505,7 @@ bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* 
   const int64_t cap = d.sm_count < STRIPE_MAX_Q ? d.sm_count : STRIPE_MAX_Q;  // one CTA per SM
   // a compute thread holds at most STRIPE_MAX_VPT vectors of a stripe
   const int64_t vec_cap = (int64_t)STRIPE_MAX_VPT * STRIPE_COMPUTE_THREADS;
-  for (const int target : {8, 6, STRIPE_LAG + 2}) {
+  for (const int target : {8, STRIPE_MIN_SLOTS}) {
     int64_t slot_cap = ring_vecs / target;
     if (slot_cap > vec_cap) slot_cap = vec_cap;
     if (slot_cap <= 0) continue;
@@ -518,19 +520,24 @@ bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* 
     const int64_t slot_vecs = (nvec + Q - 1) / Q;
     int64_t nslots = ring_vecs / slot_vecs;
     if (nslots > STRIPE_MAX_SLOTS) nslots = STRIPE_MAX_SLOTS;
-    if (nslots < STRIPE_LAG + 2) continue;
+    if (nslots < STRIPE_MIN_SLOTS) continue;
     const int64_t smem = nslots * slot_vecs * 16;
     if (stripe_occupancy(in_dtype, smem) < 1) return false;
     p->path = PATH_STRIPE;
-    p->vpt = slot_vecs <= 2LL * STRIPE_COMPUTE_THREADS ? 2 : 3;
+    p->vpt = slot_vecs <= 2LL * STRIPE_COMPUTE_THREADS ? 2 : 4;
     p->stripe_q = (int)Q;
     p->stripe_groups = (int)groups;
     p->stripe_slots = (int)nslots;
     p->stripe_slot_vecs = (int)slot_vecs;
     p->ctas = (int)(Q * groups);
     p->stripe_probe = g_count_probe.load();
-    const int wn = g_stripe_wait_ns.load();
-    p->stripe_wait_ns = wn >= 0 ? (unsigned)wn : STRIPE_WAIT_NS;
+    const int lg = g_stripe_lag.load(), pc = g_stripe_piece.load();
+    p->stripe_lag = lg > 0 && lg < nslots - 1 ? lg : (STRIPE_DEFAULT_LAG < nslots - 1 ? STRIPE_DEFAULT_LAG : (int)nslots - 2);
+    p->stripe_piece = pc >= 0 ? pc : STRIPE_DEFAULT_PIECE;
+    const int la = g_stripe_l2_ahead.load();
+    // measured on GB300 (64 rows of 4 MiB): an L2 prefetch 4 rows ahead
+    // helps fp32 rows (120 -> 109 us) and slows bf16 rows a little
+    p->stripe_l2_ahead = la >= 0 ? la : (in_dtype == SMX_F32 ? STRIPE_DEFAULT_L2_AHEAD_F32 : STRIPE_DEFAULT_L2_AHEAD_16);
     return true;
   }
   return false;
@@ -688,19 +695,17 @@ Plan plan_call(const Call& c, DeviceInfo& dev) {
                               inflight, &p);
       }
       if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
-      // rows longer than one CTA holds: a row per thread-block cluster when the
-      // rows fill every resident cluster and are shorter than 4 MiB, else
-      // chunks (path 5), which spread every row over all SMs (measured on
-      // GB300: from 4 MiB rows on, the cluster's on-chip copy no longer holds
-      // the row and the chunked path is faster)
+      // rows longer than one CTA holds: read once in column stripes over all
+      // SMs when the stripes fit the SMs' shared memory (softmax, log_softmax,
+      // cross-entropy with a gradient); the statistics rows a row per
+      // thread-block cluster when the rows fill every resident cluster and
+      // are shorter than 4 MiB; else chunks (path 5), which spread every row
+      // over all SMs
+      if (!planned && stripe_mode) planned = plan_stripe(dev, c.rows, c.cols, c.in_dtype, &p);
       if (!planned && classic && c.cols * es_in < CLUSTER_MAX_ROW_BYTES) {
         planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
         if (planned && c.rows < p.resident_clusters) planned = false;
       }
-      // longer rows, or too few to fill the clusters: read once in column
-      // stripes over all SMs when the stripes fit the SMs' shared memory
-      // (softmax, log_softmax, cross-entropy with a gradient)
-      if (!planned && stripe_mode) planned = plan_stripe(dev, c.rows, c.cols, c.in_dtype, &p);
       if (!planned) planned = plan_split(dev, c.cols, c.in_dtype, &p);
       if (!planned && classic) planned = plan_cluster(dev, c.rows, c.cols, c.in_dtype, &p);
     }
@@ -1310,7 +1315,11 @@ int64_t smx_debug_alloc_count(void) { return g_alloc_calls.load(); }
 
 void smx_debug_set_count_probe(int64_t polls) { g_count_probe.store(polls > 0 ? polls : 0); }
 
-void smx_debug_set_stripe_wait(int ns) { g_stripe_wait_ns.store(ns >= 0 && ns <= 100000 ? ns : -1); }
+void smx_debug_set_stripe_tuning(int lag, int piece_bytes, int l2_ahead) {
+  g_stripe_lag.store(lag >= 1 && lag <= STRIPE_LAG ? lag : 0);
+  g_stripe_piece.store(piece_bytes >= 0 && piece_bytes % 16 == 0 ? piece_bytes : -1);
+  g_stripe_l2_ahead.store(l2_ahead >= 0 && l2_ahead <= 64 ? l2_ahead : -1);
+}
 
 void smx_debug_set_cluster(int max_cluster, int64_t smem_bytes) {
   g_max_cluster.store(max_cluster > 0 ? max_cluster : 0);

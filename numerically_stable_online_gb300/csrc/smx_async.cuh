@@ -77,18 +77,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
-// Bounded wait that yields the issue slots while it waits: after a failed
-// blocking poll the thread sleeps about `sleep_ns` (0: poll again at once).
-// Warps that wait on data or on another warp here do not take issue slots
-// from the warps that work.
-__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, int64_t max_polls,
-                                                  unsigned sleep_ns) {
-  if (mbar_test_wait(bar, parity)) return true;
-  for (int64_t i = 1; i < max_polls; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (sleep_ns) __nanosleep(sleep_ns);
-  }
-  return false;
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
+// ahead of their use (the bulk-copy engine; no shared memory, no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

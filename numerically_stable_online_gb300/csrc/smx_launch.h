@@ -67,20 +67,34 @@ struct Plan {
   unsigned* stripe_count_next = nullptr;
   int64_t stripe_count_next_n = 0;
   int64_t stripe_probe = 0;  // > 0: the count waits' error-path probe (paths 5 fused and 6)
-  unsigned stripe_wait_ns = 0;  // path 6 compute warps: sleep between polls of a wait
+  int stripe_lag = 4;    // path 6: rows between summary and normalisation
+  int stripe_piece = 0;  // path 6: bytes per bulk copy of a stripe (0: one)
+  int stripe_l2_ahead = 0;  // path 6: rows past a fill whose stripe is prefetched into L2 (0: off)
 };
 
-// The read-once long-row kernel (kernel_stripe.cuh).
+// The read-once long-row kernel (kernel_stripe.cuh).  SMX_STRIPE_COMPUTE_WARPS
+// (a build-time tuning knob) sets its compute warps.
+#ifndef SMX_STRIPE_COMPUTE_WARPS
+#define SMX_STRIPE_COMPUTE_WARPS 27
+#endif
 constexpr int STRIPE_COLLECT_WARPS = 3;                       // collector warps (rows round robin)
 constexpr int STRIPE_SYNC_WARPS = 2 + STRIPE_COLLECT_WARPS;   // + the producer and publisher warps
-constexpr int STRIPE_LAG = 4;          // rows between a stripe's summary and its normalisation
+constexpr int STRIPE_COMPUTE_WARPS = SMX_STRIPE_COMPUTE_WARPS;
+constexpr int STRIPE_THREADS = 32 * (STRIPE_COMPUTE_WARPS + STRIPE_SYNC_WARPS);
+constexpr int STRIPE_COMPUTE_THREADS = 32 * STRIPE_COMPUTE_WARPS;
+constexpr int STRIPE_MAX_VPT = 4;      // 16-byte vectors per compute thread (registers): 2 or 4
+constexpr int STRIPE_LAG = 6;          // most rows between a stripe's summary and its normalisation
 constexpr int STRIPE_RING = 8;         // summary / row-constant ring entries (>= LAG + 1)
-constexpr int STRIPE_MAX_SLOTS = 16;   // shared-memory ring slots (>= LAG + 2)
+constexpr int STRIPE_MAX_SLOTS = 16;   // shared-memory ring slots (>= lag + 2)
+constexpr int STRIPE_MIN_SLOTS = 6;    // the planner's smallest ring (lag 4 and two copies in flight)
 constexpr int STRIPE_MAX_Q = 256;      // stripes per row (at most 8 summaries per collector lane)
-constexpr int STRIPE_THREADS = 1024;   // 27 compute warps + producer + publisher + 3 collectors
-constexpr int STRIPE_COMPUTE_THREADS = STRIPE_THREADS - 32 * STRIPE_SYNC_WARPS;
-constexpr int STRIPE_MAX_VPT = 3;      // 16-byte vectors per compute thread (registers)
-constexpr unsigned STRIPE_WAIT_NS = 0;  // compute warps' sleep between polls of a wait
+constexpr int STRIPE_DEFAULT_LAG = 6;  // rows of lag the planner gives (1..STRIPE_LAG, at most slots - 2)
+constexpr float STRIPE_FAST_RANGE = 11.0f;  // kept exponentials: a warp's range for the plain exp2 form
+constexpr int STRIPE_DEFAULT_PIECE = 0;  // bytes per bulk copy of a stripe (0: one copy)
+constexpr int STRIPE_DEFAULT_L2_AHEAD_F32 = 4;  // rows past a fill prefetched into L2: fp32 inputs
+constexpr int STRIPE_DEFAULT_L2_AHEAD_16 = 0;   // ... 16-bit inputs (off)
+static_assert(STRIPE_COMPUTE_WARPS <= 27 && STRIPE_THREADS <= 1024, "one CTA of at most 1024 threads");
+static_assert(STRIPE_RING >= STRIPE_LAG + 1, "a row's summary and constants live until its normalisation");
 
 constexpr int CLUSTER_RV = 2;  // register vectors per thread on the cluster path
 constexpr int CLUSTER_THREADS = 1024;

@@ -220,3 +220,29 @@ def test_long_row_workload_takes_the_read_once_path(lib):
     assert smx.last_device_status() == 0
     p = oracle.softmax_rows(x_host, "f32", 8, w.cols)
     parity.compare(y.cpu().numpy(), p, "f32")
+
+
+def test_fast_kept_exponentials_at_the_edge_of_their_range(lib):
+    """fp32 rows whose warps hold values within 11 of their maximum take the
+    plain exponential form; wider warps the compensated one.  Rows at the
+    edge of that range (uniform over the 11 below the maximum), at large
+    offsets (the row constant's rounding), with a few far values that send
+    some warps back to the compensated form, all within the fp32 bar."""
+    rows, cols = 6, 1_048_576
+    rng = np.random.default_rng(611)
+    x = np.empty((rows, cols), np.float32)
+    x[0] = rng.normal(0, 1, cols)                       # narrow: every warp fast
+    x[1] = rng.uniform(-10.999, 0, cols) + 5.0          # the whole range, small offset
+    x[2] = rng.uniform(-10.999, 0, cols) + 1000.0       # the whole range, large offset
+    x[3] = rng.uniform(-10.999, 0, cols) - 3000.0       # negative offset
+    x[4] = rng.normal(0, 1, cols)
+    x[4, ::9973] = -40.0                                # scattered far values: those warps compensated
+    x[5] = rng.uniform(-11.5, 0, cols)                  # straddles the range: a mix
+    lib.smx_debug_force_path(PATH_STRIPE)
+    xd = to_device(x.reshape(-1), "f32", rows, cols)
+    y = smx.softmax_rows(xd)
+    assert lib.smx_debug_last_path() == PATH_STRIPE
+    assert smx.last_device_status() == 0
+    p = oracle.softmax_rows(x.reshape(-1), "f32", rows, cols)
+    st = parity.compare(y.cpu().numpy(), p, "f32")
+    print("fast kept exponentials:", st)
