@@ -188,13 +188,17 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
     // the valid prefix, zero and NaN rows) are decided once per row.
     const int c = tid;
     bool timed_out = false;  // after one wait ran out, later waits poll once
+    // slots, fill parities and rows of rows i and i - LAG, kept incrementally
+    // (no division in the loop)
+    int sA = 0, sB = 0;
+    uint32_t pA = 0;
+    int64_t rowA = grp, rowB = grp;
     for (int64_t i = 0; i < nr + LAG; ++i) {
       if (i < nr) {
         // ---- row i: this warp's part of the stripe, its maximum, its sum
-        const int s = (int)(i % nslots), kr = (int)(i % RING);
+        const int s = sA, kr = (int)(i & (RING - 1));
         if (c == 0) SMX_STAMP(i, 0);
-        if (!mbar_wait_bounded(smem_addr(&full_bar[s]), (uint32_t)((i / nslots) & 1),
-                               timed_out ? 1 : a.max_polls))
+        if (!mbar_wait_bounded(smem_addr(&full_bar[s]), pA, timed_out ? 1 : a.max_polls))
           timed_out = true;
         if (c == 0) SMX_STAMP(i, 1);
         const int Lv = stripe_valid(slot_len[s]);
@@ -277,11 +281,16 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           warp_fast[kr][warp] = fast;
           mbar_arrive(smem_addr(&summ_bar[kr]));
         }
+        if (++sA == nslots) {
+          sA = 0;
+          pA ^= 1u;
+        }
+        rowA += a.groups;
       }
       if (i >= LAG) {
         // ---- normalise row r = i - LAG from its slot
         const int64_t r = i - LAG;
-        const int s = (int)(r % nslots), kr = (int)(r % RING);
+        const int s = sB, kr = (int)(r & (RING - 1));
         if (c == 0) SMX_STAMP(r, 2);
         if (!mbar_wait_bounded(smem_addr(&row_bar[kr]), (uint32_t)((r / RING) & 1),
                                timed_out ? 1 : a.max_polls))
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         const StripeRow& rc = rowc[kr];
         const int Lv = stripe_valid(slot_len[s]);
         const bool cut = Lv != nvq * V;
-        const int64_t row = row_of(r);
+        const int64_t row = rowB;
         OutT* yr = y + row * a.cols + col0;
         const uint4* sv = slots + (size_t)s * a.slot_vecs;
         bool zero_out = rc.zero_row, nan_out = rc.nan_row;
@@ -376,6 +385,8 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&free_bar[s]));
         if (c == 0) SMX_STAMP(r, 4);
+        if (++sB == nslots) sB = 0;
+        rowB += a.groups;
       }
     }
   } else if (warp == NC) {
@@ -383,16 +394,17 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
     if (lane == 0) {
       bool timed_out = false;
       int64_t filled = -1;  // the last row whose stripe copy was issued
-      for (int64_t j = 0; j < nr; ++j) {
-        const int s = (int)(j % nslots);
+      int s = 0;            // slot of row j (kept incrementally)
+      int64_t wraps = 0;    // j / nslots
+      int64_t row = grp;
+      for (int64_t j = 0; j < nr; ++j, row += a.groups) {
         if (j >= nslots) {
           // every compute warp has normalised row j - nslots from this slot
-          if (!mbar_wait_bounded(smem_addr(&free_bar[s]), (uint32_t)((j / nslots - 1) & 1), a.max_polls)) {
+          if (!mbar_wait_bounded(smem_addr(&free_bar[s]), (uint32_t)((wraps - 1) & 1), a.max_polls)) {
             timed_out = true;
             break;  // stop refilling; the copies in flight are drained below
           }
         }
-        const int64_t row = row_of(j);
         int64_t L = a.cols;
         if (valid_len != nullptr) {
           const int64_t v = __ldg(valid_len + row);
@@ -433,6 +445,10 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           }
           const int nvp = (stripe_valid(Lp) + V - 1) / V;
           if (nvp > 0) bulk_prefetch_l2(x + rp * a.cols + col0, (uint32_t)nvp * 16u);
+        }
+        if (++s == nslots) {
+          s = 0;
+          ++wraps;
         }
       }
       // no bulk copy may outlive the CTA: wait (bounded) for each slot's last

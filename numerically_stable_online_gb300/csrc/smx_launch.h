@@ -91,8 +91,7 @@ constexpr int STRIPE_MAX_Q = 256;      // stripes per row (at most 8 summaries p
 constexpr int STRIPE_DEFAULT_LAG = 6;  // rows of lag the planner gives (1..STRIPE_LAG, at most slots - 2)
 constexpr float STRIPE_FAST_RANGE = 11.0f;  // kept exponentials: a warp's range for the plain exp2 form
 constexpr int STRIPE_DEFAULT_PIECE = 0;  // bytes per bulk copy of a stripe (0: one copy)
-constexpr int STRIPE_DEFAULT_L2_AHEAD_F32 = 4;  // rows past a fill prefetched into L2: fp32 inputs
-constexpr int STRIPE_DEFAULT_L2_AHEAD_16 = 0;   // ... 16-bit inputs (off)
+constexpr int STRIPE_DEFAULT_L2_AHEAD = 2;  // rows past a fill whose stripe is prefetched into L2
 static_assert(STRIPE_COMPUTE_WARPS <= 27 && STRIPE_THREADS <= 1024, "one CTA of at most 1024 threads");
 static_assert(STRIPE_RING >= STRIPE_LAG + 1, "a row's summary and constants live until its normalisation");
 
