@@ -234,40 +234,6 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 2^u for a pair, on the FMA and integer pipes instead of the exp2 unit (the
-// row threads' exponentials are split between the two, so that neither
-// bounds the block): Cody-Waite split u = n + f with n = rint(u) (the
-// 1.5 * 2^23 rounding constant) and f in [-0.5, 0.5]; 2^f by a degree-4
-// polynomial (fitted here by least squares of the relative error on
-// Chebyshev nodes of [-0.5, 0.5]: relative error 2.7e-6, far below the
-// 16-bit P's spacing); 2^n added to the exponent bits.  Arguments below -125
-// (masked keys included) give +0, as the flush-to-zero exp2 would; a NaN
-// argument stays NaN.
-__device__ __forceinline__ void exp2_poly2(unsigned long long u2, float& r0, float& r1) {
-  const float RC = 12582912.0f;  // 1.5 * 2^23
-  const unsigned long long rc2 = pk(RC, RC), nrc2 = pk(-RC, -RC);
-  const float u0 = fmaxf(pk_lo(u2), -125.0f), u1 = fmaxf(pk_hi(u2), -125.0f);
-  const unsigned long long U = pk(u0, u1);
-  const unsigned long long t = add2(U, rc2);                        // n in the low mantissa bits
-  const unsigned long long f = fma2(add2(t, nrc2), pk(-1.0f, -1.0f), U);  // u - n, exact
-  // Horner, highest degree first
-  unsigned long long p = fma2(f, pk(0.009560510516166687f, 0.009560510516166687f),
-                              pk(0.05591703951358795f, 0.05591703951358795f));
-  p = fma2(p, f, pk(0.24024981260299683f, 0.24024981260299683f));
-  p = fma2(p, f, pk(0.6931219696998596f, 0.6931219696998596f));
-  p = fma2(p, f, pk(0.9999991655349731f, 0.9999991655349731f));
-  const int e0 = __float_as_int(pk_lo(t)) << 23, e1 = __float_as_int(pk_hi(t)) << 23;
-  const float a0 = pk_lo(u2), a1 = pk_hi(u2);
-  r0 = a0 >= -125.0f ? __int_as_float(__float_as_int(pk_lo(p)) + e0) : (a0 != a0 ? a0 : 0.0f);
-  r1 = a1 >= -125.0f ? __int_as_float(__float_as_int(pk_hi(p)) + e1) : (a1 != a1 ? a1 : 0.0f);
-}
-
-// SMX_ATT_POLY_EVERY (a build-time tuning knob): every n-th pair of a row's
-// exponentials takes exp2_poly2 (0: none).
-#ifndef SMX_ATT_POLY_EVERY
-#define SMX_ATT_POLY_EVERY 0
-#endif
-
 template <typename T, int D>
 __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
     k_attention_tc(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
@@ -516,14 +482,7 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
 #pragma unroll
       for (int i = 0; i < BN; i += 2) {
         const unsigned long long e = fma2(pk(sc[i], sc[i + 1]), cs2, ns2);
-        float p0, p1;
-        if (SMX_ATT_POLY_EVERY > 0 && (i >> 1) % (SMX_ATT_POLY_EVERY > 0 ? SMX_ATT_POLY_EVERY : 1) ==
-                                          (SMX_ATT_POLY_EVERY > 0 ? SMX_ATT_POLY_EVERY : 1) - 1) {
-          exp2_poly2(e, p0, p1);
-        } else {
-          p0 = ex2_ftz(pk_lo(e));
-          p1 = ex2_ftz(pk_hi(e));
-        }
+        const float p0 = ex2_ftz(pk_lo(e)), p1 = ex2_ftz(pk_hi(e));
         acc2[(i >> 1) & 1] = add2(acc2[(i >> 1) & 1], pk(p0, p1));
         pk2[i / 2] = pack2<T>(p0, p1);
       }
