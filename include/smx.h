@@ -355,9 +355,14 @@ int smx_version(void);
  *   chunk size in input bytes and its number of device staging slots (2 to
  *   4), 0 = default for either; staged = 1 sends mapped page-locked buffers
  *   through the staging slots too (0 = in place where possible).
- * smx_debug_set_attention_mma_sync(on): 1 = the attention forward runs on the
- *   mma.sync kernel (warp-level tensor-core instructions) instead of the
- *   tcgen05/TMEM kernel (default).
+ * smx_debug_set_attention_kernel(which): the attention forward's kernel:
+ *   0 = one 128-row query tile per CTA, two CTAs an SM, on the tcgen05
+ *   tensor cores, operands copied by the row threads (default); 1 = the same
+ *   tiling with K and V fetched by tensor-map bulk copies in their own warps;
+ *   2 = the mma.sync kernel (warp-level tensor-core instructions); 3 = two
+ *   query tiles per CTA, one CTA an SM, sharing tensor-map fetched K and V
+ *   stages.  Kernels 1 and 3 take calls with seq_k > 0 (kernel 0 the rest).
+ *   Other values select 0.
  * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
  *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
  *   first; -1 = automatic (1 and 2).
@@ -399,7 +404,7 @@ void smx_debug_set_split_slab(int64_t bytes);
 void smx_debug_set_split_hints(int stats, int apply);
 void smx_debug_set_stream_warp(int off);
 void smx_debug_set_split_fused(int on);
-void smx_debug_set_attention_mma_sync(int on);
+void smx_debug_set_attention_kernel(int which);
 void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged);
 void smx_debug_set_inflight(int64_t read_only_bytes, int64_t backward_bytes);
 int64_t smx_debug_alloc_count(void);

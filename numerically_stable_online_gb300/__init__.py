@@ -115,8 +115,8 @@ def library() -> ctypes.CDLL:
         lib.smx_debug_set_split_fused.restype = None
         lib.smx_debug_set_host_chunk.argtypes = [I64, I32, I32]
         lib.smx_debug_set_host_chunk.restype = None
-        lib.smx_debug_set_attention_mma_sync.argtypes = [I32]
-        lib.smx_debug_set_attention_mma_sync.restype = None
+        lib.smx_debug_set_attention_kernel.argtypes = [I32]
+        lib.smx_debug_set_attention_kernel.restype = None
         lib.smx_debug_alloc_count.argtypes = []
         lib.smx_debug_alloc_count.restype = I64
         lib.smx_debug_set_count_probe.argtypes = [I64]

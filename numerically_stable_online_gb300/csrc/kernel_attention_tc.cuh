@@ -126,6 +126,16 @@ __device__ __forceinline__ void tc_commit(uint32_t mbar) {
 // failure ends every CTA's waits quickly).  Returns false when it gave up.
 __device__ __forceinline__ bool tc_wait(uint32_t mbar, uint32_t parity, int64_t max_polls,
                                         const int* status) {
+  // a phase that has already completed costs one test (no timer read)
+  {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
   uint64_t t0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
   for (int64_t it = 0; it < max_polls; ++it) {
@@ -232,6 +242,79 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
       "r"(__float_as_uint(v[15]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One key block of one row thread's online softmax on tensor-memory tiles
+// (the thread's query row is its TMEM lane; ts and to carry the warp's lane
+// offset): read the row's 64 scores at ts, mask keys past jmax, update the
+// reference maximum m_ref and the sum l, rescale the row's O at `to` when the
+// reference moves (after the previous O += P V: the o_bar phase of parity
+// o_par), and write P (type T, packed two to a column) over the first 32
+// columns of the score tile.  The reference moves only when the block's
+// maximum exceeds it by more than 8 (base-2 units): the exponentials stay
+// below 2^8, and l and O always share one reference.
+template <typename T, int D>
+__device__ __forceinline__ void tc_rows_block(uint32_t ts, uint32_t to, int b, int64_t key0, int64_t jmax, float cs,
+                                              float& m_ref, float& l, bool& ok, uint32_t o_bar,
+                                              uint32_t o_par, int64_t max_polls, int* status) {
+  constexpr int BN = 64;
+  float sc[BN];
+  tc_ld64(ts, sc);
+  const int64_t nv64 = jmax - key0 + 1;
+  const int nv = nv64 < 0 ? 0 : (nv64 > BN ? BN : (int)nv64);
+  if (nv < BN) {
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (i >= nv) sc[i] = neg_inf();
+  }
+  // block maximum (four chains of three-input max), in scaled base-2 units
+  float mx4[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) mx4[j] = fmaxf(sc[2 * j], sc[2 * j + 1]);
+#pragma unroll
+  for (int i = 8; i < BN; i += 8)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx4[j] = max3(mx4[j], sc[i + 2 * j], sc[i + 2 * j + 1]);
+  const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
+  float alpha = 1.0f;
+  if (mx > m_ref + 8.0f) {
+    alpha = m_ref == neg_inf() ? 0.0f : ex2_full(m_ref - mx);
+    m_ref = mx;
+  }
+  const float nsub = m_ref == neg_inf() ? 0.0f : -m_ref;
+  // p = 2^(s cs - m_ref) (pairs by one f32x2 FMA), packed to the input type;
+  // two f32x2 partial sums
+  uint32_t pk2[BN / 2];
+  const unsigned long long cs2 = pk(cs, cs), ns2 = pk(nsub, nsub);
+  unsigned long long acc2[2] = {0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < BN; i += 2) {
+    const unsigned long long e = fma2(pk(sc[i], sc[i + 1]), cs2, ns2);
+    const float p0 = ex2_ftz(pk_lo(e)), p1 = ex2_ftz(pk_hi(e));
+    acc2[(i >> 1) & 1] = add2(acc2[(i >> 1) & 1], pk(p0, p1));
+    pk2[i / 2] = pack2<T>(p0, p1);
+  }
+  const float ps = (pk_lo(acc2[0]) + pk_hi(acc2[0])) + (pk_lo(acc2[1]) + pk_hi(acc2[1]));
+  l = __fmaf_rn(l, alpha, ps);
+  // TMEM loads and stores are warp-collective: a warp rescales when any of
+  // its rows must (the others multiply by 1, exactly)
+  if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+    // O += P(b - 1) V(b - 1) finished first
+    if (!tc_wait(o_bar, o_par, max_polls, status)) {
+      ok = false;
+      atomicOr(status, DEV_TIMEOUT);
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+    for (int c = 0; c < D; c += 16) {
+      float t16[16];
+      tc_ld16(to + (uint32_t)c, t16);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) t16[i] *= alpha;
+      tc_st16(to + (uint32_t)c, t16);
+    }
+  }
+  tc_st32(ts, pk2);
 }
 
 template <typename T, int D>
@@ -448,70 +531,12 @@ __global__ void __launch_bounds__(ATT_TC_BLOCK, 2)
       stage(kh, sK0, 2, b + 2);
       stage(vh, sV0, 3, b + 1);
 
-      // this row's 64 scores; the valid prefix of the block for this row
-      float sc[BN];
-      tc_ld64(t_s + lane_off + (uint32_t)((b & 1) * BN), sc);
-      const int64_t nv64 = jmax - key0 + 1;
-      const int nv = nv64 < 0 ? 0 : (nv64 > BN ? BN : (int)nv64);
-      if (nv < BN) {
-#pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (i >= nv) sc[i] = neg_inf();
-      }
-      // block maximum (four chains of three-input max), in scaled base-2 units
-      float mx4[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mx4[j] = fmaxf(sc[2 * j], sc[2 * j + 1]);
-#pragma unroll
-      for (int i = 8; i < BN; i += 8)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mx4[j] = max3(mx4[j], sc[i + 2 * j], sc[i + 2 * j + 1]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * cs;
-      // move the reference only when needed (see the header); alpha rescales l and O
-      float alpha = 1.0f;
-      if (mx > m_ref + 8.0f) {
-        alpha = m_ref == neg_inf() ? 0.0f : ex2_full(m_ref - mx);
-        m_ref = mx;
-      }
-      const float nsub = m_ref == neg_inf() ? 0.0f : -m_ref;
-      // p = 2^(s cs - m_ref) (pairs by one f32x2 FMA), packed to the input type;
-      // two f32x2 partial sums
-      uint32_t pk2[BN / 2];
-      const unsigned long long cs2 = pk(cs, cs), ns2 = pk(nsub, nsub);
-      unsigned long long acc2[2] = {0ull, 0ull};
-#pragma unroll
-      for (int i = 0; i < BN; i += 2) {
-        const unsigned long long e = fma2(pk(sc[i], sc[i + 1]), cs2, ns2);
-        const float p0 = ex2_ftz(pk_lo(e)), p1 = ex2_ftz(pk_hi(e));
-        acc2[(i >> 1) & 1] = add2(acc2[(i >> 1) & 1], pk(p0, p1));
-        pk2[i / 2] = pack2<T>(p0, p1);
-      }
-      const float ps = (pk_lo(acc2[0]) + pk_hi(acc2[0])) + (pk_lo(acc2[1]) + pk_hi(acc2[1]));
-      l = __fmaf_rn(l, alpha, ps);
-      // TMEM loads and stores are warp-collective: a warp rescales when any of
-      // its rows must (the others multiply by 1, exactly)
-      if (b > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        // O += P(b - 1) V(b - 1) finished first (mbar[2]: S(b) finished, so
-        // every product before it did, O += P(b - 2) V(b - 2) included, and
-        // O += P(b) V(b) waits for this block: its completed phases are b - 1
-        // or b, and the parity names b - 1 alone)
-        if (!tc_wait(tc_su32(&mbar[2]), (uint32_t)((b - 1) & 1), args.max_polls, args.status)) {
-          ok = false;
-          atomicOr(args.status, DEV_TIMEOUT);
-        }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          float t16[16];
-          tc_ld16(t_o + lane_off + (uint32_t)c, t16);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) t16[i] *= alpha;
-          tc_st16(t_o + lane_off + (uint32_t)c, t16);
-        }
-      }
-      // P(b) over the first columns of the score tile it came from (this
-      // thread's lane; the scores are in registers already)
-      tc_st32(t_s + lane_off + (uint32_t)((b & 1) * BN), pk2);
+      // a rescale waits for O += P(b - 1) V(b - 1) on mbar[2] (S(b) finished, so
+      // every product issued before it did, O += P(b - 2) V(b - 2) included,
+      // and O += P(b) V(b) waits for this block: the completed phases are
+      // b - 1 or b, and the parity names b - 1 alone)
+      tc_rows_block<T, D>(t_s + lane_off + (uint32_t)((b & 1) * BN), t_o + lane_off, b, key0, jmax, cs, m_ref, l,
+                          ok, tc_su32(&mbar[2]), (uint32_t)((b - 1) & 1), args.max_polls, args.status);
       // P written; block b + 2's K and block b's V landed (block b + 1's V,
       // the newest group, may still be in flight); hand the block to the
       // issuing warp without waiting for it

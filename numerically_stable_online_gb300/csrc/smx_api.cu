@@ -90,7 +90,7 @@ std::atomic<int> g_split_fused{0};
 std::atomic<int64_t> g_host_chunk{0};  // host-buffer call: input bytes a chunk (0 = default)
 std::atomic<int> g_host_slots{0};      // host-buffer call: device staging slots (0 = default)
 std::atomic<int> g_host_staged{0};     // host-buffer call: 1 = always through the staging slots
-std::atomic<int> g_attention_mma_sync{0};  // 1: the attention forward on mma.sync instead of tcgen05  // 0: long rows in one cooperative launch; 1: two launches per slab  // 0: warp walkers for rows that fit a warp; 1: CTA walkers only
+std::atomic<int> g_attention_kernel{0};  // ATTN_TILE (default), ATTN_TMA1, ATTN_MMA_SYNC, ATTN_TMA2
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
 // Device allocations, events and streams the library has created (a testing
@@ -1246,7 +1246,7 @@ smx_status smx_attention_forward(const void* q, const void* k, const void* v, vo
   const int64_t wl = g_wait_limit.load();
   c.max_polls = wl > 0 ? wl : ATTN_MAX_POLLS;
   c.probe_polls = wl < 0 ? -wl : 0;
-  c.tensor_memory = g_attention_mma_sync.load() == 0;
+  c.kernel = g_attention_kernel.load();
   const cudaError_t e = launch_attention(c);
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
   return SMX_OK;
@@ -1351,7 +1351,9 @@ void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged) {
   g_host_staged.store(staged ? 1 : 0);
 }
 
-void smx_debug_set_attention_mma_sync(int on) { g_attention_mma_sync.store(on ? 1 : 0); }
+void smx_debug_set_attention_kernel(int which) {
+  g_attention_kernel.store(which == ATTN_TMA1 || which == ATTN_MMA_SYNC || which == ATTN_TMA2 ? which : ATTN_TILE);
+}
 
 void smx_debug_set_split_hints(int stats, int apply) {
   g_split_hint_stats.store(stats >= 0 && stats <= 2 ? stats : -1);

@@ -118,8 +118,13 @@ struct AttnCall {
   int* status = nullptr;   // device status word (bounded waits of the tcgen05 kernel)
   int64_t max_polls = 0;
   int64_t probe_polls = 0;    // > 0: the tcgen05 kernel's error-path probe (a wait that runs out)
-  bool tensor_memory = true;  // tcgen05/TMEM kernel; false: the mma.sync kernel
+  int kernel = 0;              // ATTN_TILE, ATTN_TMA1, ATTN_MMA_SYNC or ATTN_TMA2
 };
+// attention kernels (tcgen05 unless named): one 128-row query tile per CTA,
+// operands copied by the row threads (cp.async); one tile per CTA, operands
+// fetched by tensor-map copies in their own warps; mma.sync; two tiles per
+// CTA sharing the tensor-map fetched stages
+constexpr int ATTN_TILE = 0, ATTN_TMA1 = 1, ATTN_MMA_SYNC = 2, ATTN_TMA2 = 3;
 cudaError_t launch_attention(const AttnCall& c);
 
 // Launch the planned kernel(s) for one input type; returns the first CUDA error.

@@ -42,12 +42,17 @@ def built():
     yield smx.library()
 
 
-@pytest.fixture(autouse=True, params=["tcgen05", "mma_sync"])
+KERNELS = {"tile": 0, "tma": 1, "mma_sync": 2, "tma2": 3}
+
+
+@pytest.fixture(autouse=True, params=list(KERNELS))
 def kernel(request, built):
-    """Every case on both kernels: tcgen05/TMEM (default) and mma.sync."""
-    built.smx_debug_set_attention_mma_sync(1 if request.param == "mma_sync" else 0)
+    """Every case on the four kernels: tcgen05 with operands copied by the row
+    threads (the default), tcgen05 with operands fetched by tensor-map copies
+    in their own warps (one or two query tiles per CTA), and mma.sync."""
+    built.smx_debug_set_attention_kernel(KERNELS[request.param])
     yield request.param
-    built.smx_debug_set_attention_mma_sync(0)
+    built.smx_debug_set_attention_kernel(0)
     assert smx.last_device_status() == 0
 
 
@@ -91,7 +96,11 @@ def run(heads, sq, sk, d, causal, dt, seed, qscale=1.0):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("sq,sk", [(64, 64), (70, 70), (130, 200), (200, 130), (1, 1), (1, 300), (257, 64)])
+# (300, 100) causal: the first 128-row tile sees no key while the second does;
+# (257, 64): a CTA whose second tile is wholly past the queries; (520, 1000):
+# more key blocks than stages, a ragged last block and a ragged last tile
+@pytest.mark.parametrize("sq,sk", [(64, 64), (70, 70), (130, 200), (200, 130), (1, 1), (1, 300), (257, 64),
+                                   (300, 100), (520, 1000)])
 def test_attention_shapes(d, dt, causal, sq, sk):
     w = run(3, sq, sk, d, causal, dt, seed=sq * 1000 + sk)
     print(d, dt, causal, sq, sk, w)
@@ -134,14 +143,14 @@ def test_attention_pages_shape_sampled(causal):
 
 
 def test_attention_timeout_reported_and_context_usable(kernel):
-    """The error path of the tcgen05 kernel: with a negative wait limit one
+    """The error path of the tcgen05 kernels: with a negative wait limit one
     thread per CTA waits on a barrier that nothing signals, the wait runs out
     and SMX_ERR_TIMEOUT is recorded; every other wait of the launch then stops
     early (its output is not meaningful), the kernel still lets its own
     products finish before it frees tensor memory, and the next call on the
     same context is correct and clean."""
-    if kernel != "tcgen05":
-        pytest.skip("the probe is in the tcgen05 kernel")
+    if kernel == "mma_sync":
+        pytest.skip("the probe is in the tcgen05 kernels")
     lib = smx.library()
     g = torch.Generator(device=DEV).manual_seed(93)
     q, k, v = (torch.randn(4, n, 128, generator=g, device=DEV).to(torch.bfloat16) for n in (256, 320, 320))
