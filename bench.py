@@ -62,8 +62,8 @@ KERNEL_SOURCES = ["smx_device.cuh", "smx_async.cuh", "row_core.cuh", "kernel_reg
                   "kernel_stream.cuh", "kernel_cluster.cuh", "kernel_generic.cuh",
                   "kernel_backward.cuh", "kernel_split_fused.cuh", "kernel_stripe.cuh", "launch_impl.cuh",
                   "smx_api.cu"]
-ATTN_SOURCES = ["smx_device.cuh", "kernel_attention.cuh", "kernel_attention_tc.cuh", "inst_attention.cu",
-                "smx_api.cu"]
+ATTN_SOURCES = ["smx_device.cuh", "smx_async.cuh", "kernel_attention.cuh", "kernel_attention_tc.cuh",
+                "kernel_attention_tma.cuh", "inst_attention.cu", "smx_api.cu"]
 
 
 def metric_of(op: str) -> str:
@@ -1066,7 +1066,9 @@ def run_attention(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} cuBLAS bf16 GEMM throughput (burst)",
-                     "kernel": kernel_name or "k_attention_tc<bf16,128> (tcgen05.mma, TMEM accumulators)",
+                     "kernel": kernel_name or ("k_attention_tma<bf16,128,2> (persistent, two query tiles, "
+                                               "tcgen05.mma, TMEM accumulators)" if causal else
+                                               "k_attention_tc<bf16,128> (tcgen05.mma, TMEM accumulators)"),
                      "flops_per_launch": flops, "mean_launch_us": mean_launch_ms * 1e3,
                      "median_launch_us": statistics.median(launch_ms) * 1e3},
         "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",

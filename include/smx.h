@@ -356,13 +356,14 @@ int smx_version(void);
  *   4), 0 = default for either; staged = 1 sends mapped page-locked buffers
  *   through the staging slots too (0 = in place where possible).
  * smx_debug_set_attention_kernel(which): the attention forward's kernel:
+ *   -1 = chosen by the call (default): 3 for causal calls, 0 otherwise;
  *   0 = one 128-row query tile per CTA, two CTAs an SM, on the tcgen05
- *   tensor cores, operands copied by the row threads (default); 1 = the same
- *   tiling with K and V fetched by tensor-map bulk copies in their own warps;
- *   2 = the mma.sync kernel (warp-level tensor-core instructions); 3 = two
- *   query tiles per CTA, one CTA an SM, sharing tensor-map fetched K and V
- *   stages.  Kernels 1 and 3 take calls with seq_k > 0 (kernel 0 the rest).
- *   Other values select 0.
+ *   tensor cores, operands copied by the row threads; 1 = persistent CTAs of
+ *   one tile, K and V fetched by tensor-map bulk copies in their own warps;
+ *   2 = the mma.sync kernel (warp-level tensor-core instructions); 3 =
+ *   persistent CTAs of two query tiles, one CTA an SM, sharing tensor-map
+ *   fetched K and V stages.  Kernels 1 and 3 take calls with seq_k > 0
+ *   (kernel 0 the rest).  Other values select -1.
  * smx_debug_set_split_hints(stats, apply): L2 policy of path 5's reads in its
  *   statistics and normalising passes: 0 = none, 1 = evict last, 2 = evict
  *   first; -1 = automatic (1 and 2).

@@ -153,7 +153,11 @@ cudaError_t launch_attention_tma_t(const AttnCall& c) {
   a.status = c.status;
   a.max_polls = c.max_polls;
   a.probe_polls = c.probe_polls;
-  const dim3 grid((unsigned)((c.sq + TILES * ATM_BM - 1) / (TILES * ATM_BM)), (unsigned)c.heads);
+  // persistent CTAs: as many as fit at once, each walking items grid-stride
+  a.nq = (c.sq + TILES * ATM_BM - 1) / (TILES * ATM_BM);
+  a.items = a.nq * c.heads;
+  const int64_t resident = (int64_t)(c.sm_count > 0 ? c.sm_count : 1) * S::CTAS_PER_SM;
+  const unsigned grid = (unsigned)(a.items < resident ? a.items : resident);
   note_launch();
   kern<<<grid, S::BLOCK, (size_t)smem, c.stream>>>(mq, mk, mv, static_cast<T*>(c.o), c.lse, a);
   return cudaGetLastError();

@@ -90,7 +90,7 @@ std::atomic<int> g_split_fused{0};
 std::atomic<int64_t> g_host_chunk{0};  // host-buffer call: input bytes a chunk (0 = default)
 std::atomic<int> g_host_slots{0};      // host-buffer call: device staging slots (0 = default)
 std::atomic<int> g_host_staged{0};     // host-buffer call: 1 = always through the staging slots
-std::atomic<int> g_attention_kernel{0};  // ATTN_TILE (default), ATTN_TMA1, ATTN_MMA_SYNC, ATTN_TMA2
+std::atomic<int> g_attention_kernel{-1};  // -1: by the call (causal: ATTN_TMA2, else ATTN_TILE); or one of them
 std::atomic<int64_t> g_read_only_inflight{96 * 1024};  // LSE / statistics: reads in flight per SM
 
 // Device allocations, events and streams the library has created (a testing
@@ -1246,7 +1246,12 @@ smx_status smx_attention_forward(const void* q, const void* k, const void* v, vo
   const int64_t wl = g_wait_limit.load();
   c.max_polls = wl > 0 ? wl : ATTN_MAX_POLLS;
   c.probe_polls = wl < 0 ? -wl : 0;
-  c.kernel = g_attention_kernel.load();
+  // measured on the pages' 4096 x 4096 shape: the two-tile persistent kernel
+  // balances causal work best (1276 against 1194 TFLOP/s); the one-tile
+  // kernel is level or ahead without a mask (1423 against 1407)
+  const int which = g_attention_kernel.load();
+  c.kernel = which >= 0 ? which : (causal ? ATTN_TMA2 : ATTN_TILE);
+  c.sm_count = dev->sm_count;
   const cudaError_t e = launch_attention(c);
   if (e != cudaSuccess) return cuda_fail(e, SMX_ERR_LAUNCH);
   return SMX_OK;
@@ -1352,7 +1357,9 @@ void smx_debug_set_host_chunk(int64_t bytes, int slots, int staged) {
 }
 
 void smx_debug_set_attention_kernel(int which) {
-  g_attention_kernel.store(which == ATTN_TMA1 || which == ATTN_MMA_SYNC || which == ATTN_TMA2 ? which : ATTN_TILE);
+  g_attention_kernel.store(which == ATTN_TILE || which == ATTN_TMA1 || which == ATTN_MMA_SYNC || which == ATTN_TMA2
+                               ? which
+                               : -1);
 }
 
 void smx_debug_set_split_hints(int stats, int apply) {

@@ -119,6 +119,7 @@ struct AttnCall {
   int64_t max_polls = 0;
   int64_t probe_polls = 0;    // > 0: the tcgen05 kernel's error-path probe (a wait that runs out)
   int kernel = 0;              // ATTN_TILE, ATTN_TMA1, ATTN_MMA_SYNC or ATTN_TMA2
+  int sm_count = 0;            // the persistent kernels' grid
 };
 // attention kernels (tcgen05 unless named): one 128-row query tile per CTA,
 // operands copied by the row threads (cp.async); one tile per CTA, operands

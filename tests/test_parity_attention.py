@@ -42,17 +42,18 @@ def built():
     yield smx.library()
 
 
-KERNELS = {"tile": 0, "tma": 1, "mma_sync": 2, "tma2": 3}
+KERNELS = {"auto": -1, "tile": 0, "tma": 1, "mma_sync": 2, "tma2": 3}
 
 
 @pytest.fixture(autouse=True, params=list(KERNELS))
 def kernel(request, built):
-    """Every case on the four kernels: tcgen05 with operands copied by the row
-    threads (the default), tcgen05 with operands fetched by tensor-map copies
-    in their own warps (one or two query tiles per CTA), and mma.sync."""
+    """Every case on the default choice and on each of the four kernels:
+    tcgen05 with operands copied by the row threads, tcgen05 with operands
+    fetched by tensor-map copies in their own warps (persistent CTAs of one
+    or two query tiles), and mma.sync."""
     built.smx_debug_set_attention_kernel(KERNELS[request.param])
     yield request.param
-    built.smx_debug_set_attention_kernel(0)
+    built.smx_debug_set_attention_kernel(-1)
     assert smx.last_device_status() == 0
 
 
