@@ -731,8 +731,11 @@ def time_op(g, steps, warmup, stream, torch, dev, sampler=None, world=1, sample_
     if g.smx.last_device_status() != 0:
         raise RuntimeError("device status set during warm-up")
     # per-launch durations from event pairs around every LAUNCH_SAMPLE-th step
-    # (an event pair around every launch would add its own gaps to the steps)
-    sampled = set(range(0, steps, LAUNCH_SAMPLE)) if sample_launches else set()
+    # (an event pair around every launch would add its own gaps to the steps),
+    # starting half a period in: the first launch follows the region's start
+    # with nothing recorded in between
+    first = min(LAUNCH_SAMPLE // 2, steps - 1)
+    sampled = set(range(first, steps, LAUNCH_SAMPLE)) if sample_launches else set()
     ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
