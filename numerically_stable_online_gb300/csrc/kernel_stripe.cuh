@@ -37,8 +37,13 @@
 // Every merge here, of warps and of stripes, is the pages' two-block update
 // applied to all blocks at once: the maximum M exactly (a NaN-propagating warp
 // maximum), then D = sum_b d_b e^(m_b - M) in a fixed order, so every CTA of a
-// group gets the same bits.  Modes: softmax, log_softmax, and cross-entropy
-// with its gradient (the loss is written by the thread holding x_t).  Every
+// group gets the same bits.  Modes: softmax, log_softmax, cross-entropy
+// with its gradient (the loss is written by the thread holding x_t), and the
+// softmax backward ("Softmax numerics architecture...", "The Jacobian, and the
+// backward pass that never divides": dx = p (g - s), s = sum g p): a slot holds
+// the row's stripes of p and of g, the warps' and the stripes' partial dots are
+// added in a fixed order in place of the (m, d) merge, and dx is formed from
+// the slot -- two reads and one write per element.  Every
 // wait is bounded; a wait that runs out records SMX_ERR_TIMEOUT in the device
 // status word, and the producer lets its bulk copies land before it exits.
 #pragma once
@@ -49,12 +54,17 @@
 
 namespace smx {
 
+// the stripe kernel's mode value of the softmax backward
+constexpr int MODE_BWD = CALL_BACKWARD;
+
 struct StripeArgs {
   int64_t rows, cols;
   int Q;            // stripes (CTAs) per row
   int groups;       // row groups; the grid is groups x Q CTAs
   int nslots;       // shared-memory ring slots
-  int slot_vecs;    // 16-byte vectors per slot (>= the longest stripe)
+  int slot_vecs;    // 16-byte vectors per slot (>= the longest stripe; the backward: two stripes,
+                    // p in the first half, g in the second)
+  const void* g;    // the backward's upstream gradient (x is the forward output p)
   float2* sums;     // [rows][Q] stripe summaries (m, d)
   unsigned* count;  // [rows] stripes published (zero at launch)
   unsigned* count_next;  // the other counter array: zeroed here for the next call
@@ -126,7 +136,9 @@ template <typename InT, typename OutT, int MODE, int VPT>
 __global__ void __launch_bounds__(STRIPE_THREADS, 1)
     k_rows_stripe(const InT* __restrict__ x, OutT* __restrict__ y, StripeArgs a,
                   const int32_t* __restrict__ valid_len) {
-  static_assert(MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE, "modes of the stripe kernel");
+  static_assert(MODE == MODE_SOFTMAX || MODE == MODE_LOG || MODE == MODE_CE || MODE == MODE_BWD,
+                "modes of the stripe kernel");
+  constexpr bool BWD = MODE == MODE_BWD;
   constexpr int V = Elem<InT>::V;
   constexpr bool KEEP_E = StripePolicy<InT, OutT, MODE>::KEEP_E;
   constexpr int RING = STRIPE_RING;
@@ -204,6 +216,34 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         const int Lv = stripe_valid(slot_len[s]);
         const bool cut = Lv != nvq * V;  // the valid prefix ends inside the stripe
         uint4* sv = slots + (size_t)s * a.slot_vecs;
+        if constexpr (BWD) {
+          // this warp's part of sum g p over the valid lanes (an FMA chain per
+          // thread, then the warp's butterfly)
+          const uint4* sg = sv + a.slot_vecs / 2;
+          float acc = 0.0f;
+#pragma unroll
+          for (int j = 0; j < VPT; ++j) {
+            const int k = j * TC + c;
+            if (k < nvq) {
+              float fp[V], fg[V];
+              unpack16<InT>(sv[k], fp);
+              unpack16<InT>(sg[k], fg);
+#pragma unroll
+              for (int u = 0; u < V; ++u)
+                if (!cut || k * V + u < Lv) acc = __fmaf_rn(fg[u], fp[u], acc);
+            }
+          }
+          const float dw = warp_sum(acc);
+          if (lane == 0) {
+            warp_md[kr][warp] = make_float2(dw, 0.0f);
+            mbar_arrive(smem_addr(&summ_bar[kr]));
+          }
+          if (++sA == nslots) {
+            sA = 0;
+            pA ^= 1u;
+          }
+          rowA += a.groups;
+        } else {
         float f[VPT][V];
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
@@ -286,6 +326,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           pA ^= 1u;
         }
         rowA += a.groups;
+        }
       }
       if (i >= LAG) {
         // ---- normalise row r = i - LAG from its slot
@@ -302,6 +343,24 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         const int64_t row = rowB;
         OutT* yr = y + row * a.cols + col0;
         const uint4* sv = slots + (size_t)s * a.slot_vecs;
+        if constexpr (BWD) {
+          // dx = p (g - s) over the valid lanes, +0 past them
+          const float sd = rc.M;
+          const uint4* sg = sv + a.slot_vecs / 2;
+#pragma unroll
+          for (int j = 0; j < VPT; ++j) {
+            const int k = j * TC + c;
+            if (k < nvq) {
+              float fp[V], fg[V], o[V];
+              unpack16<InT>(sv[k], fp);
+              unpack16<InT>(sg[k], fg);
+#pragma unroll
+              for (int u = 0; u < V; ++u)
+                o[u] = (!cut || k * V + u < Lv) ? __fmul_rn(fp[u], __fsub_rn(fg[u], sd)) : 0.0f;
+              store_vec<OutT, V>(yr + k * V, o);
+            }
+          }
+        } else {
         bool zero_out = rc.zero_row, nan_out = rc.nan_row;
         int64_t tl = -1;
         if constexpr (MODE == MODE_CE) {
@@ -381,6 +440,7 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
           }
           if (slot_t[s] < 0 && q == 0 && c == 0) a.loss[row] = 0.0f;
         }
+        }
         // this warp is done with the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&free_bar[s]));
@@ -420,15 +480,21 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const uint32_t bar = smem_addr(&full_bar[s]);
         if (nv > 0) {
-          // one expect-tx for the stripe, then its bytes in pieces of at most
-          // piece_bytes (several copies in flight at once)
+          // one expect-tx for the stripe (the backward: both stripes), then its
+          // bytes in pieces of at most piece_bytes (several copies in flight)
           const uint32_t total = (uint32_t)nv * 16u;
           const uint32_t piece = a.piece_bytes > 0 ? (uint32_t)a.piece_bytes : total;
-          mbar_arrive_expect_tx(bar, total);
+          mbar_arrive_expect_tx(bar, BWD ? 2u * total : total);
           const char* src = reinterpret_cast<const char*>(x + row * a.cols + col0);
           const uint32_t dst = smem_addr(slots + (size_t)s * a.slot_vecs);
           for (uint32_t off = 0; off < total; off += piece)
             bulk_load_g2s(dst + off, src + off, total - off < piece ? total - off : piece, bar);
+          if constexpr (BWD) {
+            const char* gsrc = reinterpret_cast<const char*>(static_cast<const InT*>(a.g) + row * a.cols + col0);
+            const uint32_t gdst = dst + (uint32_t)(a.slot_vecs / 2) * 16u;
+            for (uint32_t off = 0; off < total; off += piece)
+              bulk_load_g2s(gdst + off, gsrc + off, total - off < piece ? total - off : piece, bar);
+          }
         } else {
           mbar_arrive(bar);  // an empty stripe: the phase completes with no bytes
         }
@@ -444,7 +510,10 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
             Lp = v < 0 ? 0 : (v > a.cols ? a.cols : v);
           }
           const int nvp = (stripe_valid(Lp) + V - 1) / V;
-          if (nvp > 0) bulk_prefetch_l2(x + rp * a.cols + col0, (uint32_t)nvp * 16u);
+          if (nvp > 0) {
+            bulk_prefetch_l2(x + rp * a.cols + col0, (uint32_t)nvp * 16u);
+            if constexpr (BWD) bulk_prefetch_l2(static_cast<const InT*>(a.g) + rp * a.cols + col0, (uint32_t)nvp * 16u);
+          }
         }
         if (++s == nslots) {
           s = 0;
@@ -467,11 +536,18 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
       if (!mbar_wait_bounded(smem_addr(&summ_bar[kr]), (uint32_t)((r / RING) & 1),
                              timed_out ? 1 : a.max_polls))
         timed_out = true;
-      const float2 p = lane < NC ? warp_md[kr][lane] : make_float2(neg_inf(), 0.0f);
-      const MD md = warp_flat_merge(p.x, p.y);
+      float2 outv;
+      if constexpr (BWD) {
+        // the warps' partial dots, added in a fixed (butterfly) order
+        outv = make_float2(warp_sum(lane < NC ? warp_md[kr][lane].x : 0.0f), 0.0f);
+      } else {
+        const float2 p = lane < NC ? warp_md[kr][lane] : make_float2(neg_inf(), 0.0f);
+        const MD md = warp_flat_merge(p.x, p.y);
+        outv = make_float2(md.m, md.d);
+      }
       if (lane == 0) {
         const int64_t row = row_of(r);
-        a.sums[row * a.Q + q] = make_float2(md.m, md.d);
+        a.sums[row * a.Q + q] = outv;
         red_release_add(a.count + row, 1u);
         SMX_STAMP(r, 6);
       }
@@ -507,6 +583,24 @@ __global__ void __launch_bounds__(STRIPE_THREADS, 1)
       for (int u = 0; u < STRIPE_MAX_Q / 32; ++u) {
         const int t = lane + 32 * u;
         b[u] = t < a.Q ? ld_cg_f2(rs + t) : make_float2(neg_inf(), 0.0f);
+      }
+      if constexpr (BWD) {
+        // the row's dot: each lane's partials in order, then the lanes
+        float sl = 0.0f;
+#pragma unroll
+        for (int u = 0; u < STRIPE_MAX_Q / 32; ++u) sl = __fadd_rn(sl, lane + 32 * u < a.Q ? b[u].x : 0.0f);
+        const float sd = warp_sum(sl);
+        if (lane == 0) {
+          StripeRow& rc = rowc[kr];
+          rc.M = sd;
+          rc.D = 0.0f;
+          rc.zero_row = 0;
+          rc.nan_row = 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&row_bar[kr]));
+        __syncwarp();
+        continue;
       }
       // each lane's summaries first (the same merge, lane-local), then the lanes
       float ml = neg_inf();

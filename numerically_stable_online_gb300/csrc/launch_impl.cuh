@@ -260,7 +260,8 @@ cudaError_t launch_stripe_v(const Call& c, const Plan& p) {
   cudaError_t e = smem_raise(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   if (p.scratch == nullptr || p.stripe_count == nullptr) return cudaErrorInvalidValue;
-  if (p.stripe_slot_vecs > VPT * STRIPE_COMPUTE_THREADS) return cudaErrorInvalidValue;  // registers hold a stripe
+  // a compute thread's vectors of one stripe (the backward's slots hold two)
+  if (p.stripe_slot_vecs / (MODE == MODE_BWD ? 2 : 1) > VPT * STRIPE_COMPUTE_THREADS) return cudaErrorInvalidValue;
   StripeArgs a;
   a.rows = c.rows;
   a.cols = c.cols;
@@ -268,6 +269,7 @@ cudaError_t launch_stripe_v(const Call& c, const Plan& p) {
   a.groups = p.stripe_groups;
   a.nslots = p.stripe_slots;
   a.slot_vecs = p.stripe_slot_vecs;
+  a.g = c.g;
   a.sums = reinterpret_cast<float2*>(p.scratch);
   a.count = p.stripe_count;
   a.count_next = p.stripe_count_next;
@@ -301,7 +303,7 @@ cudaError_t launch_stripe(const Call& c, const Plan& p) {
 
 // Resident CTAs per SM of the stripe kernel with `smem` bytes of ring (every
 // mode and output type must fit as many; the fp32 softmax, the bf16 and fp32
-// cross-entropy and the log_softmax stand for them).
+// cross-entropy, the log_softmax and the fp32 backward stand for them).
 template <typename InT>
 int stripe_occupancy(int64_t smem) {
   auto query = [&](auto kern) -> int {
@@ -317,8 +319,10 @@ int stripe_occupancy(int64_t smem) {
   const int n2 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_CE, STRIPE_MAX_VPT>);
   const int n3 = query(k_rows_stripe<InT, float, MODE_CE, STRIPE_MAX_VPT>);
   const int n4 = query(k_rows_stripe<InT, __nv_bfloat16, MODE_LOG, STRIPE_MAX_VPT>);
+  const int n5 = query(k_rows_stripe<InT, float, MODE_BWD, STRIPE_MAX_VPT>);
   n = n2 < n ? n2 : n;
   n = n3 < n ? n3 : n;
+  n = n5 < n ? n5 : n;
   return n4 < n ? n4 : n;
 }
 
@@ -465,6 +469,7 @@ template <typename InT, typename OutT>
 cudaError_t launch_backward(const Call& c, const Plan& p) {
   constexpr int V = Elem<InT>::V;
   constexpr int SV = 16 / V;
+  if (p.path == PATH_STRIPE) return launch_stripe<InT, OutT, MODE_BWD>(c, p);
   if (p.path == PATH_GENERIC) {
     for (int64_t r0 = 0; r0 < c.rows; r0 += MAX_GRID_X_ROWS) {
       const int64_t n = c.rows - r0 < MAX_GRID_X_ROWS ? c.rows - r0 : MAX_GRID_X_ROWS;

@@ -488,7 +488,9 @@ int stripe_occupancy(int in_dtype, int64_t smem) {
 // normalisation, plus copies in flight); the preferred ring is 8 slots, then
 // 6, then 4.  Not planned when a row needs more CTAs than the device holds or
 // the device cannot launch cooperatively.
-bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p) {
+// `two`: the backward's slots hold two stripes (p and g), so fewer fit: down
+// to four slots (two rows of lag) instead of STRIPE_MIN_SLOTS
+bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* p, bool two = false) {
   if (!d.coop) return false;
   const int es = elem_size(in_dtype);
   const int V = 16 / es;
@@ -505,8 +507,11 @@ bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* 
   const int64_t cap = d.sm_count < STRIPE_MAX_Q ? d.sm_count : STRIPE_MAX_Q;  // one CTA per SM
   // a compute thread holds at most STRIPE_MAX_VPT vectors of a stripe
   const int64_t vec_cap = (int64_t)STRIPE_MAX_VPT * STRIPE_COMPUTE_THREADS;
-  for (const int target : {8, STRIPE_MIN_SLOTS}) {
-    int64_t slot_cap = ring_vecs / target;
+  const int per_slot = two ? 2 : 1;  // stripes a slot holds
+  const int min_slots = two ? STRIPE_MIN_SLOTS_TWO : STRIPE_MIN_SLOTS;
+  for (const int target : {8, STRIPE_MIN_SLOTS, STRIPE_MIN_SLOTS_TWO}) {
+    if (target < min_slots) continue;
+    int64_t slot_cap = ring_vecs / target / per_slot;  // vectors of one stripe
     if (slot_cap > vec_cap) slot_cap = vec_cap;
     if (slot_cap <= 0) continue;
     const int64_t q_min = (nvec + slot_cap - 1) / slot_cap;
@@ -517,14 +522,15 @@ bool plan_stripe(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, Plan* 
     int64_t Q = d.sm_count / groups;
     if (Q > STRIPE_MAX_Q) Q = STRIPE_MAX_Q;
     if (Q > nvec) Q = nvec;
-    const int64_t slot_vecs = (nvec + Q - 1) / Q;
+    const int64_t stripe_vecs = (nvec + Q - 1) / Q;
+    const int64_t slot_vecs = stripe_vecs * per_slot;
     int64_t nslots = ring_vecs / slot_vecs;
     if (nslots > STRIPE_MAX_SLOTS) nslots = STRIPE_MAX_SLOTS;
-    if (nslots < STRIPE_MIN_SLOTS) continue;
+    if (nslots < min_slots) continue;
     const int64_t smem = nslots * slot_vecs * 16;
     if (stripe_occupancy(in_dtype, smem) < 1) return false;
     p->path = PATH_STRIPE;
-    p->vpt = slot_vecs <= 2LL * STRIPE_COMPUTE_THREADS ? 2 : 4;
+    p->vpt = stripe_vecs <= 2LL * STRIPE_COMPUTE_THREADS ? 2 : 4;
     p->stripe_q = (int)Q;
     p->stripe_groups = (int)groups;
     p->stripe_slots = (int)nslots;
@@ -619,6 +625,11 @@ void plan_backward(DeviceInfo& d, const Call& c, bool vec_ok, Plan* p) {
       }
     }
   }
+  // long rows read once in column stripes (p and g of a row kept on chip
+  // from its dot to dx) when the stripes fit the SMs' shared memory
+  if (force != PATH_SPLIT && (force == 0 || force == PATH_STRIPE) &&
+      plan_stripe(d, c.rows, c.cols, c.in_dtype, p, true))
+    return;
   const int vpt = 16 / V;
   const int threads = 256;
   const int64_t chunk = (int64_t)threads * vpt * V;

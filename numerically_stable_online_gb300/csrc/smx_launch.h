@@ -87,6 +87,7 @@ constexpr int STRIPE_LAG = 6;          // most rows between a stripe's summary a
 constexpr int STRIPE_RING = 8;         // summary / row-constant ring entries (>= LAG + 1)
 constexpr int STRIPE_MAX_SLOTS = 16;   // shared-memory ring slots (>= lag + 2)
 constexpr int STRIPE_MIN_SLOTS = 6;    // the planner's smallest ring (lag 4 and two copies in flight)
+constexpr int STRIPE_MIN_SLOTS_TWO = 4;  // ... for the backward, whose slots hold two stripes (lag 2)
 constexpr int STRIPE_MAX_Q = 256;      // stripes per row (at most 8 summaries per collector lane)
 constexpr int STRIPE_DEFAULT_LAG = 6;  // rows of lag the planner gives (1..STRIPE_LAG, at most slots - 2)
 constexpr float STRIPE_FAST_RANGE = 11.0f;  // kept exponentials: a warp's range for the plain exp2 form

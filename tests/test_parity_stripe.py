@@ -6,7 +6,10 @@ on many groups of a few stripes each; valid lengths 0, 1, cols and lengths
 that end exactly on a stripe boundary or inside one; the policy rows (NaN and
 +inf in one stripe, a stripe of -inf only, an all -inf row, an empty row);
 log_softmax and the cross-entropy with its gradient (targets in any stripe,
-ignored targets); calls in a row with different row counts and streams (the
+ignored targets); the softmax backward (slots holding the stripes of p and
+g, partial dots added across warps and stripes; NaN in one stripe, valid
+lengths cut anywhere, rows of several groups); calls in a row with different
+row counts and streams (the
 kernel's per-row counters alternate between two arrays, and a call zeroes the
 other one for the next); the error path of the per-row count waits; and that
 the long-row workload takes this path by default in one launch.
@@ -246,3 +249,109 @@ def test_fast_kept_exponentials_at_the_edge_of_their_range(lib):
     p = oracle.softmax_rows(x.reshape(-1), "f32", rows, cols)
     st = parity.compare(y.cpu().numpy(), p, "f32")
     print("fast kept exponentials:", st)
+
+
+# ------------------------------------------------------------------ backward
+
+def backward_inputs(rows, cols, dtype, seed, valid_len=None):
+    """p: the stored softmax of rising logits (0 in masked lanes); g: N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    x = rising_rows(rows, cols, seed).astype(np.float64)
+    L = parity.lengths(rows, cols, valid_len)
+    p = np.zeros((rows, cols), np.float64)
+    for r in range(rows):
+        if L[r]:
+            e = np.exp(x[r, :L[r]] - x[r, :L[r]].max())
+            p[r, :L[r]] = e / e.sum()
+    g = rng.normal(0, 1, (rows, cols))
+    return (stored(p.astype(np.float32).reshape(-1), dtype), stored(g.astype(np.float32).reshape(-1), dtype))
+
+
+def backward_and_compare(p_store, g_store, dtype, dx_dtype, rows, cols, valid_len=None):
+    p = to_device(p_store, dtype, rows, cols)
+    g = to_device(g_store, dtype, rows, cols)
+    dx = smx.softmax_backward(p, g, valid_len=lengths_t(valid_len), out_dtype=DT[dx_dtype])
+    ref = oracle.softmax_backward(p_store, g_store, dtype, rows, cols, valid_len)
+    pv = oracle.decode(p_store, dtype).reshape(rows, cols)
+    gv = oracle.decode(g_store, dtype).reshape(rows, cols)
+    return parity.compare_backward(wl.torch_to_storage(dx.cpu()), ref, pv, gv, dx_dtype, valid_len)
+
+
+@pytest.mark.parametrize("dtype,dx_dtype", [("f32", "f32"), ("bf16", "bf16"), ("f16", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("rows,cols", [(3, 1_048_576), (6, 300_000 + 8), (40, 65_536 + 24)])
+def test_backward_rows(lib, dtype, dx_dtype, rows, cols):
+    """The backward read once: valid lengths 0, 1, cols, on a stripe boundary
+    and inside a stripe; rows of one group of 152 stripes and of many groups."""
+    b = stripe_bounds(cols, dtype, 152)
+    vl = np.full(rows, cols, np.int32)
+    if rows > 1:
+        vl[1] = 0
+    if rows > 2:
+        vl[2] = b[37]
+    if rows > 3:
+        vl[3] = 1
+    if rows > 4:
+        vl[4] = b[100] + 3
+    p, g = backward_inputs(rows, cols, dtype, rows + cols, vl)
+    lib.smx_debug_force_path(PATH_STRIPE)
+    backward_and_compare(p, g, dtype, dx_dtype, rows, cols, vl)
+    assert lib.smx_debug_last_path() == PATH_STRIPE
+    assert lib.smx_debug_last_launches() == 1
+    assert smx.last_device_status() == 0
+    p, g = backward_inputs(rows, cols, dtype, rows + cols + 1)
+    backward_and_compare(p, g, dtype, dx_dtype, rows, cols)
+    assert lib.smx_debug_last_path() == PATH_STRIPE
+
+
+def test_backward_nan_and_default_path(lib):
+    """NaN in g inside one stripe makes that row's dx NaN in its valid lanes
+    (the dot is NaN), NaN past the valid prefix changes nothing; long rows take
+    the read-once path by default, in one launch."""
+    rows, cols = 5, 400_000
+    b = stripe_bounds(cols, "f32", 152)
+    vl = np.array([cols, cols, b[80], cols, 7], np.int32)
+    p, g = backward_inputs(rows, cols, "f32", 99, vl)
+    gv = g.view(np.float32).reshape(rows, cols) if g.dtype != np.float32 else g.reshape(rows, cols)
+    gv[0, b[50] + 5] = np.nan
+    gv[2, b[90]] = np.nan  # past the valid prefix
+    backward_and_compare(p, g, "f32", "f32", rows, cols, vl)
+    assert lib.smx_debug_last_path() == PATH_STRIPE
+    assert lib.smx_debug_last_launches() == 1
+    assert smx.last_device_status() == 0
+
+
+def test_backward_workload_sampled(lib):
+    """The long-row workload's shape (64 rows of 1M fp32) on the default path,
+    checked on sampled rows against the reference."""
+    rows, cols = 64, 1_048_576
+    gen = torch.Generator(device=DEV).manual_seed(64)
+    x = torch.randn(rows, cols, generator=gen, device=DEV) * 3
+    pd = torch.softmax(x, dim=1)
+    gd = torch.randn(rows, cols, generator=gen, device=DEV)
+    dx = smx.softmax_backward(pd, gd)
+    assert lib.smx_debug_last_path() == PATH_STRIPE
+    assert smx.last_device_status() == 0
+    sel = [0, 13, 63]
+    ps = wl.torch_to_storage(pd[sel].cpu()).reshape(-1)
+    gs = wl.torch_to_storage(gd[sel].cpu()).reshape(-1)
+    ref = oracle.softmax_backward(ps, gs, "f32", len(sel), cols)
+    parity.compare_backward(wl.torch_to_storage(dx[sel].cpu()), ref, oracle.decode(ps, "f32").reshape(-1, cols),
+                            oracle.decode(gs, "f32").reshape(-1, cols), "f32")
+
+
+def test_backward_count_wait_runs_out(lib):
+    """The backward's per-row count waits share the error path: with the probe
+    each asks for one stripe more than exists, gives up after 64 polls and
+    records SMX_ERR_TIMEOUT; the next call is correct and reports nothing."""
+    rows, cols = 6, 300_000
+    p, g = backward_inputs(rows, cols, "f32", 5)
+    lib.smx_debug_force_path(PATH_STRIPE)
+    pd, gd = to_device(p, "f32", rows, cols), to_device(g, "f32", rows, cols)
+    lib.smx_debug_set_count_probe(64)
+    smx.softmax_backward(pd, gd)
+    st = smx.last_device_status()
+    lib.smx_debug_set_count_probe(0)
+    assert lib.smx_debug_last_path() == PATH_STRIPE
+    assert st == 5, f"expected SMX_ERR_TIMEOUT, got {st}"
+    backward_and_compare(p, g, "f32", "f32", rows, cols)
+    assert smx.last_device_status() == 0
