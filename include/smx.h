@@ -227,6 +227,9 @@ smx_status smx_softmax_apply_stats(const void *x, const float *m_in, const float
  *            Must not overlap p, g or valid_len (SMX_ERR_ALIAS).
  *   valid_len, rows, cols: as smx_softmax_rows.  The sum is fp32 whatever the
  *   types.  A NaN among a row's valid p or g makes its valid lanes NaN.
+ *   Long rows are read once where their stripes of p and g fit the SMs'
+ *   shared memory (one cooperative launch; the partial sums are added in a
+ *   fixed order, so the result does not depend on timing).
  */
 smx_status smx_softmax_backward(const void *p, const void *g, void *dx, int64_t rows, int64_t cols,
                                 const int32_t *valid_len, smx_dtype dtype, smx_dtype dx_dtype,
@@ -320,8 +323,8 @@ int smx_version(void);
  *   normalise; one slab of all rows unless smx_debug_set_split_slab); 6 =
  *   long rows read once, each row in column stripes held in the shared
  *   memory of a cooperative grid (softmax, log_softmax, cross-entropy with a
- *   gradient).  A forced path that cannot run the shape falls back to the
- *   automatic choice.
+ *   gradient, and the backward: the stripes of p and g).  A forced path that
+ *   cannot run the shape falls back to the automatic choice.
  * smx_debug_set_cluster(n): cap the cluster size of path 2 (1, 2, 4, 8, 16;
  *   0 = automatic); smem_bytes caps its shared-memory staging (0 = automatic).
  * smx_debug_set_wait_limit(n): n > 0: polls of a staging barrier (path 2)
