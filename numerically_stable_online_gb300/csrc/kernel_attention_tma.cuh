@@ -20,7 +20,7 @@
 // tile, whose lane 0 issues that tile's tcgen05.mma (one issuing thread was
 // measured to leave the tensor core idle with two tiles' 64-key products:
 // issuing a product waits for room in the tensor pipe); one warp that
-// fetches Q and the K stages and one that fetches the V stages, each by
+// fetches the K stages and one that fetches Q and the V stages, each by
 // tensor-map bulk copies (cp.async.bulk.tensor, 128-byte swizzle, no
 // multicast) completing on full barriers.  The row warps issue no copies.
 //
@@ -33,17 +33,17 @@
 // completes when every product of the round (and before it) has finished.
 // Everything else waits on those: the rows for their scores (round b), a
 // rescale for the previous O += P V (round b + 1), the output for the last
-// one (round n + 1), the K fetcher for a stage's previous scores and for the
-// item's last scores before it refills Q, and the V fetcher for a stage's
-// previous O += P V.  The round 16 later on the same barrier cannot finish
+// one (round n + 1), the K fetcher for a stage's previous scores, and the V
+// fetcher for a stage's previous O += P V and for the item's last scores
+// before it refills Q.  The round 16 later on the same barrier cannot finish
 // before the waiter has moved on: it needs the waiter's own progress (rows
 // it has not yet let through, or at least five stages it has not yet
 // fetched: a round per block plus two per item never outruns the fetches
 // three to one), so a phase parity names one round.  One commit a round:
 // each commit is costly for the issuing thread, and a 64-key round is short.
 // The next item's first scores are issued right after the current item's
-// last round, so they overlap the rows' output; its Q is prefetched into L2
-// when the current item starts.  Rows past the end of the query or key range
+// last round, so they overlap the rows' output; eight blocks before an item
+// ends, the fetchers bring the next item's Q and first K and V stages into L2.  Rows past the end of the query or key range
 // are zero in shared memory (the copies fill them) and masked.  Every
 // mbarrier wait is bounded; running out records SMX_ERR_TIMEOUT.
 #pragma once
