@@ -118,7 +118,8 @@ __global__ void SMX_STREAM_REGS
                   const int64_t* __restrict__ target, float* __restrict__ loss) {
   constexpr bool APPLY = (MODE == MODE_APPLY || MODE == MODE_APPLY_LOG || MODE == MODE_APPLY_CE);
   constexpr bool CE = (MODE == MODE_CE || MODE == MODE_APPLY_CE);
-  static_assert(CHUNKED || !APPLY, "the apply modes walk chunks");
+  static_assert(CHUNKED || !APPLY || (MODE == MODE_APPLY && WARP),
+                "the apply modes walk chunks, or (given per-row statistics) whole rows a warp each");
   static_assert(!(WARP && CHUNKED), "a warp walks whole rows");
   constexpr int V = Elem<InT>::V;
   // [walkers][DEPTH][VPT][G] uint4: thread g of a walker owns column g; then
@@ -338,7 +339,7 @@ __global__ void SMX_STREAM_REGS
 
     if constexpr (APPLY) {
       if (cur.r != have_row) {  // uniform: every thread walks the same items
-        if (it.row_stats) {
+        if (it.row_stats || WARP) {  // a warp walker has the row's statistics given
           row_md = MD{m_item, d_item};
         } else {
           MD acc{neg_inf(), 0.0f};

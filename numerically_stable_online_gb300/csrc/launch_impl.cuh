@@ -128,7 +128,8 @@ cudaError_t launch_stream_k(const Call& c, const Plan& p, const Items& it, float
   constexpr int V = Elem<InT>::V;
   // at most 16 elements per thread with the compensated exponential (fp32
   // outputs) or a per-element exponential after the sum, and 32 otherwise
-  constexpr bool PER_ELEMENT_EXP = ExpPolicy<OutT, MODE>::ACCURATE || MODE == MODE_APPLY ||
+  constexpr bool PER_ELEMENT_EXP = ExpPolicy<OutT, MODE>::ACCURATE ||
+                                   (MODE == MODE_APPLY && (!WARP || ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE)) ||
                                    MODE == MODE_APPLY_CE ||
                                    (MODE == MODE_CE && ExpPolicy<OutT, MODE_SOFTMAX>::ACCURATE);
   if constexpr (VPT * V > (PER_ELEMENT_EXP ? 16 : 32)) {
@@ -175,6 +176,15 @@ template <typename InT, typename OutT, int MODE>
 cudaError_t launch_stream(const Call& c, const Plan& p) {
   if constexpr (MODE == MODE_APPLY) {
     const Items it{c.rows, 0, c.cols, (int)c.cols, 1, 0, 1};
+    if (p.warp_rows) {  // whole rows a warp each (16-bit outputs), the given statistics per row
+      switch (p.vpt) {
+        case 1: return launch_stream_k<InT, OutT, MODE, 1, 2, false, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+        case 2: return launch_stream_k<InT, OutT, MODE, 2, 2, false, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+        case 4: return launch_stream_k<InT, OutT, MODE, 4, 2, false, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+        case 8: return launch_stream_k<InT, OutT, MODE, 8, 2, false, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
+        default: return cudaErrorInvalidValue;
+      }
+    }
     switch (p.vpt) {
       case 1: return launch_stream_k<InT, OutT, MODE, 1, 2, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
       case 2: return launch_stream_k<InT, OutT, MODE, 2, 2, true>(c, p, it, nullptr, nullptr, c.m_in, c.d_in);
@@ -635,6 +645,19 @@ int stream_occupancy_mode(int vpt, int threads, int depth, bool warp) {
     if (CH) return query(k2);
     return depth == 3 ? query(k3) : (depth == 4 ? query(k4) : query(k2));
   };
+  if constexpr (CH) {
+    if (warp) {  // the apply mode's warp walkers prefetch 2 rows
+      switch (vpt) {
+        case 1: return query(k_rows_stream<InT, OutT, 1, MODE, 2, false, true>);
+        case 2: return query(k_rows_stream<InT, OutT, 2, MODE, 2, false, true>);
+        case 4: return query(k_rows_stream<InT, OutT, 4, MODE, 2, false, true>);
+        case 8:
+          if constexpr (8 * V <= 32) return query(k_rows_stream<InT, OutT, 8, MODE, 2, false, true>);
+          return 0;
+        default: return 0;
+      }
+    }
+  }
   if constexpr (!CH) {
     if (warp) {
       auto wd = [&](auto k2, auto k3, auto k4) { return depth == 3 ? query(k3) : (depth == 4 ? query(k4) : query(k2)); };
@@ -688,7 +711,7 @@ int stream_occupancy(int vpt, int threads, int depth, int mode, bool warp) {
     case MODE_LOG: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_LOG>(vpt, threads, depth, warp);
     case MODE_CE: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_CE>(vpt, threads, depth, warp);
     case MODE_APPLY:
-      return stream_occupancy_mode<InT, __nv_bfloat16, MODE_APPLY>(vpt, threads, depth, false);
+      return stream_occupancy_mode<InT, __nv_bfloat16, MODE_APPLY>(vpt, threads, depth, warp);
     default: return stream_occupancy_mode<InT, __nv_bfloat16, MODE_SOFTMAX>(vpt, threads, depth, warp);
   }
 }

@@ -355,7 +355,7 @@ constexpr int64_t CLUSTER_MAX_ROW_BYTES = 4 << 20;
 constexpr int64_t ATTN_MAX_POLLS = int64_t(1) << 24;  // each tensor-core wait: tens of ms at most
 
 bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool accurate_exp,
-                 bool has_lengths, int mode, int64_t inflight, Plan* p) {
+                 bool has_lengths, int mode, int64_t inflight, Plan* p, bool apply_out16 = false) {
   const bool apply = mode == MODE_APPLY;
   const int es = elem_size(in_dtype);
   if (cols * es > STREAM_MAX_ROW_BYTES) return false;
@@ -365,9 +365,12 @@ bool plan_stream(DeviceInfo& d, int64_t rows, int64_t cols, int in_dtype, bool a
   Plan r;
   // a row that fits one warp is walked by one warp (no block barrier), unless
   // a CTA shape is forced or the warp walkers are switched off
+  // (the apply rows too when their outputs are 16-bit: no compensated
+  // exponential, so a lane holds up to 32 elements, as the softmax's do)
   bool warp = false;
-  if (!apply && g_stream_warp.load() == 0 && g_regs_threads.load() == 0 &&
-      nvec <= 32LL * max_vpt) {
+  const int warp_vpt = (apply && apply_out16) ? 32 / V : max_vpt;
+  if ((!apply || apply_out16) && g_stream_warp.load() == 0 && g_regs_threads.load() == 0 &&
+      nvec <= 32LL * warp_vpt) {
     r.vpt = 1;
     while (32LL * r.vpt < nvec) r.vpt <<= 1;
     r.threads = WARP_WALKER_THREADS;
@@ -704,7 +707,7 @@ Plan plan_call(const Call& c, DeviceInfo& dev) {
                                  : c.mode == MODE_CE  ? CE_INFLIGHT_BYTES
                                                       : STREAM_INFLIGHT_BYTES;
         planned = plan_stream(dev, c.rows, c.cols, c.in_dtype, acc, c.valid_len != nullptr, c.mode,
-                              inflight, &p);
+                              inflight, &p, c.mode == MODE_APPLY && c.out_dtype != SMX_F32);
       }
       if (!planned && classic) planned = plan_regs(c.cols, c.in_dtype, acc, &p);
       // rows longer than one CTA holds: read once in column stripes over all

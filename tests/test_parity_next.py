@@ -216,6 +216,30 @@ def test_apply_given_row_stats(lib, cols, in_dtype, out_dtype):
     print(cols, lib.smx_debug_last_path(), st)
 
 
+@pytest.mark.parametrize("cols", [96, 512, 1000, 1024])
+@pytest.mark.parametrize("in_dtype,out_dtype", [("f16", "f16"), ("bf16", "bf16"), ("f32", "bf16"), ("bf16", "f16")])
+def test_apply_warp_walkers(lib, cols, in_dtype, out_dtype):
+    """Rows that fit one warp with 16-bit outputs: a row per warp, many rows per
+    walker, the given statistics per row (including the policy's special
+    values: -inf m, NaN m or d, +inf m), lengths 0, 1 and cols."""
+    rows = 3000
+    rng = np.random.default_rng(cols + 17)
+    x = stored(rng.normal(0, 4, rows * cols), in_dtype)
+    vl = rng.integers(0, cols + 1, rows).astype(np.int32)
+    vl[::97] = 0
+    vl[1::89] = 1
+    vl[2::83] = cols
+    m, d = own_stats(x, in_dtype, rows, cols, vl)
+    m[5], d[5] = -np.inf, 0.0
+    m[6] = np.nan
+    d[7] = np.nan
+    m[8] = np.inf
+    lib.smx_debug_force_path(PATH_STREAM)
+    run_apply(x, in_dtype, out_dtype, rows, cols, m, d, vl)
+    assert lib.smx_debug_last_path() == PATH_STREAM
+    assert smx.last_device_status() == 0
+
+
 def test_apply_unaligned_and_policy(lib):
     rows, cols = 5, 1001
     rng = np.random.default_rng(9)
